@@ -1,0 +1,64 @@
+"""Pins the roofline arithmetic to the numbers the course pages print (CPU)."""
+import json
+import os
+
+import pytest
+
+from roofline_gb300 import roofline as rf
+
+with open(os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
+                       "page_facts.json")) as _f:
+    FACTS = json.load(_f)
+
+
+def test_fp32_peak_formula():
+    f = FACTS["h100_fp32_peak"]
+    peak = rf.fp32_peak_flops(f["sm"], f["clock_hz"], f["lanes"])
+    assert round(peak / 1e9, -2) == f["peak_gflops_rounded"]
+    # forgetting that an FMA is two FLOP halves the figure
+    assert round(peak / 2 / 1e9, -1) == f["forgot_fma_factor_gflops_rounded"]
+
+
+def test_results_table_consistency():
+    t = FACTS["results_table_4096"]
+    flops = rf.gemm_flops(4096, 4096, 4096)
+    naive_ms = t["rows"][0]["ms"]
+    for row in t["rows"]:
+        g = rf.gflops(flops, row["ms"])
+        assert abs(g - row["gflops"]) <= 1.0, row
+        assert round(rf.pct_of_peak(row["gflops"], t["peak_gflops"]), 1) == row["pct"]
+        assert round(naive_ms / row["ms"], 1) == row["speedup"]
+
+
+def test_tile_reuse_counts():
+    f = FACTS["tile_reuse"]
+    T = f["tile"]
+    assert 2 * T * T == f["loads"] and T ** 3 == f["fmas"]
+    assert f["fmas"] // f["loads"] == f["fma_per_load"]
+    assert 2 * f["fmas"] // f["loads"] == f["flop_per_load_rounded"]
+
+
+def test_copy_bytes_and_band():
+    f = FACTS["copy_kernel"]
+    assert f["n"] * 4 == f["bytes_per_array"]
+    assert rf.copy_bytes(f["n"]) == f["bytes_moved"]
+    # a copy taking exactly bytes / (0.9 * 3350 GB/s) sits inside the 85-92 % band
+    ms = f["bytes_moved"] / (0.9 * f["hbm_gbs"] * 1e9) * 1e3
+    pct = rf.pct_of_peak(rf.gbps(f["bytes_moved"], ms), f["hbm_gbs"])
+    assert f["expected_pct_low"] <= pct <= f["expected_pct_high"]
+
+
+def test_ridge_points():
+    f = FACTS["ridge_points"]
+    assert round(rf.ridge_point(f["bf16_tflops"] * 1e12, f["hbm_tbs"] * 1e12)) == \
+        f["bf16_ridge_rounded"]
+    assert round(rf.ridge_point(f["fp8_tflops"] * 1e12, f["hbm_tbs"] * 1e12)) == \
+        f["fp8_ridge_rounded"]
+    assert rf.intensity(f["scale_flop"], f["scale_bytes"]) == f["scale_ai"]
+
+
+def test_gemm_bytes():
+    assert rf.gemm_bytes(512, 512, 512) == 3 * 512 * 512 * 4
+    # ragged shape with beta != 0 reads C as well
+    assert rf.gemm_bytes(1023, 1025, 777, True) == 4 * (1023 * 777 + 777 * 1025 + 2 * 1023 * 1025)
+    assert rf.gemm_bytes(65536, 64, 4096) == 1_091_567_616
