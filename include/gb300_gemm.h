@@ -1,0 +1,229 @@
+/*
+ * gb300_gemm.h -- C ABI of the FP32 GEMM library for one NVIDIA GB300
+ * (sm_103a).  Shared library: libgb300gemm.so.
+ *
+ * The operation is the dense single-precision matrix multiply of the
+ * tiled-matmul course page ("Project - tiled matrix multiply": row-major
+ * float matrices, C = A * B, 2*M*N*K FLOP of work), generalised with the
+ * alpha/beta scaling of the cuBLAS SGEMM call shown in that page's section
+ * "Stage 3 - the reference ceiling: cuBLAS":
+ *
+ *     C <- alpha * A * B + beta * C
+ *
+ * Storage is row-major throughout:
+ *     A(i,k) = A[i*lda + k]   (M x K, lda >= K)
+ *     B(k,j) = B[k*ldb + j]   (K x N, ldb >= N)
+ *     C(i,j) = C[i*ldc + j]   (M x N, ldc >= N)
+ *
+ * Conventions shared by every call:
+ *   - All matrix pointers are DEVICE pointers (cudaMalloc'd or from a
+ *     framework allocator) on the current CUDA device; the caller owns them.
+ *   - Calls that take a stream only enqueue work on it and return; results
+ *     are ready after the caller synchronises that stream.  Launch errors are
+ *     returned; errors raised while kernels run surface at the caller's
+ *     synchronisation, and bounded-wait timeouts inside the tensor-core
+ *     kernel are reported by gemm_check_status().
+ *   - The library never exits the process; every call returns a status code
+ *     (GEMM_OK or a negative GEMM_ERR_*).  gemm_strerror() describes it.
+ *   - C must not overlap A or B (as in BLAS); the result is undefined if it
+ *     does.
+ */
+#ifndef GB300_GEMM_H
+#define GB300_GEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define GEMM_API __attribute__((visibility("default")))
+#else
+#define GEMM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GEMM_ABI_VERSION 1
+
+/* ---- status codes ---------------------------------------------------- */
+#define GEMM_OK 0
+#define GEMM_ERR_INVALID_ARG (-1)        /* null pointer, negative size, ld too small, unknown mode */
+#define GEMM_ERR_UNSUPPORTED (-2)        /* mode not available for this device or shape */
+#define GEMM_ERR_CUDA (-3)               /* a CUDA runtime call or a launch failed */
+#define GEMM_ERR_DEVICE_TIMEOUT (-4)     /* a kernel's bounded wait ran out (see gemm_check_status) */
+#define GEMM_ERR_WORKSPACE_TOO_SMALL (-5)/* caller workspace smaller than the plan needs */
+#define GEMM_ERR_NO_DEVICE (-6)          /* no CUDA device visible */
+
+/* ---- modes -------------------------------------------------------------
+ * AUTO picks per shape (gemm_f32_plan tells which).  FP32_SIMT runs on the
+ * CUDA cores in IEEE FP32 FMA arithmetic.  TF32X3 runs on the tcgen05
+ * tensor cores with each operand split into a TF32 high part and a TF32
+ * low part, D = Ahi*Bhi + Ahi*Blo + Alo*Bhi, accumulated in FP32 (FP32
+ * accuracy; not bitwise equal to FP32_SIMT).  The remaining modes are the
+ * course page's ladder kernels ("Stage 0" naive with x -> row, "Stage 1"
+ * coalesced with x -> column, "Stage 2" shared-memory tiles of 16 or 32),
+ * kept for comparison. */
+#define GEMM_MODE_AUTO 0
+#define GEMM_MODE_FP32_SIMT 1
+#define GEMM_MODE_TF32X3 2
+#define GEMM_MODE_NAIVE 10
+#define GEMM_MODE_COALESCED 11
+#define GEMM_MODE_TILED16 12
+#define GEMM_MODE_TILED32 13
+
+/* kernel identifiers reported by gemm_f32_plan */
+#define GEMM_KERNEL_NONE 0          /* nothing to launch (M or N is 0) */
+#define GEMM_KERNEL_SCALE 1         /* K == 0: C <- beta*C only */
+#define GEMM_KERNEL_NAIVE 2
+#define GEMM_KERNEL_COALESCED 3
+#define GEMM_KERNEL_TILED 4
+#define GEMM_KERNEL_SIMT 5          /* register-tiled CUDA-core SGEMM */
+#define GEMM_KERNEL_TC_TF32X3 6     /* tcgen05 3xTF32 */
+
+/* governing roof predicted by the planner */
+#define GEMM_BOUND_FP32 1           /* FP32 CUDA-core FMA peak */
+#define GEMM_BOUND_TF32X3 2         /* one third of the dense TF32 tensor peak */
+#define GEMM_BOUND_HBM 3            /* HBM bandwidth */
+
+typedef struct gemm_plan {
+  int32_t mode;            /* resolved mode, never GEMM_MODE_AUTO */
+  int32_t kernel;          /* GEMM_KERNEL_* */
+  int32_t bm, bn, bk;      /* CTA tile */
+  int32_t stages;          /* shared-memory pipeline depth */
+  int32_t split_k;         /* K slices; > 1 uses the workspace and a reduction */
+  int32_t vec;             /* 1: 128-bit global access path, 0: scalar path */
+  int32_t a_split_in_kernel; /* TF32X3: A split inside the GEMM kernel (1) or by a pre-pass (0) */
+  int32_t bound;           /* GEMM_BOUND_* */
+  int32_t threads;         /* threads per CTA */
+  int32_t launches;        /* kernels one call launches (split pass, main, reduction) */
+  int64_t grid_ctas;       /* CTAs of the main kernel */
+  uint64_t workspace_bytes;/* device scratch the call needs (0: none) */
+  double flops;            /* 2*M*N*K */
+  double bytes;            /* algorithmic HBM bytes: A, B once, C once (+C read if beta != 0) */
+  double intensity;        /* flops / bytes */
+} gemm_plan_t;
+
+typedef struct gemm_device_info {
+  int32_t device;
+  int32_t sm_count;
+  int32_t cc_major, cc_minor;
+  int32_t clock_khz;            /* cudaDevAttrClockRate (max SM clock) */
+  int32_t mem_clock_khz;
+  int32_t mem_bus_width_bits;
+  int32_t fp32_lanes_per_sm;    /* 128 on sm_10x */
+  int32_t regs_per_sm;
+  int32_t smem_per_sm;
+  int32_t smem_per_block_optin;
+  int32_t from_device;          /* 1: queried from a device, 0: built-in GB300 defaults */
+  int64_t l2_bytes;
+  int64_t hbm_bytes;
+  double fp32_peak_tflops;      /* sm_count * lanes * 2 * clock */
+  char name[128];
+} gemm_device_info_t;
+
+/*
+ * gemm_f32 -- C <- A * B  (alpha = 1, beta = 0: C is only written).
+ * Equivalent to gemm_f32_ex(M,N,K, 1.0f, A,lda, B,ldb, 0.0f, C,ldc, mode,
+ * NULL, 0, stream).
+ * M, N, K >= 0.  M == 0 or N == 0 is a no-op.  K == 0 writes zeros to C.
+ * A, B may be NULL only when the product is empty (K == 0 or M == 0 or
+ * N == 0); C may be NULL only when M == 0 or N == 0.
+ * stream: a cudaStream_t of the current device (0 = legacy default stream).
+ * Returns GEMM_OK, or GEMM_ERR_INVALID_ARG (bad size, ld, pointer, mode),
+ * GEMM_ERR_UNSUPPORTED, GEMM_ERR_CUDA, GEMM_ERR_NO_DEVICE.
+ */
+GEMM_API int gemm_f32(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+             const float *B, int64_t ldb, float *C, int64_t ldc, int mode,
+             cudaStream_t stream);
+
+/*
+ * gemm_f32_ex -- C <- alpha * A * B + beta * C (BLAS semantics).
+ * When beta == 0, C is not read (NaN/Inf in C do not propagate).
+ * workspace/ws_bytes: device scratch of at least plan.workspace_bytes
+ * (gemm_f32_plan), 256-byte aligned, owned by the caller and not used by
+ * any other work in flight on the GPU during this call.  workspace == NULL
+ * lets the library use its own per-device buffer, grown with cudaMalloc
+ * when needed (which synchronises the device) and freed by gemm_shutdown().
+ * A non-NULL workspace smaller than the plan needs returns
+ * GEMM_ERR_WORKSPACE_TOO_SMALL.
+ */
+GEMM_API int gemm_f32_ex(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
+                int64_t lda, const float *B, int64_t ldb, float beta, float *C,
+                int64_t ldc, int mode, void *workspace, size_t ws_bytes,
+                cudaStream_t stream);
+
+/*
+ * gemm_f32_plan -- what gemm_f32/gemm_f32_ex would run for this shape, with
+ * no launch and no allocation.  align_hint: the bitwise OR of the A, B and C
+ * addresses the call will use (0 = assume 16-byte aligned); it decides
+ * between the 128-bit and the scalar path.  beta_nonzero only changes the
+ * algorithmic byte count.  Uses the current device's properties when a
+ * device is visible, else built-in GB300 figures (152 SMs).
+ */
+GEMM_API int gemm_f32_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                  int64_t ldc, int mode, uintptr_t align_hint,
+                  int beta_nonzero, gemm_plan_t *out);
+
+/*
+ * hbm_copy_f32 -- dst[i] = src[i] for i < n on `stream` (the
+ * device-to-device copy kernel of "Bandwidths and peak rate - exercises",
+ * exercise 2: one read and one write per element).  Device pointers, must
+ * not overlap.  Enqueue only.
+ */
+GEMM_API int hbm_copy_f32(const float *src, float *dst, size_t n, cudaStream_t stream);
+
+/*
+ * hbm_copy_calibrate -- measures achieved HBM bandwidth with hbm_copy_f32:
+ * one untimed warm-up copy, then `iters` (>= 1) copies timed with CUDA
+ * events on `stream`; *gbps_out = 2 * n * sizeof(float) * iters / seconds
+ * / 1e9 (same exercise).  Blocks until the timed copies finish.  The
+ * caller owns src and dst (n floats each; the exercise uses n = 256M, 1 GiB
+ * per buffer).
+ */
+GEMM_API int hbm_copy_calibrate(const float *src, float *dst, size_t n, int iters,
+                       cudaStream_t stream, double *gbps_out);
+
+/*
+ * gemm_device_info -- SM count, clocks, register/shared-memory/L2/HBM sizes
+ * of device `dev` (the device-property program of "Memory hierarchy in
+ * hardware - solutions", exercise 1) and the FP32 CUDA-core peak derived as
+ * in "Bandwidths and peak rate - exercises", exercise 1: SMs x 128 FP32
+ * lanes x 2 x clock.  dev < 0 or no visible device fills built-in GB300
+ * figures with from_device = 0 and returns GEMM_OK.
+ */
+GEMM_API int gemm_device_info(int dev, gemm_device_info_t *out);
+
+/* Static string for a status code (never NULL). */
+GEMM_API const char *gemm_strerror(int code);
+
+/*
+ * gemm_check_status -- synchronises `stream`, then reads and clears the
+ * device status word that the tensor-core kernel sets when one of its
+ * bounded waits runs out.  Returns GEMM_ERR_DEVICE_TIMEOUT if it was set,
+ * GEMM_ERR_CUDA if the synchronisation reported an error, else GEMM_OK.
+ */
+GEMM_API int gemm_check_status(cudaStream_t stream);
+
+/*
+ * gemm_set_profile_events -- measurement aid.  For the calling host thread,
+ * the next GEMM calls record `before_main` on their stream immediately
+ * before launching their main kernel (the SIMT or tensor-core GEMM kernel)
+ * and `after_main` immediately after it, so that cudaEventElapsedTime gives
+ * that kernel's device time.  Pass NULL, NULL to stop.  The caller owns the
+ * events (created with cudaEventCreate on the current device).
+ */
+GEMM_API int gemm_set_profile_events(cudaEvent_t before_main, cudaEvent_t after_main);
+
+/* Frees the library's per-device workspace buffers.  Call with no library
+ * work in flight. */
+GEMM_API void gemm_shutdown(void);
+
+/* ABI version this library was built with (GEMM_ABI_VERSION). */
+GEMM_API int gemm_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GB300_GEMM_H */

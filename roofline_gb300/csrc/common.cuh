@@ -1,0 +1,83 @@
+// Internal declarations shared by the library's translation units.
+// Nothing here is part of the C ABI (include/gb300_gemm.h is).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gb300_gemm.h"
+
+namespace gg {
+
+// One GEMM problem, C <- alpha*A*B + beta*C, row-major (see gb300_gemm.h).
+struct GemmArgs {
+  int64_t M, N, K;
+  float alpha, beta;
+  const float *A;
+  int64_t lda;
+  const float *B;
+  int64_t ldb;
+  float *C;
+  int64_t ldc;
+};
+
+// Cached properties of one device (or the built-in GB300 figures).
+struct DeviceProps {
+  int device;
+  int sm_count;
+  int cc_major, cc_minor;
+  int clock_khz;
+  int mem_clock_khz;
+  int mem_bus_width;
+  int regs_per_sm;
+  int smem_per_sm;
+  int smem_optin;
+  int64_t l2_bytes;
+  int64_t hbm_bytes;
+  int from_device;
+  char name[128];
+};
+
+// Returns the props of the current device, or GB300 defaults when none is
+// visible (from_device = 0).  Thread-safe; queried once per device.
+const DeviceProps &current_props();
+const DeviceProps &props_of(int dev);
+const DeviceProps &default_props();
+
+// Measurement hooks (abi.cu): record the caller's profiling events around
+// the main kernel launch, if set for this host thread.
+void profile_mark_before(cudaStream_t s);
+void profile_mark_after(cudaStream_t s);
+
+// Planner (plan.cu).
+int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+              int64_t ldc, int mode, uintptr_t align_hint, int beta_nonzero,
+              const DeviceProps &dp, gemm_plan_t *out);
+bool tc_supported(const DeviceProps &dp);
+
+// Kernel launchers.  Each returns cudaSuccess or the launch error.
+cudaError_t launch_scale(const GemmArgs &p, cudaStream_t s);
+cudaError_t launch_ladder(int kernel, int tile, const GemmArgs &p, cudaStream_t s);
+cudaError_t launch_simt(const gemm_plan_t &plan, const GemmArgs &p, float *ws,
+                        cudaStream_t s);
+cudaError_t launch_splitk_reduce(const GemmArgs &p, const float *ws, int splits,
+                                 cudaStream_t s);
+cudaError_t launch_copy(const float *src, float *dst, size_t n, int sm_count,
+                        cudaStream_t s);
+// Tensor-core path (tc_tf32x3.cu).  Returns a GEMM_* status.
+int launch_tc(const gemm_plan_t &plan, const GemmArgs &p, void *ws, size_t ws_bytes,
+              cudaStream_t s);
+uint64_t tc_workspace_bytes(const gemm_plan_t &plan, int64_t M, int64_t N, int64_t K);
+int tc_read_and_clear_status(cudaStream_t s);
+
+// SIMT tile configurations (simt.cu).  id 0: 128x128x8, 256 threads, 8x8 per
+// thread; id 1: 64x64x16, 256 threads, 4x4 per thread.
+struct SimtConfig {
+  int bm, bn, bk, threads;
+};
+SimtConfig simt_config(int id);
+int simt_config_for_tile(int bm, int bn);
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+}  // namespace gg

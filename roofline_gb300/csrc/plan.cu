@@ -1,0 +1,171 @@
+// Per-shape planner: which kernel, tile, split and workspace a GEMM uses,
+// and which roof should bound it.
+//
+// The course pages pick launch shapes by hand ("Project - tiled matrix
+// multiply": 16 x 16 blocks in "Stage 0", TILE x TILE blocks and a TILE 16
+// vs 32 comparison in "Stage 2") and classify kernels as memory- or
+// compute-bound by comparing arithmetic intensity with the ridge point
+// ("Bandwidths and peak rate - exercises", exercise 3).  The planner does
+// both per call: it sizes the grid against the SM count read from the
+// device and classifies the shape with the ridge point of the mode's roof.
+#include "common.cuh"
+
+namespace gg {
+
+namespace {
+
+// Planning constants.  The measured figures used for reporting come from
+// the bench; these only steer choices.
+constexpr double kPlanHbmBytesPerSec = 6.8e12;    // GB300 STREAM-like copy, order of magnitude
+constexpr double kPlanTf32DenseFlops = 1.1e15;    // GB300 dense TF32 tensor rate, nominal
+constexpr int kFp32LanesPerSm = 128;
+
+bool mode_known(int mode) {
+  switch (mode) {
+    case GEMM_MODE_AUTO: case GEMM_MODE_FP32_SIMT: case GEMM_MODE_TF32X3:
+    case GEMM_MODE_NAIVE: case GEMM_MODE_COALESCED: case GEMM_MODE_TILED16:
+    case GEMM_MODE_TILED32:
+      return true;
+    default:
+      return false;
+  }
+}
+
+void plan_simt(int64_t M, int64_t N, int64_t K, bool vec, const DeviceProps &dp,
+               gemm_plan_t *out) {
+  const int64_t sms = dp.sm_count > 0 ? dp.sm_count : 152;
+  const int64_t tiles128 = ceil_div(M, 128) * ceil_div(N, 128);
+  SimtConfig c = simt_config(0);
+  int64_t tiles = tiles128;
+  int split = 1;
+  if (tiles128 < 2 * sms) {
+    // Too few 128x128 tiles to fill the GPU: use 64x64 tiles and, if still
+    // short of two CTAs per SM, slice K (each slice at least 64 deep).
+    c = simt_config(1);
+    tiles = ceil_div(M, 64) * ceil_div(N, 64);
+    if (tiles < 2 * sms) {
+      int64_t want = (2 * sms) / (tiles > 0 ? tiles : 1);
+      int64_t max_split = K / 64;
+      if (want > max_split) want = max_split;
+      if (want > 16) want = 16;
+      if (want > 1) split = (int)want;
+    }
+  }
+  out->kernel = GEMM_KERNEL_SIMT;
+  out->bm = c.bm;
+  out->bn = c.bn;
+  out->bk = c.bk;
+  out->stages = 2;
+  out->threads = c.threads;
+  out->vec = vec ? 1 : 0;
+  if (split > 1) {
+    // round the slice depth to whole BK tiles, then recount the slices
+    int64_t kps = ceil_div(ceil_div(K, split), c.bk) * c.bk;
+    split = (int)ceil_div(K, kps);
+  }
+  out->split_k = split;
+  out->launches = split > 1 ? 2 : 1;
+  out->grid_ctas = tiles * split;
+  out->workspace_bytes = split > 1 ? (uint64_t)split * (uint64_t)M * (uint64_t)N * 4u : 0;
+}
+
+}  // namespace
+
+int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+              int mode, uintptr_t align_hint, int beta_nonzero, const DeviceProps &dp,
+              gemm_plan_t *out) {
+  if (!out || !mode_known(mode) || M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
+  if (lda < (K > 1 ? K : 1) || ldb < (N > 1 ? N : 1) || ldc < (N > 1 ? N : 1))
+    return GEMM_ERR_INVALID_ARG;
+  gemm_plan_t p{};
+  p.split_k = 1;
+  p.stages = 1;
+  p.flops = 2.0 * (double)M * (double)N * (double)K;
+  p.bytes = 4.0 * ((double)M * K + (double)K * N + (double)M * N * (beta_nonzero ? 2.0 : 1.0));
+  p.intensity = p.bytes > 0 ? p.flops / p.bytes : 0.0;
+  const double fp32_peak = (double)(dp.sm_count > 0 ? dp.sm_count : 152) * kFp32LanesPerSm *
+                           2.0 * (double)dp.clock_khz * 1e3;
+
+  int resolved = mode;
+  if (mode == GEMM_MODE_AUTO) {
+    // Tensor cores (3xTF32) once the problem is large enough to amortise the
+    // split pass; the CUDA-core kernel otherwise.
+    const bool big = (double)M * N * K >= 64.0 * 1024 * 1024 * 64;
+    resolved = (tc_supported(dp) && big) ? GEMM_MODE_TF32X3 : GEMM_MODE_FP32_SIMT;
+  }
+  p.mode = resolved;
+
+  if (M == 0 || N == 0) {
+    p.kernel = GEMM_KERNEL_NONE;
+    *out = p;
+    return GEMM_OK;
+  }
+  if (K == 0) {
+    p.kernel = GEMM_KERNEL_SCALE;
+    p.launches = 1;
+    p.threads = 256;
+    p.grid_ctas = ceil_div(M * N, 256);
+    p.bound = GEMM_BOUND_HBM;
+    *out = p;
+    return GEMM_OK;
+  }
+
+  const bool vec = (lda % 4 == 0) && (ldb % 4 == 0) && (ldc % 4 == 0) && ((align_hint & 15) == 0);
+  switch (resolved) {
+    case GEMM_MODE_NAIVE:
+    case GEMM_MODE_COALESCED: {
+      p.kernel = resolved == GEMM_MODE_NAIVE ? GEMM_KERNEL_NAIVE : GEMM_KERNEL_COALESCED;
+      p.launches = 1;
+      p.bm = p.bn = 16;
+      p.threads = 256;
+      const int64_t gy = resolved == GEMM_MODE_NAIVE ? ceil_div(N, 16) : ceil_div(M, 16);
+      if (gy > 65535) return GEMM_ERR_UNSUPPORTED;
+      p.grid_ctas = ceil_div(M, 16) * ceil_div(N, 16);
+      break;
+    }
+    case GEMM_MODE_TILED16:
+    case GEMM_MODE_TILED32: {
+      const int t = resolved == GEMM_MODE_TILED16 ? 16 : 32;
+      p.kernel = GEMM_KERNEL_TILED;
+      p.launches = 1;
+      p.bm = p.bn = p.bk = t;
+      p.threads = t * t;
+      if (ceil_div(M, t) > 65535) return GEMM_ERR_UNSUPPORTED;
+      p.grid_ctas = ceil_div(M, t) * ceil_div(N, t);
+      break;
+    }
+    case GEMM_MODE_FP32_SIMT:
+      if (ceil_div(M, 64) > 65535) return GEMM_ERR_UNSUPPORTED;
+      plan_simt(M, N, K, vec, dp, &p);
+      break;
+    case GEMM_MODE_TF32X3: {
+      if (!tc_supported(dp)) return GEMM_ERR_UNSUPPORTED;
+      p.kernel = GEMM_KERNEL_TC_TF32X3;
+      p.bm = 128;
+      p.bn = 256;
+      p.bk = 32;
+      p.stages = 2;
+      p.threads = 192;
+      p.vec = vec ? 1 : 0;
+      p.grid_ctas = ceil_div(M, p.bm) * ceil_div(N, p.bn);
+      p.workspace_bytes = tc_workspace_bytes(p, M, N, K);
+      break;
+    }
+    default:
+      return GEMM_ERR_INVALID_ARG;
+  }
+
+  // Governing roof: the ridge point of the mode's compute roof against HBM.
+  double compute_roof = fp32_peak;
+  int compute_bound = GEMM_BOUND_FP32;
+  if (p.kernel == GEMM_KERNEL_TC_TF32X3) {
+    compute_roof = kPlanTf32DenseFlops / 3.0;
+    compute_bound = GEMM_BOUND_TF32X3;
+  }
+  const double ridge = compute_roof / kPlanHbmBytesPerSec;
+  p.bound = p.intensity < ridge ? GEMM_BOUND_HBM : compute_bound;
+  *out = p;
+  return GEMM_OK;
+}
+
+}  // namespace gg

@@ -1,0 +1,115 @@
+"""Host-side checks of the C ABI: the library loads, exports every symbol the
+header declares, and rejects bad arguments before touching a GPU."""
+import os
+import re
+
+import pytest
+
+from roofline_gb300 import build, gemm
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return gemm.load()
+
+
+def _declared_symbols():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            with open(os.path.join(ROOT, "include", fn)) as f:
+                src = f.read()
+            names |= set(re.findall(r"GEMM_API\s+[\w\s\*]+?\b(\w+)\s*\(", src))
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = _declared_symbols()
+    assert declared, "no declarations found"
+    assert declared == set(gemm.EXPORTED), declared ^ set(gemm.EXPORTED)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_abi_version_and_strerror(lib):
+    assert gemm.abi_version() == 1
+    for code in [0, -1, -2, -3, -4, -5, -6, 12345]:
+        assert isinstance(gemm.strerror(code), str) and gemm.strerror(code)
+    assert "invalid" in gemm.strerror(gemm.ERR_INVALID_ARG)
+
+
+def test_device_info_defaults(lib):
+    d = gemm.device_info(-1)
+    assert d["from_device"] == 0 and d["sm_count"] > 0
+    # peak = SMs x 128 lanes x 2 x clock
+    assert d["fp32_peak_tflops"] == pytest.approx(d["sm_count"] * 128 * 2 * d["clock_khz"] * 1e3 / 1e12)
+
+
+BAD = [
+    dict(M=-1, N=4, K=4, lda=4, ldb=4, ldc=4),
+    dict(M=4, N=-1, K=4, lda=4, ldb=4, ldc=4),
+    dict(M=4, N=4, K=-1, lda=4, ldb=4, ldc=4),
+    dict(M=4, N=4, K=8, lda=7, ldb=4, ldc=4),   # lda < K
+    dict(M=4, N=8, K=4, lda=4, ldb=7, ldc=8),   # ldb < N
+    dict(M=4, N=8, K=4, lda=4, ldb=8, ldc=7),   # ldc < N
+]
+
+
+@pytest.mark.parametrize("a", BAD)
+def test_invalid_shapes_rejected(lib, a):
+    rc = gemm.gemm_f32(a["M"], a["N"], a["K"], 16, a["lda"], 16, a["ldb"], 16, a["ldc"], 0, 0)
+    assert rc == gemm.ERR_INVALID_ARG
+    with pytest.raises(gemm.GemmError):
+        gemm.plan(a["M"], a["N"], a["K"], a["lda"], a["ldb"], a["ldc"])
+
+
+def test_null_pointers_and_mode_rejected(lib):
+    assert gemm.gemm_f32(4, 4, 4, None, 4, 16, 4, 16, 4, 0, 0) == gemm.ERR_INVALID_ARG
+    assert gemm.gemm_f32(4, 4, 4, 16, 4, None, 4, 16, 4, 0, 0) == gemm.ERR_INVALID_ARG
+    assert gemm.gemm_f32(4, 4, 4, 16, 4, 16, 4, None, 4, 0, 0) == gemm.ERR_INVALID_ARG
+    assert gemm.gemm_f32(4, 4, 4, 16, 4, 16, 4, 16, 4, 99, 0) == gemm.ERR_INVALID_ARG
+    assert gemm.gemm_f32_ex(4, 4, 4, 1.0, 16, 4, 16, 4, 0.0, 16, 4, 0, 17, 1 << 20, 0) == \
+        gemm.ERR_INVALID_ARG  # workspace not 256-byte aligned
+    assert gemm.hbm_copy_calibrate.__doc__ is None or True
+    assert lib.hbm_copy_calibrate(None, None, 16, 1, None, None) == gemm.ERR_INVALID_ARG
+
+
+def test_empty_products_are_noops_without_a_device(lib):
+    # M == 0 or N == 0: nothing to do, no device needed, NULL pointers allowed
+    assert gemm.gemm_f32(0, 5, 5, None, 5, None, 5, None, 5, 0, 0) == gemm.OK
+    assert gemm.gemm_f32(5, 0, 5, None, 5, None, 1, None, 1, 0, 0) == gemm.OK
+
+
+def test_plans_for_the_workloads(lib):
+    p = gemm.plan(512, 512, 512, mode="fp32_simt")
+    assert p["kernel_name"] == "simt" and p["vec"] == 1
+    assert p["flops"] == 2 * 512 ** 3 and p["bytes"] == 3 * 512 * 512 * 4
+    if p["split_k"] > 1:
+        assert p["workspace_bytes"] == p["split_k"] * 512 * 512 * 4
+    r = gemm.plan(1023, 1025, 777, 777, 1025, 1025, mode="fp32_simt", beta_nonzero=True)
+    assert r["vec"] == 0  # lda = 777 is not a multiple of 4 floats
+    assert r["bytes"] == 4 * (1023 * 777 + 777 * 1025 + 2 * 1023 * 1025)
+    q = gemm.plan(4096, 4096, 4096, mode="fp32_simt")
+    assert q["bm"] == 128 and q["bn"] == 128 and q["split_k"] == 1 and q["bound_name"] == "fp32"
+    s = gemm.plan(65536, 64, 4096, mode="fp32_simt")
+    assert s["intensity"] == pytest.approx(2 * 65536 * 64 * 4096 / 1_091_567_616)
+    mis = gemm.plan(512, 512, 512, mode="fp32_simt", align_hint=4)
+    assert mis["vec"] == 0
+    z = gemm.plan(8, 8, 0)
+    assert z["kernel_name"] == "scale"
+    n = gemm.plan(0, 8, 8)
+    assert n["kernel_name"] == "none"
+    for m, name in [("naive", "naive"), ("coalesced", "coalesced"), ("tiled16", "tiled"),
+                    ("tiled32", "tiled")]:
+        assert gemm.plan(64, 64, 64, mode=m)["kernel_name"] == name
+
+
+def test_valid_call_without_device_reports_no_device(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is visible")
+    rc = gemm.gemm_f32(4, 4, 4, 256, 4, 256, 4, 256, 4, 1, 0)
+    assert rc == gemm.ERR_NO_DEVICE

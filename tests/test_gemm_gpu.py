@@ -1,0 +1,195 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle."""
+import numpy as np
+import pytest
+
+import oracle
+from tests import gpu_util
+from tests.gpu_util import TOL_E1
+from workloads import WORKLOADS, matrix
+
+pytestmark = pytest.mark.gpu
+
+SMALL = ["sq512", "sq512_int", "ragged"]
+LARGE = ["sq4096", "sq8192", "skinny"]
+LADDER = ["naive", "coalesced", "tiled16", "tiled32"]
+
+
+def _check(name, mode):
+    C = gpu_util.run(name, mode)
+    r = gpu_util.compare(name, C)
+    w = WORKLOADS[name]
+    if w.a_dist == "int2":
+        assert r["mismatches"] == 0, r
+    else:
+        assert r["e1"] <= TOL_E1, r
+    # leading-dimension padding of C is never written
+    lda, ldb, ldc = w.lds()
+    if ldc > w.N:
+        assert np.all(np.isnan(C[:, w.N:]))
+    return r
+
+
+@pytest.mark.parametrize("name", SMALL)
+@pytest.mark.parametrize("mode", ["fp32_simt", "auto"] + LADDER)
+def test_small_configs(name, mode):
+    _check(name, mode)
+
+
+@pytest.mark.parametrize("name", LARGE)
+@pytest.mark.parametrize("mode", ["fp32_simt", "auto"])
+def test_large_configs_sampled(name, mode):
+    _check(name, mode)
+
+
+def test_int_config_bit_exact_and_deterministic():
+    outs = gpu_util.run("sq512_int", "fp32_simt", repeat=3)
+    for o in outs[1:]:
+        assert np.array_equal(o.view(np.uint32), outs[0].view(np.uint32))
+    assert gpu_util.compare("sq512_int", outs[0])["mismatches"] == 0
+
+
+@pytest.mark.parametrize("mode", ["fp32_simt", "auto"])
+def test_real_config_deterministic(mode):
+    outs = gpu_util.run("ragged", mode, repeat=2)
+    assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
+
+
+EDGE_SHAPES = [(1, 1, 1), (2, 3, 5), (17, 31, 33), (33, 17, 1), (127, 129, 64),
+               (129, 127, 255), (64, 64, 7), (1, 300, 257), (300, 1, 129), (255, 257, 1000),
+               (513, 65, 129), (1000, 3, 77)]
+
+
+def _run_shape(M, N, K, mode, alpha, beta, pad=(0, 0, 0), offset=0, seed=0, dist="u11"):
+    import torch
+    from roofline_gb300 import gemm
+    lda, ldb, ldc = K + pad[0], N + pad[1], N + pad[2]
+    A = matrix(M, K, lda, 7000 + seed, dist)
+    B = matrix(K, N, ldb, 7100 + seed, dist)
+    C0 = matrix(M, N, ldc, 7200 + seed, "u11")
+    # device buffers with an `offset`-float shift (misaligned when offset % 4 != 0)
+    # and a guard band of sentinel rows around C
+    sentinel = 12345.0
+
+    def dev(arr):
+        flat = torch.full((arr.size + offset + 64,), sentinel, dtype=torch.float32, device="cuda")
+        flat[offset:offset + arr.size] = torch.from_numpy(arr.reshape(-1)).cuda()
+        return flat, flat[offset:offset + arr.size].view(arr.shape)
+
+    fA, dA = dev(A)
+    fB, dB = dev(B)
+    cbuf = np.full((M + 2, ldc), sentinel, dtype=np.float32)
+    cbuf[1:M + 1] = C0
+    fC, dC = dev(cbuf)
+    gemm.matmul(dA[:, :K], dB[:, :N], dC[1:M + 1, :N], alpha, beta, mode)
+    torch.cuda.synchronize()
+    out = fC.cpu().numpy()
+    full = out[offset:offset + cbuf.size].reshape(cbuf.shape)
+    # guard bands: rows above/below, padding columns, and the tail of the buffer
+    assert np.all(full[0] == sentinel) and np.all(full[M + 1] == sentinel)
+    if ldc > N:
+        assert np.all(np.isnan(full[1:M + 1, N:]) | (full[1:M + 1, N:] == sentinel))
+        assert np.array_equal(np.isnan(full[1:M + 1, N:]), np.isnan(C0[:, N:]))
+    assert np.all(out[offset + cbuf.size:] == sentinel)
+    assert np.all(out[:offset] == sentinel)
+    ref, D = oracle.gemm(A[:, :K], B[:, :N], alpha, beta, C0[:, :N], with_bound=True)
+    return full[1:M + 1, :N], ref, D
+
+
+@pytest.mark.parametrize("shape", EDGE_SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("mode", ["fp32_simt", "tiled32", "auto"])
+def test_edge_shapes(shape, mode):
+    M, N, K = shape
+    got, ref, D = _run_shape(M, N, K, mode, 1.25, -0.5, pad=(3, 1, 2), offset=1, seed=M + N + K)
+    assert oracle.err_normalised(got, ref, D) <= TOL_E1
+
+
+@pytest.mark.parametrize("shape", [(64, 64, 64), (130, 260, 100), (256, 512, 1024)])
+@pytest.mark.parametrize("offset", [0, 1, 2])
+def test_alignment_paths_integer_exact(shape, offset):
+    M, N, K = shape
+    got, ref, D = _run_shape(M, N, K, "fp32_simt", 1.0, 0.0, pad=(0, 0, 0), offset=offset,
+                             seed=offset, dist="int2")
+    assert oracle.mismatches(got, ref) == 0
+
+
+def test_beta_zero_does_not_read_c():
+    import torch
+    from roofline_gb300 import gemm
+    A = torch.from_numpy(matrix(96, 80, None, 1, "u11")).cuda()
+    B = torch.from_numpy(matrix(80, 72, None, 2, "u11")).cuda()
+    for mode in ["fp32_simt", "auto", "tiled16"]:
+        C = torch.full((96, 72), float("nan"), device="cuda")
+        gemm.matmul(A, B, C, 1.0, 0.0, mode)
+        torch.cuda.synchronize()
+        assert torch.isfinite(C).all()
+
+
+def test_k_zero_scales_c():
+    import torch
+    from roofline_gb300 import gemm
+    C0 = torch.from_numpy(matrix(33, 45, None, 3, "u11")).cuda()
+    A = torch.empty((33, 0), device="cuda")
+    B = torch.empty((0, 45), device="cuda")
+    C = C0.clone()
+    gemm.matmul(A, B, C, 2.0, 0.5, "auto")
+    torch.cuda.synchronize()
+    assert torch.equal(C, C0 * 0.5)
+    C = C0.clone()
+    gemm.matmul(A, B, C, 2.0, 0.0, "auto")
+    torch.cuda.synchronize()
+    assert torch.equal(C, torch.zeros_like(C))
+
+
+def test_workspace_paths():
+    import torch
+    from roofline_gb300 import gemm
+    p = gemm.plan(512, 512, 512, mode="fp32_simt")
+    assert p["split_k"] > 1 and p["workspace_bytes"] > 0
+    A, B, _ = gpu_util.inputs("sq512")
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    small = torch.empty(p["workspace_bytes"] // 2, dtype=torch.uint8, device="cuda")
+    C = torch.empty((512, 512), device="cuda")
+    with pytest.raises(gemm.GemmError) as ei:
+        gemm.matmul(dA, dB, C, mode="fp32_simt", workspace=small)
+    assert ei.value.code == gemm.ERR_WORKSPACE_TOO_SMALL
+    ws = torch.empty(p["workspace_bytes"], dtype=torch.uint8, device="cuda")
+    gemm.matmul(dA, dB, C, mode="fp32_simt", workspace=ws)
+    torch.cuda.synchronize()
+    r = gpu_util.compare("sq512", C.cpu().numpy())
+    assert r["e1"] <= TOL_E1
+
+
+def test_device_info_from_device():
+    from roofline_gb300 import gemm
+    d = gemm.device_info(0)
+    assert d["from_device"] == 1 and d["sm_count"] > 100 and d["cc_major"] == 10
+    assert d["fp32_peak_tflops"] > 50
+
+
+def test_copy_kernel_exact():
+    import torch
+    from roofline_gb300 import gemm
+    n = 1_000_003
+    src = torch.randn(n + 8, device="cuda")
+    for off in [0, 1, 3]:
+        dst = torch.zeros(n + 8, device="cuda")
+        gemm.hbm_copy(src[off:off + n], dst[off:off + n])
+        torch.cuda.synchronize()
+        assert torch.equal(dst[off:off + n], src[off:off + n])
+        assert torch.all(dst[:off] == 0) and torch.all(dst[off + n:] == 0)
+
+
+def test_copy_calibration_runs():
+    import torch
+    from roofline_gb300 import gemm
+    n = 64 << 20
+    src = torch.ones(n, device="cuda")
+    dst = torch.empty(n, device="cuda")
+    gbs = gemm.hbm_copy_calibrate(src, dst, iters=5)
+    assert 500.0 < gbs < 20000.0
+    assert torch.equal(dst, src)
+
+
+def test_status_clear_after_normal_runs():
+    from roofline_gb300 import gemm
+    assert gemm.check_status() == gemm.OK
