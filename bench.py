@@ -288,6 +288,8 @@ def run_ours(args):
 
     ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for e in ev_b + ev_a:  # torch creates the underlying cudaEvent on first record
+        e.record(stream)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         dist.barrier()

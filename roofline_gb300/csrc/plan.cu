@@ -140,13 +140,34 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
       break;
     case GEMM_MODE_TF32X3: {
       if (!tc_supported(dp)) return GEMM_ERR_UNSUPPORTED;
+      if (ceil_div(M, 128) > 65535) return GEMM_ERR_UNSUPPORTED;
       p.kernel = GEMM_KERNEL_TC_TF32X3;
       p.bm = 128;
-      p.bn = 256;
-      p.bk = 32;
-      p.stages = 2;
       p.threads = 192;
       p.vec = vec ? 1 : 0;
+      const bool a_aligned = (lda % 4 == 0) && ((align_hint & 15) == 0);
+      if (N <= 64 && a_aligned) {
+        // narrow B: read A once, splitting it inside the GEMM kernel
+        p.bn = 64;
+        p.bk = 32;
+        p.stages = 4;
+        p.a_split_in_kernel = 1;
+        p.launches = 2;
+      } else {
+        const int64_t sms = dp.sm_count > 0 ? dp.sm_count : 152;
+        const int64_t tiles256 = ceil_div(M, 128) * ceil_div(N, 256);
+        if (tiles256 >= 4 * sms) {
+          p.bn = 256;
+          p.bk = 16;
+          p.stages = 4;
+        } else {
+          p.bn = 128;
+          p.bk = 16;
+          p.stages = 3;
+        }
+        p.a_split_in_kernel = 0;
+        p.launches = 3;
+      }
       p.grid_ctas = ceil_div(M, p.bm) * ceil_div(N, p.bn);
       p.workspace_bytes = tc_workspace_bytes(p, M, N, K);
       break;

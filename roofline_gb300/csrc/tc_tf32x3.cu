@@ -1,16 +1,677 @@
-// tcgen05 3xTF32 tensor-core GEMM (placeholder until the kernel lands).
+// 3xTF32 GEMM on the tcgen05 tensor cores (sm_103a).
+//
+// The course page points at Tensor Cores as the last rung of the GEMM
+// ladder and notes that letting cuBLAS use TF32 would beat the FP32 peak
+// ("Project - tiled matrix multiply", sections "Stage 3 - the reference
+// ceiling: cuBLAS" and "What comes next").  TF32 alone keeps only 11
+// significant bits, so each FP32 operand x is split into two TF32 values,
+//     x_hi = tf32_rna(x),   x_lo = tf32_rna(x - x_hi)   (x - x_hi is exact),
+// and the product is formed from three TF32 MMAs accumulated in FP32:
+//     A*B ~= A_hi*B_lo + A_lo*B_hi + A_hi*B_hi
+// (the dropped A_lo*B_lo term is below 2^-22 of |A||B|).
+//
+// Kernel structure (one 128 x BN output tile per CTA, 192 threads):
+//   warp 0      TMA producer: one lane streams K-blocks of the operand tiles
+//               into a STAGES-deep shared-memory ring (cp.async.bulk.tensor,
+//               completion counted on per-stage mbarriers);
+//   warp 1      allocates the TMEM accumulator (BN fp32 columns x 128 lanes)
+//               and one lane issues tcgen05.mma kind::tf32, committing each
+//               stage back to the producer when its MMAs retire;
+//   warps 2-5   (a) when A is split inside the kernel: convert each landed
+//               FP32 A tile into its hi part (in place) and lo part, then
+//               release it to the MMA warp; (b) epilogue: tcgen05.ld the
+//               accumulator rows, apply C = alpha*acc + beta*C, store.
+// Operands live in shared memory K-major with the TMA swizzle (64 B rows for
+// BK = 16, 128 B rows for BK = 32), which is the layout the MMA's smem
+// descriptors describe.  B is row-major (N contiguous) in global memory, so
+// the split pass writes B_hi/B_lo transposed (N x K, K contiguous).
+//
+// Every mbarrier wait is bounded by a %globaltimer deadline; on expiry the
+// kernel records GEMM_ERR_DEVICE_TIMEOUT in a device status word, stops
+// issuing work, waits (bounded) for the copies and MMAs it already issued,
+// frees its TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstdlib>
+#include <mutex>
+
 #include "common.cuh"
 
 namespace gg {
 
-bool tc_supported(const DeviceProps &) { return false; }
+namespace {
 
-uint64_t tc_workspace_bytes(const gemm_plan_t &, int64_t, int64_t, int64_t) { return 0; }
+__device__ int g_tc_status;  // 0 = ok, else a GEMM_ERR_* code
 
-int launch_tc(const gemm_plan_t &, const GemmArgs &, void *, size_t, cudaStream_t) {
+constexpr int kBM = 128;
+constexpr int kThreadsTC = 192;
+constexpr int kConvThreads = 128;  // warps 2..5
+
+// ------------------------------------------------------------------ PTX helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for the phase of `bar` with the given parity.  Gives up when the
+// deadline passes or another role has raised the CTA's abort flag.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t deadline,
+                                          volatile int *abort_flag) {
+  uint32_t spins = 0;
+  while (!mbar_try_wait(bar, parity)) {
+    if ((++spins & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer() > deadline) return false;
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                            int32_t x, int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(dst)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+// D(tmem) (+)= A(smem) * B(smem)^T, both K-major, kind::tf32.
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrives on `bar` once every previously issued tcgen05 op of this thread completes.
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ float tf32_rna(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return __uint_as_float(r);
+}
+
+// Shared-memory matrix descriptor of a K-major, swizzled operand tile whose
+// 8-row groups are `sbo` bytes apart.  layout: 2 = 128 B swizzle, 4 = 64 B.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t sbo, uint32_t layout) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1u << 16;                            // leading byte offset (unused here)
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;        // stride byte offset
+  d |= (uint64_t)1u << 46;                            // descriptor version for tcgen05
+  d |= (uint64_t)layout << 61;
+  return d;
+}
+
+// Instruction descriptor: D = F32, A = B = TF32, both K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
+  return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
+// ------------------------------------------------------------------ the GEMM kernel
+
+struct TcParams {
+  int64_t M, N, K;
+  float alpha, beta;
+  float *C;
+  int64_t ldc;
+  int num_kb;
+  uint64_t timeout_ns;
+  int stall_producer;  // test hook: the producer issues nothing
+};
+
+template <int BN, int BK, int STAGES, bool A_INKERNEL>
+struct TcCfg {
+  static constexpr int A_BYTES = kBM * BK * 4;
+  static constexpr int B_BYTES = BN * BK * 4;
+  // per stage: A_hi, A_lo, B_hi, B_lo
+  static constexpr int STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;
+  static constexpr int TX_BYTES = A_INKERNEL ? (A_BYTES + 2 * B_BYTES) : STAGE_BYTES;
+  static constexpr int ROW_BYTES = BK * 4;              // 64 or 128
+  static constexpr uint32_t LAYOUT = ROW_BYTES == 128 ? 2u : 4u;
+  static constexpr uint32_t SBO = 8 * ROW_BYTES;        // 8-row group stride
+  static constexpr int TMEM_COLS = BN < 32 ? 32 : BN;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+  static_assert(ROW_BYTES == 64 || ROW_BYTES == 128, "BK must be 16 or 32");
+  static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN");
+};
+
+template <int BN, int BK, int STAGES, bool A_INKERNEL>
+__global__ void __launch_bounds__(kThreadsTC, 1)
+tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when A_INKERNEL
+                 const __grid_constant__ CUtensorMap tmA_lo,
+                 const __grid_constant__ CUtensorMap tmB_hi,
+                 const __grid_constant__ CUtensorMap tmB_lo, TcParams p) {
+  using Cfg = TcCfg<BN, BK, STAGES, A_INKERNEL>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * Cfg::STAGE_BYTES);
+  uint64_t *conv = full + STAGES;    // A tile converted (A_INKERNEL)
+  uint64_t *empty = conv + STAGES;   // stage free again
+  uint64_t *acc_full = empty + STAGES;
+  uint64_t *drain = acc_full + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  auto a_hi = [&](int s) { return smem + s * Cfg::STAGE_BYTES; };
+  auto a_lo = [&](int s) { return smem + s * Cfg::STAGE_BYTES + Cfg::A_BYTES; };
+  auto b_hi = [&](int s) { return smem + s * Cfg::STAGE_BYTES + 2 * Cfg::A_BYTES; };
+  auto b_lo = [&](int s) {
+    return smem + s * Cfg::STAGE_BYTES + 2 * Cfg::A_BYTES + Cfg::B_BYTES;
+  };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t m0 = (int64_t)blockIdx.y * kBM;
+  const int64_t n0 = (int64_t)blockIdx.x * BN;
+  const uint64_t deadline = globaltimer() + p.timeout_ns;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&conv[s], kConvThreads);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA_hi);
+    prefetch_tmap(&tmB_hi);
+    prefetch_tmap(&tmB_lo);
+    if (!A_INKERNEL) prefetch_tmap(&tmA_lo);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  bool ok = true;
+  if (warp == 0) {
+    // ---------------- TMA producer
+    int issued = 0;
+    if (lane == 0 && !p.stall_producer) {
+      for (int kb = 0; kb < p.num_kb; ++kb) {
+        const int s = kb % STAGES;
+        const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
+        if (!mbar_wait(&empty[s], ph ^ 1u, deadline, abort_flag)) {
+          ok = false;
+          break;
+        }
+        mbar_expect_tx(&full[s], Cfg::TX_BYTES);
+        const int32_t kx = kb * BK;
+        tma_load_2d(a_hi(s), &tmA_hi, &full[s], kx, (int32_t)m0);
+        if (!A_INKERNEL) tma_load_2d(a_lo(s), &tmA_lo, &full[s], kx, (int32_t)m0);
+        tma_load_2d(b_hi(s), &tmB_hi, &full[s], kx, (int32_t)n0);
+        tma_load_2d(b_lo(s), &tmB_lo, &full[s], kx, (int32_t)n0);
+        ++issued;
+      }
+      if (!ok) *abort_flag = 1;
+      // wait (bounded) for every load this lane issued, whatever happened
+      const uint64_t drain_deadline = globaltimer() + 2000000000ull;
+      volatile int never = 0;
+      for (int kb = issued - STAGES < 0 ? 0 : issued - STAGES; kb < issued; ++kb)
+        mbar_wait(&full[kb % STAGES], (uint32_t)(kb / STAGES) & 1u, drain_deadline, &never);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_tf32(kBM, BN);
+      bool any = false;
+      for (int kb = 0; kb < p.num_kb; ++kb) {
+        const int s = kb % STAGES;
+        const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
+        if (!mbar_wait(A_INKERNEL ? &conv[s] : &full[s], ph, deadline, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t ah = smem_u32(a_hi(s)), al = smem_u32(a_lo(s));
+        const uint32_t bh = smem_u32(b_hi(s)), bl = smem_u32(b_lo(s));
+#pragma unroll
+        for (int kk = 0; kk < BK / 8; ++kk) {
+          const uint32_t off = kk * 32;  // 8 TF32 values = 32 bytes along K
+          const uint64_t dah = smem_desc(ah + off, Cfg::SBO, Cfg::LAYOUT);
+          const uint64_t dal = smem_desc(al + off, Cfg::SBO, Cfg::LAYOUT);
+          const uint64_t dbh = smem_desc(bh + off, Cfg::SBO, Cfg::LAYOUT);
+          const uint64_t dbl = smem_desc(bl + off, Cfg::SBO, Cfg::LAYOUT);
+          const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+          mma_tf32(tmem_base, dah, dbl, idesc, acc);  // small terms first
+          mma_tf32(tmem_base, dal, dbh, idesc, 1u);
+          mma_tf32(tmem_base, dah, dbh, idesc, 1u);
+        }
+        mma_commit(&empty[s]);
+        any = true;
+      }
+      if (ok) {
+        mma_commit(acc_full);
+      } else {
+        *abort_flag = 1;
+      }
+      if (any) {
+        // every MMA issued so far must retire before TMEM is freed
+        mma_commit(drain);
+        volatile int never = 0;
+        mbar_wait(drain, 0, globaltimer() + 2000000000ull, &never);
+      }
+    }
+  } else {
+    // ---------------- converters (A split in kernel) and epilogue, warps 2..5
+    const int ct = threadIdx.x - 64;  // 0..127
+    if (A_INKERNEL) {
+      constexpr int VEC = Cfg::A_BYTES / 16;  // 16-byte chunks per A tile
+      for (int kb = 0; kb < p.num_kb; ++kb) {
+        const int s = kb % STAGES;
+        const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
+        if (!mbar_wait(&full[s], ph, deadline, abort_flag)) {
+          ok = false;
+          break;
+        }
+        float4 *hi = reinterpret_cast<float4 *>(a_hi(s));
+        float4 *lo = reinterpret_cast<float4 *>(a_lo(s));
+        // the swizzle permutes 16-byte chunks only, so an elementwise pass
+        // over the raw buffer keeps hi and lo in the MMA's layout
+        for (int i = ct; i < VEC; i += kConvThreads) {
+          float4 x = hi[i];
+          float4 h, l;
+          h.x = tf32_rna(x.x); l.x = tf32_rna(x.x - h.x);
+          h.y = tf32_rna(x.y); l.y = tf32_rna(x.y - h.y);
+          h.z = tf32_rna(x.z); l.z = tf32_rna(x.z - h.z);
+          h.w = tf32_rna(x.w); l.w = tf32_rna(x.w - h.w);
+          hi[i] = h;
+          lo[i] = l;
+        }
+        fence_async_smem();
+        mbar_arrive(&conv[s]);
+      }
+      if (!ok) *abort_flag = 1;
+    }
+    if (ok) {
+      if (!mbar_wait(acc_full, 0, deadline, abort_flag)) {
+        ok = false;
+        *abort_flag = 1;
+      }
+    }
+    // tcgen05.ld is warp-collective: the whole warp drains or none of it
+    const bool warp_ok = __all_sync(0xffffffffu, ok);
+    if (warp_ok) {
+      tc_fence_after();
+      const int quarter = warp & 3;  // TMEM lanes this warp may read
+      const int64_t row = m0 + quarter * 32 + lane;
+      const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16);
+      const bool vec = ((p.ldc & 3) == 0) && ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0);
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 32) {
+        uint32_t r[32];
+        tmem_ld32(tbase + (uint32_t)c, r);
+        tmem_ld_wait();
+        if (row < p.M) {
+          float *dst = p.C + row * p.ldc + n0 + c;
+          const int64_t left = p.N - (n0 + c);
+          if (vec && left >= 32) {
+#pragma unroll
+            for (int q = 0; q < 32; q += 4) {
+              float4 o = make_float4(p.alpha * __uint_as_float(r[q]),
+                                     p.alpha * __uint_as_float(r[q + 1]),
+                                     p.alpha * __uint_as_float(r[q + 2]),
+                                     p.alpha * __uint_as_float(r[q + 3]));
+              if (p.beta != 0.0f) {
+                const float4 old = *reinterpret_cast<const float4 *>(dst + q);
+                o.x = fmaf(p.beta, old.x, o.x);
+                o.y = fmaf(p.beta, old.y, o.y);
+                o.z = fmaf(p.beta, old.z, o.z);
+                o.w = fmaf(p.beta, old.w, o.w);
+              }
+              *reinterpret_cast<float4 *>(dst + q) = o;
+            }
+          } else {
+#pragma unroll
+            for (int q = 0; q < 32; ++q) {
+              if (q < left) {
+                float o = p.alpha * __uint_as_float(r[q]);
+                if (p.beta != 0.0f) o = fmaf(p.beta, dst[q], o);
+                dst[q] = o;
+              }
+            }
+          }
+        }
+      }
+    }
+  }
+
+  if (!ok) atomicExch(&g_tc_status, GEMM_ERR_DEVICE_TIMEOUT);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+}
+
+// ------------------------------------------------------------------ split pass
+
+// dst_hi/dst_lo (rows x kp, row-major) <- split of src (rows x k, ld), zero for k <= c < kp.
+__global__ void split_rows_kernel(const float *__restrict__ src, int64_t ld, int64_t rows,
+                                  int64_t k, int64_t kp, float *__restrict__ hi,
+                                  float *__restrict__ lo) {
+  const int64_t groups = rows * (kp / 4);
+  for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < groups;
+       g += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = g / (kp / 4);
+    const int64_t c = (g % (kp / 4)) * 4;
+    const float *s = src + r * ld + c;
+    float v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = (c + i < k) ? __ldg(s + i) : 0.0f;
+    float4 h, l;
+    h.x = tf32_rna(v[0]); l.x = tf32_rna(v[0] - h.x);
+    h.y = tf32_rna(v[1]); l.y = tf32_rna(v[1] - h.y);
+    h.z = tf32_rna(v[2]); l.z = tf32_rna(v[2] - h.z);
+    h.w = tf32_rna(v[3]); l.w = tf32_rna(v[3] - h.w);
+    *reinterpret_cast<float4 *>(hi + r * kp + c) = h;
+    *reinterpret_cast<float4 *>(lo + r * kp + c) = l;
+  }
+}
+
+// B (k x n, ld, row-major) -> Bt_hi/Bt_lo (n x kp, row-major), 32 x 32 tiles
+// through shared memory so both the reads (along n) and the writes (along
+// k) are coalesced; columns k <= c < kp are zero.
+__global__ void split_transpose_kernel(const float *__restrict__ src, int64_t ld, int64_t k,
+                                       int64_t n, int64_t kp, float *__restrict__ hi,
+                                       float *__restrict__ lo) {
+  __shared__ float tile[32][33];
+  const int64_t k0 = (int64_t)blockIdx.y * 32;
+  const int64_t n0 = (int64_t)blockIdx.x * 32;
+  const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8
+  for (int j = ty; j < 32; j += 8) {
+    const int64_t kk = k0 + j, nn = n0 + tx;
+    tile[j][tx] = (kk < k && nn < n) ? __ldg(src + kk * ld + nn) : 0.0f;
+  }
+  __syncthreads();
+  for (int j = ty; j < 32; j += 8) {
+    const int64_t nn = n0 + j, kk = k0 + tx;
+    if (nn < n && kk < kp) {
+      const float v = tile[tx][j];
+      const float h = tf32_rna(v);
+      hi[nn * kp + kk] = h;
+      lo[nn * kp + kk] = tf32_rna(v - h);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encoder() {
+  std::call_once(g_encode_once, [] {
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    else
+      cudaGetLastError();
+  });
+  return g_encode != nullptr;
+}
+
+// 2-D FP32 tensor map: inner dimension `inner` (contiguous), `outer` rows
+// `stride_elems` apart; box = box_inner x box_rows with the swizzle that
+// matches box_inner * 4 bytes.
+bool encode_2d(CUtensorMap *m, const float *base, int64_t inner, int64_t outer,
+               int64_t stride_elems, int box_inner, int box_rows) {
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+  cuuint64_t strides[1] = {(cuuint64_t)(stride_elems * 4)};
+  cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapSwizzle sw =
+      box_inner * 4 == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+uint64_t env_u64(const char *name, uint64_t dflt) {
+  const char *v = std::getenv(name);
+  if (!v || !*v) return dflt;
+  return std::strtoull(v, nullptr, 10);
+}
+
+inline int64_t round_up(int64_t a, int64_t b) { return (a + b - 1) / b * b; }
+inline uint64_t align256(uint64_t x) { return (x + 255) & ~uint64_t(255); }
+
+struct WsLayout {
+  uint64_t a_hi, a_lo, b_hi, b_lo, total;
+  int64_t kp;
+};
+
+WsLayout ws_layout(int64_t M, int64_t N, int64_t K, bool a_inkernel) {
+  WsLayout w{};
+  w.kp = round_up(K, 4);
+  const uint64_t a_bytes = a_inkernel ? 0 : align256((uint64_t)M * w.kp * 4);
+  const uint64_t b_bytes = align256((uint64_t)N * w.kp * 4);
+  w.a_hi = 0;
+  w.a_lo = a_bytes;
+  w.b_hi = 2 * a_bytes;
+  w.b_lo = 2 * a_bytes + b_bytes;
+  w.total = 2 * a_bytes + 2 * b_bytes;
+  return w;
+}
+
+template <int BN, int BK, int STAGES, bool AK>
+int launch_cfg(const gemm_plan_t &plan, const GemmArgs &a, char *ws, cudaStream_t s) {
+  using Cfg = TcCfg<BN, BK, STAGES, AK>;
+  const WsLayout L = ws_layout(a.M, a.N, a.K, AK);
+  float *ahi = reinterpret_cast<float *>(ws + L.a_hi);
+  float *alo = reinterpret_cast<float *>(ws + L.a_lo);
+  float *bhi = reinterpret_cast<float *>(ws + L.b_hi);
+  float *blo = reinterpret_cast<float *>(ws + L.b_lo);
+
+  // split pass
+  if (!AK) {
+    int64_t groups = a.M * (L.kp / 4);
+    int64_t blocks = ceil_div(groups, 256);
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    split_rows_kernel<<<(unsigned)blocks, 256, 0, s>>>(a.A, a.lda, a.M, a.K, L.kp, ahi, alo);
+  }
+  {
+    dim3 grid((unsigned)ceil_div(a.N, 32), (unsigned)ceil_div(L.kp, 32));
+    split_transpose_kernel<<<grid, dim3(32, 8), 0, s>>>(a.B, a.ldb, a.K, a.N, L.kp, bhi, blo);
+  }
+  if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_CUDA;
+
+  CUtensorMap tA0, tA1, tB0, tB1;
+  bool ok;
+  if (AK) {
+    ok = encode_2d(&tA0, a.A, a.K, a.M, a.lda, BK, kBM);
+    tA1 = tA0;
+  } else {
+    ok = encode_2d(&tA0, ahi, L.kp, a.M, L.kp, BK, kBM) &&
+         encode_2d(&tA1, alo, L.kp, a.M, L.kp, BK, kBM);
+  }
+  ok = ok && encode_2d(&tB0, bhi, L.kp, a.N, L.kp, BK, BN) &&
+       encode_2d(&tB1, blo, L.kp, a.N, L.kp, BK, BN);
+  if (!ok) return GEMM_ERR_UNSUPPORTED;
+
+  TcParams p;
+  p.M = a.M;
+  p.N = a.N;
+  p.K = a.K;
+  p.alpha = a.alpha;
+  p.beta = a.beta;
+  p.C = a.C;
+  p.ldc = a.ldc;
+  p.num_kb = (int)ceil_div(a.K, BK);
+  p.timeout_ns = env_u64("GEMM_DEBUG_WAIT_LIMIT_NS", 2000000000ull);
+  p.stall_producer = (int)env_u64("GEMM_DEBUG_STALL_PRODUCER", 0);
+
+  auto kern = tc_tf32x3_kernel<BN, BK, STAGES, AK>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Cfg::SMEM_BYTES) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+  dim3 grid((unsigned)ceil_div(a.N, BN), (unsigned)ceil_div(a.M, kBM));
+  profile_mark_before(s);
+  kern<<<grid, kThreadsTC, Cfg::SMEM_BYTES, s>>>(tA0, tA1, tB0, tB1, p);
+  profile_mark_after(s);
+  (void)plan;
+  return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+}  // namespace
+
+// The tcgen05 kernels are built for sm_103a only.
+bool tc_supported(const DeviceProps &dp) { return dp.cc_major == 10 && dp.cc_minor == 3; }
+
+// Tile configurations the planner may pick (bn, bk, stages, A split in kernel).
+bool tc_config_valid(int bn, int bk, int stages, int a_inkernel) {
+  return (bn == 256 && bk == 16 && stages == 4 && !a_inkernel) ||
+         (bn == 128 && bk == 16 && stages == 3 && !a_inkernel) ||
+         (bn == 64 && bk == 32 && stages == 4 && a_inkernel);
+}
+
+uint64_t tc_workspace_bytes(const gemm_plan_t &plan, int64_t M, int64_t N, int64_t K) {
+  return ws_layout(M, N, K, plan.a_split_in_kernel != 0).total;
+}
+
+int launch_tc(const gemm_plan_t &plan, const GemmArgs &a, void *ws, size_t ws_bytes,
+              cudaStream_t s) {
+  if (!get_encoder()) return GEMM_ERR_UNSUPPORTED;
+  if (ws_bytes < tc_workspace_bytes(plan, a.M, a.N, a.K) || ws == nullptr)
+    return GEMM_ERR_WORKSPACE_TOO_SMALL;
+  char *w = static_cast<char *>(ws);
+  if (plan.a_split_in_kernel) {
+    if ((a.lda & 3) || (reinterpret_cast<uintptr_t>(a.A) & 15)) return GEMM_ERR_UNSUPPORTED;
+    if (plan.bn == 64 && plan.bk == 32 && plan.stages == 4)
+      return launch_cfg<64, 32, 4, true>(plan, a, w, s);
+    return GEMM_ERR_UNSUPPORTED;
+  }
+  if (plan.bn == 256 && plan.bk == 16 && plan.stages == 4)
+    return launch_cfg<256, 16, 4, false>(plan, a, w, s);
+  if (plan.bn == 128 && plan.bk == 16 && plan.stages == 3)
+    return launch_cfg<128, 16, 3, false>(plan, a, w, s);
   return GEMM_ERR_UNSUPPORTED;
 }
 
-int tc_read_and_clear_status(cudaStream_t) { return GEMM_OK; }
+int tc_read_and_clear_status(cudaStream_t s) {
+  int v = 0;
+  if (cudaMemcpyFromSymbolAsync(&v, g_tc_status, sizeof(int), 0, cudaMemcpyDeviceToHost, s) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbolAsync(g_tc_status, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, s) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess) {
+      cudaGetLastError();
+      return GEMM_ERR_CUDA;
+    }
+    return v;
+  }
+  return GEMM_OK;
+}
 
 }  // namespace gg

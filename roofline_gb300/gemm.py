@@ -191,6 +191,8 @@ def set_profile_events(before=None, after=None) -> None:
     following calls made from this thread (None, None to stop)."""
     b = None if before is None else before.cuda_event
     a = None if after is None else after.cuda_event
+    if (before is not None and not b) or (after is not None and not a):
+        raise ValueError("record the events once before passing them (torch creates them lazily)")
     rc = load().gemm_set_profile_events(b, a)
     if rc != OK:
         raise GemmError(rc, "gemm_set_profile_events")

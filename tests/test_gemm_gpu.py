@@ -30,13 +30,13 @@ def _check(name, mode):
 
 
 @pytest.mark.parametrize("name", SMALL)
-@pytest.mark.parametrize("mode", ["fp32_simt", "auto"] + LADDER)
+@pytest.mark.parametrize("mode", ["fp32_simt", "tf32x3", "auto"] + LADDER)
 def test_small_configs(name, mode):
     _check(name, mode)
 
 
 @pytest.mark.parametrize("name", LARGE)
-@pytest.mark.parametrize("mode", ["fp32_simt", "auto"])
+@pytest.mark.parametrize("mode", ["fp32_simt", "tf32x3", "auto"])
 def test_large_configs_sampled(name, mode):
     _check(name, mode)
 
@@ -48,7 +48,7 @@ def test_int_config_bit_exact_and_deterministic():
     assert gpu_util.compare("sq512_int", outs[0])["mismatches"] == 0
 
 
-@pytest.mark.parametrize("mode", ["fp32_simt", "auto"])
+@pytest.mark.parametrize("mode", ["fp32_simt", "tf32x3", "auto"])
 def test_real_config_deterministic(mode):
     outs = gpu_util.run("ragged", mode, repeat=2)
     assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
@@ -96,20 +96,34 @@ def _run_shape(M, N, K, mode, alpha, beta, pad=(0, 0, 0), offset=0, seed=0, dist
 
 
 @pytest.mark.parametrize("shape", EDGE_SHAPES, ids=lambda s: "x".join(map(str, s)))
-@pytest.mark.parametrize("mode", ["fp32_simt", "tiled32", "auto"])
+@pytest.mark.parametrize("mode", ["fp32_simt", "tf32x3", "tiled32", "auto"])
 def test_edge_shapes(shape, mode):
     M, N, K = shape
     got, ref, D = _run_shape(M, N, K, mode, 1.25, -0.5, pad=(3, 1, 2), offset=1, seed=M + N + K)
     assert oracle.err_normalised(got, ref, D) <= TOL_E1
 
 
-@pytest.mark.parametrize("shape", [(64, 64, 64), (130, 260, 100), (256, 512, 1024)])
+@pytest.mark.parametrize("shape", [(64, 64, 64), (130, 260, 100), (256, 512, 1024),
+                                   (384, 48, 520), (1000, 64, 96)])
 @pytest.mark.parametrize("offset", [0, 1, 2])
-def test_alignment_paths_integer_exact(shape, offset):
+@pytest.mark.parametrize("mode", ["fp32_simt", "tf32x3"])
+def test_alignment_paths_integer_exact(shape, offset, mode):
     M, N, K = shape
-    got, ref, D = _run_shape(M, N, K, "fp32_simt", 1.0, 0.0, pad=(0, 0, 0), offset=offset,
+    got, ref, D = _run_shape(M, N, K, mode, 1.0, 0.0, pad=(0, 0, 0), offset=offset,
                              seed=offset, dist="int2")
     assert oracle.mismatches(got, ref) == 0
+
+
+@pytest.mark.parametrize("shape", [(1000, 64, 96), (513, 33, 1000), (256, 64, 4096),
+                                   (129, 17, 40)])
+def test_tf32x3_split_in_kernel(shape):
+    """N <= 64 with an aligned A takes the path that splits A inside the GEMM."""
+    from roofline_gb300 import gemm
+    M, N, K = shape
+    p = gemm.plan(M, N, K, K, N, N, mode="tf32x3")
+    assert p["a_split_in_kernel"] == (1 if K % 4 == 0 else 0)
+    got, ref, D = _run_shape(M, N, K, "tf32x3", 0.75, 0.25, pad=(0, 0, 0), offset=0, seed=K)
+    assert oracle.err_normalised(got, ref, D) <= TOL_E1
 
 
 def test_beta_zero_does_not_read_c():
@@ -117,7 +131,7 @@ def test_beta_zero_does_not_read_c():
     from roofline_gb300 import gemm
     A = torch.from_numpy(matrix(96, 80, None, 1, "u11")).cuda()
     B = torch.from_numpy(matrix(80, 72, None, 2, "u11")).cuda()
-    for mode in ["fp32_simt", "auto", "tiled16"]:
+    for mode in ["fp32_simt", "tf32x3", "auto", "tiled16"]:
         C = torch.full((96, 72), float("nan"), device="cuda")
         gemm.matmul(A, B, C, 1.0, 0.0, mode)
         torch.cuda.synchronize()
