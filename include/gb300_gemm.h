@@ -216,6 +216,39 @@ GEMM_API int gemm_check_status(cudaStream_t stream);
  */
 GEMM_API int gemm_set_profile_events(cudaEvent_t before_main, cudaEvent_t after_main);
 
+/*
+ * gemm_f32_splitk_noalloc -- C <- alpha * A * B + beta * C on the CUDA cores
+ * (the FP32_SIMT kernel), allocating no device memory at all.  The course
+ * pages have no counterpart to this call; it exists for callers that cannot
+ * allocate: code held to a device-memory budget fixed at start-up (for
+ * example under a framework allocator that has already reserved the free
+ * memory) and latency-critical loops that cannot take the device-wide
+ * synchronisation of cudaMalloc/cudaFree.  The split-K partial sums go to a
+ * static array of GEMM_NOALLOC_SCRATCH_BYTES that the library keeps in
+ * device memory on every GPU that loads it, until the process exits.
+ *
+ * Arguments and layout are those of gemm_f32_ex (device pointers, row-major,
+ * lda >= K, ldb >= N, ldc >= N).  split_k = 0 takes the planner's slice
+ * count for FP32_SIMT; split_k >= 1 asks for that many K slices (rounded to
+ * whole 8- or 16-deep tiles).  When the slices' partial sums,
+ * split_k * M * N * 4 bytes, exceed GEMM_NOALLOC_SCRATCH_BYTES the call
+ * returns GEMM_ERR_WORKSPACE_TOO_SMALL and launches nothing; one slice needs
+ * no scratch.  Other errors as gemm_f32_ex.
+ *
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  All
+ * calls share the one array, and a call leaves its partial sums there:
+ * calls whose kernels overlap on the GPU (different streams, or different
+ * host threads) race on it and must be serialised by the caller.  Nothing
+ * in the array needs clearing between calls: each call writes every partial
+ * sum before reading it.
+ */
+#define GEMM_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+GEMM_API int gemm_f32_splitk_noalloc(int64_t M, int64_t N, int64_t K, float alpha,
+                                     const float *A, int64_t lda, const float *B,
+                                     int64_t ldb, float beta, float *C, int64_t ldc,
+                                     int split_k, cudaStream_t stream);
+
 /* Frees the library's per-device workspace buffers.  Call with no library
  * work in flight. */
 GEMM_API void gemm_shutdown(void);

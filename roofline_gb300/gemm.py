@@ -42,7 +42,10 @@ BOUNDS = {0: "none", 1: "fp32", 2: "tf32x3", 3: "hbm"}
 # Every symbol include/gb300_gemm.h declares.
 EXPORTED = ["gemm_f32", "gemm_f32_ex", "gemm_f32_plan", "hbm_copy_f32", "hbm_copy_calibrate",
             "gemm_device_info", "gemm_strerror", "gemm_check_status", "gemm_shutdown",
-            "gemm_abi_version", "gemm_set_profile_events"]
+            "gemm_abi_version", "gemm_set_profile_events", "gemm_f32_splitk_noalloc"]
+
+# size of the static scratch array behind gemm_f32_splitk_noalloc
+NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 class GemmPlan(ctypes.Structure):
@@ -129,6 +132,9 @@ def load(path: str | None = None):
         lib.gemm_abi_version.restype = i32
         lib.gemm_set_profile_events.argtypes = [vp, vp]
         lib.gemm_set_profile_events.restype = i32
+        lib.gemm_f32_splitk_noalloc.argtypes = [i64, i64, i64, f32, vp, i64, vp, i64, f32, vp,
+                                                i64, i32, vp]
+        lib.gemm_f32_splitk_noalloc.restype = i32
         if path is None:
             _lib = lib
         return lib
@@ -152,6 +158,15 @@ def gemm_f32_ex(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, mode=MODE_AUTO,
                 workspace=None, ws_bytes=0, stream=0) -> int:
     return load().gemm_f32_ex(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, _mode(mode),
                               workspace, ws_bytes, stream)
+
+
+def gemm_f32_splitk_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, split_k=0,
+                            stream=0) -> int:
+    """Split-K CUDA-core GEMM whose scratch is the library's static device
+    array: no device allocation happens in the call (for callers that cannot
+    allocate).  Raw device pointers; returns the status code."""
+    return load().gemm_f32_splitk_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                                          split_k, stream)
 
 
 def plan(M, N, K, lda=None, ldb=None, ldc=None, mode=MODE_AUTO, align_hint=0,
