@@ -103,6 +103,8 @@ typedef struct gemm_plan {
   double flops;            /* 2*M*N*K */
   double bytes;            /* algorithmic HBM bytes: A, B once, C once (+C read if beta != 0) */
   double intensity;        /* flops / bytes */
+  int32_t b_concat;        /* TF32X3: A_hi*[B_hi|B_lo] issued as one MMA of width 2*bn (1) or two MMAs (0) */
+  int32_t ctas_per_sm;     /* CTAs of the main kernel resident per SM (shared memory and TMEM budget) */
 } gemm_plan_t;
 
 typedef struct gemm_device_info {

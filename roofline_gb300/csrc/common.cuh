@@ -68,7 +68,8 @@ cudaError_t launch_copy(const float *src, float *dst, size_t n, int sm_count,
 int launch_tc(const gemm_plan_t &plan, const GemmArgs &p, void *ws, size_t ws_bytes,
               cudaStream_t s);
 uint64_t tc_workspace_bytes(const gemm_plan_t &plan, int64_t M, int64_t N, int64_t K);
-bool tc_config_valid(int bn, int bk, int stages, int a_inkernel);
+bool tc_config_valid(int bn, int bk, int stages, int a_inkernel, int concat);
+int tc_ctas_per_sm(int bn, int bk, int stages, int a_inkernel, int concat, int smem_per_sm);
 int tc_read_and_clear_status(cudaStream_t s);
 
 // SIMT tile configurations (simt.cu).  id 0: 128x128x8, 256 threads, 8x8 per

@@ -8,6 +8,9 @@
 // ("Bandwidths and peak rate - exercises", exercise 3).  The planner does
 // both per call: it sizes the grid against the SM count read from the
 // device and classifies the shape with the ridge point of the mode's roof.
+#include <cstdio>
+#include <cstdlib>
+
 #include "common.cuh"
 
 namespace gg {
@@ -65,6 +68,7 @@ void plan_simt(int64_t M, int64_t N, int64_t K, bool vec, const DeviceProps &dp,
   }
   out->split_k = split;
   out->launches = split > 1 ? 2 : 1;
+  out->ctas_per_sm = 2;
   out->grid_ctas = tiles * split;
   out->workspace_bytes = split > 1 ? (uint64_t)split * (uint64_t)M * (uint64_t)N * 4u : 0;
 }
@@ -145,29 +149,41 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
       p.bm = 128;
       p.threads = 192;
       p.vec = vec ? 1 : 0;
+      // A aligned for TMA (16-byte base, lda a multiple of 4): the GEMM kernel
+      // reads FP32 A once and splits it on chip; otherwise a pre-pass
+      // writes A_hi/A_lo to the workspace.  B is always pre-split
+      // (transposed to K-major).
       const bool a_aligned = (lda % 4 == 0) && ((align_hint & 15) == 0);
-      if (N <= 64 && a_aligned) {
-        // narrow B: read A once, splitting it inside the GEMM kernel
-        p.bn = 64;
-        p.bk = 32;
-        p.stages = 4;
-        p.a_split_in_kernel = 1;
-        p.launches = 2;
+      const int64_t sms = dp.sm_count > 0 ? dp.sm_count : 152;
+      const int64_t tiles256 = ceil_div(M, 128) * ceil_div(N, 256);
+      const bool wide = N > 128 && tiles256 >= 2 * sms;
+      p.a_split_in_kernel = a_aligned ? 1 : 0;
+      p.launches = a_aligned ? 2 : 3;
+      auto set = [&](int bn, int bk, int st, int cc) {
+        p.bn = bn; p.bk = bk; p.stages = st; p.b_concat = cc;
+      };
+      if (a_aligned) {
+        if (N <= 64) set(64, 32, 3, 1);        // narrow: 2 CTAs per SM stream A
+        else if (wide) set(256, 16, 5, 0);
+        else set(128, 32, 4, 1);
       } else {
-        const int64_t sms = dp.sm_count > 0 ? dp.sm_count : 152;
-        const int64_t tiles256 = ceil_div(M, 128) * ceil_div(N, 256);
-        if (tiles256 >= 4 * sms) {
-          p.bn = 256;
-          p.bk = 16;
-          p.stages = 4;
-        } else {
-          p.bn = 128;
-          p.bk = 16;
-          p.stages = 3;
-        }
-        p.a_split_in_kernel = 0;
-        p.launches = 3;
+        if (wide) set(256, 16, 4, 0);
+        else set(128, 16, 3, 1);
       }
+      // Tuning knob: GEMM_TC_CONFIG="bn,bk,stages,a_split_in_kernel,b_concat"
+      // picks one of the built configurations (ignored if it names none, or
+      // asks for the in-kernel split with a misaligned A).
+      if (const char *cfg = std::getenv("GEMM_TC_CONFIG")) {
+        int bn = 0, bk = 0, st = 0, ak = 0, cc = 0;
+        if (std::sscanf(cfg, "%d,%d,%d,%d,%d", &bn, &bk, &st, &ak, &cc) == 5 &&
+            tc_config_valid(bn, bk, st, ak, cc) && (!ak || a_aligned)) {
+          set(bn, bk, st, cc);
+          p.a_split_in_kernel = ak;
+          p.launches = ak ? 2 : 3;
+        }
+      }
+      p.ctas_per_sm = tc_ctas_per_sm(p.bn, p.bk, p.stages, p.a_split_in_kernel, p.b_concat,
+                                     dp.smem_per_sm > 0 ? dp.smem_per_sm : 233472);
       p.grid_ctas = ceil_div(M, p.bm) * ceil_div(N, p.bn);
       p.workspace_bytes = tc_workspace_bytes(p, M, N, K);
       break;

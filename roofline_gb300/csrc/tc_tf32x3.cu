@@ -198,6 +198,49 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
          ((uint32_t)(M >> 4) << 24);
 }
 
+// D(tmem) (+)= A(tmem) * B(smem)^T, kind::tf32 (A read from tensor memory).
+__device__ __forceinline__ void mma_tf32_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void tmem_st(uint32_t taddr, const uint32_t (&r)[N]);
+
+template <>
+__device__ __forceinline__ void tmem_st<16>(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+template <>
+__device__ __forceinline__ void tmem_st<32>(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ the GEMM kernel
 
 struct TcParams {
@@ -210,34 +253,51 @@ struct TcParams {
   int stall_producer;  // test hook: the producer issues nothing
 };
 
-template <int BN, int BK, int STAGES, bool A_INKERNEL>
+// BN: output columns per CTA.  BK: K depth of one stage (16 -> 64-byte
+// swizzle, 32 -> 128-byte swizzle).  AK: A arrives raw (FP32) and the
+// converter warps split it, A_hi in place in shared memory and A_lo into a
+// tensor-memory ring that the A_lo*B_hi MMA reads directly; otherwise A_hi
+// and A_lo come pre-split from the workspace.  CONCAT: B_hi and B_lo sit
+// next to each other in the stage, so A_hi*[B_hi | B_lo] is one MMA of width
+// 2*BN into two accumulators that the epilogue adds.
+template <int BN, int BK, int STAGES, bool AK, bool CONCAT>
 struct TcCfg {
   static constexpr int A_BYTES = kBM * BK * 4;
   static constexpr int B_BYTES = BN * BK * 4;
-  // per stage: A_hi, A_lo, B_hi, B_lo
-  static constexpr int STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;
-  static constexpr int TX_BYTES = A_INKERNEL ? (A_BYTES + 2 * B_BYTES) : STAGE_BYTES;
+  static constexpr int A_SMEM = AK ? A_BYTES : 2 * A_BYTES;
+  static constexpr int STAGE_BYTES = A_SMEM + 2 * B_BYTES;
+  static constexpr int TX_BYTES = STAGE_BYTES;
   static constexpr int ROW_BYTES = BK * 4;              // 64 or 128
   static constexpr uint32_t LAYOUT = ROW_BYTES == 128 ? 2u : 4u;
   static constexpr uint32_t SBO = 8 * ROW_BYTES;        // 8-row group stride
-  static constexpr int TMEM_COLS = BN < 32 ? 32 : BN;
+  static constexpr int ACC_COLS = CONCAT ? 2 * BN : BN;
+  static constexpr int LO_COL0 = ACC_COLS;
+  static constexpr int LO_COLS = AK ? STAGES * BK : 0;
+  static constexpr int TMEM_NEED = ACC_COLS + LO_COLS;
+  static constexpr int TMEM_COLS = TMEM_NEED <= 32    ? 32
+                                   : TMEM_NEED <= 64  ? 64
+                                   : TMEM_NEED <= 128 ? 128
+                                   : TMEM_NEED <= 256 ? 256
+                                                      : 512;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
   static_assert(ROW_BYTES == 64 || ROW_BYTES == 128, "BK must be 16 or 32");
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN");
+  static_assert(!CONCAT || 2 * BN <= 256, "concatenated B must fit one MMA");
+  static_assert(TMEM_NEED <= 512, "tensor memory");
 };
 
-template <int BN, int BK, int STAGES, bool A_INKERNEL>
+template <int BN, int BK, int STAGES, bool AK, bool CONCAT>
 __global__ void __launch_bounds__(kThreadsTC, 1)
-tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when A_INKERNEL
+tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
                  const __grid_constant__ CUtensorMap tmA_lo,
                  const __grid_constant__ CUtensorMap tmB_hi,
                  const __grid_constant__ CUtensorMap tmB_lo, TcParams p) {
-  using Cfg = TcCfg<BN, BK, STAGES, A_INKERNEL>;
+  using Cfg = TcCfg<BN, BK, STAGES, AK, CONCAT>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * Cfg::STAGE_BYTES);
-  uint64_t *conv = full + STAGES;    // A tile converted (A_INKERNEL)
+  uint64_t *conv = full + STAGES;    // A tile split (AK)
   uint64_t *empty = conv + STAGES;   // stage free again
   uint64_t *acc_full = empty + STAGES;
   uint64_t *drain = acc_full + 1;
@@ -246,10 +306,8 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when A_I
 
   auto a_hi = [&](int s) { return smem + s * Cfg::STAGE_BYTES; };
   auto a_lo = [&](int s) { return smem + s * Cfg::STAGE_BYTES + Cfg::A_BYTES; };
-  auto b_hi = [&](int s) { return smem + s * Cfg::STAGE_BYTES + 2 * Cfg::A_BYTES; };
-  auto b_lo = [&](int s) {
-    return smem + s * Cfg::STAGE_BYTES + 2 * Cfg::A_BYTES + Cfg::B_BYTES;
-  };
+  auto b_hi = [&](int s) { return smem + s * Cfg::STAGE_BYTES + Cfg::A_SMEM; };
+  auto b_lo = [&](int s) { return smem + s * Cfg::STAGE_BYTES + Cfg::A_SMEM + Cfg::B_BYTES; };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -272,7 +330,7 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when A_I
     prefetch_tmap(&tmA_hi);
     prefetch_tmap(&tmB_hi);
     prefetch_tmap(&tmB_lo);
-    if (!A_INKERNEL) prefetch_tmap(&tmA_lo);
+    if (!AK) prefetch_tmap(&tmA_lo);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
@@ -298,7 +356,7 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when A_I
         mbar_expect_tx(&full[s], Cfg::TX_BYTES);
         const int32_t kx = kb * BK;
         tma_load_2d(a_hi(s), &tmA_hi, &full[s], kx, (int32_t)m0);
-        if (!A_INKERNEL) tma_load_2d(a_lo(s), &tmA_lo, &full[s], kx, (int32_t)m0);
+        if (!AK) tma_load_2d(a_lo(s), &tmA_lo, &full[s], kx, (int32_t)m0);
         tma_load_2d(b_hi(s), &tmB_hi, &full[s], kx, (int32_t)n0);
         tma_load_2d(b_lo(s), &tmB_lo, &full[s], kx, (int32_t)n0);
         ++issued;
@@ -314,28 +372,41 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when A_I
     // ---------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_tf32(kBM, BN);
+      constexpr uint32_t idesc2 = idesc_tf32(kBM, CONCAT ? 2 * BN : BN);
       bool any = false;
       for (int kb = 0; kb < p.num_kb; ++kb) {
         const int s = kb % STAGES;
         const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
-        if (!mbar_wait(A_INKERNEL ? &conv[s] : &full[s], ph, deadline, abort_flag)) {
+        if (!mbar_wait(AK ? &conv[s] : &full[s], ph, deadline, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t ah = smem_u32(a_hi(s)), al = smem_u32(a_lo(s));
         const uint32_t bh = smem_u32(b_hi(s)), bl = smem_u32(b_lo(s));
+        const uint32_t lo_t = tmem_base + (uint32_t)(Cfg::LO_COL0 + s * BK);
 #pragma unroll
         for (int kk = 0; kk < BK / 8; ++kk) {
           const uint32_t off = kk * 32;  // 8 TF32 values = 32 bytes along K
           const uint64_t dah = smem_desc(ah + off, Cfg::SBO, Cfg::LAYOUT);
-          const uint64_t dal = smem_desc(al + off, Cfg::SBO, Cfg::LAYOUT);
           const uint64_t dbh = smem_desc(bh + off, Cfg::SBO, Cfg::LAYOUT);
-          const uint64_t dbl = smem_desc(bl + off, Cfg::SBO, Cfg::LAYOUT);
           const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
-          mma_tf32(tmem_base, dah, dbl, idesc, acc);  // small terms first
-          mma_tf32(tmem_base, dal, dbh, idesc, 1u);
-          mma_tf32(tmem_base, dah, dbh, idesc, 1u);
+          if (CONCAT) {
+            // columns [0, BN): A_hi*B_hi (+ A_lo*B_hi); [BN, 2BN): A_hi*B_lo
+            mma_tf32(tmem_base, dah, dbh, idesc2, acc);
+            if (AK)
+              mma_tf32_ts(tmem_base, lo_t + kk * 8, dbh, idesc, 1u);
+            else
+              mma_tf32(tmem_base, smem_desc(al + off, Cfg::SBO, Cfg::LAYOUT), dbh, idesc, 1u);
+          } else {
+            const uint64_t dbl = smem_desc(bl + off, Cfg::SBO, Cfg::LAYOUT);
+            mma_tf32(tmem_base, dah, dbl, idesc, acc);  // small terms first
+            if (AK)
+              mma_tf32_ts(tmem_base, lo_t + kk * 8, dbh, idesc, 1u);
+            else
+              mma_tf32(tmem_base, smem_desc(al + off, Cfg::SBO, Cfg::LAYOUT), dbh, idesc, 1u);
+            mma_tf32(tmem_base, dah, dbh, idesc, 1u);
+          }
         }
         mma_commit(&empty[s]);
         any = true;
@@ -353,57 +424,76 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when A_I
       }
     }
   } else {
-    // ---------------- converters (A split in kernel) and epilogue, warps 2..5
-    const int ct = threadIdx.x - 64;  // 0..127
-    if (A_INKERNEL) {
-      constexpr int VEC = Cfg::A_BYTES / 16;  // 16-byte chunks per A tile
+    // ---------------- converters (AK) and epilogue, warps 2..5
+    const int quarter = warp & 3;  // TMEM lanes this warp may touch
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16);
+    if (AK) {
       for (int kb = 0; kb < p.num_kb; ++kb) {
         const int s = kb % STAGES;
         const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
-        if (!mbar_wait(&full[s], ph, deadline, abort_flag)) {
+        // tcgen05.st below is warp-collective: the warp proceeds or stops as one
+        if (!__all_sync(0xffffffffu, mbar_wait(&full[s], ph, deadline, abort_flag))) {
           ok = false;
           break;
         }
-        float4 *hi = reinterpret_cast<float4 *>(a_hi(s));
-        float4 *lo = reinterpret_cast<float4 *>(a_lo(s));
-        // the swizzle permutes 16-byte chunks only, so an elementwise pass
-        // over the raw buffer keeps hi and lo in the MMA's layout
-        for (int i = ct; i < VEC; i += kConvThreads) {
-          float4 x = hi[i];
-          float4 h, l;
-          h.x = tf32_rna(x.x); l.x = tf32_rna(x.x - h.x);
-          h.y = tf32_rna(x.y); l.y = tf32_rna(x.y - h.y);
-          h.z = tf32_rna(x.z); l.z = tf32_rna(x.z - h.z);
-          h.w = tf32_rna(x.w); l.w = tf32_rna(x.w - h.w);
-          hi[i] = h;
-          lo[i] = l;
+        // Row `row` of the landed tile: 16-byte chunk c sits at chunk
+        // c ^ f(row) of its 64- or 128-byte line (the TMA swizzle).
+        uint8_t *line = a_hi(s) + row * Cfg::ROW_BYTES;
+        uint32_t lo[BK];
+#pragma unroll
+        for (int c = 0; c < BK / 4; ++c) {
+          const int phys = (BK == 32) ? (c ^ (row & 7)) : (c ^ ((row >> 1) & 3));
+          float4 *ptr = reinterpret_cast<float4 *>(line + phys * 16);
+          const float4 x = *ptr;
+          float4 h;
+          h.x = tf32_rna(x.x);
+          h.y = tf32_rna(x.y);
+          h.z = tf32_rna(x.z);
+          h.w = tf32_rna(x.w);
+          lo[4 * c + 0] = __float_as_uint(tf32_rna(x.x - h.x));
+          lo[4 * c + 1] = __float_as_uint(tf32_rna(x.y - h.y));
+          lo[4 * c + 2] = __float_as_uint(tf32_rna(x.z - h.z));
+          lo[4 * c + 3] = __float_as_uint(tf32_rna(x.w - h.w));
+          *ptr = h;
         }
-        fence_async_smem();
+        tmem_st<BK>(lane_base + (uint32_t)(Cfg::LO_COL0 + s * BK), lo);
+        tmem_st_wait();
+        fence_async_smem();  // A_hi written by this thread -> visible to the MMA
+        tc_fence_before();
         mbar_arrive(&conv[s]);
       }
       if (!ok) *abort_flag = 1;
     }
     if (ok) {
-      if (!mbar_wait(acc_full, 0, deadline, abort_flag)) {
-        ok = false;
-        *abort_flag = 1;
-      }
+      if (!mbar_wait(acc_full, 0, deadline, abort_flag)) ok = false;
     }
     // tcgen05.ld is warp-collective: the whole warp drains or none of it
     const bool warp_ok = __all_sync(0xffffffffu, ok);
+    if (!warp_ok) {
+      ok = false;
+      *abort_flag = 1;
+    }
     if (warp_ok) {
       tc_fence_after();
-      const int quarter = warp & 3;  // TMEM lanes this warp may read
-      const int64_t row = m0 + quarter * 32 + lane;
-      const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16);
+      const int64_t grow = m0 + row;
       const bool vec = ((p.ldc & 3) == 0) && ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0);
 #pragma unroll 1
       for (int c = 0; c < BN; c += 32) {
         uint32_t r[32];
-        tmem_ld32(tbase + (uint32_t)c, r);
-        tmem_ld_wait();
-        if (row < p.M) {
-          float *dst = p.C + row * p.ldc + n0 + c;
+        tmem_ld32(lane_base + (uint32_t)c, r);
+        if (CONCAT) {
+          uint32_t r2[32];
+          tmem_ld32(lane_base + (uint32_t)(BN + c), r2);
+          tmem_ld_wait();
+#pragma unroll
+          for (int q = 0; q < 32; ++q)
+            r[q] = __float_as_uint(__uint_as_float(r[q]) + __uint_as_float(r2[q]));
+        } else {
+          tmem_ld_wait();
+        }
+        if (grow < p.M) {
+          float *dst = p.C + grow * p.ldc + n0 + c;
           const int64_t left = p.N - (n0 + c);
           if (vec && left >= 32) {
 #pragma unroll
@@ -557,9 +647,9 @@ WsLayout ws_layout(int64_t M, int64_t N, int64_t K, bool a_inkernel) {
   return w;
 }
 
-template <int BN, int BK, int STAGES, bool AK>
+template <int BN, int BK, int STAGES, bool AK, bool CONCAT>
 int launch_cfg(const gemm_plan_t &plan, const GemmArgs &a, char *ws, cudaStream_t s) {
-  using Cfg = TcCfg<BN, BK, STAGES, AK>;
+  using Cfg = TcCfg<BN, BK, STAGES, AK, CONCAT>;
   const WsLayout L = ws_layout(a.M, a.N, a.K, AK);
   float *ahi = reinterpret_cast<float *>(ws + L.a_hi);
   float *alo = reinterpret_cast<float *>(ws + L.a_lo);
@@ -604,7 +694,7 @@ int launch_cfg(const gemm_plan_t &plan, const GemmArgs &a, char *ws, cudaStream_
   p.timeout_ns = env_u64("GEMM_DEBUG_WAIT_LIMIT_NS", 2000000000ull);
   p.stall_producer = (int)env_u64("GEMM_DEBUG_STALL_PRODUCER", 0);
 
-  auto kern = tc_tf32x3_kernel<BN, BK, STAGES, AK>;
+  auto kern = tc_tf32x3_kernel<BN, BK, STAGES, AK, CONCAT>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Cfg::SMEM_BYTES) != cudaSuccess) {
     cudaGetLastError();
@@ -623,11 +713,41 @@ int launch_cfg(const gemm_plan_t &plan, const GemmArgs &a, char *ws, cudaStream_
 // The tcgen05 kernels are built for sm_103a only.
 bool tc_supported(const DeviceProps &dp) { return dp.cc_major == 10 && dp.cc_minor == 3; }
 
-// Tile configurations the planner may pick (bn, bk, stages, A split in kernel).
-bool tc_config_valid(int bn, int bk, int stages, int a_inkernel) {
-  return (bn == 256 && bk == 16 && stages == 4 && !a_inkernel) ||
-         (bn == 128 && bk == 16 && stages == 3 && !a_inkernel) ||
-         (bn == 64 && bk == 32 && stages == 4 && a_inkernel);
+// Tile configurations the planner may pick:
+// (bn, bk, stages, A split in kernel, concatenated B MMA).
+#define GG_TC_CONFIGS(X)          \
+  X(256, 16, 5, true, false)      \
+  X(128, 32, 4, true, true)       \
+  X(64, 32, 6, true, true)        \
+  X(64, 32, 3, true, true)        \
+  X(64, 32, 2, true, false)       \
+  X(64, 16, 4, true, false)       \
+  X(256, 16, 4, false, false)     \
+  X(128, 16, 3, false, true)
+
+bool tc_config_valid(int bn, int bk, int stages, int a_inkernel, int concat) {
+#define GG_MATCH(BN_, BK_, ST_, AK_, CC_)                                          \
+  if (bn == BN_ && bk == BK_ && stages == ST_ && (a_inkernel != 0) == AK_ && \
+      (concat != 0) == CC_)                                                        \
+    return true;
+  GG_TC_CONFIGS(GG_MATCH)
+#undef GG_MATCH
+  return false;
+}
+
+// CTAs of one configuration that fit on an SM (shared memory and TMEM).
+int tc_ctas_per_sm(int bn, int bk, int stages, int a_inkernel, int concat, int smem_per_sm) {
+#define GG_OCC(BN_, BK_, ST_, AK_, CC_)                                            \
+  if (bn == BN_ && bk == BK_ && stages == ST_ && (a_inkernel != 0) == AK_ && \
+      (concat != 0) == CC_) {                                                      \
+    using C = TcCfg<BN_, BK_, ST_, AK_, CC_>;                                      \
+    int by_smem = smem_per_sm / (C::SMEM_BYTES + 1024);                            \
+    int by_tmem = 512 / C::TMEM_COLS;                                              \
+    return by_smem < by_tmem ? by_smem : by_tmem;                                  \
+  }
+  GG_TC_CONFIGS(GG_OCC)
+#undef GG_OCC
+  return 0;
 }
 
 uint64_t tc_workspace_bytes(const gemm_plan_t &plan, int64_t M, int64_t N, int64_t K) {
@@ -639,17 +759,15 @@ int launch_tc(const gemm_plan_t &plan, const GemmArgs &a, void *ws, size_t ws_by
   if (!get_encoder()) return GEMM_ERR_UNSUPPORTED;
   if (ws_bytes < tc_workspace_bytes(plan, a.M, a.N, a.K) || ws == nullptr)
     return GEMM_ERR_WORKSPACE_TOO_SMALL;
-  char *w = static_cast<char *>(ws);
-  if (plan.a_split_in_kernel) {
-    if ((a.lda & 3) || (reinterpret_cast<uintptr_t>(a.A) & 15)) return GEMM_ERR_UNSUPPORTED;
-    if (plan.bn == 64 && plan.bk == 32 && plan.stages == 4)
-      return launch_cfg<64, 32, 4, true>(plan, a, w, s);
+  if (plan.a_split_in_kernel && ((a.lda & 3) || (reinterpret_cast<uintptr_t>(a.A) & 15)))
     return GEMM_ERR_UNSUPPORTED;
-  }
-  if (plan.bn == 256 && plan.bk == 16 && plan.stages == 4)
-    return launch_cfg<256, 16, 4, false>(plan, a, w, s);
-  if (plan.bn == 128 && plan.bk == 16 && plan.stages == 3)
-    return launch_cfg<128, 16, 3, false>(plan, a, w, s);
+  char *w = static_cast<char *>(ws);
+#define GG_LAUNCH(BN_, BK_, ST_, AK_, CC_)                                              \
+  if (plan.bn == BN_ && plan.bk == BK_ && plan.stages == ST_ &&                         \
+      (plan.a_split_in_kernel != 0) == AK_ && (plan.b_concat != 0) == CC_)              \
+    return launch_cfg<BN_, BK_, ST_, AK_, CC_>(plan, a, w, s);
+  GG_TC_CONFIGS(GG_LAUNCH)
+#undef GG_LAUNCH
   return GEMM_ERR_UNSUPPORTED;
 }
 

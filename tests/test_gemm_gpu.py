@@ -207,3 +207,55 @@ def test_copy_calibration_runs():
 def test_status_clear_after_normal_runs():
     from roofline_gb300 import gemm
     assert gemm.check_status() == gemm.OK
+
+
+# The planner's own choice for representative shapes:
+# (M, N, K, lda) -> (bn, bk, stages, A split in kernel, concatenated B)
+TC_PLANS = [
+    ((1000, 64, 96, 96), (64, 32, 3, 1, 1)),
+    ((512, 512, 512, 512), (128, 32, 4, 1, 1)),
+    ((2432, 8192, 128, 128), (256, 16, 5, 1, 0)),
+    ((1023, 1025, 777, 777), (128, 16, 3, 0, 1)),
+    ((2432, 8192, 129, 129), (256, 16, 4, 0, 0)),
+]
+
+
+@pytest.mark.parametrize("shape,cfg", TC_PLANS, ids=lambda v: "x".join(map(str, v)))
+def test_tf32x3_planner_choices(shape, cfg):
+    import torch
+    from roofline_gb300 import gemm
+    from workloads import sample_entries
+    M, N, K, lda = shape
+    p = gemm.plan(M, N, K, lda, N, N, mode="tf32x3")
+    assert (p["bn"], p["bk"], p["stages"], p["a_split_in_kernel"], p["b_concat"]) == cfg
+    assert p["ctas_per_sm"] >= 1
+    A = matrix(M, K, lda, 4000 + K, "u11")
+    B = matrix(K, N, None, 4100 + K, "u11")
+    C0 = matrix(M, N, None, 4200 + K, "u11")
+    dA, dB, dC = (torch.from_numpy(x).cuda() for x in (A, B, C0))
+    gemm.matmul(dA[:, :K], dB, dC, 0.5, -1.5, "tf32x3")
+    torch.cuda.synchronize()
+    got = dC.cpu().numpy()
+    rows, cols = sample_entries(M, N, 2048, seed=K)
+    ref, D = oracle.gemm_entries(A[:, :K], B, rows, cols, 0.5, -1.5, C0)
+    assert oracle.err_normalised(got[rows, cols], ref, D) <= TOL_E1
+
+
+# Every tensor-core configuration the library is built with, forced through
+# the GEMM_TC_CONFIG knob, on one ragged shape (full check).
+TC_BUILT = ["256,16,5,1,0", "128,32,4,1,1", "64,32,6,1,1", "64,32,3,1,1", "64,32,2,1,0",
+            "64,16,4,1,0", "256,16,4,0,0", "128,16,3,0,1"]
+
+
+@pytest.mark.parametrize("cfg", TC_BUILT)
+def test_tf32x3_every_built_configuration(cfg, monkeypatch):
+    from roofline_gb300 import gemm
+    bn, bk, st, ak, cc = map(int, cfg.split(","))
+    monkeypatch.setenv("GEMM_TC_CONFIG", cfg)
+    M, N, K = 777, 200, 300
+    pad = (0 if ak else 1, 0, 0)
+    p = gemm.plan(M, N, K, K + pad[0], N, N, mode="tf32x3")
+    assert (p["bn"], p["bk"], p["stages"], p["a_split_in_kernel"], p["b_concat"]) == \
+        (bn, bk, st, ak, cc)
+    got, ref, D = _run_shape(M, N, K, "tf32x3", 1.5, 0.5, pad=pad, offset=0, seed=st + bn)
+    assert oracle.err_normalised(got, ref, D) <= TOL_E1
