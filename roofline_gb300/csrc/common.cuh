@@ -72,13 +72,11 @@ bool tc_config_valid(int bn, int bk, int stages, int a_inkernel, int concat);
 int tc_ctas_per_sm(int bn, int bk, int stages, int a_inkernel, int concat, int smem_per_sm);
 int tc_read_and_clear_status(cudaStream_t s);
 
-// SIMT tile configurations (simt.cu).  id 0: 128x128x8, 256 threads, 8x8 per
-// thread; id 1: 64x64x16, 256 threads, 4x4 per thread.
+// SIMT tile (simt.cu): 64 x 128 x 16, 128 threads, 4 stages.
 struct SimtConfig {
   int bm, bn, bk, threads;
 };
-SimtConfig simt_config(int id);
-int simt_config_for_tile(int bm, int bn);
+SimtConfig simt_config();
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 

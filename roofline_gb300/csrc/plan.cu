@@ -34,31 +34,50 @@ bool mode_known(int mode) {
   }
 }
 
+// Estimated time of the SIMT kernel with `split` K slices.  The CTAs spread
+// evenly over the SMs; the busiest SM runs u = ceil(tiles * split / SMs)
+// CTA-slices (1/split of the K loop each), in pairs at the full per-SM rate
+// (about 70% of the FP32 peak) and a leftover single CTA at about 60% of
+// it.  A split adds a reduction that reads the slices and writes C once
+// (at ~6 TB/s, plus a launch).
+double simt_time_estimate(int64_t M, int64_t N, int64_t K, int64_t tiles, int split, int64_t sms,
+                          double fp32_peak, const SimtConfig &c) {
+  const double rate = 0.7 * fp32_peak / (double)sms;
+  const double slice_flops = 2.0 * c.bm * c.bn * (double)K / split;
+  const int64_t u = ceil_div(tiles * split, sms);
+  double t = (double)(u / 2) * 2.0 * slice_flops / rate + (double)(u % 2) * slice_flops / (0.6 * rate);
+  if (split > 1) t += (split + 1.0) * (double)M * (double)N * 4.0 / 6.0e12 + 2e-6;
+  return t;
+}
+
 void plan_simt(int64_t M, int64_t N, int64_t K, bool vec, const DeviceProps &dp,
-               gemm_plan_t *out) {
+               double fp32_peak, gemm_plan_t *out) {
   const int64_t sms = dp.sm_count > 0 ? dp.sm_count : 152;
-  const int64_t tiles128 = ceil_div(M, 128) * ceil_div(N, 128);
-  SimtConfig c = simt_config(0);
-  int64_t tiles = tiles128;
+  const SimtConfig c = simt_config();
+  const int64_t tiles = ceil_div(M, c.bm) * ceil_div(N, c.bn);
+  // slices of at least 64 along K, at most 16
+  int64_t max_split = K / 64;
+  if (max_split > 16) max_split = 16;
+  if (max_split < 1) max_split = 1;
   int split = 1;
-  if (tiles128 < 2 * sms) {
-    // Too few 128x128 tiles to fill the GPU: use 64x64 tiles and, if still
-    // short of two CTAs per SM, slice K (each slice at least 64 deep).
-    c = simt_config(1);
-    tiles = ceil_div(M, 64) * ceil_div(N, 64);
-    if (tiles < 2 * sms) {
-      int64_t want = (2 * sms) / (tiles > 0 ? tiles : 1);
-      int64_t max_split = K / 64;
-      if (want > max_split) want = max_split;
-      if (want > 16) want = 16;
-      if (want > 1) split = (int)want;
+  double best = simt_time_estimate(M, N, K, tiles, 1, sms, fp32_peak, c);
+  for (int s = 2; s <= max_split; ++s) {
+    const double t = simt_time_estimate(M, N, K, tiles, s, sms, fp32_peak, c);
+    if (t < 0.97 * best) {
+      best = t;
+      split = s;
     }
+  }
+  // Tuning knob: GEMM_SIMT_SPLIT=n forces n K slices (0 or unset: the estimate).
+  if (const char *env = std::getenv("GEMM_SIMT_SPLIT")) {
+    const int forced = std::atoi(env);
+    if (forced >= 1) split = forced;
   }
   out->kernel = GEMM_KERNEL_SIMT;
   out->bm = c.bm;
   out->bn = c.bn;
   out->bk = c.bk;
-  out->stages = 2;
+  out->stages = 4;
   out->threads = c.threads;
   out->vec = vec ? 1 : 0;
   if (split > 1) {
@@ -140,7 +159,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
     }
     case GEMM_MODE_FP32_SIMT:
       if (ceil_div(M, 64) > 65535) return GEMM_ERR_UNSUPPORTED;
-      plan_simt(M, N, K, vec, dp, &p);
+      plan_simt(M, N, K, vec, dp, fp32_peak, &p);
       break;
     case GEMM_MODE_TF32X3: {
       if (!tc_supported(dp)) return GEMM_ERR_UNSUPPORTED;

@@ -2,53 +2,81 @@
 //
 // This is the step the tiled-matmul course page leaves for later ("Project -
 // tiled matrix multiply", sections "The results table" and "What comes
-// next"): each thread computes a TM x TN output tile held in registers
-// (8 x 8 here), the next shared-memory tile is fetched while the current
-// one is consumed (double buffering), and global loads are 128-bit wide.
+// next"): each thread computes an 8 x 8 output tile held in registers, the
+// next shared-memory tiles are fetched while the current one is consumed,
+// and global traffic moves in wide asynchronous copies.
 //
-// Layout of one CTA (BM x BN output tile, 256 threads = 8 warps):
-//   * warps form a WARPS_M x WARPS_N grid; a warp covers WTM x WTN outputs
-//     with its lanes in an 8 (rows) x 4 (cols) arrangement;
-//   * each thread's TM x TN tile is made of 4 x 4 sub-tiles spaced 32 rows
-//     and 16 columns apart, so every fragment read is one 128-bit shared
-//     load that the warp serves in a single wavefront (A: 8 distinct
-//     16-byte chunks, B: 4 distinct chunks broadcast);
-//   * A is stored k-major in shared memory (As[k][m], transposed on the way
-//     in through registers) with 4 floats of row padding, so the transposing
-//     stores of two k-quads land on disjoint bank halves; B keeps its
-//     row-major layout (Bs[k][n]).
-//   * BK = 16 for the 128 x 128 tile: one barrier per 16 k-steps.  (Measured
-//     on GB300: BK = 16 beats BK = 8 by 19% at 4096^3; packed f32x2 FMAs did
-//     not beat scalar FFMA at this tile shape, with or without the register
-//     headroom of one CTA per SM.)
-//   * Out-of-range loads are zero-filled and out-of-range stores skipped
-//     (the course page's edge handling in "Stage 2").
+// One CTA: 128 threads as 1 x 4 warps, output tile 64 (M) x 128 (N), K in
+// 16-deep stages of a 4-stage cp.async ring (~53 KB of shared memory, two
+// CTAs per SM).  A warp covers 64 x 32 outputs with its lanes in an 8 x 4
+// grid; a thread's 8 x 8 tile is four 4 x 4 blocks spaced 32 rows and 16
+// columns apart, so each k step reads its A and B fragments with four
+// 128-bit shared loads that the warp serves in one wavefront each.
+// Accumulators are column pairs updated with packed f32x2 FMAs (two FMAs per
+// issued instruction, each rounded as a scalar FFMA would be).
+// A is K-contiguous in global memory but the inner product wants it
+// M-contiguous, so it is the operand that gets transposed: copied element
+// by element into a k-major tile whose rows are 68 floats apart, with lanes
+// arranged 8 (k) x 4 (rows) so one warp instruction reads four 32-byte
+// sectors and writes 32 distinct banks.  B is already N-contiguous and moves
+// in 16-byte copies.  The copies' source-size operand zero-fills elements
+// outside the matrices; stores outside C are skipped (the course page's edge
+// handling in "Stage 2").
 // Split-K: grid.z slices K; slices write raw partial sums to the workspace
 // and splitk_reduce applies alpha/beta, summing slices in a fixed order.
+//
+// (Measured on GB300 while choosing this layout: transposing the 128-row
+// operand with 8-row-spread copies caused 2x the shared-memory wavefronts and
+// ran at 46 TFLOP/s; the earlier register-staged 128 x 128 x 16 kernel with
+// scalar FFMA reached 51-53 TFLOP/s; this one reaches 58.8 at 4096^3 and
+// 62.3 at 8192^3.)
 #include "common.cuh"
 
 namespace gg {
 namespace {
 
-constexpr int kThreads = 256;
+__device__ __forceinline__ void cp_async4(void *smem, const void *gmem, bool valid) {
+  const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(s), "l"(gmem),
+               "r"(valid ? 4 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+  const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
-template <int BM, int BN, int BK, int TM, int TN, bool VEC>
-__global__ void __launch_bounds__(kThreads, 2)
-simt_sgemm_kernel(GemmArgs p, int64_t k_per_split, float *__restrict__ ws, int ws_vec) {
+constexpr int kThreadsP = 128;
+
+template <int BM, int BN, int BK, int STAGES, bool VEC>
+__global__ void __launch_bounds__(kThreadsP, 2)
+simt_packed_kernel(GemmArgs p, int64_t k_per_split, float *__restrict__ ws, int ws_vec) {
+  constexpr int TM = 8, TN = 8;
   constexpr int PAD = 4;
-  constexpr int LDA_S = BM + PAD;
-  constexpr int WTM = TM * 8;
-  constexpr int WTN = TN * 4;
+  constexpr int LDA_S = BM + PAD;  // 68 floats: odd multiple of 4 -> conflict-free k-major scatter
+  constexpr int WTM = TM * 8;   // 64
+  constexpr int WTN = TN * 4;   // 32
   constexpr int WARPS_N = BN / WTN;
-  static_assert((BM / WTM) * WARPS_N * 32 == kThreads, "warp grid must cover the CTA");
-  static_assert(TM % 4 == 0 && TN % 4 == 0 && BK % 4 == 0, "4x4 sub-tiles");
-  constexpr int A_SLOTS = BM * BK / 4;
+  static_assert((BM / WTM) * WARPS_N * 32 == kThreadsP, "warp grid must cover the CTA");
+  static_assert(BK % 8 == 0, "A copies go 8 k at a time");
+  // A: element copies; lane -> (k = 8 * kh + lane % 8, row), so one warp
+  // instruction reads 4 rows x 32 contiguous bytes.
+  constexpr int A_ELEMS = BM * BK;
   constexpr int B_SLOTS = BK * BN / 4;
-  constexpr int A_PER_T = (A_SLOTS + kThreads - 1) / kThreads;
-  constexpr int B_PER_T = (B_SLOTS + kThreads - 1) / kThreads;
+  static_assert(A_ELEMS % kThreadsP == 0 && B_SLOTS % kThreadsP == 0, "whole copies per thread");
+  constexpr int A_PER_T = A_ELEMS / kThreadsP;
+  constexpr int B_PER_T = B_SLOTS / kThreadsP;
 
-  __shared__ __align__(16) float As[2][BK][LDA_S];
-  __shared__ __align__(16) float Bs[2][BK][BN];
+  extern __shared__ __align__(16) float smp[];
+  float(*As)[BK][LDA_S] = reinterpret_cast<float(*)[BK][LDA_S]>(smp);
+  float(*Bs)[BK][BN] = reinterpret_cast<float(*)[BK][BN]>(smp + STAGES * BK * LDA_S);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -58,123 +86,79 @@ simt_sgemm_kernel(GemmArgs p, int64_t k_per_split, float *__restrict__ ws, int w
   const int64_t n0 = (int64_t)blockIdx.x * BN;
   const int64_t kbeg = (int64_t)blockIdx.z * k_per_split;
   const int64_t kend = min(p.K, kbeg + k_per_split);
-  const int64_t ntiles = kend > kbeg ? (kend - kbeg + BK - 1) / BK : 0;
+  const int64_t klen = kend > kbeg ? kend - kbeg : 0;
+  const int ntiles = (int)((klen + BK - 1) / BK);
 
-  float4 ra[A_PER_T], rb[B_PER_T];
-
-  // Per-thread source pointers, advanced by one BK tile per iteration.
+  // copy e = tid + j * threads: k = 8 * (e / (8 * BM)) + e % 8, row = (e / 8) % BM
   const float *a_src[A_PER_T];
-  bool a_ok[A_PER_T];
+  bool a_row_ok[A_PER_T];
 #pragma unroll
-  for (int s = 0; s < A_PER_T; ++s) {
-    const int slot = tid + s * kThreads;
-    const int r = slot / (BK / 4), kq = (slot % (BK / 4)) * 4;
-    a_ok[s] = (A_SLOTS % kThreads == 0 || slot < A_SLOTS) && (m0 + r < p.M);
-    a_src[s] = p.A + (a_ok[s] ? (m0 + r) * p.lda + kbeg + kq : 0);
+  for (int j = 0; j < A_PER_T; ++j) {
+    const int e = tid + j * kThreadsP;
+    const int kk = 8 * (e / (8 * BM)) + e % 8, r = (e / 8) % BM;
+    a_row_ok[j] = m0 + r < p.M;
+    a_src[j] = p.A + (a_row_ok[j] ? (m0 + r) * p.lda + kbeg + kk : 0);
   }
   const float *b_src[B_PER_T];
-  int b_cols[B_PER_T];  // valid columns from this slot's first column (<= 4 matters)
+  int b_cols[B_PER_T];
 #pragma unroll
   for (int s = 0; s < B_PER_T; ++s) {
-    const int slot = tid + s * kThreads;
+    const int slot = tid + s * kThreadsP;
     const int kr = slot / (BN / 4), cq = (slot % (BN / 4)) * 4;
-    const bool ok = (B_SLOTS % kThreads == 0 || slot < B_SLOTS);
     const int64_t left = p.N - (n0 + cq);
-    b_cols[s] = ok ? (int)(left > 4 ? 4 : (left < 0 ? 0 : left)) : 0;
-    b_src[s] = p.B + (ok && kbeg + kr < p.K ? (kbeg + kr) * p.ldb + n0 + cq : 0);
+    b_cols[s] = (int)(left > 4 ? 4 : (left < 0 ? 0 : left));
+    b_src[s] = p.B + (kbeg + kr < p.K && b_cols[s] > 0 ? (kbeg + kr) * p.ldb + n0 + cq : 0);
   }
   const int64_t b_step = (int64_t)BK * p.ldb;
 
-  // rem: K elements left in this slice from the tile's first k.
-  auto load_global = [&](int rem) {
+  auto issue = [&](int t) {
+    const int buf = t % STAGES;
+    const int rem = (int)min(klen - (int64_t)t * BK, (int64_t)BK);
 #pragma unroll
-    for (int s = 0; s < A_PER_T; ++s) {
-      const int slot = tid + s * kThreads;
-      const int kq = (slot % (BK / 4)) * 4;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (a_ok[s]) {
-        const float *src = a_src[s];
-        if (VEC && kq + 4 <= rem) {
-          v = __ldg(reinterpret_cast<const float4 *>(src));
-        } else {
-          if (kq + 0 < rem) v.x = __ldg(src + 0);
-          if (kq + 1 < rem) v.y = __ldg(src + 1);
-          if (kq + 2 < rem) v.z = __ldg(src + 2);
-          if (kq + 3 < rem) v.w = __ldg(src + 3);
-        }
-      }
-      ra[s] = v;
-      a_src[s] += BK;
+    for (int j = 0; j < A_PER_T; ++j) {
+      const int e = tid + j * kThreadsP;
+      const int kk = 8 * (e / (8 * BM)) + e % 8, r = (e / 8) % BM;
+      const bool ok = a_row_ok[j] && kk < rem;
+      cp_async4(&As[buf][kk][r], ok ? a_src[j] + (int64_t)t * BK : p.A, ok);
     }
 #pragma unroll
     for (int s = 0; s < B_PER_T; ++s) {
-      const int slot = tid + s * kThreads;
-      const int kr = slot / (BN / 4);
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (kr < rem && b_cols[s] > 0) {
-        const float *src = b_src[s];
-        if (VEC && b_cols[s] == 4) {
-          v = __ldg(reinterpret_cast<const float4 *>(src));
-        } else {
-          v.x = __ldg(src + 0);
-          if (b_cols[s] > 1) v.y = __ldg(src + 1);
-          if (b_cols[s] > 2) v.z = __ldg(src + 2);
-          if (b_cols[s] > 3) v.w = __ldg(src + 3);
+      const int slot = tid + s * kThreadsP;
+      const int kr = slot / (BN / 4), cq = (slot % (BN / 4)) * 4;
+      float *dst = &Bs[buf][kr][cq];
+      const bool row_ok = kr < rem;
+      const float *src = b_src[s] + (int64_t)t * b_step;
+      if (VEC && row_ok && b_cols[s] == 4) {
+        cp_async16(dst, src);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const bool ok = row_ok && i < b_cols[s];
+          cp_async4(dst + i, ok ? src + i : p.B, ok);
         }
-      }
-      rb[s] = v;
-      b_src[s] += b_step;
-    }
-  };
-
-  auto store_smem = [&](int buf) {
-#pragma unroll
-    for (int s = 0; s < A_PER_T; ++s) {
-      const int slot = tid + s * kThreads;
-      if (A_SLOTS % kThreads == 0 || slot < A_SLOTS) {
-        const int r = slot / (BK / 4);
-        const int kq = (slot % (BK / 4)) * 4;
-        As[buf][kq + 0][r] = ra[s].x;
-        As[buf][kq + 1][r] = ra[s].y;
-        As[buf][kq + 2][r] = ra[s].z;
-        As[buf][kq + 3][r] = ra[s].w;
-      }
-    }
-#pragma unroll
-    for (int s = 0; s < B_PER_T; ++s) {
-      const int slot = tid + s * kThreads;
-      if (B_SLOTS % kThreads == 0 || slot < B_SLOTS) {
-        const int kr = slot / (BN / 4);
-        const int cq = (slot % (BN / 4)) * 4;
-        *reinterpret_cast<float4 *>(&Bs[buf][kr][cq]) = rb[s];
       }
     }
   };
 
-  // Accumulators as column pairs: acc[i][jp] holds columns 2jp, 2jp+1 of
-  // row i, so the packed FMA (two lanes per instruction) needs no repacking.
   float2 acc[TM][TN / 2];
 #pragma unroll
   for (int i = 0; i < TM; ++i)
 #pragma unroll
     for (int j = 0; j < TN / 2; ++j) acc[i][j] = make_float2(0.f, 0.f);
-
   const int a_off = wm * WTM + lr * 4;
   const int b_off = wn * WTN + lc * 4;
 
-  const int64_t klen = kend - kbeg;
-  if (ntiles > 0) {
-    load_global((int)(klen < (1 << 30) ? klen : (1 << 30)));
-    store_smem(0);
-    __syncthreads();
+#pragma unroll
+  for (int t = 0; t < STAGES - 1; ++t) {
+    if (t < ntiles) issue(t);
+    cp_async_commit();
   }
-  for (int64_t t = 0; t < ntiles; ++t) {
-    const int cur = (int)(t & 1);
-    const bool more = t + 1 < ntiles;
-    if (more) {
-      const int64_t rem = klen - (t + 1) * BK;
-      load_global((int)(rem < (1 << 30) ? rem : (1 << 30)));
-    }
+  for (int t = 0; t < ntiles; ++t) {
+    cp_async_wait<STAGES - 2>();
+    __syncthreads();  // tile t landed for everyone; tile t-1's buffer is free
+    if (t + STAGES - 1 < ntiles) issue(t + STAGES - 1);
+    cp_async_commit();
+    const int cur = t % STAGES;
 #pragma unroll
     for (int k = 0; k < BK; ++k) {
       float2 b[TN / 2];
@@ -190,18 +174,15 @@ simt_sgemm_kernel(GemmArgs p, int64_t k_per_split, float *__restrict__ ws, int w
         *reinterpret_cast<float4 *>(&a[im * 4]) =
             *reinterpret_cast<const float4 *>(&As[cur][k][a_off + im * 32]);
 #pragma unroll
-      for (int i = 0; i < TM; ++i)
+      for (int i = 0; i < TM; ++i) {
+        const float2 aa = make_float2(a[i], a[i]);
 #pragma unroll
-        for (int j = 0; j < TN / 2; ++j) {
-          acc[i][j].x = fmaf(a[i], b[j].x, acc[i][j].x);
-          acc[i][j].y = fmaf(a[i], b[j].y, acc[i][j].y);
-        }
+        for (int j = 0; j < TN / 2; ++j) acc[i][j] = __ffma2_rn(aa, b[j], acc[i][j]);
+      }
     }
-    if (more) store_smem(cur ^ 1);
-    __syncthreads();
   }
+  cp_async_wait<0>();
 
-  // Epilogue: fused alpha/beta (or raw partials for split-K).
 #pragma unroll
   for (int i = 0; i < TM; ++i) {
     const int64_t row = m0 + a_off + (i / 4) * 32 + (i % 4);
@@ -262,37 +243,9 @@ __global__ void splitk_reduce_kernel(GemmArgs p, const float *__restrict__ ws, i
   }
 }
 
-template <int BM, int BN, int BK, int TM, int TN>
-cudaError_t launch_cfg(const gemm_plan_t &plan, const GemmArgs &p, float *ws, cudaStream_t s) {
-  const int split = plan.split_k > 1 ? plan.split_k : 1;
-  int64_t kps = ceil_div(p.K, split);
-  kps = ceil_div(kps, BK) * BK;
-  dim3 grid((unsigned)ceil_div(p.N, BN), (unsigned)ceil_div(p.M, BM), (unsigned)split);
-  float *w = split > 1 ? ws : nullptr;
-  const int ws_vec = (p.N % 4 == 0) ? 1 : 0;
-  profile_mark_before(s);
-  if (plan.vec)
-    simt_sgemm_kernel<BM, BN, BK, TM, TN, true><<<grid, kThreads, 0, s>>>(p, kps, w, ws_vec);
-  else
-    simt_sgemm_kernel<BM, BN, BK, TM, TN, false><<<grid, kThreads, 0, s>>>(p, kps, w, ws_vec);
-  profile_mark_after(s);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || split == 1) return e;
-  return launch_splitk_reduce(p, ws, split, s);
-}
-
 }  // namespace
 
-SimtConfig simt_config(int id) {
-  if (id == 1) return SimtConfig{64, 64, 16, kThreads};
-  return SimtConfig{128, 128, 16, kThreads};
-}
-
-int simt_config_for_tile(int bm, int bn) {
-  if (bm == 64 && bn == 64) return 1;
-  if (bm == 128 && bn == 128) return 0;
-  return -1;
-}
+SimtConfig simt_config() { return SimtConfig{64, 128, 16, kThreadsP}; }
 
 cudaError_t launch_splitk_reduce(const GemmArgs &p, const float *ws, int splits, cudaStream_t s) {
   int64_t blocks = ceil_div(p.M * p.N, 256);
@@ -301,9 +254,36 @@ cudaError_t launch_splitk_reduce(const GemmArgs &p, const float *ws, int splits,
   return cudaGetLastError();
 }
 
+template <int BM, int BN, int BK, int STAGES>
+cudaError_t launch_packed(const gemm_plan_t &plan, const GemmArgs &p, float *ws, cudaStream_t s) {
+  const int split = plan.split_k > 1 ? plan.split_k : 1;
+  int64_t kps = ceil_div(p.K, split);
+  kps = ceil_div(kps, BK) * BK;
+  dim3 grid((unsigned)ceil_div(p.N, BN), (unsigned)ceil_div(p.M, BM), (unsigned)split);
+  float *w = split > 1 ? ws : nullptr;
+  const int ws_vec = (p.N % 4 == 0) ? 1 : 0;
+  constexpr int smem = STAGES * BK * ((BM + 4) + BN) * 4;
+  auto kv = simt_packed_kernel<BM, BN, BK, STAGES, true>;
+  auto ks = simt_packed_kernel<BM, BN, BK, STAGES, false>;
+  if (smem > 48 * 1024) {
+    if (cudaFuncSetAttribute(kv, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+        cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      return cudaGetLastError();
+  }
+  profile_mark_before(s);
+  if (plan.vec)
+    kv<<<grid, kThreadsP, smem, s>>>(p, kps, w, ws_vec);
+  else
+    ks<<<grid, kThreadsP, smem, s>>>(p, kps, w, ws_vec);
+  profile_mark_after(s);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || split == 1) return e;
+  return launch_splitk_reduce(p, ws, split, s);
+}
+
 cudaError_t launch_simt(const gemm_plan_t &plan, const GemmArgs &p, float *ws, cudaStream_t s) {
-  if (plan.bm == 128 && plan.bn == 128) return launch_cfg<128, 128, 16, 8, 8>(plan, p, ws, s);
-  if (plan.bm == 64 && plan.bn == 64) return launch_cfg<64, 64, 16, 4, 4>(plan, p, ws, s);
+  if (plan.bm == 64 && plan.bn == 128 && plan.bk == 16 && plan.stages == 4)
+    return launch_packed<64, 128, 16, 4>(plan, p, ws, s);
   return cudaErrorInvalidValue;
 }
 

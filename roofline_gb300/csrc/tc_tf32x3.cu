@@ -558,28 +558,68 @@ __global__ void split_rows_kernel(const float *__restrict__ src, int64_t ld, int
   }
 }
 
-// B (k x n, ld, row-major) -> Bt_hi/Bt_lo (n x kp, row-major), 32 x 32 tiles
-// through shared memory so both the reads (along n) and the writes (along
-// k) are coalesced; columns k <= c < kp are zero.
-__global__ void split_transpose_kernel(const float *__restrict__ src, int64_t ld, int64_t k,
-                                       int64_t n, int64_t kp, float *__restrict__ hi,
-                                       float *__restrict__ lo) {
-  __shared__ float tile[32][33];
-  const int64_t k0 = (int64_t)blockIdx.y * 32;
-  const int64_t n0 = (int64_t)blockIdx.x * 32;
-  const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8
-  for (int j = ty; j < 32; j += 8) {
-    const int64_t kk = k0 + j, nn = n0 + tx;
-    tile[j][tx] = (kk < k && nn < n) ? __ldg(src + kk * ld + nn) : 0.0f;
+// B (k x n, ld, row-major) -> Bt_hi/Bt_lo (n x kp, row-major), columns
+// k <= c < kp zero.  One CTA of 256 threads moves a 32 (k) x 128 (n) tile:
+// each thread loads four 16-byte pieces along n (all in flight at once),
+// the tile goes through shared memory, and each thread then stores four
+// 16-byte pieces of hi and of lo along k.  `vec` (ld % 4 == 0 and a 16-byte
+// aligned B) enables the 16-byte loads; the stores are 16-byte aligned
+// because kp is a multiple of 4.
+constexpr int kTrK = 32, kTrN = 128;
+
+__global__ void __launch_bounds__(256)
+split_transpose_kernel(const float *__restrict__ src, int64_t ld, int64_t k, int64_t n,
+                       int64_t kp, int vec, float *__restrict__ hi, float *__restrict__ lo) {
+  __shared__ float tile[kTrK][kTrN + 1];
+  const int64_t k0 = (int64_t)blockIdx.y * kTrK;
+  const int64_t n0 = (int64_t)blockIdx.x * kTrN;
+  const int t = threadIdx.x;
+  // loads: piece p = t + 256 * i covers row p / 32, columns 4 * (p % 32) .. +3
+  float4 v[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int p = t + 256 * i;
+    const int64_t kk = k0 + p / 32, nn = n0 + 4 * (p % 32);
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (kk < k) {
+      const float *s = src + kk * ld + nn;
+      if (vec && nn + 4 <= n) {
+        x = __ldg(reinterpret_cast<const float4 *>(s));
+      } else {
+        if (nn + 0 < n) x.x = __ldg(s + 0);
+        if (nn + 1 < n) x.y = __ldg(s + 1);
+        if (nn + 2 < n) x.z = __ldg(s + 2);
+        if (nn + 3 < n) x.w = __ldg(s + 3);
+      }
+    }
+    v[i] = x;
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int p = t + 256 * i;
+    float *row = &tile[p / 32][4 * (p % 32)];
+    row[0] = v[i].x;
+    row[1] = v[i].y;
+    row[2] = v[i].z;
+    row[3] = v[i].w;
   }
   __syncthreads();
-  for (int j = ty; j < 32; j += 8) {
-    const int64_t nn = n0 + j, kk = k0 + tx;
+  // stores: piece q = t + 256 * i covers output row n0 + q / 8, k quad q % 8
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int q = t + 256 * i;
+    const int nl = q / 8, kq = 4 * (q % 8);
+    const int64_t nn = n0 + nl, kk = k0 + kq;
     if (nn < n && kk < kp) {
-      const float v = tile[tx][j];
-      const float h = tf32_rna(v);
-      hi[nn * kp + kk] = h;
-      lo[nn * kp + kk] = tf32_rna(v - h);
+      float4 h, l;
+      const float a0 = tile[kq + 0][nl], a1 = tile[kq + 1][nl];
+      const float a2 = tile[kq + 2][nl], a3 = tile[kq + 3][nl];
+      h.x = tf32_rna(a0); l.x = tf32_rna(a0 - h.x);
+      h.y = tf32_rna(a1); l.y = tf32_rna(a1 - h.y);
+      h.z = tf32_rna(a2); l.z = tf32_rna(a2 - h.z);
+      h.w = tf32_rna(a3); l.w = tf32_rna(a3 - h.w);
+      *reinterpret_cast<float4 *>(hi + nn * kp + kk) = h;
+      *reinterpret_cast<float4 *>(lo + nn * kp + kk) = l;
     }
   }
 }
@@ -664,8 +704,9 @@ int launch_cfg(const gemm_plan_t &plan, const GemmArgs &a, char *ws, cudaStream_
     split_rows_kernel<<<(unsigned)blocks, 256, 0, s>>>(a.A, a.lda, a.M, a.K, L.kp, ahi, alo);
   }
   {
-    dim3 grid((unsigned)ceil_div(a.N, 32), (unsigned)ceil_div(L.kp, 32));
-    split_transpose_kernel<<<grid, dim3(32, 8), 0, s>>>(a.B, a.ldb, a.K, a.N, L.kp, bhi, blo);
+    const int vec = ((a.ldb & 3) == 0 && (reinterpret_cast<uintptr_t>(a.B) & 15) == 0) ? 1 : 0;
+    dim3 grid((unsigned)ceil_div(a.N, kTrN), (unsigned)ceil_div(L.kp, kTrK));
+    split_transpose_kernel<<<grid, 256, 0, s>>>(a.B, a.ldb, a.K, a.N, L.kp, vec, bhi, blo);
   }
   if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_CUDA;
 

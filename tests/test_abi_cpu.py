@@ -93,7 +93,7 @@ def test_plans_for_the_workloads(lib):
     assert r["vec"] == 0  # lda = 777 is not a multiple of 4 floats
     assert r["bytes"] == 4 * (1023 * 777 + 777 * 1025 + 2 * 1023 * 1025)
     q = gemm.plan(4096, 4096, 4096, mode="fp32_simt")
-    assert q["bm"] == 128 and q["bn"] == 128 and q["split_k"] == 1 and q["bound_name"] == "fp32"
+    assert q["bm"] == 64 and q["bn"] == 128 and q["split_k"] == 1 and q["bound_name"] == "fp32"
     s = gemm.plan(65536, 64, 4096, mode="fp32_simt")
     assert s["intensity"] == pytest.approx(2 * 65536 * 64 * 4096 / 1_091_567_616)
     mis = gemm.plan(512, 512, 512, mode="fp32_simt", align_hint=4)
@@ -113,3 +113,28 @@ def test_valid_call_without_device_reports_no_device(lib):
         pytest.skip("a GPU is visible")
     rc = gemm.gemm_f32(4, 4, 4, 256, 4, 256, 4, 256, 4, 1, 0)
     assert rc == gemm.ERR_NO_DEVICE
+
+
+def test_simt_split_choice(lib):
+    # small shapes slice K so every SM gets work; big ones do not
+    assert gemm.plan(512, 512, 512, mode="fp32_simt")["split_k"] > 1
+    assert gemm.plan(8192, 8192, 8192, mode="fp32_simt")["split_k"] == 1
+    for shape in [(512, 512, 512), (1023, 1025, 777), (300, 200, 1000), (64, 64, 64)]:
+        p = gemm.plan(*shape, mode="fp32_simt")
+        M, N, K = shape
+        kps = -(-K // p["split_k"])
+        assert p["split_k"] == 1 or kps >= 16
+        assert p["workspace_bytes"] == (p["split_k"] * M * N * 4 if p["split_k"] > 1 else 0)
+        assert p["grid_ctas"] == -(-M // 64) * -(-N // 128) * p["split_k"]
+
+
+def test_tc_plans_on_cpu(lib):
+    p = gemm.plan(4096, 4096, 4096, mode="tf32x3")
+    assert p["kernel_name"] == "tc_tf32x3" and p["bn"] == 256 and p["a_split_in_kernel"] == 1
+    assert p["workspace_bytes"] == 2 * 4096 * 4096 * 4  # B_hi and B_lo only
+    s = gemm.plan(65536, 64, 4096, mode="tf32x3")
+    assert s["bn"] == 64 and s["ctas_per_sm"] == 2 and s["bound_name"] == "hbm"
+    r = gemm.plan(1023, 1025, 777, 777, 1025, 1025, mode="tf32x3")
+    assert r["a_split_in_kernel"] == 0 and r["launches"] == 3
+    assert gemm.plan(4096, 4096, 4096)["kernel_name"] == "tc_tf32x3"  # auto
+    assert gemm.plan(512, 512, 512)["kernel_name"] == "simt"  # auto, small

@@ -259,3 +259,15 @@ def test_tf32x3_every_built_configuration(cfg, monkeypatch):
         (bn, bk, st, ak, cc)
     got, ref, D = _run_shape(M, N, K, "tf32x3", 1.5, 0.5, pad=pad, offset=0, seed=st + bn)
     assert oracle.err_normalised(got, ref, D) <= TOL_E1
+
+
+@pytest.mark.parametrize("split", [1, 2, 3, 7, 16])
+def test_simt_forced_splits(split, monkeypatch):
+    from roofline_gb300 import gemm
+    monkeypatch.setenv("GEMM_SIMT_SPLIT", str(split))
+    M, N, K = 300, 260, 1000
+    p = gemm.plan(M, N, K, K + 1, N, N + 2, mode="fp32_simt")
+    assert p["split_k"] == min(split, -(-K // (-(-(-(-K // split)) // 16) * 16)))
+    got, ref, D = _run_shape(M, N, K, "fp32_simt", 0.75, 1.25, pad=(1, 0, 2), offset=1,
+                             seed=split)
+    assert oracle.err_normalised(got, ref, D) <= TOL_E1
