@@ -286,28 +286,36 @@ def run_ours(args):
             torch.cuda.synchronize()
     torch.cuda.synchronize()
 
-    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    for e in ev_b + ev_a:  # torch creates the underlying cudaEvent on first record
-        e.record(stream)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     start.record(stream)
     for i in range(args.steps):
-        gemm.set_profile_events(ev_b[i], ev_a[i])
         step(i)
-    gemm.set_profile_events(None, None)
     end.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
     ms_total = start.elapsed_time(end)
-    main_ms = [ev_b[i].elapsed_time(ev_a[i]) for i in range(args.steps)]
     if gemm.check_status() != gemm.OK:
         raise RuntimeError("device status reported a timeout during the timed region")
+
+    # Separate pass for the roofline: the library records events around its
+    # main kernel (plain stream order for these calls), one pair per step.
+    nk = max(3, min(args.steps, 50))
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(nk)]
+    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(nk)]
+    for e in ev_b + ev_a:  # torch creates the underlying cudaEvent on first record
+        e.record(stream)
+    torch.cuda.synchronize()
+    for i in range(nk):
+        gemm.set_profile_events(ev_b[i], ev_a[i])
+        step(i)
+    gemm.set_profile_events(None, None)
+    torch.cuda.synchronize()
+    main_ms = [ev_b[i].elapsed_time(ev_a[i]) for i in range(nk)]
 
     t_max = ms_total
     if world > 1:
@@ -337,6 +345,7 @@ def run_ours(args):
     roof["traffic"] = traffic
     roof["kernel"] = kname
     roof["kernel_ms"] = main_avg
+    roof["kernel_timing"] = f"mean of {nk} launches, CUDA events recorded around the kernel on its stream"
     roof["algorithmic"] = (f"{alg_bytes} B" if roof["unit"] == "GB/s" else f"{flops:.0f} FLOP") + \
         " per launch"
     roof["peak_source"] = {"alu": "SMs x 128 FP32 lanes x 2 x max SM clock (device attributes)",

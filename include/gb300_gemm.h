@@ -105,6 +105,9 @@ typedef struct gemm_plan {
   double intensity;        /* flops / bytes */
   int32_t b_concat;        /* TF32X3: A_hi*[B_hi|B_lo] issued as one MMA of width 2*bn (1) or two MMAs (0) */
   int32_t ctas_per_sm;     /* CTAs of the main kernel resident per SM (shared memory and TMEM budget) */
+  int32_t stream_k;        /* TF32X3: grid_ctas persistent CTAs share the (tile, K block) work evenly;
+                              a fix-up kernel sums the parts of tiles shared between CTAs */
+  int32_t reserved;
 } gemm_plan_t;
 
 typedef struct gemm_device_info {

@@ -128,6 +128,7 @@ void profile_mark_before(cudaStream_t s) {
 void profile_mark_after(cudaStream_t s) {
   if (t_prof_after) cudaEventRecord(t_prof_after, s);
 }
+bool profile_events_set() { return t_prof_before != nullptr; }
 
 const DeviceProps &default_props() {
   static const DeviceProps d = make_default_props();

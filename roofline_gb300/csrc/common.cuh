@@ -48,6 +48,7 @@ const DeviceProps &default_props();
 // the main kernel launch, if set for this host thread.
 void profile_mark_before(cudaStream_t s);
 void profile_mark_after(cudaStream_t s);
+bool profile_events_set();
 
 // Planner (plan.cu).
 int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,

@@ -203,7 +203,25 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
       }
       p.ctas_per_sm = tc_ctas_per_sm(p.bn, p.bk, p.stages, p.a_split_in_kernel, p.b_concat,
                                      dp.smem_per_sm > 0 ? dp.smem_per_sm : 233472);
-      p.grid_ctas = ceil_div(M, p.bm) * ceil_div(N, p.bn);
+      // Stream-K: when the tiles do not fill whole waves of resident CTAs,
+      // launch one wave of persistent CTAs that split the (tile, K block)
+      // work evenly (each at least 4 K blocks); a fix-up kernel sums the
+      // parts of tiles shared between CTAs, in CTA order.
+      {
+        const int64_t tiles = ceil_div(M, p.bm) * ceil_div(N, p.bn);
+        const int64_t slots = (int64_t)(p.ctas_per_sm > 0 ? p.ctas_per_sm : 1) * sms;
+        const int64_t total = tiles * ceil_div(K, p.bk);
+        // at least 4 K blocks per CTA, and at most 250 CTAs per tile (the
+        // fix-up sums up to 256 parts)
+        int64_t g = slots < total / 4 ? slots : total / 4;
+        if (g > 250 * tiles) g = 250 * tiles;
+        const char *sk = std::getenv("GEMM_TC_STREAMK");  // tuning knob: 0 off, 1 on
+        bool want = (tiles % slots) != 0 && tiles < 8 * slots;
+        if (sk) want = std::atoi(sk) != 0;
+        p.stream_k = (want && g >= 2 && g < tiles * 64) ? 1 : 0;
+        p.grid_ctas = p.stream_k ? g : tiles;
+        if (p.stream_k) p.launches += 1;
+      }
       p.workspace_bytes = tc_workspace_bytes(p, M, N, K);
       break;
     }

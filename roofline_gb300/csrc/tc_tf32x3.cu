@@ -174,6 +174,15 @@ __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Programmatic dependent launch: wait for the previous kernel in the stream
+// (no-op when launched without the attribute), and let the next one launch.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ float tf32_rna(float x) {
   uint32_t r;
   asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
@@ -248,10 +257,35 @@ struct TcParams {
   float alpha, beta;
   float *C;
   int64_t ldc;
-  int num_kb;
+  int num_kb;        // K blocks per output tile
+  int tiles_n;       // output tiles along N (tile t = m_tile * tiles_n + n_tile)
+  int64_t total;     // tiles * num_kb: the (tile, K block) work units
+  float *partial;    // stream-K partial tiles: 2 slots of 128 x BN per CTA
   uint64_t timeout_ns;
   int stall_producer;  // test hook: the producer issues nothing
 };
+
+// Work split (stream-K): CTA c of G owns the work units [c*total/G,
+// (c+1)*total/G), walked tile by tile.  With G = tiles each CTA owns exactly
+// one whole tile.
+struct Segment {
+  int tile, kb0, kb1;  // K blocks [kb0, kb1) of output tile `tile`
+};
+
+__host__ __device__ __forceinline__ int64_t unit_begin(int64_t total, int64_t c, int64_t G) {
+  return total * c / G;
+}
+
+// Segment `i` of the walk [u0, u1) (valid while the returned kb1 > kb0).
+__device__ __forceinline__ bool next_segment(int64_t &u, int64_t u1, int num_kb, Segment &sg) {
+  if (u >= u1) return false;
+  sg.tile = (int)(u / num_kb);
+  sg.kb0 = (int)(u % num_kb);
+  const int64_t left = u1 - u;
+  sg.kb1 = (int)(sg.kb0 + left < num_kb ? sg.kb0 + left : num_kb);
+  u += sg.kb1 - sg.kb0;
+  return true;
+}
 
 // BN: output columns per CTA.  BK: K depth of one stage (16 -> 64-byte
 // swizzle, 32 -> 128-byte swizzle).  AK: A arrives raw (FP32) and the
@@ -300,7 +334,8 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
   uint64_t *conv = full + STAGES;    // A tile split (AK)
   uint64_t *empty = conv + STAGES;   // stage free again
   uint64_t *acc_full = empty + STAGES;
-  uint64_t *drain = acc_full + 1;
+  uint64_t *acc_empty = acc_full + 1;
+  uint64_t *drain = acc_empty + 1;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -311,8 +346,9 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int64_t m0 = (int64_t)blockIdx.y * kBM;
-  const int64_t n0 = (int64_t)blockIdx.x * BN;
+  const int64_t G = gridDim.x;
+  const int64_t u_begin = unit_begin(p.total, blockIdx.x, G);
+  const int64_t u_end = unit_begin(p.total, blockIdx.x + 1, G);
   const uint64_t deadline = globaltimer() + p.timeout_ns;
 
   if (threadIdx.x == 0) {
@@ -322,6 +358,7 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
       mbar_init(&empty[s], 1);
     }
     mbar_init(acc_full, 1);
+    mbar_init(acc_empty, kConvThreads);
     mbar_init(drain, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -340,33 +377,41 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // B_hi/B_lo (and A_hi/A_lo) come from the split kernels before this one
+  grid_dependency_wait();
 
   bool ok = true;
   if (warp == 0) {
-    // ---------------- TMA producer
+    // ---------------- TMA producer: every stage of every segment, in order
     int issued = 0;
     if (lane == 0 && !p.stall_producer) {
-      for (int kb = 0; kb < p.num_kb; ++kb) {
-        const int s = kb % STAGES;
-        const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
-        if (!mbar_wait(&empty[s], ph ^ 1u, deadline, abort_flag)) {
-          ok = false;
-          break;
+      int64_t u = u_begin;
+      Segment sg;
+      while (ok && next_segment(u, u_end, p.num_kb, sg)) {
+        const int32_t m0 = (sg.tile / p.tiles_n) * kBM;
+        const int32_t n0 = (sg.tile % p.tiles_n) * BN;
+        for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
+          const int s = issued % STAGES;
+          const uint32_t ph = (uint32_t)(issued / STAGES) & 1u;
+          if (!mbar_wait(&empty[s], ph ^ 1u, deadline, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(&full[s], Cfg::TX_BYTES);
+          const int32_t kx = kb * BK;
+          tma_load_2d(a_hi(s), &tmA_hi, &full[s], kx, m0);
+          if (!AK) tma_load_2d(a_lo(s), &tmA_lo, &full[s], kx, m0);
+          tma_load_2d(b_hi(s), &tmB_hi, &full[s], kx, n0);
+          tma_load_2d(b_lo(s), &tmB_lo, &full[s], kx, n0);
+          ++issued;
         }
-        mbar_expect_tx(&full[s], Cfg::TX_BYTES);
-        const int32_t kx = kb * BK;
-        tma_load_2d(a_hi(s), &tmA_hi, &full[s], kx, (int32_t)m0);
-        if (!AK) tma_load_2d(a_lo(s), &tmA_lo, &full[s], kx, (int32_t)m0);
-        tma_load_2d(b_hi(s), &tmB_hi, &full[s], kx, (int32_t)n0);
-        tma_load_2d(b_lo(s), &tmB_lo, &full[s], kx, (int32_t)n0);
-        ++issued;
       }
       if (!ok) *abort_flag = 1;
       // wait (bounded) for every load this lane issued, whatever happened
       const uint64_t drain_deadline = globaltimer() + 2000000000ull;
       volatile int never = 0;
-      for (int kb = issued - STAGES < 0 ? 0 : issued - STAGES; kb < issued; ++kb)
-        mbar_wait(&full[kb % STAGES], (uint32_t)(kb / STAGES) & 1u, drain_deadline, &never);
+      for (int it = issued - STAGES < 0 ? 0 : issued - STAGES; it < issued; ++it)
+        mbar_wait(&full[it % STAGES], (uint32_t)(it / STAGES) & 1u, drain_deadline, &never);
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer
@@ -374,48 +419,62 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
       constexpr uint32_t idesc = idesc_tf32(kBM, BN);
       constexpr uint32_t idesc2 = idesc_tf32(kBM, CONCAT ? 2 * BN : BN);
       bool any = false;
-      for (int kb = 0; kb < p.num_kb; ++kb) {
-        const int s = kb % STAGES;
-        const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
-        if (!mbar_wait(AK ? &conv[s] : &full[s], ph, deadline, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t ah = smem_u32(a_hi(s)), al = smem_u32(a_lo(s));
-        const uint32_t bh = smem_u32(b_hi(s)), bl = smem_u32(b_lo(s));
-        const uint32_t lo_t = tmem_base + (uint32_t)(Cfg::LO_COL0 + s * BK);
-#pragma unroll
-        for (int kk = 0; kk < BK / 8; ++kk) {
-          const uint32_t off = kk * 32;  // 8 TF32 values = 32 bytes along K
-          const uint64_t dah = smem_desc(ah + off, Cfg::SBO, Cfg::LAYOUT);
-          const uint64_t dbh = smem_desc(bh + off, Cfg::SBO, Cfg::LAYOUT);
-          const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
-          if (CONCAT) {
-            // columns [0, BN): A_hi*B_hi (+ A_lo*B_hi); [BN, 2BN): A_hi*B_lo
-            mma_tf32(tmem_base, dah, dbh, idesc2, acc);
-            if (AK)
-              mma_tf32_ts(tmem_base, lo_t + kk * 8, dbh, idesc, 1u);
-            else
-              mma_tf32(tmem_base, smem_desc(al + off, Cfg::SBO, Cfg::LAYOUT), dbh, idesc, 1u);
-          } else {
-            const uint64_t dbl = smem_desc(bl + off, Cfg::SBO, Cfg::LAYOUT);
-            mma_tf32(tmem_base, dah, dbl, idesc, acc);  // small terms first
-            if (AK)
-              mma_tf32_ts(tmem_base, lo_t + kk * 8, dbh, idesc, 1u);
-            else
-              mma_tf32(tmem_base, smem_desc(al + off, Cfg::SBO, Cfg::LAYOUT), dbh, idesc, 1u);
-            mma_tf32(tmem_base, dah, dbh, idesc, 1u);
+      int it = 0, si = 0;
+      int64_t u = u_begin;
+      Segment sg;
+      while (ok && next_segment(u, u_end, p.num_kb, sg)) {
+        if (si > 0) {
+          // the epilogue must have drained the previous segment's accumulator
+          if (!mbar_wait(acc_empty, (uint32_t)(si - 1) & 1u, deadline, abort_flag)) {
+            ok = false;
+            break;
           }
+          tc_fence_after();
         }
-        mma_commit(&empty[s]);
-        any = true;
-      }
-      if (ok) {
+        for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
+          const int s = it % STAGES;
+          const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+          if (!mbar_wait(AK ? &conv[s] : &full[s], ph, deadline, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t ah = smem_u32(a_hi(s)), al = smem_u32(a_lo(s));
+          const uint32_t bh = smem_u32(b_hi(s)), bl = smem_u32(b_lo(s));
+          const uint32_t lo_t = tmem_base + (uint32_t)(Cfg::LO_COL0 + s * BK);
+#pragma unroll
+          for (int kk = 0; kk < BK / 8; ++kk) {
+            const uint32_t off = kk * 32;  // 8 TF32 values = 32 bytes along K
+            const uint64_t dah = smem_desc(ah + off, Cfg::SBO, Cfg::LAYOUT);
+            const uint64_t dbh = smem_desc(bh + off, Cfg::SBO, Cfg::LAYOUT);
+            const uint32_t acc = (kb > sg.kb0 || kk > 0) ? 1u : 0u;
+            if (CONCAT) {
+              // columns [0, BN): A_hi*B_hi (+ A_lo*B_hi); [BN, 2BN): A_hi*B_lo
+              mma_tf32(tmem_base, dah, dbh, idesc2, acc);
+              if (AK)
+                mma_tf32_ts(tmem_base, lo_t + kk * 8, dbh, idesc, 1u);
+              else
+                mma_tf32(tmem_base, smem_desc(al + off, Cfg::SBO, Cfg::LAYOUT), dbh, idesc, 1u);
+            } else {
+              const uint64_t dbl = smem_desc(bl + off, Cfg::SBO, Cfg::LAYOUT);
+              mma_tf32(tmem_base, dah, dbl, idesc, acc);  // small terms first
+              if (AK)
+                mma_tf32_ts(tmem_base, lo_t + kk * 8, dbh, idesc, 1u);
+              else
+                mma_tf32(tmem_base, smem_desc(al + off, Cfg::SBO, Cfg::LAYOUT), dbh, idesc, 1u);
+              mma_tf32(tmem_base, dah, dbh, idesc, 1u);
+            }
+          }
+          mma_commit(&empty[s]);
+          any = true;
+          ++it;
+        }
+        if (!ok) break;
         mma_commit(acc_full);
-      } else {
-        *abort_flag = 1;
+        ++si;
       }
+      if (!ok) *abort_flag = 1;
+      grid_launch_dependents();  // the fix-up may start launching
       if (any) {
         // every MMA issued so far must retire before TMEM is freed
         mma_commit(drain);
@@ -428,56 +487,62 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
     const int quarter = warp & 3;  // TMEM lanes this warp may touch
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16);
-    if (AK) {
-      for (int kb = 0; kb < p.num_kb; ++kb) {
-        const int s = kb % STAGES;
-        const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
-        // tcgen05.st below is warp-collective: the warp proceeds or stops as one
-        if (!__all_sync(0xffffffffu, mbar_wait(&full[s], ph, deadline, abort_flag))) {
-          ok = false;
-          break;
-        }
-        // Row `row` of the landed tile: 16-byte chunk c sits at chunk
-        // c ^ f(row) of its 64- or 128-byte line (the TMA swizzle).
-        uint8_t *line = a_hi(s) + row * Cfg::ROW_BYTES;
-        uint32_t lo[BK];
+    const bool vec = ((p.ldc & 3) == 0) && ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0);
+    int it = 0, si = 0;
+    int64_t u = u_begin;
+    Segment sg;
+    while (ok && next_segment(u, u_end, p.num_kb, sg)) {
+      if (AK) {
+        for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+          // tcgen05.st below is warp-collective: the warp proceeds or stops as one
+          if (!__all_sync(0xffffffffu, mbar_wait(&full[s], ph, deadline, abort_flag))) {
+            ok = false;
+            break;
+          }
+          // Row `row` of the landed tile: 16-byte chunk c sits at chunk
+          // c ^ f(row) of its 64- or 128-byte line (the TMA swizzle).
+          uint8_t *line = a_hi(s) + row * Cfg::ROW_BYTES;
+          uint32_t lo[BK];
 #pragma unroll
-        for (int c = 0; c < BK / 4; ++c) {
-          const int phys = (BK == 32) ? (c ^ (row & 7)) : (c ^ ((row >> 1) & 3));
-          float4 *ptr = reinterpret_cast<float4 *>(line + phys * 16);
-          const float4 x = *ptr;
-          float4 h;
-          h.x = tf32_rna(x.x);
-          h.y = tf32_rna(x.y);
-          h.z = tf32_rna(x.z);
-          h.w = tf32_rna(x.w);
-          lo[4 * c + 0] = __float_as_uint(tf32_rna(x.x - h.x));
-          lo[4 * c + 1] = __float_as_uint(tf32_rna(x.y - h.y));
-          lo[4 * c + 2] = __float_as_uint(tf32_rna(x.z - h.z));
-          lo[4 * c + 3] = __float_as_uint(tf32_rna(x.w - h.w));
-          *ptr = h;
+          for (int c = 0; c < BK / 4; ++c) {
+            const int phys = (BK == 32) ? (c ^ (row & 7)) : (c ^ ((row >> 1) & 3));
+            float4 *ptr = reinterpret_cast<float4 *>(line + phys * 16);
+            const float4 x = *ptr;
+            float4 h;
+            h.x = tf32_rna(x.x);
+            h.y = tf32_rna(x.y);
+            h.z = tf32_rna(x.z);
+            h.w = tf32_rna(x.w);
+            lo[4 * c + 0] = __float_as_uint(tf32_rna(x.x - h.x));
+            lo[4 * c + 1] = __float_as_uint(tf32_rna(x.y - h.y));
+            lo[4 * c + 2] = __float_as_uint(tf32_rna(x.z - h.z));
+            lo[4 * c + 3] = __float_as_uint(tf32_rna(x.w - h.w));
+            *ptr = h;
+          }
+          tmem_st<BK>(lane_base + (uint32_t)(Cfg::LO_COL0 + s * BK), lo);
+          tmem_st_wait();
+          fence_async_smem();  // A_hi written by this thread -> visible to the MMA
+          tc_fence_before();
+          mbar_arrive(&conv[s]);
         }
-        tmem_st<BK>(lane_base + (uint32_t)(Cfg::LO_COL0 + s * BK), lo);
-        tmem_st_wait();
-        fence_async_smem();  // A_hi written by this thread -> visible to the MMA
-        tc_fence_before();
-        mbar_arrive(&conv[s]);
+        if (!ok) break;
       }
-      if (!ok) *abort_flag = 1;
-    }
-    if (ok) {
-      if (!mbar_wait(acc_full, 0, deadline, abort_flag)) ok = false;
-    }
-    // tcgen05.ld is warp-collective: the whole warp drains or none of it
-    const bool warp_ok = __all_sync(0xffffffffu, ok);
-    if (!warp_ok) {
-      ok = false;
-      *abort_flag = 1;
-    }
-    if (warp_ok) {
+      // ---- epilogue of this segment
+      const bool got = mbar_wait(acc_full, (uint32_t)si & 1u, deadline, abort_flag);
+      // tcgen05.ld is warp-collective: the whole warp drains or none of it
+      if (!__all_sync(0xffffffffu, got)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
+      const bool whole = sg.kb0 == 0 && sg.kb1 == p.num_kb;
+      const int64_t m0 = (int64_t)(sg.tile / p.tiles_n) * kBM;
+      const int64_t n0 = (int64_t)(sg.tile % p.tiles_n) * BN;
       const int64_t grow = m0 + row;
-      const bool vec = ((p.ldc & 3) == 0) && ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0);
+      // partial tiles: slot 0 for this CTA's first segment, 1 for its last
+      float *prow = p.partial + ((int64_t)(blockIdx.x * 2 + (si == 0 ? 0 : 1)) * kBM + row) * BN;
 #pragma unroll 1
       for (int c = 0; c < BN; c += 32) {
         uint32_t r[32];
@@ -492,7 +557,13 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
         } else {
           tmem_ld_wait();
         }
-        if (grow < p.M) {
+        if (!whole) {
+#pragma unroll
+          for (int q = 0; q < 32; q += 4)
+            *reinterpret_cast<float4 *>(prow + c + q) =
+                make_float4(__uint_as_float(r[q]), __uint_as_float(r[q + 1]),
+                            __uint_as_float(r[q + 2]), __uint_as_float(r[q + 3]));
+        } else if (grow < p.M) {
           float *dst = p.C + grow * p.ldc + n0 + c;
           const int64_t left = p.N - (n0 + c);
           if (vec && left >= 32) {
@@ -523,7 +594,11 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
           }
         }
       }
+      tc_fence_before();
+      mbar_arrive(acc_empty);  // the accumulator may be overwritten
+      ++si;
     }
+    if (!ok) *abort_flag = 1;
   }
 
   if (!ok) atomicExch(&g_tc_status, GEMM_ERR_DEVICE_TIMEOUT);
@@ -533,12 +608,81 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
   if (warp == 1) tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
 }
 
+// Stream-K fix-up: an output tile whose K blocks were split between CTAs
+// gets C = alpha * (sum of its partial tiles, in CTA order) + beta * C.
+// Block j looks at the boundary between CTAs j and j+1; the block whose
+// boundary is the first one strictly inside a tile handles that tile, all
+// other blocks return at once (whole tiles were written by the GEMM).
+constexpr int kFixMaxParts = 256;
+
+__global__ void __launch_bounds__(256)
+streamk_fixup_kernel(TcParams p, int BN, int64_t G) {
+  __shared__ int64_t part_off[kFixMaxParts];
+  __shared__ int nparts;
+  grid_dependency_wait();  // the GEMM's partial tiles
+  const int64_t c = (int64_t)blockIdx.x + 1;  // boundary between CTAs c-1 and c
+  const int64_t b = unit_begin(p.total, c, G);
+  const int64_t t = b / p.num_kb;
+  const int64_t first = t * p.num_kb, last = first + p.num_kb - 1;
+  if (b == first || b > last) return;                    // not strictly inside a tile
+  if (unit_begin(p.total, c - 1, G) > first) return;     // an earlier boundary owns it
+  if (threadIdx.x == 0) {
+    int n = 0;
+    for (int64_t cta = c - 1; cta < G && unit_begin(p.total, cta, G) <= last; ++cta) {
+      const int64_t ub = unit_begin(p.total, cta, G), ue = unit_begin(p.total, cta + 1, G);
+      if (ub == ue) continue;  // no work
+      // the tile is this CTA's first segment (slot 0) or its last (slot 1)
+      const int slot = (ub >= first) ? 0 : 1;
+      if (n < kFixMaxParts) part_off[n++] = (cta * 2 + slot) * (int64_t)kBM * BN;
+    }
+    nparts = n;
+  }
+  __syncthreads();
+  const int n = nparts;
+  const int64_t m0 = (t / p.tiles_n) * kBM;
+  const int64_t n0 = (t % p.tiles_n) * BN;
+  const bool vec = ((p.ldc & 3) == 0) && ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0);
+  for (int e = threadIdx.x * 4; e < kBM * BN; e += blockDim.x * 4) {
+    const int r = e / BN, col = e % BN;
+    const int64_t gr = m0 + r, gc = n0 + col;
+    if (gr >= p.M || gc >= p.N) continue;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = 0; i < n; ++i) {
+      const float4 v = *reinterpret_cast<const float4 *>(p.partial + part_off[i] + e);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    float *dst = p.C + gr * p.ldc + gc;
+    const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+    if (vec && gc + 4 <= p.N) {
+      float4 o = make_float4(p.alpha * a4[0], p.alpha * a4[1], p.alpha * a4[2], p.alpha * a4[3]);
+      if (p.beta != 0.0f) {
+        const float4 old = *reinterpret_cast<const float4 *>(dst);
+        o.x = fmaf(p.beta, old.x, o.x);
+        o.y = fmaf(p.beta, old.y, o.y);
+        o.z = fmaf(p.beta, old.z, o.z);
+        o.w = fmaf(p.beta, old.w, o.w);
+      }
+      *reinterpret_cast<float4 *>(dst) = o;
+    } else {
+      for (int q = 0; q < 4 && gc + q < p.N; ++q) {
+        float o = p.alpha * a4[q];
+        if (p.beta != 0.0f) o = fmaf(p.beta, dst[q], o);
+        dst[q] = o;
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------------ split pass
 
 // dst_hi/dst_lo (rows x kp, row-major) <- split of src (rows x k, ld), zero for k <= c < kp.
 __global__ void split_rows_kernel(const float *__restrict__ src, int64_t ld, int64_t rows,
                                   int64_t k, int64_t kp, float *__restrict__ hi,
                                   float *__restrict__ lo) {
+  grid_launch_dependents();
   const int64_t groups = rows * (kp / 4);
   for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < groups;
        g += (int64_t)gridDim.x * blockDim.x) {
@@ -571,6 +715,8 @@ __global__ void __launch_bounds__(256)
 split_transpose_kernel(const float *__restrict__ src, int64_t ld, int64_t k, int64_t n,
                        int64_t kp, int vec, float *__restrict__ hi, float *__restrict__ lo) {
   __shared__ float tile[kTrK][kTrN + 1];
+  grid_dependency_wait();   // A_hi/A_lo pass before this one (if any) is done
+  grid_launch_dependents();  // the GEMM may launch; it waits for this grid to finish
   const int64_t k0 = (int64_t)blockIdx.y * kTrK;
   const int64_t n0 = (int64_t)blockIdx.x * kTrN;
   const int t = threadIdx.x;
@@ -670,11 +816,14 @@ inline int64_t round_up(int64_t a, int64_t b) { return (a + b - 1) / b * b; }
 inline uint64_t align256(uint64_t x) { return (x + 255) & ~uint64_t(255); }
 
 struct WsLayout {
-  uint64_t a_hi, a_lo, b_hi, b_lo, total;
+  uint64_t a_hi, a_lo, b_hi, b_lo, partial, total;
   int64_t kp;
 };
 
-WsLayout ws_layout(int64_t M, int64_t N, int64_t K, bool a_inkernel) {
+// Workspace regions: A_hi, A_lo (unless A is split in the kernel), B_hi,
+// B_lo (transposed), then for stream-K the partial tiles (2 per CTA).
+WsLayout ws_layout(int64_t M, int64_t N, int64_t K, bool a_inkernel, int64_t streamk_ctas,
+                   int bn) {
   WsLayout w{};
   w.kp = round_up(K, 4);
   const uint64_t a_bytes = a_inkernel ? 0 : align256((uint64_t)M * w.kp * 4);
@@ -683,14 +832,20 @@ WsLayout ws_layout(int64_t M, int64_t N, int64_t K, bool a_inkernel) {
   w.a_lo = a_bytes;
   w.b_hi = 2 * a_bytes;
   w.b_lo = 2 * a_bytes + b_bytes;
-  w.total = 2 * a_bytes + 2 * b_bytes;
+  w.partial = 2 * a_bytes + 2 * b_bytes;
+  w.total = w.partial + (uint64_t)streamk_ctas * 2 * kBM * bn * 4;
   return w;
 }
 
 template <int BN, int BK, int STAGES, bool AK, bool CONCAT>
 int launch_cfg(const gemm_plan_t &plan, const GemmArgs &a, char *ws, cudaStream_t s) {
   using Cfg = TcCfg<BN, BK, STAGES, AK, CONCAT>;
-  const WsLayout L = ws_layout(a.M, a.N, a.K, AK);
+  const int64_t tiles_m = ceil_div(a.M, kBM), tiles_n = ceil_div(a.N, BN);
+  const int64_t tiles = tiles_m * tiles_n;
+  const int num_kb = (int)ceil_div(a.K, BK);
+  const int64_t G = plan.stream_k ? plan.grid_ctas : tiles;
+  if (G < 1 || G > 0x7fffffff || tiles > 0x7fffffff) return GEMM_ERR_UNSUPPORTED;
+  const WsLayout L = ws_layout(a.M, a.N, a.K, AK, plan.stream_k ? G : 0, BN);
   float *ahi = reinterpret_cast<float *>(ws + L.a_hi);
   float *alo = reinterpret_cast<float *>(ws + L.a_lo);
   float *bhi = reinterpret_cast<float *>(ws + L.b_hi);
@@ -731,7 +886,10 @@ int launch_cfg(const gemm_plan_t &plan, const GemmArgs &a, char *ws, cudaStream_
   p.beta = a.beta;
   p.C = a.C;
   p.ldc = a.ldc;
-  p.num_kb = (int)ceil_div(a.K, BK);
+  p.num_kb = num_kb;
+  p.tiles_n = (int)tiles_n;
+  p.total = tiles * num_kb;
+  p.partial = reinterpret_cast<float *>(ws + L.partial);
   p.timeout_ns = env_u64("GEMM_DEBUG_WAIT_LIMIT_NS", 2000000000ull);
   p.stall_producer = (int)env_u64("GEMM_DEBUG_STALL_PRODUCER", 0);
 
@@ -741,12 +899,42 @@ int launch_cfg(const gemm_plan_t &plan, const GemmArgs &a, char *ws, cudaStream_
     cudaGetLastError();
     return GEMM_ERR_CUDA;
   }
-  dim3 grid((unsigned)ceil_div(a.N, BN), (unsigned)ceil_div(a.M, kBM));
+  // Programmatic dependent launch lets each kernel be scheduled while the one
+  // before it drains (each waits for its predecessor before reading its
+  // output).  With the caller's profiling events set, plain stream order is
+  // kept so the events bracket the GEMM kernel alone.
+  const bool pdl = !profile_events_set();
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3((unsigned)G);
+  lc.blockDim = dim3(kThreadsTC);
+  lc.dynamicSmemBytes = Cfg::SMEM_BYTES;
+  lc.stream = s;
+  lc.attrs = attr;
+  lc.numAttrs = pdl ? 1 : 0;
   profile_mark_before(s);
-  kern<<<grid, kThreadsTC, Cfg::SMEM_BYTES, s>>>(tA0, tA1, tB0, tB1, p);
+  cudaError_t e = cudaLaunchKernelEx(&lc, kern, tA0, tA1, tB0, tB1, p);
   profile_mark_after(s);
-  (void)plan;
-  return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+  if (plan.stream_k) {
+    cudaLaunchConfig_t fc = {};
+    fc.gridDim = dim3((unsigned)(G - 1));
+    fc.blockDim = dim3(256);
+    fc.stream = s;
+    fc.attrs = attr;
+    fc.numAttrs = pdl ? 1 : 0;
+    e = cudaLaunchKernelEx(&fc, streamk_fixup_kernel, p, (int)BN, G);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return GEMM_ERR_CUDA;
+    }
+  }
+  return GEMM_OK;
 }
 
 }  // namespace
@@ -792,7 +980,9 @@ int tc_ctas_per_sm(int bn, int bk, int stages, int a_inkernel, int concat, int s
 }
 
 uint64_t tc_workspace_bytes(const gemm_plan_t &plan, int64_t M, int64_t N, int64_t K) {
-  return ws_layout(M, N, K, plan.a_split_in_kernel != 0).total;
+  return ws_layout(M, N, K, plan.a_split_in_kernel != 0, plan.stream_k ? plan.grid_ctas : 0,
+                   plan.bn)
+      .total;
 }
 
 int launch_tc(const gemm_plan_t &plan, const GemmArgs &a, void *ws, size_t ws_bytes,

@@ -57,7 +57,8 @@ class GemmPlan(ctypes.Structure):
                 ("launches", ctypes.c_int32), ("grid_ctas", ctypes.c_int64),
                 ("workspace_bytes", ctypes.c_uint64), ("flops", ctypes.c_double),
                 ("bytes", ctypes.c_double), ("intensity", ctypes.c_double),
-                ("b_concat", ctypes.c_int32), ("ctas_per_sm", ctypes.c_int32)]
+                ("b_concat", ctypes.c_int32), ("ctas_per_sm", ctypes.c_int32),
+                ("stream_k", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
     def as_dict(self):
         d = {name: getattr(self, name) for name, _ in self._fields_}

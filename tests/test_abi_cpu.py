@@ -131,10 +131,25 @@ def test_simt_split_choice(lib):
 def test_tc_plans_on_cpu(lib):
     p = gemm.plan(4096, 4096, 4096, mode="tf32x3")
     assert p["kernel_name"] == "tc_tf32x3" and p["bn"] == 256 and p["a_split_in_kernel"] == 1
-    assert p["workspace_bytes"] == 2 * 4096 * 4096 * 4  # B_hi and B_lo only
+    # B_hi and B_lo, plus two partial 128 x 256 tiles per stream-K CTA
+    extra = p["grid_ctas"] * 2 * 128 * 256 * 4 if p["stream_k"] else 0
+    assert p["workspace_bytes"] == 2 * 4096 * 4096 * 4 + extra
     s = gemm.plan(65536, 64, 4096, mode="tf32x3")
     assert s["bn"] == 64 and s["ctas_per_sm"] == 2 and s["bound_name"] == "hbm"
     r = gemm.plan(1023, 1025, 777, 777, 1025, 1025, mode="tf32x3")
-    assert r["a_split_in_kernel"] == 0 and r["launches"] == 3
+    assert r["a_split_in_kernel"] == 0 and r["launches"] == 3 + r["stream_k"]
     assert gemm.plan(4096, 4096, 4096)["kernel_name"] == "tc_tf32x3"  # auto
     assert gemm.plan(512, 512, 512)["kernel_name"] == "simt"  # auto, small
+
+
+def test_stream_k_plan_bounds(lib):
+    # each CTA owns at least 4 K blocks and a tile is split among at most ~250 CTAs
+    for shape in [(128, 128, 65536), (65536, 64, 4096), (4096, 4096, 4096), (256, 256, 256)]:
+        p = gemm.plan(*shape, mode="tf32x3")
+        if not p["stream_k"]:
+            continue
+        M, N, K = shape
+        tiles = -(-M // 128) * -(-N // p["bn"])
+        total = tiles * -(-K // p["bk"])
+        assert 2 <= p["grid_ctas"] <= total // 4
+        assert p["grid_ctas"] <= 250 * tiles

@@ -271,3 +271,29 @@ def test_simt_forced_splits(split, monkeypatch):
     got, ref, D = _run_shape(M, N, K, "fp32_simt", 0.75, 1.25, pad=(1, 0, 2), offset=1,
                              seed=split)
     assert oracle.err_normalised(got, ref, D) <= TOL_E1
+
+
+@pytest.mark.parametrize("shape", [(1000, 64, 96), (777, 200, 300), (300, 520, 64), (2100, 900, 1000),
+                                   (129, 300, 4000)])
+@pytest.mark.parametrize("streamk", ["0", "1"])
+def test_tf32x3_stream_k(shape, streamk, monkeypatch):
+    """Persistent stream-K scheduling (tiles split between CTAs, summed by the
+    fix-up kernel) against one CTA per tile, with aligned and unaligned A."""
+    from roofline_gb300 import gemm
+    monkeypatch.setenv("GEMM_TC_STREAMK", streamk)
+    M, N, K = shape
+    for pad in (0, 1):
+        p = gemm.plan(M, N, K, K + pad, N, N, mode="tf32x3")
+        if streamk == "0":
+            assert p["stream_k"] == 0
+        else:
+            assert p["stream_k"] == 1 and p["grid_ctas"] >= 2
+        got, ref, D = _run_shape(M, N, K, "tf32x3", -1.25, 0.5, pad=(pad, 0, 0), offset=0,
+                                 seed=M + pad)
+        assert oracle.err_normalised(got, ref, D) <= TOL_E1
+
+
+def test_tf32x3_stream_k_deterministic():
+    outs = gpu_util.run("ragged", "tf32x3", repeat=3)
+    for o in outs[1:]:
+        assert np.array_equal(o.view(np.uint32), outs[0].view(np.uint32))
