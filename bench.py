@@ -235,7 +235,6 @@ def run_ours(args):
     import torch.distributed as dist
 
     from roofline_gb300 import gemm
-    from roofline_gb300 import roofline as rf
     from workloads import WORKLOADS
 
     rank, world, local = dist_env()
@@ -250,17 +249,8 @@ def run_ours(args):
     w = WORKLOADS[args.workload]
     lda, ldb, ldc = w.lds()
     A, B, C0 = w.make()
-    set_bytes = 4 * (w.M * lda + w.K * ldb + w.M * ldc)
-    nsets = max(2, min(8, -(-3 * L2_BYTES // set_bytes)))
-    sets = []
-    hA, hB = torch.from_numpy(A), torch.from_numpy(B)
-    hC = torch.from_numpy(C0) if C0 is not None else None
-    for _ in range(nsets):
-        dA = hA.to(dev)
-        dB = hB.to(dev)
-        dC = hC.to(dev) if hC is not None else torch.zeros((w.M, ldc), dtype=torch.float32,
-                                                             device=dev)
-        sets.append((dA[:, :w.K], dB[:, :w.N], dC[:, :w.N]))
+    sets, set_bytes = device_sets(w, dev, (A, B, C0))
+    nsets = len(sets)
     rotation = f"inputs rotated over {nsets} buffer sets ({nsets * set_bytes / 2**20:.0f} MiB > L2)"
 
     plan = gemm.plan(w.M, w.N, w.K, lda, ldb, ldc, args.mode, 0, w.beta != 0.0)
@@ -328,31 +318,8 @@ def run_ours(args):
 
     # roofline of the dominant (main GEMM) kernel
     main_avg = statistics.mean(main_ms)
-    kname = plan["kernel_name"]
-    alg_bytes = rf.gemm_bytes(w.M, w.N, w.K, w.beta != 0.0)
-    if plan["bound_name"] == "hbm":
-        roof = {"bound": "hbm", "achieved": rf.gbps(alg_bytes, main_avg), "peak": peaks["hbm_gbs"],
-                "unit": "GB/s"}
-    elif kname == "tc_tf32x3":
-        tf32 = peaks["bf16_tflops"] * TF32_OVER_BF16
-        roof = {"bound": "tensor", "achieved": rf.tflops(flops, main_avg), "peak": tf32 / 3.0,
-                "unit": "TFLOP/s"}
-    else:
-        roof = {"bound": "alu", "achieved": rf.tflops(flops, main_avg),
-                "peak": info["fp32_peak_tflops"], "unit": "TFLOP/s"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    traffic, tnote = ncu_traffic(f"{kname}:{w.name}")
-    roof["traffic"] = traffic
-    roof["kernel"] = kname
-    roof["kernel_ms"] = main_avg
+    roof = roofline_for(plan, w, main_avg, info, peaks, peaks_src)
     roof["kernel_timing"] = f"mean of {nk} launches, CUDA events recorded around the kernel on its stream"
-    roof["algorithmic"] = (f"{alg_bytes} B" if roof["unit"] == "GB/s" else f"{flops:.0f} FLOP") + \
-        " per launch"
-    roof["peak_source"] = {"alu": "SMs x 128 FP32 lanes x 2 x max SM clock (device attributes)",
-                           "tensor": f"{peaks_src} bf16 burst x {TF32_OVER_BF16:.3f} (dense TF32/BF16 "
-                                     "nominal ratio) / 3 (three TF32 products per FP32 product)",
-                           "hbm": f"{peaks_src} copy bandwidth"}[roof["bound"]]
-    roof["traffic_note"] = tnote
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -360,8 +327,9 @@ def run_ours(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded SplitMix64 inputs, workload shapes and distributions)",
         "config": workload_config(w, args.mode, rotation),
-        "plan": {k: plan[k] for k in ("kernel_name", "bm", "bn", "bk", "split_k", "vec",
-                                      "launches", "grid_ctas", "bound_name")},
+        "plan": {k: plan[k] for k in ("kernel_name", "bm", "bn", "bk", "stages", "split_k",
+                                      "stream_k", "a_split_in_kernel", "b_concat", "vec",
+                                      "launches", "grid_ctas", "ctas_per_sm", "bound_name")},
         "gpu_launches": args.steps * int(plan["launches"]),
         "roofline": roof,
         "clocks": clocks,
@@ -380,7 +348,7 @@ def run_ours(args):
         line["e2e"] = e2e(args, w, A, B, C0, sets[0], dev, world)
 
     if rank == 0 and not args.no_extras:
-        line["extras"] = extras(args, w, sets, info, peaks)
+        line["extras"] = extras(args, w, sets, info, peaks, peaks_src)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(A, B, C0, w)
     if rank == 0:
@@ -455,32 +423,128 @@ def time_steps(fn, steps, warmup):
     return e0.elapsed_time(e1) / steps
 
 
-def extras(args, w, sets, info, peaks):
-    """Per-mode figures on the same workload, the HBM copy roof, and cuBLAS
-    reference points (timed beside the library, never inside it)."""
+def roofline_for(plan, w, kernel_ms, info, peaks, peaks_src):
+    """Roofline record of the main kernel of `plan` on workload `w`."""
+    from roofline_gb300 import roofline as rf
+    flops = float(w.flops)
+    alg_bytes = rf.gemm_bytes(w.M, w.N, w.K, w.beta != 0.0)
+    kname = plan["kernel_name"]
+    if plan["bound_name"] == "hbm":
+        roof = {"bound": "hbm", "achieved": rf.gbps(alg_bytes, kernel_ms),
+                "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    elif kname == "tc_tf32x3":
+        roof = {"bound": "tensor", "achieved": rf.tflops(flops, kernel_ms),
+                "peak": peaks["bf16_tflops"] * TF32_OVER_BF16 / 3.0, "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "alu", "achieved": rf.tflops(flops, kernel_ms),
+                "peak": info["fp32_peak_tflops"], "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    traffic, tnote = ncu_traffic(f"{kname}:{w.name}")
+    roof["traffic"] = traffic
+    roof["kernel"] = kname
+    roof["kernel_ms"] = kernel_ms
+    roof["algorithmic"] = (f"{alg_bytes} B" if roof["unit"] == "GB/s" else f"{flops:.0f} FLOP") + \
+        " per launch"
+    roof["peak_source"] = {"alu": "SMs x 128 FP32 lanes x 2 x max SM clock (device attributes)",
+                           "tensor": f"{peaks_src} bf16 burst x {TF32_OVER_BF16:.3f} (dense TF32/BF16 "
+                                     "nominal ratio) / 3 (three TF32 products per FP32 product)",
+                           "hbm": f"{peaks_src} copy bandwidth"}[roof["bound"]]
+    roof["traffic_note"] = tnote
+    return roof
+
+
+def measure(w, mode, sets, steps, warmup=3):
+    """(mean step ms, mean main-kernel ms, plan) for `steps` library calls."""
     import torch
 
     from roofline_gb300 import gemm
+    n = len(sets)
+    plan = gemm.plan(w.M, w.N, w.K, *w.lds(), mode, 0, w.beta != 0.0)
+
+    def fn(i):
+        a, b, c = sets[i % n]
+        gemm.matmul(a, b, c, w.alpha, w.beta, mode)
+    step_ms = time_steps(fn, steps, warmup)
+    s = torch.cuda.current_stream()
+    eb = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ea = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for e in eb + ea:
+        e.record(s)
+    torch.cuda.synchronize()
+    for i in range(steps):
+        gemm.set_profile_events(eb[i], ea[i])
+        fn(i)
+    gemm.set_profile_events(None, None)
+    torch.cuda.synchronize()
+    kernel_ms = statistics.mean(eb[i].elapsed_time(ea[i]) for i in range(steps))
+    return step_ms, kernel_ms, plan
+
+
+def device_sets(w, dev, arrays=None, min_sets=2):
+    """Device copies of the workload's inputs, enough sets to exceed L2 three times."""
+    import torch
+    A, B, C0 = arrays if arrays is not None else w.make()
+    lda, ldb, ldc = w.lds()
+    set_bytes = 4 * (w.M * lda + w.K * ldb + w.M * ldc)
+    nsets = max(min_sets, min(8, -(-3 * L2_BYTES // set_bytes)))
+    hA, hB = torch.from_numpy(A), torch.from_numpy(B)
+    hC = torch.from_numpy(C0) if C0 is not None else None
+    sets = []
+    for _ in range(nsets):
+        dA, dB = hA.to(dev), hB.to(dev)
+        dC = hC.to(dev) if hC is not None else torch.zeros((w.M, ldc), dtype=torch.float32,
+                                                           device=dev)
+        sets.append((dA[:, :w.K], dB[:, :w.N], dC[:, :w.N]))
+    return sets, set_bytes
+
+
+def extras(args, w, sets, info, peaks, peaks_src):
+    """Both modes on the same workload, the other large workloads, the FMA and
+    HBM copy roofs, and cuBLAS reference points (timed beside the library,
+    never inside it)."""
+    import torch
+
+    from roofline_gb300 import gemm
+    from workloads import WORKLOADS
     out = {}
     n = len(sets)
     for mode in ["fp32_simt", "tf32x3"]:
         try:
-            p = gemm.plan(w.M, w.N, w.K, *w.lds(), mode, 0, w.beta != 0.0)
+            step_ms, kernel_ms, p = measure(w, mode, sets, 20)
         except gemm.GemmError as e:
             out[mode] = {"unavailable": str(e)}
             continue
-
-        def fn(i, mode=mode):
-            a, b, c = sets[i % n]
-            gemm.matmul(a, b, c, w.alpha, w.beta, mode)
-        ms = time_steps(fn, 50, 5)
-        tf = float(w.flops) / (ms * 1e-3) / 1e12
-        r = {"tflops": tf, "ms": ms, "kernel": p["kernel_name"], "split_k": p["split_k"]}
-        if mode == "fp32_simt":
-            r["pct_fp32_peak"] = 100.0 * tf / info["fp32_peak_tflops"]
-        else:
-            r["pct_third_tf32_peak"] = 100.0 * tf / (peaks["bf16_tflops"] * TF32_OVER_BF16 / 3.0)
-        out[mode] = r
+        out[mode] = {"tflops": float(w.flops) / (step_ms * 1e-3) / 1e12, "ms": step_ms,
+                     "kernel": p["kernel_name"], "kernel_ms": kernel_ms,
+                     "roofline_frac": roofline_for(p, w, kernel_ms, info, peaks, peaks_src)["frac"]}
+    # the other large workloads: a short timing per mode
+    for name, modes in [("sq8192", ["auto", "fp32_simt"]), ("skinny", ["auto"])]:
+        if name == w.name:
+            continue
+        wl = WORKLOADS[name]
+        try:
+            wsets, _ = device_sets(wl, torch.device("cuda"))
+            res = {}
+            for mode in modes:
+                steps = 5 if (name == "sq8192" and mode == "fp32_simt") else 20
+                step_ms, kernel_ms, p = measure(wl, mode, wsets, steps)
+                r = roofline_for(p, wl, kernel_ms, info, peaks, peaks_src)
+                res[mode] = {"tflops": float(wl.flops) / (step_ms * 1e-3) / 1e12, "ms": step_ms,
+                             "kernel": p["kernel_name"], "kernel_ms": kernel_ms,
+                             "roofline": {k: r[k] for k in ("bound", "achieved", "peak", "unit",
+                                                            "frac")}}
+            out[name] = res
+            del wsets
+            torch.cuda.empty_cache()
+        except Exception as e:  # pragma: no cover
+            out[name] = {"failed": str(e)}
+    # FP32 FMA roof, measured ("Bandwidths and peak rate - exercises", exercise 5)
+    try:
+        out["fp32_fma_peak_tflops"] = {"scalar": gemm.fp32_fma_peak(1 << 16, False),
+                                       "packed": gemm.fp32_fma_peak(1 << 16, True),
+                                       "derived": info["fp32_peak_tflops"]}
+    except Exception as e:  # pragma: no cover
+        out["fp32_fma_peak_tflops"] = f"failed: {e}"
     # HBM copy calibration: 2 x 256M floats (1 GiB each), 50 timed copies
     try:
         src = torch.ones(256 << 20, dtype=torch.float32, device="cuda")
@@ -490,7 +554,6 @@ def extras(args, w, sets, info, peaks):
     except Exception as e:  # pragma: no cover
         out["hbm_copy_gbs"] = f"failed: {e}"
     # cuBLAS through torch, FP32 (no TF32) and TF32, same inputs
-    a, b, c = sets[0]
     old = torch.backends.cuda.matmul.allow_tf32
     try:
         for tag, tf32 in [("torch_fp32", False), ("torch_tf32", True)]:

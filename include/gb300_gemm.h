@@ -191,6 +191,23 @@ GEMM_API int hbm_copy_calibrate(const float *src, float *dst, size_t n, int iter
                        cudaStream_t stream, double *gbps_out);
 
 /*
+ * fp32_fma_peak -- measures the FP32 FMA throughput of the CUDA cores with a
+ * register-only kernel ("Bandwidths and peak rate - exercises", exercise 5:
+ * long chains acc = acc * x + y, several independent chains per thread,
+ * FLOP = threads x iterations x chains x 2).  packed = 1 uses the f32x2 FMA
+ * (two lanes per instruction), 0 the scalar FMA.  One untimed warm-up
+ * launch, then one launch of `iters` iterations timed with CUDA events on
+ * `stream`; blocks until it finishes.  sink: device buffer of at least
+ * fp32_fma_peak_sink_floats() floats (receives each thread's result).
+ * *tflops_out = FLOP / seconds / 1e12.
+ */
+GEMM_API int fp32_fma_peak(int64_t iters, int packed, float *sink, cudaStream_t stream,
+                           double *tflops_out);
+
+/* Floats fp32_fma_peak writes to its sink on the current device. */
+GEMM_API int64_t fp32_fma_peak_sink_floats(void);
+
+/*
  * gemm_device_info -- SM count, clocks, register/shared-memory/L2/HBM sizes
  * of device `dev` (the device-property program of "Memory hierarchy in
  * hardware - solutions", exercise 1) and the FP32 CUDA-core peak derived as

@@ -327,6 +327,41 @@ int hbm_copy_calibrate(const float *src, float *dst, size_t n, int iters, cudaSt
   return GEMM_OK;
 }
 
+int64_t fp32_fma_peak_sink_floats(void) {
+  return (int64_t)fma_peak_blocks(current_props().sm_count) * 256;
+}
+
+int fp32_fma_peak(int64_t iters, int packed, float *sink, cudaStream_t stream,
+                  double *tflops_out) {
+  if (!sink || !tflops_out || iters < 1) return GEMM_ERR_INVALID_ARG;
+  int dev = -1;
+  int st = current_device(&dev);
+  if (st != GEMM_OK) return st;
+  const int sms = props_of(dev).sm_count;
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) {
+    cudaGetLastError();
+    if (e0) cudaEventDestroy(e0);
+    return GEMM_ERR_CUDA;
+  }
+  double flops = 0.0;
+  cudaError_t e = launch_fma_peak(iters < 1024 ? iters : 1024, packed, sms, sink, stream, &flops);
+  if (e == cudaSuccess) e = cudaEventRecord(e0, stream);
+  if (e == cudaSuccess) e = launch_fma_peak(iters, packed, sms, sink, stream, &flops);
+  if (e == cudaSuccess) e = cudaEventRecord(e1, stream);
+  if (e == cudaSuccess) e = cudaEventSynchronize(e1);
+  float ms = 0.f;
+  if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, e0, e1);
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  if (e != cudaSuccess || ms <= 0.f) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+  *tflops_out = flops / ((double)ms * 1e-3) / 1e12;
+  return GEMM_OK;
+}
+
 int gemm_check_status(cudaStream_t stream) {
   if (cudaStreamSynchronize(stream) != cudaSuccess) {
     cudaGetLastError();

@@ -65,6 +65,9 @@ cudaError_t launch_splitk_reduce(const GemmArgs &p, const float *ws, int splits,
                                  cudaStream_t s);
 cudaError_t launch_copy(const float *src, float *dst, size_t n, int sm_count,
                         cudaStream_t s);
+int fma_peak_blocks(int sm_count);
+cudaError_t launch_fma_peak(int64_t iters, int packed, int sm_count, float *sink, cudaStream_t s,
+                            double *flops);
 // Tensor-core path (tc_tf32x3.cu).  Returns a GEMM_* status.
 int launch_tc(const gemm_plan_t &plan, const GemmArgs &p, void *ws, size_t ws_bytes,
               cudaStream_t s);

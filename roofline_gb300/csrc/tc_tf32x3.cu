@@ -639,38 +639,56 @@ streamk_fixup_kernel(TcParams p, int BN, int64_t G) {
   }
   __syncthreads();
   const int n = nparts;
-  const int64_t m0 = (t / p.tiles_n) * kBM;
+  // blockIdx.y picks 32 of the tile's 128 rows; each thread keeps four
+  // independent 16-byte sums so several loads are in flight
+  const int64_t m0 = (t / p.tiles_n) * kBM + blockIdx.y * 32;
   const int64_t n0 = (t % p.tiles_n) * BN;
+  const int64_t row0 = (int64_t)blockIdx.y * 32 * BN;  // offset of these rows in a part
   const bool vec = ((p.ldc & 3) == 0) && ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0);
-  for (int e = threadIdx.x * 4; e < kBM * BN; e += blockDim.x * 4) {
-    const int r = e / BN, col = e % BN;
-    const int64_t gr = m0 + r, gc = n0 + col;
-    if (gr >= p.M || gc >= p.N) continue;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int span = 32 * BN;
+  for (int e0 = threadIdx.x * 4; e0 < span; e0 += blockDim.x * 16) {
+    float4 acc[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int i = 0; i < n; ++i) {
-      const float4 v = *reinterpret_cast<const float4 *>(p.partial + part_off[i] + e);
-      acc.x += v.x;
-      acc.y += v.y;
-      acc.z += v.z;
-      acc.w += v.w;
-    }
-    float *dst = p.C + gr * p.ldc + gc;
-    const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
-    if (vec && gc + 4 <= p.N) {
-      float4 o = make_float4(p.alpha * a4[0], p.alpha * a4[1], p.alpha * a4[2], p.alpha * a4[3]);
-      if (p.beta != 0.0f) {
-        const float4 old = *reinterpret_cast<const float4 *>(dst);
-        o.x = fmaf(p.beta, old.x, o.x);
-        o.y = fmaf(p.beta, old.y, o.y);
-        o.z = fmaf(p.beta, old.z, o.z);
-        o.w = fmaf(p.beta, old.w, o.w);
+      const float *base = p.partial + part_off[i] + row0;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int e = e0 + u * blockDim.x * 4;
+        if (e < span) {
+          const float4 v = *reinterpret_cast<const float4 *>(base + e);
+          acc[u].x += v.x;
+          acc[u].y += v.y;
+          acc[u].z += v.z;
+          acc[u].w += v.w;
+        }
       }
-      *reinterpret_cast<float4 *>(dst) = o;
-    } else {
-      for (int q = 0; q < 4 && gc + q < p.N; ++q) {
-        float o = p.alpha * a4[q];
-        if (p.beta != 0.0f) o = fmaf(p.beta, dst[q], o);
-        dst[q] = o;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int e = e0 + u * blockDim.x * 4;
+      if (e >= span) continue;
+      const int r = e / BN, col = e % BN;
+      const int64_t gr = m0 + r, gc = n0 + col;
+      if (gr >= p.M || gc >= p.N) continue;
+      float *dst = p.C + gr * p.ldc + gc;
+      const float a4[4] = {acc[u].x, acc[u].y, acc[u].z, acc[u].w};
+      if (vec && gc + 4 <= p.N) {
+        float4 o = make_float4(p.alpha * a4[0], p.alpha * a4[1], p.alpha * a4[2], p.alpha * a4[3]);
+        if (p.beta != 0.0f) {
+          const float4 old = *reinterpret_cast<const float4 *>(dst);
+          o.x = fmaf(p.beta, old.x, o.x);
+          o.y = fmaf(p.beta, old.y, o.y);
+          o.z = fmaf(p.beta, old.z, o.z);
+          o.w = fmaf(p.beta, old.w, o.w);
+        }
+        *reinterpret_cast<float4 *>(dst) = o;
+      } else {
+        for (int q = 0; q < 4 && gc + q < p.N; ++q) {
+          float o = p.alpha * a4[q];
+          if (p.beta != 0.0f) o = fmaf(p.beta, dst[q], o);
+          dst[q] = o;
+        }
       }
     }
   }
@@ -923,7 +941,7 @@ int launch_cfg(const gemm_plan_t &plan, const GemmArgs &a, char *ws, cudaStream_
   }
   if (plan.stream_k) {
     cudaLaunchConfig_t fc = {};
-    fc.gridDim = dim3((unsigned)(G - 1));
+    fc.gridDim = dim3((unsigned)(G - 1), kBM / 32);
     fc.blockDim = dim3(256);
     fc.stream = s;
     fc.attrs = attr;

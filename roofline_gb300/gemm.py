@@ -42,7 +42,8 @@ BOUNDS = {0: "none", 1: "fp32", 2: "tf32x3", 3: "hbm"}
 # Every symbol include/gb300_gemm.h declares.
 EXPORTED = ["gemm_f32", "gemm_f32_ex", "gemm_f32_plan", "hbm_copy_f32", "hbm_copy_calibrate",
             "gemm_device_info", "gemm_strerror", "gemm_check_status", "gemm_shutdown",
-            "gemm_abi_version", "gemm_set_profile_events", "gemm_f32_splitk_noalloc"]
+            "gemm_abi_version", "gemm_set_profile_events", "gemm_f32_splitk_noalloc",
+            "fp32_fma_peak", "fp32_fma_peak_sink_floats"]
 
 # size of the static scratch array behind gemm_f32_splitk_noalloc
 NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -137,6 +138,10 @@ def load(path: str | None = None):
         lib.gemm_f32_splitk_noalloc.argtypes = [i64, i64, i64, f32, vp, i64, vp, i64, f32, vp,
                                                 i64, i32, vp]
         lib.gemm_f32_splitk_noalloc.restype = i32
+        lib.fp32_fma_peak.argtypes = [i64, i32, vp, vp, ctypes.POINTER(ctypes.c_double)]
+        lib.fp32_fma_peak.restype = i32
+        lib.fp32_fma_peak_sink_floats.argtypes = []
+        lib.fp32_fma_peak_sink_floats.restype = i64
         if path is None:
             _lib = lib
         return lib
@@ -276,4 +281,16 @@ def hbm_copy_calibrate(src, dst, iters=50, stream=None) -> float:
                                    _stream_handle(stream), ctypes.byref(out))
     if rc != OK:
         raise GemmError(rc, "hbm_copy_calibrate")
+    return out.value
+
+
+def fp32_fma_peak(iters=1 << 16, packed=True, stream=None) -> float:
+    """Measured FP32 FMA throughput of the CUDA cores, TFLOP/s."""
+    import torch
+    sink = torch.empty(load().fp32_fma_peak_sink_floats(), dtype=torch.float32, device="cuda")
+    out = ctypes.c_double(0.0)
+    rc = load().fp32_fma_peak(int(iters), 1 if packed else 0, sink.data_ptr(),
+                              _stream_handle(stream), ctypes.byref(out))
+    if rc != OK:
+        raise GemmError(rc, "fp32_fma_peak")
     return out.value

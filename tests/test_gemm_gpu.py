@@ -297,3 +297,12 @@ def test_tf32x3_stream_k_deterministic():
     outs = gpu_util.run("ragged", "tf32x3", repeat=3)
     for o in outs[1:]:
         assert np.array_equal(o.view(np.uint32), outs[0].view(np.uint32))
+
+
+def test_fma_peak_probe():
+    from roofline_gb300 import gemm
+    d = gemm.device_info(0)
+    for packed in (False, True):
+        tf = gemm.fp32_fma_peak(1 << 14, packed)
+        # the probe cannot beat the derived peak by more than clock noise
+        assert 0.2 * d["fp32_peak_tflops"] < tf < 1.05 * d["fp32_peak_tflops"], (packed, tf)
