@@ -435,6 +435,9 @@ def roofline_for(plan, w, kernel_ms, info, peaks, peaks_src):
     elif kname == "tc_tf32x3":
         roof = {"bound": "tensor", "achieved": rf.tflops(flops, kernel_ms),
                 "peak": peaks["bf16_tflops"] * TF32_OVER_BF16 / 3.0, "unit": "TFLOP/s"}
+    elif kname == "tc_tf32":
+        roof = {"bound": "tensor", "achieved": rf.tflops(flops, kernel_ms),
+                "peak": peaks["bf16_tflops"] * TF32_OVER_BF16, "unit": "TFLOP/s"}
     else:
         roof = {"bound": "alu", "achieved": rf.tflops(flops, kernel_ms),
                 "peak": info["fp32_peak_tflops"], "unit": "TFLOP/s"}
@@ -445,9 +448,11 @@ def roofline_for(plan, w, kernel_ms, info, peaks, peaks_src):
     roof["kernel_ms"] = kernel_ms
     roof["algorithmic"] = (f"{alg_bytes} B" if roof["unit"] == "GB/s" else f"{flops:.0f} FLOP") + \
         " per launch"
+    tensor_src = f"{peaks_src} bf16 burst x {TF32_OVER_BF16:.3f} (dense TF32/BF16 nominal ratio)"
+    if kname == "tc_tf32x3":
+        tensor_src += " / 3 (three TF32 products per FP32 product)"
     roof["peak_source"] = {"alu": "SMs x 128 FP32 lanes x 2 x max SM clock (device attributes)",
-                           "tensor": f"{peaks_src} bf16 burst x {TF32_OVER_BF16:.3f} (dense TF32/BF16 "
-                                     "nominal ratio) / 3 (three TF32 products per FP32 product)",
+                           "tensor": tensor_src,
                            "hbm": f"{peaks_src} copy bandwidth"}[roof["bound"]]
     roof["traffic_note"] = tnote
     return roof

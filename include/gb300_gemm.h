@@ -61,13 +61,17 @@ extern "C" {
  * CUDA cores in IEEE FP32 FMA arithmetic.  TF32X3 runs on the tcgen05
  * tensor cores with each operand split into a TF32 high part and a TF32
  * low part, D = Ahi*Bhi + Ahi*Blo + Alo*Bhi, accumulated in FP32 (FP32
- * accuracy; not bitwise equal to FP32_SIMT).  The remaining modes are the
+ * accuracy; not bitwise equal to FP32_SIMT).  TF32 is one TF32 MMA per
+ * product (operands rounded to TF32, 11 significant bits; FP32
+ * accumulation): about three times the 3xTF32 rate, TF32-accurate only
+ * (error up to about 2^-10 of sum |A||B|).  The remaining modes are the
  * course page's ladder kernels ("Stage 0" naive with x -> row, "Stage 1"
  * coalesced with x -> column, "Stage 2" shared-memory tiles of 16 or 32),
  * kept for comparison. */
 #define GEMM_MODE_AUTO 0
 #define GEMM_MODE_FP32_SIMT 1
 #define GEMM_MODE_TF32X3 2
+#define GEMM_MODE_TF32 3
 #define GEMM_MODE_NAIVE 10
 #define GEMM_MODE_COALESCED 11
 #define GEMM_MODE_TILED16 12
@@ -81,11 +85,13 @@ extern "C" {
 #define GEMM_KERNEL_TILED 4
 #define GEMM_KERNEL_SIMT 5          /* register-tiled CUDA-core SGEMM */
 #define GEMM_KERNEL_TC_TF32X3 6     /* tcgen05 3xTF32 */
+#define GEMM_KERNEL_TC_TF32 7       /* tcgen05 1xTF32 */
 
 /* governing roof predicted by the planner */
 #define GEMM_BOUND_FP32 1           /* FP32 CUDA-core FMA peak */
 #define GEMM_BOUND_TF32X3 2         /* one third of the dense TF32 tensor peak */
 #define GEMM_BOUND_HBM 3            /* HBM bandwidth */
+#define GEMM_BOUND_TF32 4           /* the dense TF32 tensor peak */
 
 typedef struct gemm_plan {
   int32_t mode;            /* resolved mode, never GEMM_MODE_AUTO */

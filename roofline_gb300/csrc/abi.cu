@@ -277,6 +277,7 @@ int gemm_f32_ex(int64_t M, int64_t N, int64_t K, float alpha, const float *A, in
     case GEMM_KERNEL_SIMT:
       return to_status(launch_simt(plan, p, static_cast<float *>(ws), stream));
     case GEMM_KERNEL_TC_TF32X3:
+    case GEMM_KERNEL_TC_TF32:
       return launch_tc(plan, p, ws, wsb, stream);
     default:
       return GEMM_ERR_UNSUPPORTED;

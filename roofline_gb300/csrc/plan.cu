@@ -25,7 +25,7 @@ constexpr int kFp32LanesPerSm = 128;
 
 bool mode_known(int mode) {
   switch (mode) {
-    case GEMM_MODE_AUTO: case GEMM_MODE_FP32_SIMT: case GEMM_MODE_TF32X3:
+    case GEMM_MODE_AUTO: case GEMM_MODE_FP32_SIMT: case GEMM_MODE_TF32X3: case GEMM_MODE_TF32:
     case GEMM_MODE_NAIVE: case GEMM_MODE_COALESCED: case GEMM_MODE_TILED16:
     case GEMM_MODE_TILED32:
       return true;
@@ -161,10 +161,13 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
       if (ceil_div(M, 64) > 65535) return GEMM_ERR_UNSUPPORTED;
       plan_simt(M, N, K, vec, dp, fp32_peak, &p);
       break;
-    case GEMM_MODE_TF32X3: {
+    case GEMM_MODE_TF32X3:
+    case GEMM_MODE_TF32: {
       if (!tc_supported(dp)) return GEMM_ERR_UNSUPPORTED;
       if (ceil_div(M, 128) > 65535) return GEMM_ERR_UNSUPPORTED;
-      p.kernel = GEMM_KERNEL_TC_TF32X3;
+      const bool x3 = resolved == GEMM_MODE_TF32X3;
+      const int nprod = x3 ? 3 : 1;
+      p.kernel = x3 ? GEMM_KERNEL_TC_TF32X3 : GEMM_KERNEL_TC_TF32;
       p.bm = 128;
       p.threads = 192;
       p.vec = vec ? 1 : 0;
@@ -181,7 +184,15 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
       auto set = [&](int bn, int bk, int st, int cc) {
         p.bn = bn; p.bk = bk; p.stages = st; p.b_concat = cc;
       };
-      if (a_aligned) {
+      if (!x3) {
+        // 1xTF32: no A_lo / B_lo, so more stages fit
+        if (a_aligned) {
+          if (N <= 64) set(64, 32, 4, 0);
+          else set(256, 16, 8, 0);
+        } else {
+          set(256, 16, 8, 0);
+        }
+      } else if (a_aligned) {
         if (N <= 64) set(64, 32, 3, 1);        // narrow: 2 CTAs per SM stream A
         else if (wide) set(256, 16, 5, 0);
         else set(128, 32, 4, 1);
@@ -195,13 +206,13 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
       if (const char *cfg = std::getenv("GEMM_TC_CONFIG")) {
         int bn = 0, bk = 0, st = 0, ak = 0, cc = 0;
         if (std::sscanf(cfg, "%d,%d,%d,%d,%d", &bn, &bk, &st, &ak, &cc) == 5 &&
-            tc_config_valid(bn, bk, st, ak, cc) && (!ak || a_aligned)) {
+            tc_config_valid(bn, bk, st, ak, cc, nprod) && (!ak || a_aligned)) {
           set(bn, bk, st, cc);
           p.a_split_in_kernel = ak;
           p.launches = ak ? 2 : 3;
         }
       }
-      p.ctas_per_sm = tc_ctas_per_sm(p.bn, p.bk, p.stages, p.a_split_in_kernel, p.b_concat,
+      p.ctas_per_sm = tc_ctas_per_sm(p.bn, p.bk, p.stages, p.a_split_in_kernel, p.b_concat, nprod,
                                      dp.smem_per_sm > 0 ? dp.smem_per_sm : 233472);
       // Stream-K: when the tiles do not fill whole waves of resident CTAs,
       // launch one wave of persistent CTAs that split the (tile, K block)
@@ -235,6 +246,9 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
   if (p.kernel == GEMM_KERNEL_TC_TF32X3) {
     compute_roof = kPlanTf32DenseFlops / 3.0;
     compute_bound = GEMM_BOUND_TF32X3;
+  } else if (p.kernel == GEMM_KERNEL_TC_TF32) {
+    compute_roof = kPlanTf32DenseFlops;
+    compute_bound = GEMM_BOUND_TF32;
   }
   const double ridge = compute_roof / kPlanHbmBytesPerSec;
   p.bound = p.intensity < ridge ? GEMM_BOUND_HBM : compute_bound;

@@ -294,19 +294,23 @@ __device__ __forceinline__ bool next_segment(int64_t &u, int64_t u1, int num_kb,
 // and A_lo come pre-split from the workspace.  CONCAT: B_hi and B_lo sit
 // next to each other in the stage, so A_hi*[B_hi | B_lo] is one MMA of width
 // 2*BN into two accumulators that the epilogue adds.
-template <int BN, int BK, int STAGES, bool AK, bool CONCAT>
+template <int BN, int BK, int STAGES, bool AK, bool CONCAT, int NPROD>
 struct TcCfg {
+  static_assert(NPROD == 3 || NPROD == 1, "3xTF32 or 1xTF32");
+  static_assert(NPROD == 3 || !CONCAT, "1xTF32 has no B_lo to concatenate");
+  static constexpr bool X3 = NPROD == 3;
   static constexpr int A_BYTES = kBM * BK * 4;
   static constexpr int B_BYTES = BN * BK * 4;
-  static constexpr int A_SMEM = AK ? A_BYTES : 2 * A_BYTES;
-  static constexpr int STAGE_BYTES = A_SMEM + 2 * B_BYTES;
+  static constexpr int A_SMEM = (AK || !X3) ? A_BYTES : 2 * A_BYTES;  // A (raw/hi) [+ A_lo]
+  static constexpr int B_SMEM = X3 ? 2 * B_BYTES : B_BYTES;           // B_hi [+ B_lo]
+  static constexpr int STAGE_BYTES = A_SMEM + B_SMEM;
   static constexpr int TX_BYTES = STAGE_BYTES;
   static constexpr int ROW_BYTES = BK * 4;              // 64 or 128
   static constexpr uint32_t LAYOUT = ROW_BYTES == 128 ? 2u : 4u;
   static constexpr uint32_t SBO = 8 * ROW_BYTES;        // 8-row group stride
   static constexpr int ACC_COLS = CONCAT ? 2 * BN : BN;
   static constexpr int LO_COL0 = ACC_COLS;
-  static constexpr int LO_COLS = AK ? STAGES * BK : 0;
+  static constexpr int LO_COLS = (AK && X3) ? STAGES * BK : 0;
   static constexpr int TMEM_NEED = ACC_COLS + LO_COLS;
   static constexpr int TMEM_COLS = TMEM_NEED <= 32    ? 32
                                    : TMEM_NEED <= 64  ? 64
@@ -320,13 +324,14 @@ struct TcCfg {
   static_assert(TMEM_NEED <= 512, "tensor memory");
 };
 
-template <int BN, int BK, int STAGES, bool AK, bool CONCAT>
+template <int BN, int BK, int STAGES, bool AK, bool CONCAT, int NPROD>
 __global__ void __launch_bounds__(kThreadsTC, 1)
 tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
                  const __grid_constant__ CUtensorMap tmA_lo,
                  const __grid_constant__ CUtensorMap tmB_hi,
                  const __grid_constant__ CUtensorMap tmB_lo, TcParams p) {
-  using Cfg = TcCfg<BN, BK, STAGES, AK, CONCAT>;
+  using Cfg = TcCfg<BN, BK, STAGES, AK, CONCAT, NPROD>;
+  constexpr bool X3 = Cfg::X3;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
@@ -366,8 +371,8 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmA_hi);
     prefetch_tmap(&tmB_hi);
-    prefetch_tmap(&tmB_lo);
-    if (!AK) prefetch_tmap(&tmA_lo);
+    if (X3) prefetch_tmap(&tmB_lo);
+    if (!AK && X3) prefetch_tmap(&tmA_lo);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
@@ -400,9 +405,9 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
           mbar_expect_tx(&full[s], Cfg::TX_BYTES);
           const int32_t kx = kb * BK;
           tma_load_2d(a_hi(s), &tmA_hi, &full[s], kx, m0);
-          if (!AK) tma_load_2d(a_lo(s), &tmA_lo, &full[s], kx, m0);
+          if (!AK && X3) tma_load_2d(a_lo(s), &tmA_lo, &full[s], kx, m0);
           tma_load_2d(b_hi(s), &tmB_hi, &full[s], kx, n0);
-          tma_load_2d(b_lo(s), &tmB_lo, &full[s], kx, n0);
+          if (X3) tma_load_2d(b_lo(s), &tmB_lo, &full[s], kx, n0);
           ++issued;
         }
       }
@@ -448,7 +453,9 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
             const uint64_t dah = smem_desc(ah + off, Cfg::SBO, Cfg::LAYOUT);
             const uint64_t dbh = smem_desc(bh + off, Cfg::SBO, Cfg::LAYOUT);
             const uint32_t acc = (kb > sg.kb0 || kk > 0) ? 1u : 0u;
-            if (CONCAT) {
+            if (!X3) {
+              mma_tf32(tmem_base, dah, dbh, idesc, acc);  // 1xTF32: A_hi * B_hi only
+            } else if (CONCAT) {
               // columns [0, BN): A_hi*B_hi (+ A_lo*B_hi); [BN, 2BN): A_hi*B_lo
               mma_tf32(tmem_base, dah, dbh, idesc2, acc);
               if (AK)
@@ -504,6 +511,25 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
           // Row `row` of the landed tile: 16-byte chunk c sits at chunk
           // c ^ f(row) of its 64- or 128-byte line (the TMA swizzle).
           uint8_t *line = a_hi(s) + row * Cfg::ROW_BYTES;
+          if (!X3) {
+            // 1xTF32: round in place, nothing goes to tensor memory.  Chunks
+            // are visited in swizzled order so a warp's 32 rows hit 32
+            // different banks.
+#pragma unroll
+            for (int c = 0; c < BK / 4; ++c) {
+              const int phys = (BK == 32) ? (c ^ (row & 7)) : (c ^ ((row >> 1) & 3));
+              float4 *ptr = reinterpret_cast<float4 *>(line + phys * 16);
+              float4 x = *ptr;
+              x.x = tf32_rna(x.x);
+              x.y = tf32_rna(x.y);
+              x.z = tf32_rna(x.z);
+              x.w = tf32_rna(x.w);
+              *ptr = x;
+            }
+            fence_async_smem();
+            mbar_arrive(&conv[s]);
+            continue;
+          }
           uint32_t lo[BK];
 #pragma unroll
           for (int c = 0; c < BK / 4; ++c) {
@@ -696,7 +722,8 @@ streamk_fixup_kernel(TcParams p, int BN, int64_t G) {
 
 // ------------------------------------------------------------------ split pass
 
-// dst_hi/dst_lo (rows x kp, row-major) <- split of src (rows x k, ld), zero for k <= c < kp.
+// dst_hi/dst_lo (rows x kp, row-major) <- split of src (rows x k, ld), zero for k <= c < kp
+// (lo == nullptr: the hi part only, for 1xTF32).
 __global__ void split_rows_kernel(const float *__restrict__ src, int64_t ld, int64_t rows,
                                   int64_t k, int64_t kp, float *__restrict__ hi,
                                   float *__restrict__ lo) {
@@ -716,7 +743,7 @@ __global__ void split_rows_kernel(const float *__restrict__ src, int64_t ld, int
     h.z = tf32_rna(v[2]); l.z = tf32_rna(v[2] - h.z);
     h.w = tf32_rna(v[3]); l.w = tf32_rna(v[3] - h.w);
     *reinterpret_cast<float4 *>(hi + r * kp + c) = h;
-    *reinterpret_cast<float4 *>(lo + r * kp + c) = l;
+    if (lo) *reinterpret_cast<float4 *>(lo + r * kp + c) = l;
   }
 }
 
@@ -783,7 +810,7 @@ split_transpose_kernel(const float *__restrict__ src, int64_t ld, int64_t k, int
       h.z = tf32_rna(a2); l.z = tf32_rna(a2 - h.z);
       h.w = tf32_rna(a3); l.w = tf32_rna(a3 - h.w);
       *reinterpret_cast<float4 *>(hi + nn * kp + kk) = h;
-      *reinterpret_cast<float4 *>(lo + nn * kp + kk) = l;
+      if (lo) *reinterpret_cast<float4 *>(lo + nn * kp + kk) = l;
     }
   }
 }
@@ -841,29 +868,32 @@ struct WsLayout {
 // Workspace regions: A_hi, A_lo (unless A is split in the kernel), B_hi,
 // B_lo (transposed), then for stream-K the partial tiles (2 per CTA).
 WsLayout ws_layout(int64_t M, int64_t N, int64_t K, bool a_inkernel, int64_t streamk_ctas,
-                   int bn) {
+                   int bn, bool x3) {
   WsLayout w{};
   w.kp = round_up(K, 4);
   const uint64_t a_bytes = a_inkernel ? 0 : align256((uint64_t)M * w.kp * 4);
+  const uint64_t a_lo_bytes = x3 ? a_bytes : 0;
   const uint64_t b_bytes = align256((uint64_t)N * w.kp * 4);
+  const uint64_t b_lo_bytes = x3 ? b_bytes : 0;
   w.a_hi = 0;
   w.a_lo = a_bytes;
-  w.b_hi = 2 * a_bytes;
-  w.b_lo = 2 * a_bytes + b_bytes;
-  w.partial = 2 * a_bytes + 2 * b_bytes;
+  w.b_hi = a_bytes + a_lo_bytes;
+  w.b_lo = w.b_hi + b_bytes;
+  w.partial = w.b_lo + b_lo_bytes;
   w.total = w.partial + (uint64_t)streamk_ctas * 2 * kBM * bn * 4;
   return w;
 }
 
-template <int BN, int BK, int STAGES, bool AK, bool CONCAT>
+template <int BN, int BK, int STAGES, bool AK, bool CONCAT, int NPROD>
 int launch_cfg(const gemm_plan_t &plan, const GemmArgs &a, char *ws, cudaStream_t s) {
-  using Cfg = TcCfg<BN, BK, STAGES, AK, CONCAT>;
+  using Cfg = TcCfg<BN, BK, STAGES, AK, CONCAT, NPROD>;
+  constexpr bool X3 = Cfg::X3;
   const int64_t tiles_m = ceil_div(a.M, kBM), tiles_n = ceil_div(a.N, BN);
   const int64_t tiles = tiles_m * tiles_n;
   const int num_kb = (int)ceil_div(a.K, BK);
   const int64_t G = plan.stream_k ? plan.grid_ctas : tiles;
   if (G < 1 || G > 0x7fffffff || tiles > 0x7fffffff) return GEMM_ERR_UNSUPPORTED;
-  const WsLayout L = ws_layout(a.M, a.N, a.K, AK, plan.stream_k ? G : 0, BN);
+  const WsLayout L = ws_layout(a.M, a.N, a.K, AK, plan.stream_k ? G : 0, BN, X3);
   float *ahi = reinterpret_cast<float *>(ws + L.a_hi);
   float *alo = reinterpret_cast<float *>(ws + L.a_lo);
   float *bhi = reinterpret_cast<float *>(ws + L.b_hi);
@@ -874,12 +904,14 @@ int launch_cfg(const gemm_plan_t &plan, const GemmArgs &a, char *ws, cudaStream_
     int64_t groups = a.M * (L.kp / 4);
     int64_t blocks = ceil_div(groups, 256);
     if (blocks > 152 * 16) blocks = 152 * 16;
-    split_rows_kernel<<<(unsigned)blocks, 256, 0, s>>>(a.A, a.lda, a.M, a.K, L.kp, ahi, alo);
+    split_rows_kernel<<<(unsigned)blocks, 256, 0, s>>>(a.A, a.lda, a.M, a.K, L.kp, ahi,
+                                                        X3 ? alo : nullptr);
   }
   {
     const int vec = ((a.ldb & 3) == 0 && (reinterpret_cast<uintptr_t>(a.B) & 15) == 0) ? 1 : 0;
     dim3 grid((unsigned)ceil_div(a.N, kTrN), (unsigned)ceil_div(L.kp, kTrK));
-    split_transpose_kernel<<<grid, 256, 0, s>>>(a.B, a.ldb, a.K, a.N, L.kp, vec, bhi, blo);
+    split_transpose_kernel<<<grid, 256, 0, s>>>(a.B, a.ldb, a.K, a.N, L.kp, vec, bhi,
+                                                X3 ? blo : nullptr);
   }
   if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_CUDA;
 
@@ -889,11 +921,13 @@ int launch_cfg(const gemm_plan_t &plan, const GemmArgs &a, char *ws, cudaStream_
     ok = encode_2d(&tA0, a.A, a.K, a.M, a.lda, BK, kBM);
     tA1 = tA0;
   } else {
-    ok = encode_2d(&tA0, ahi, L.kp, a.M, L.kp, BK, kBM) &&
-         encode_2d(&tA1, alo, L.kp, a.M, L.kp, BK, kBM);
+    ok = encode_2d(&tA0, ahi, L.kp, a.M, L.kp, BK, kBM);
+    tA1 = tA0;
+    if (X3) ok = ok && encode_2d(&tA1, alo, L.kp, a.M, L.kp, BK, kBM);
   }
-  ok = ok && encode_2d(&tB0, bhi, L.kp, a.N, L.kp, BK, BN) &&
-       encode_2d(&tB1, blo, L.kp, a.N, L.kp, BK, BN);
+  ok = ok && encode_2d(&tB0, bhi, L.kp, a.N, L.kp, BK, BN);
+  tB1 = tB0;
+  if (X3) ok = ok && encode_2d(&tB1, blo, L.kp, a.N, L.kp, BK, BN);
   if (!ok) return GEMM_ERR_UNSUPPORTED;
 
   TcParams p;
@@ -911,7 +945,7 @@ int launch_cfg(const gemm_plan_t &plan, const GemmArgs &a, char *ws, cudaStream_
   p.timeout_ns = env_u64("GEMM_DEBUG_WAIT_LIMIT_NS", 2000000000ull);
   p.stall_producer = (int)env_u64("GEMM_DEBUG_STALL_PRODUCER", 0);
 
-  auto kern = tc_tf32x3_kernel<BN, BK, STAGES, AK, CONCAT>;
+  auto kern = tc_tf32x3_kernel<BN, BK, STAGES, AK, CONCAT, NPROD>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Cfg::SMEM_BYTES) != cudaSuccess) {
     cudaGetLastError();
@@ -960,22 +994,25 @@ int launch_cfg(const gemm_plan_t &plan, const GemmArgs &a, char *ws, cudaStream_
 // The tcgen05 kernels are built for sm_103a only.
 bool tc_supported(const DeviceProps &dp) { return dp.cc_major == 10 && dp.cc_minor == 3; }
 
-// Tile configurations the planner may pick:
-// (bn, bk, stages, A split in kernel, concatenated B MMA).
-#define GG_TC_CONFIGS(X)          \
-  X(256, 16, 5, true, false)      \
-  X(128, 32, 4, true, true)       \
-  X(64, 32, 6, true, true)        \
-  X(64, 32, 3, true, true)        \
-  X(64, 32, 2, true, false)       \
-  X(64, 16, 4, true, false)       \
-  X(256, 16, 4, false, false)     \
-  X(128, 16, 3, false, true)
+// Tile configurations the planner may pick: (bn, bk, stages, A split in
+// kernel, concatenated B MMA, TF32 products per FP32 product).
+#define GG_TC_CONFIGS(X)             \
+  X(256, 16, 5, true, false, 3)      \
+  X(128, 32, 4, true, true, 3)       \
+  X(64, 32, 6, true, true, 3)        \
+  X(64, 32, 3, true, true, 3)        \
+  X(64, 32, 2, true, false, 3)       \
+  X(64, 16, 4, true, false, 3)       \
+  X(256, 16, 4, false, false, 3)     \
+  X(128, 16, 3, false, true, 3)      \
+  X(256, 16, 8, true, false, 1)      \
+  X(64, 32, 4, true, false, 1)       \
+  X(256, 16, 8, false, false, 1)
 
-bool tc_config_valid(int bn, int bk, int stages, int a_inkernel, int concat) {
-#define GG_MATCH(BN_, BK_, ST_, AK_, CC_)                                          \
-  if (bn == BN_ && bk == BK_ && stages == ST_ && (a_inkernel != 0) == AK_ && \
-      (concat != 0) == CC_)                                                        \
+bool tc_config_valid(int bn, int bk, int stages, int a_inkernel, int concat, int nprod) {
+#define GG_MATCH(BN_, BK_, ST_, AK_, CC_, NP_)                                       \
+  if (bn == BN_ && bk == BK_ && stages == ST_ && (a_inkernel != 0) == AK_ &&   \
+      (concat != 0) == CC_ && nprod == NP_)                                          \
     return true;
   GG_TC_CONFIGS(GG_MATCH)
 #undef GG_MATCH
@@ -983,14 +1020,15 @@ bool tc_config_valid(int bn, int bk, int stages, int a_inkernel, int concat) {
 }
 
 // CTAs of one configuration that fit on an SM (shared memory and TMEM).
-int tc_ctas_per_sm(int bn, int bk, int stages, int a_inkernel, int concat, int smem_per_sm) {
-#define GG_OCC(BN_, BK_, ST_, AK_, CC_)                                            \
-  if (bn == BN_ && bk == BK_ && stages == ST_ && (a_inkernel != 0) == AK_ && \
-      (concat != 0) == CC_) {                                                      \
-    using C = TcCfg<BN_, BK_, ST_, AK_, CC_>;                                      \
-    int by_smem = smem_per_sm / (C::SMEM_BYTES + 1024);                            \
-    int by_tmem = 512 / C::TMEM_COLS;                                              \
-    return by_smem < by_tmem ? by_smem : by_tmem;                                  \
+int tc_ctas_per_sm(int bn, int bk, int stages, int a_inkernel, int concat, int nprod,
+                   int smem_per_sm) {
+#define GG_OCC(BN_, BK_, ST_, AK_, CC_, NP_)                                         \
+  if (bn == BN_ && bk == BK_ && stages == ST_ && (a_inkernel != 0) == AK_ &&   \
+      (concat != 0) == CC_ && nprod == NP_) {                                        \
+    using C = TcCfg<BN_, BK_, ST_, AK_, CC_, NP_>;                                   \
+    int by_smem = smem_per_sm / (C::SMEM_BYTES + 1024);                              \
+    int by_tmem = 512 / C::TMEM_COLS;                                                \
+    return by_smem < by_tmem ? by_smem : by_tmem;                                    \
   }
   GG_TC_CONFIGS(GG_OCC)
 #undef GG_OCC
@@ -999,7 +1037,7 @@ int tc_ctas_per_sm(int bn, int bk, int stages, int a_inkernel, int concat, int s
 
 uint64_t tc_workspace_bytes(const gemm_plan_t &plan, int64_t M, int64_t N, int64_t K) {
   return ws_layout(M, N, K, plan.a_split_in_kernel != 0, plan.stream_k ? plan.grid_ctas : 0,
-                   plan.bn)
+                   plan.bn, plan.mode != GEMM_MODE_TF32)
       .total;
 }
 
@@ -1011,10 +1049,11 @@ int launch_tc(const gemm_plan_t &plan, const GemmArgs &a, void *ws, size_t ws_by
   if (plan.a_split_in_kernel && ((a.lda & 3) || (reinterpret_cast<uintptr_t>(a.A) & 15)))
     return GEMM_ERR_UNSUPPORTED;
   char *w = static_cast<char *>(ws);
-#define GG_LAUNCH(BN_, BK_, ST_, AK_, CC_)                                              \
-  if (plan.bn == BN_ && plan.bk == BK_ && plan.stages == ST_ &&                         \
-      (plan.a_split_in_kernel != 0) == AK_ && (plan.b_concat != 0) == CC_)              \
-    return launch_cfg<BN_, BK_, ST_, AK_, CC_>(plan, a, w, s);
+  const int nprod = plan.mode == GEMM_MODE_TF32 ? 1 : 3;
+#define GG_LAUNCH(BN_, BK_, ST_, AK_, CC_, NP_)                                          \
+  if (plan.bn == BN_ && plan.bk == BK_ && plan.stages == ST_ &&                          \
+      (plan.a_split_in_kernel != 0) == AK_ && (plan.b_concat != 0) == CC_ && nprod == NP_) \
+    return launch_cfg<BN_, BK_, ST_, AK_, CC_, NP_>(plan, a, w, s);
   GG_TC_CONFIGS(GG_LAUNCH)
 #undef GG_LAUNCH
   return GEMM_ERR_UNSUPPORTED;

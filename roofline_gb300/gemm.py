@@ -19,11 +19,12 @@ from . import build as _build
 MODE_AUTO = 0
 MODE_FP32_SIMT = 1
 MODE_TF32X3 = 2
+MODE_TF32 = 3
 MODE_NAIVE = 10
 MODE_COALESCED = 11
 MODE_TILED16 = 12
 MODE_TILED32 = 13
-MODES = {"auto": MODE_AUTO, "fp32_simt": MODE_FP32_SIMT, "tf32x3": MODE_TF32X3,
+MODES = {"auto": MODE_AUTO, "fp32_simt": MODE_FP32_SIMT, "tf32x3": MODE_TF32X3, "tf32": MODE_TF32,
          "naive": MODE_NAIVE, "coalesced": MODE_COALESCED, "tiled16": MODE_TILED16,
          "tiled32": MODE_TILED32}
 
@@ -36,8 +37,8 @@ ERR_WORKSPACE_TOO_SMALL = -5
 ERR_NO_DEVICE = -6
 
 KERNELS = {0: "none", 1: "scale", 2: "naive", 3: "coalesced", 4: "tiled", 5: "simt",
-           6: "tc_tf32x3"}
-BOUNDS = {0: "none", 1: "fp32", 2: "tf32x3", 3: "hbm"}
+           6: "tc_tf32x3", 7: "tc_tf32"}
+BOUNDS = {0: "none", 1: "fp32", 2: "tf32x3", 3: "hbm", 4: "tf32"}
 
 # Every symbol include/gb300_gemm.h declares.
 EXPORTED = ["gemm_f32", "gemm_f32_ex", "gemm_f32_plan", "hbm_copy_f32", "hbm_copy_calibrate",

@@ -153,3 +153,14 @@ def test_stream_k_plan_bounds(lib):
         total = tiles * -(-K // p["bk"])
         assert 2 <= p["grid_ctas"] <= total // 4
         assert p["grid_ctas"] <= 250 * tiles
+
+
+def test_tf32_mode_plans(lib):
+    p = gemm.plan(4096, 4096, 4096, mode="tf32")
+    assert p["kernel_name"] == "tc_tf32" and p["bound_name"] == "tf32"
+    # B_hi only (no B_lo), plus stream-K partials
+    extra = p["grid_ctas"] * 2 * 128 * p["bn"] * 4 if p["stream_k"] else 0
+    assert p["workspace_bytes"] == 4096 * 4096 * 4 + extra
+    s = gemm.plan(65536, 64, 4096, mode="tf32")
+    assert s["bound_name"] == "hbm" and s["ctas_per_sm"] == 2
+    assert gemm.plan(64, 64, 64, mode="tf32")["mode"] == gemm.MODE_TF32

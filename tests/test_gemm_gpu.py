@@ -306,3 +306,41 @@ def test_fma_peak_probe():
         tf = gemm.fp32_fma_peak(1 << 14, packed)
         # the probe cannot beat the derived peak by more than clock noise
         assert 0.2 * d["fp32_peak_tflops"] < tf < 1.05 * d["fp32_peak_tflops"], (packed, tf)
+
+
+# 1xTF32 mode: each operand rounded to TF32 (11 significant bits, round to
+# nearest, ties away): |x - tf32(x)| <= 2^-11 |x|, so each product is within
+# about 2^-10 of |a||b| and the normalised error stays below 2^-10 plus the
+# FP32 accumulation error; 2e-3 bounds both for the shapes here.
+TOL_TF32 = 2e-3
+TF32_BUILT = ["256,16,8,1,0", "64,32,4,1,0", "256,16,8,0,0"]
+
+
+@pytest.mark.parametrize("cfg", TF32_BUILT)
+@pytest.mark.parametrize("streamk", ["0", "1"])
+def test_tf32_mode_every_configuration(cfg, streamk, monkeypatch):
+    from roofline_gb300 import gemm
+    bn, bk, st, ak, cc = map(int, cfg.split(","))
+    monkeypatch.setenv("GEMM_TC_CONFIG", cfg)
+    monkeypatch.setenv("GEMM_TC_STREAMK", streamk)
+    M, N, K = 777, 200, 300
+    pad = (0 if ak else 1, 0, 0)
+    p = gemm.plan(M, N, K, K + pad[0], N, N, mode="tf32")
+    assert p["kernel_name"] == "tc_tf32"
+    assert (p["bn"], p["bk"], p["stages"], p["a_split_in_kernel"]) == (bn, bk, st, ak)
+    got, ref, D = _run_shape(M, N, K, "tf32", 1.5, 0.5, pad=pad, offset=0, seed=st + bn)
+    e1 = oracle.err_normalised(got, ref, D)
+    assert e1 <= TOL_TF32, e1
+    # integer inputs are exact in TF32: bit-exact
+    got, ref, D = _run_shape(M, N, K, "tf32", 1.0, 0.0, pad=pad, offset=0, seed=7, dist="int2")
+    assert oracle.mismatches(got, ref) == 0
+
+
+@pytest.mark.parametrize("name", ["sq512_int", "ragged", "sq4096", "skinny"])
+def test_tf32_mode_workloads(name):
+    C = gpu_util.run(name, "tf32")
+    r = gpu_util.compare(name, C)
+    if WORKLOADS[name].a_dist == "int2":
+        assert r["mismatches"] == 0, r
+    else:
+        assert r["e1"] <= TOL_TF32, r
