@@ -4,11 +4,14 @@
 // ladder and notes that letting cuBLAS use TF32 would beat the FP32 peak
 // ("Project - tiled matrix multiply", sections "Stage 3 - the reference
 // ceiling: cuBLAS" and "What comes next").  TF32 alone keeps only 11
-// significant bits, so each FP32 operand x is split into two TF32 values,
-//     x_hi = tf32_rna(x),   x_lo = tf32_rna(x - x_hi)   (x - x_hi is exact),
+// significant bits, so each FP32 operand x is split in two,
+//     x_hi = tf32_rna(x)   (exactly a TF32 value),
+//     x_lo = x - x_hi      (exact in FP32; the MMA reads its leading 11
+//                           significant bits, which changes the product by
+//                           at most 2^-21 of |x| |y|),
 // and the product is formed from three TF32 MMAs accumulated in FP32:
 //     A*B ~= A_hi*B_lo + A_lo*B_hi + A_hi*B_hi
-// (the dropped A_lo*B_lo term is below 2^-22 of |A||B|).
+// (the dropped A_lo*B_lo term is below 2^-20 of |A||B|).
 //
 // Kernel structure (one 128 x BN output tile per CTA, 192 threads):
 //   warp 0      TMA producer: one lane streams K-blocks of the operand tiles
@@ -541,10 +544,10 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
             h.y = tf32_rna(x.y);
             h.z = tf32_rna(x.z);
             h.w = tf32_rna(x.w);
-            lo[4 * c + 0] = __float_as_uint(tf32_rna(x.x - h.x));
-            lo[4 * c + 1] = __float_as_uint(tf32_rna(x.y - h.y));
-            lo[4 * c + 2] = __float_as_uint(tf32_rna(x.z - h.z));
-            lo[4 * c + 3] = __float_as_uint(tf32_rna(x.w - h.w));
+            lo[4 * c + 0] = __float_as_uint(x.x - h.x);
+            lo[4 * c + 1] = __float_as_uint(x.y - h.y);
+            lo[4 * c + 2] = __float_as_uint(x.z - h.z);
+            lo[4 * c + 3] = __float_as_uint(x.w - h.w);
             *ptr = h;
           }
           tmem_st<BK>(lane_base + (uint32_t)(Cfg::LO_COL0 + s * BK), lo);
@@ -738,10 +741,10 @@ __global__ void split_rows_kernel(const float *__restrict__ src, int64_t ld, int
 #pragma unroll
     for (int i = 0; i < 4; ++i) v[i] = (c + i < k) ? __ldg(s + i) : 0.0f;
     float4 h, l;
-    h.x = tf32_rna(v[0]); l.x = tf32_rna(v[0] - h.x);
-    h.y = tf32_rna(v[1]); l.y = tf32_rna(v[1] - h.y);
-    h.z = tf32_rna(v[2]); l.z = tf32_rna(v[2] - h.z);
-    h.w = tf32_rna(v[3]); l.w = tf32_rna(v[3] - h.w);
+    h.x = tf32_rna(v[0]); l.x = v[0] - h.x;
+    h.y = tf32_rna(v[1]); l.y = v[1] - h.y;
+    h.z = tf32_rna(v[2]); l.z = v[2] - h.z;
+    h.w = tf32_rna(v[3]); l.w = v[3] - h.w;
     *reinterpret_cast<float4 *>(hi + r * kp + c) = h;
     if (lo) *reinterpret_cast<float4 *>(lo + r * kp + c) = l;
   }
@@ -805,10 +808,10 @@ split_transpose_kernel(const float *__restrict__ src, int64_t ld, int64_t k, int
       float4 h, l;
       const float a0 = tile[kq + 0][nl], a1 = tile[kq + 1][nl];
       const float a2 = tile[kq + 2][nl], a3 = tile[kq + 3][nl];
-      h.x = tf32_rna(a0); l.x = tf32_rna(a0 - h.x);
-      h.y = tf32_rna(a1); l.y = tf32_rna(a1 - h.y);
-      h.z = tf32_rna(a2); l.z = tf32_rna(a2 - h.z);
-      h.w = tf32_rna(a3); l.w = tf32_rna(a3 - h.w);
+      h.x = tf32_rna(a0); l.x = a0 - h.x;
+      h.y = tf32_rna(a1); l.y = a1 - h.y;
+      h.z = tf32_rna(a2); l.z = a2 - h.z;
+      h.w = tf32_rna(a3); l.w = a3 - h.w;
       *reinterpret_cast<float4 *>(hi + nn * kp + kk) = h;
       if (lo) *reinterpret_cast<float4 *>(lo + nn * kp + kk) = l;
     }
