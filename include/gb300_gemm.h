@@ -178,6 +178,51 @@ GEMM_API int gemm_f32_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t
                   int beta_nonzero, gemm_plan_t *out);
 
 /*
+ * gemm_f32_op -- C <- alpha * op(A) * op(B) + beta * C with the storage
+ * order and operand ops of a BLAS SGEMM call.
+ *
+ * The course page's cuBLAS stage ("Project - tiled matrix multiply",
+ * "Stage 3 - the reference ceiling: cuBLAS") calls a column-major library
+ * on row-major data by computing C^T = B^T * A^T with the operands swapped;
+ * this call takes either storage order and either op directly, so callers
+ * with column-major or transposed matrices need no such rewrite.
+ *
+ * layout: GEMM_ROW_MAJOR (X(r,c) = X[r*ld + c]) or GEMM_COL_MAJOR
+ *         (X(r,c) = X[c*ld + r]); applies to A, B and C alike.
+ * op_a, op_b: GEMM_OP_N (op(X) = X) or GEMM_OP_T (op(X) = X^T).
+ * op(A) is M x K, op(B) is K x N, C is M x N.  A is stored as the M x K
+ * matrix (op_a = N) or the K x M matrix (op_a = T) in `layout`, and so on:
+ *   stored rows x cols of A = op_a == N ? M x K : K x M, likewise B
+ *   (K x N or N x K); ld >= the stored number of columns (row-major) or
+ *   rows (column-major), and >= 1.
+ * Everything else (device pointers, workspace, stream, beta == 0 not
+ * reading C, return codes) is as gemm_f32_ex; mode must be AUTO,
+ * FP32_SIMT, TF32X3 or TF32 (the teaching kernels take plain row-major
+ * operands only: GEMM_ERR_UNSUPPORTED otherwise).  A layout or op outside
+ * the constants below returns GEMM_ERR_INVALID_ARG.
+ * Results equal gemm_f32_ex's on the same logical matrices, bit for bit,
+ * whenever both run the same kernel configuration.
+ */
+#define GEMM_ROW_MAJOR 0
+#define GEMM_COL_MAJOR 1
+#define GEMM_OP_N 0
+#define GEMM_OP_T 1
+
+GEMM_API int gemm_f32_op(int layout, int op_a, int op_b, int64_t M, int64_t N, int64_t K,
+                         float alpha, const float *A, int64_t lda, const float *B,
+                         int64_t ldb, float beta, float *C, int64_t ldc, int mode,
+                         void *workspace, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * gemm_f32_op_plan -- gemm_f32_plan for a gemm_f32_op call.  The returned
+ * plan describes the row-major problem the call runs (for GEMM_COL_MAJOR:
+ * C^T = op(B)^T * op(A)^T, so M and N are exchanged in its tile grid).
+ */
+GEMM_API int gemm_f32_op_plan(int layout, int op_a, int op_b, int64_t M, int64_t N, int64_t K,
+                              int64_t lda, int64_t ldb, int64_t ldc, int mode,
+                              uintptr_t align_hint, int beta_nonzero, gemm_plan_t *out);
+
+/*
  * hbm_copy_f32 -- dst[i] = src[i] for i < n on `stream` (the
  * device-to-device copy kernel of "Bandwidths and peak rate - exercises",
  * exercise 2: one read and one write per element).  Device pointers, must

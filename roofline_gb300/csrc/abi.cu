@@ -72,9 +72,10 @@ bool query_props(int dev, DeviceProps *d) {
 bool valid_ld(int64_t ld, int64_t width) { return ld >= (width > 1 ? width : 1); }
 
 int check_args(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *B,
-               int64_t ldb, const float *C, int64_t ldc) {
+               int64_t ldb, const float *C, int64_t ldc, int ta = 0, int tb = 0) {
   if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
-  if (!valid_ld(lda, K) || !valid_ld(ldb, N) || !valid_ld(ldc, N)) return GEMM_ERR_INVALID_ARG;
+  if (!valid_ld(lda, ta ? M : K) || !valid_ld(ldb, tb ? K : N) || !valid_ld(ldc, N))
+    return GEMM_ERR_INVALID_ARG;
   // keep every element offset well inside int64
   const int64_t lim = (int64_t)1 << 40;
   if (M > lim || N > lim || K > lim || lda > lim || ldb > lim || ldc > lim) return GEMM_ERR_INVALID_ARG;
@@ -227,15 +228,22 @@ int gemm_f32_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int
   return make_plan(M, N, K, lda, ldb, ldc, mode, align_hint, beta_nonzero, current_props(), out);
 }
 
-int gemm_f32_ex(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t lda,
-                const float *B, int64_t ldb, float beta, float *C, int64_t ldc, int mode,
-                void *workspace, size_t ws_bytes, cudaStream_t stream) {
-  int st = check_args(M, N, K, A, lda, B, ldb, C, ldc);
+}  // extern "C"
+
+namespace gg {
+namespace {
+
+// One row-major GEMM (operand storage per p.ta / p.tb): checks, plan,
+// workspace, launch.
+int run_gemm(const GemmArgs &p, int mode, void *workspace, size_t ws_bytes, cudaStream_t stream) {
+  const int64_t M = p.M, N = p.N, K = p.K;
+  int st = check_args(M, N, K, p.A, p.lda, p.B, p.ldb, p.C, p.ldc, p.ta, p.tb);
   if (st != GEMM_OK) return st;
   gemm_plan_t plan;
+  const uintptr_t align = (uintptr_t)p.A | (uintptr_t)p.B | (uintptr_t)p.C;
   // Mode and shape checks first (host only), then the device.
-  st = make_plan(M, N, K, lda, ldb, ldc, mode,
-                 (uintptr_t)A | (uintptr_t)B | (uintptr_t)C, beta != 0.0f, default_props(), &plan);
+  st = make_plan(M, N, K, p.lda, p.ldb, p.ldc, mode, align, p.beta != 0.0f, default_props(),
+                 &plan, p.ta, p.tb);
   if (st == GEMM_ERR_INVALID_ARG) return st;
   if (M == 0 || N == 0) return GEMM_OK;
   if (workspace && (((uintptr_t)workspace) & 255)) return GEMM_ERR_INVALID_ARG;
@@ -244,11 +252,9 @@ int gemm_f32_ex(int64_t M, int64_t N, int64_t K, float alpha, const float *A, in
   st = current_device(&dev);
   if (st != GEMM_OK) return st;
   const DeviceProps &dp = props_of(dev);
-  st = make_plan(M, N, K, lda, ldb, ldc, mode, (uintptr_t)A | (uintptr_t)B | (uintptr_t)C,
-                 beta != 0.0f, dp, &plan);
+  st = make_plan(M, N, K, p.lda, p.ldb, p.ldc, mode, align, p.beta != 0.0f, dp, &plan, p.ta,
+                 p.tb);
   if (st != GEMM_OK) return st;
-
-  GemmArgs p{M, N, K, alpha, beta, A, lda, B, ldb, C, ldc};
   if (plan.kernel == GEMM_KERNEL_SCALE) return to_status(launch_scale(p, stream));
 
   void *ws = nullptr;
@@ -282,6 +288,58 @@ int gemm_f32_ex(int64_t M, int64_t N, int64_t K, float alpha, const float *A, in
     default:
       return GEMM_ERR_UNSUPPORTED;
   }
+}
+
+// gemm_f32_op's problem as a row-major one.  Column-major storage is the
+// row-major storage of the transpose, so C^T = op(B)^T * op(A)^T: the
+// operands swap places, M and N swap, and each operand keeps its storage
+// flag (a column-major B stored K x N is a row-major N x K matrix, i.e. the
+// new A stored as M' x K with no transpose).
+int op_args(int layout, int op_a, int op_b, int64_t M, int64_t N, int64_t K, float alpha,
+            const float *A, int64_t lda, const float *B, int64_t ldb, float beta, float *C,
+            int64_t ldc, GemmArgs *out) {
+  if ((layout != GEMM_ROW_MAJOR && layout != GEMM_COL_MAJOR) ||
+      (op_a != GEMM_OP_N && op_a != GEMM_OP_T) || (op_b != GEMM_OP_N && op_b != GEMM_OP_T))
+    return GEMM_ERR_INVALID_ARG;
+  if (layout == GEMM_ROW_MAJOR)
+    *out = GemmArgs{M, N, K, alpha, beta, A, lda, B, ldb, C, ldc, op_a, op_b};
+  else
+    *out = GemmArgs{N, M, K, alpha, beta, B, ldb, A, lda, C, ldc, op_b, op_a};
+  return GEMM_OK;
+}
+
+}  // namespace
+}  // namespace gg
+
+extern "C" {
+
+int gemm_f32_ex(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t lda,
+                const float *B, int64_t ldb, float beta, float *C, int64_t ldc, int mode,
+                void *workspace, size_t ws_bytes, cudaStream_t stream) {
+  return run_gemm(GemmArgs{M, N, K, alpha, beta, A, lda, B, ldb, C, ldc}, mode, workspace,
+                  ws_bytes, stream);
+}
+
+int gemm_f32_op(int layout, int op_a, int op_b, int64_t M, int64_t N, int64_t K, float alpha,
+                const float *A, int64_t lda, const float *B, int64_t ldb, float beta, float *C,
+                int64_t ldc, int mode, void *workspace, size_t ws_bytes, cudaStream_t stream) {
+  GemmArgs p;
+  int st = op_args(layout, op_a, op_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, &p);
+  if (st != GEMM_OK) return st;
+  return run_gemm(p, mode, workspace, ws_bytes, stream);
+}
+
+int gemm_f32_op_plan(int layout, int op_a, int op_b, int64_t M, int64_t N, int64_t K,
+                     int64_t lda, int64_t ldb, int64_t ldc, int mode, uintptr_t align_hint,
+                     int beta_nonzero, gemm_plan_t *out) {
+  if (!out) return GEMM_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
+  GemmArgs p;
+  int st = op_args(layout, op_a, op_b, M, N, K, 1.0f, nullptr, lda, nullptr, ldb, 0.0f, nullptr,
+                   ldc, &p);
+  if (st != GEMM_OK) return st;
+  return make_plan(p.M, p.N, p.K, p.lda, p.ldb, p.ldc, mode, align_hint, beta_nonzero,
+                   current_props(), out, p.ta, p.tb);
 }
 
 int gemm_f32(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *B,

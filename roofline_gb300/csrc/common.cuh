@@ -19,6 +19,10 @@ struct GemmArgs {
   int64_t ldb;
   float *C;
   int64_t ldc;
+  // operand storage: ta = 1 means A is stored K x M (A(i,k) = A[k*lda + i]),
+  // tb = 1 means B is stored N x K (B(k,j) = B[j*ldb + k]); 0 is the
+  // row-major M x K / K x N storage of gemm_f32.
+  int ta = 0, tb = 0;
 };
 
 // Cached properties of one device (or the built-in GB300 figures).
@@ -51,9 +55,10 @@ void profile_mark_after(cudaStream_t s);
 bool profile_events_set();
 
 // Planner (plan.cu).
+// ta / tb: operand storage as in GemmArgs.
 int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
               int64_t ldc, int mode, uintptr_t align_hint, int beta_nonzero,
-              const DeviceProps &dp, gemm_plan_t *out);
+              const DeviceProps &dp, gemm_plan_t *out, int ta = 0, int tb = 0);
 bool tc_supported(const DeviceProps &dp);
 
 // Kernel launchers.  Each returns cudaSuccess or the launch error.

@@ -94,11 +94,17 @@ void plan_simt(int64_t M, int64_t N, int64_t K, bool vec, const DeviceProps &dp,
 
 }  // namespace
 
+// The split pre-passes tile K in 32-deep rows of a grid's y dimension.
+static bool tc_k_fits(int64_t K) { return ceil_div(K, 32) <= 65535; }
+
 int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
               int mode, uintptr_t align_hint, int beta_nonzero, const DeviceProps &dp,
-              gemm_plan_t *out) {
+              gemm_plan_t *out, int ta, int tb) {
   if (!out || !mode_known(mode) || M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
-  if (lda < (K > 1 ? K : 1) || ldb < (N > 1 ? N : 1) || ldc < (N > 1 ? N : 1))
+  // stored widths: A is M x K (K x M when ta), B is K x N (N x K when tb)
+  const int64_t a_cols = ta ? M : K, b_cols = tb ? K : N;
+  if (lda < (a_cols > 1 ? a_cols : 1) || ldb < (b_cols > 1 ? b_cols : 1) ||
+      ldc < (N > 1 ? N : 1))
     return GEMM_ERR_INVALID_ARG;
   gemm_plan_t p{};
   p.split_k = 1;
@@ -114,7 +120,8 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
     // Tensor cores (3xTF32) once the problem is large enough to amortise the
     // split pass; the CUDA-core kernel otherwise.
     const bool big = (double)M * N * K >= 64.0 * 1024 * 1024 * 64;
-    resolved = (tc_supported(dp) && big) ? GEMM_MODE_TF32X3 : GEMM_MODE_FP32_SIMT;
+    resolved = (tc_supported(dp) && big && tc_k_fits(K)) ? GEMM_MODE_TF32X3
+                                                         : GEMM_MODE_FP32_SIMT;
   }
   p.mode = resolved;
 
@@ -134,6 +141,10 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
   }
 
   const bool vec = (lda % 4 == 0) && (ldb % 4 == 0) && (ldc % 4 == 0) && ((align_hint & 15) == 0);
+  // The teaching kernels take the course page's plain row-major operands only.
+  const bool ladder = resolved == GEMM_MODE_NAIVE || resolved == GEMM_MODE_COALESCED ||
+                      resolved == GEMM_MODE_TILED16 || resolved == GEMM_MODE_TILED32;
+  if (ladder && (ta || tb)) return GEMM_ERR_UNSUPPORTED;
   switch (resolved) {
     case GEMM_MODE_NAIVE:
     case GEMM_MODE_COALESCED: {
@@ -164,18 +175,18 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
     case GEMM_MODE_TF32X3:
     case GEMM_MODE_TF32: {
       if (!tc_supported(dp)) return GEMM_ERR_UNSUPPORTED;
-      if (ceil_div(M, 128) > 65535) return GEMM_ERR_UNSUPPORTED;
+      if (ceil_div(M, 128) > 65535 || !tc_k_fits(K)) return GEMM_ERR_UNSUPPORTED;
       const bool x3 = resolved == GEMM_MODE_TF32X3;
       const int nprod = x3 ? 3 : 1;
       p.kernel = x3 ? GEMM_KERNEL_TC_TF32X3 : GEMM_KERNEL_TC_TF32;
       p.bm = 128;
       p.threads = 192;
       p.vec = vec ? 1 : 0;
-      // A aligned for TMA (16-byte base, lda a multiple of 4): the GEMM kernel
-      // reads FP32 A once and splits it on chip; otherwise a pre-pass
-      // writes A_hi/A_lo to the workspace.  B is always pre-split
-      // (transposed to K-major).
-      const bool a_aligned = (lda % 4 == 0) && ((align_hint & 15) == 0);
+      // A stored M x K and aligned for TMA (16-byte base, lda a multiple of
+      // 4): the GEMM kernel reads FP32 A once and splits it on chip;
+      // otherwise a pre-pass writes A_hi/A_lo (K-major) to the workspace.
+      // B is always pre-split to K-major.
+      const bool a_aligned = !ta && (lda % 4 == 0) && ((align_hint & 15) == 0);
       const int64_t sms = dp.sm_count > 0 ? dp.sm_count : 152;
       const int64_t tiles256 = ceil_div(M, 128) * ceil_div(N, 256);
       const bool wide = N > 128 && tiles256 >= 2 * sms;

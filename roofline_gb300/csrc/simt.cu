@@ -22,6 +22,9 @@
 // in 16-byte copies.  The copies' source-size operand zero-fills elements
 // outside the matrices; stores outside C are skipped (the course page's edge
 // handling in "Stage 2").
+// Transposed storage (A stored K x M, B stored N x K) swaps the two copy
+// kinds per operand: an M- or N-contiguous operand moves in 16-byte copies,
+// a K-contiguous one is scattered element by element into padded rows.
 // Split-K: grid.z slices K; slices write raw partial sums to the workspace
 // and splitk_reduce applies alpha/beta, summing slices in a fixed order.
 //
@@ -55,28 +58,34 @@ __device__ __forceinline__ void cp_async_wait() {
 
 constexpr int kThreadsP = 128;
 
-template <int BM, int BN, int BK, int STAGES, bool VEC>
+template <int BM, int BN, int BK, int STAGES, bool VEC, bool TA, bool TB>
 __global__ void __launch_bounds__(kThreadsP, 2)
 simt_packed_kernel(GemmArgs p, int64_t k_per_split, float *__restrict__ ws, int ws_vec) {
   constexpr int TM = 8, TN = 8;
-  constexpr int PAD = 4;
-  constexpr int LDA_S = BM + PAD;  // 68 floats: odd multiple of 4 -> conflict-free k-major scatter
+  // k-major tiles As[k][m], Bs[k][n].  An operand stored with K contiguous (A
+  // as M x K, or B as N x K) is copied element by element into rows of
+  // (tile width + 4) floats: an odd multiple of 4, so a warp's 8 k x 4 rows
+  // scatter lands in 32 distinct banks.  An operand stored with M or N
+  // contiguous moves in 16-byte copies into unpadded-width rows.
+  constexpr int LDA_S = BM + 4;
+  constexpr int LDB_S = BN + (TB ? 4 : 0);
   constexpr int WTM = TM * 8;   // 64
   constexpr int WTN = TN * 4;   // 32
   constexpr int WARPS_N = BN / WTN;
   static_assert((BM / WTM) * WARPS_N * 32 == kThreadsP, "warp grid must cover the CTA");
-  static_assert(BK % 8 == 0, "A copies go 8 k at a time");
-  // A: element copies; lane -> (k = 8 * kh + lane % 8, row), so one warp
-  // instruction reads 4 rows x 32 contiguous bytes.
-  constexpr int A_ELEMS = BM * BK;
-  constexpr int B_SLOTS = BK * BN / 4;
-  static_assert(A_ELEMS % kThreadsP == 0 && B_SLOTS % kThreadsP == 0, "whole copies per thread");
-  constexpr int A_PER_T = A_ELEMS / kThreadsP;
-  constexpr int B_PER_T = B_SLOTS / kThreadsP;
+  static_assert(BK % 8 == 0, "element copies go 8 k at a time");
+  // element copy e: k = 8 * (e / (8 * rows)) + e % 8, row = (e / 8) % rows, so
+  // one warp instruction reads 4 rows x 32 contiguous bytes.
+  // vector copy e: k = e / (cols / 4), first column = 4 * (e % (cols / 4)).
+  constexpr int A_COPIES = TA ? BK * BM / 4 : BM * BK;
+  constexpr int B_COPIES = TB ? BK * BN : BK * BN / 4;
+  static_assert(A_COPIES % kThreadsP == 0 && B_COPIES % kThreadsP == 0, "whole copies per thread");
+  constexpr int A_PER_T = A_COPIES / kThreadsP;
+  constexpr int B_PER_T = B_COPIES / kThreadsP;
 
   extern __shared__ __align__(16) float smp[];
   float(*As)[BK][LDA_S] = reinterpret_cast<float(*)[BK][LDA_S]>(smp);
-  float(*Bs)[BK][BN] = reinterpret_cast<float(*)[BK][BN]>(smp + STAGES * BK * LDA_S);
+  float(*Bs)[BK][LDB_S] = reinterpret_cast<float(*)[BK][LDB_S]>(smp + STAGES * BK * LDA_S);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -89,27 +98,43 @@ simt_packed_kernel(GemmArgs p, int64_t k_per_split, float *__restrict__ ws, int 
   const int64_t klen = kend > kbeg ? kend - kbeg : 0;
   const int ntiles = (int)((klen + BK - 1) / BK);
 
-  // copy e = tid + j * threads: k = 8 * (e / (8 * BM)) + e % 8, row = (e / 8) % BM
+  // Per-copy source pointers at k = kbeg, and how much of each copy lies in
+  // the matrix: element copy -> its row is in range (0/1); vector copy -> the
+  // number of its 4 columns in range.
   const float *a_src[A_PER_T];
-  bool a_row_ok[A_PER_T];
+  int a_ok[A_PER_T];
 #pragma unroll
   for (int j = 0; j < A_PER_T; ++j) {
     const int e = tid + j * kThreadsP;
-    const int kk = 8 * (e / (8 * BM)) + e % 8, r = (e / 8) % BM;
-    a_row_ok[j] = m0 + r < p.M;
-    a_src[j] = p.A + (a_row_ok[j] ? (m0 + r) * p.lda + kbeg + kk : 0);
+    if (!TA) {
+      const int kk = 8 * (e / (8 * BM)) + e % 8, r = (e / 8) % BM;
+      a_ok[j] = m0 + r < p.M;
+      a_src[j] = p.A + (a_ok[j] ? (m0 + r) * p.lda + kbeg + kk : 0);
+    } else {
+      const int kr = e / (BM / 4), mq = (e % (BM / 4)) * 4;
+      const int64_t left = p.M - (m0 + mq);
+      a_ok[j] = (int)(left > 4 ? 4 : (left < 0 ? 0 : left));
+      a_src[j] = p.A + (kbeg + kr < p.K && a_ok[j] > 0 ? (kbeg + kr) * p.lda + m0 + mq : 0);
+    }
   }
+  const int64_t a_step = TA ? (int64_t)BK * p.lda : BK;
   const float *b_src[B_PER_T];
-  int b_cols[B_PER_T];
+  int b_ok[B_PER_T];
 #pragma unroll
   for (int s = 0; s < B_PER_T; ++s) {
-    const int slot = tid + s * kThreadsP;
-    const int kr = slot / (BN / 4), cq = (slot % (BN / 4)) * 4;
-    const int64_t left = p.N - (n0 + cq);
-    b_cols[s] = (int)(left > 4 ? 4 : (left < 0 ? 0 : left));
-    b_src[s] = p.B + (kbeg + kr < p.K && b_cols[s] > 0 ? (kbeg + kr) * p.ldb + n0 + cq : 0);
+    const int e = tid + s * kThreadsP;
+    if (!TB) {
+      const int kr = e / (BN / 4), cq = (e % (BN / 4)) * 4;
+      const int64_t left = p.N - (n0 + cq);
+      b_ok[s] = (int)(left > 4 ? 4 : (left < 0 ? 0 : left));
+      b_src[s] = p.B + (kbeg + kr < p.K && b_ok[s] > 0 ? (kbeg + kr) * p.ldb + n0 + cq : 0);
+    } else {
+      const int kk = 8 * (e / (8 * BN)) + e % 8, c = (e / 8) % BN;
+      b_ok[s] = n0 + c < p.N;
+      b_src[s] = p.B + (b_ok[s] ? (n0 + c) * p.ldb + kbeg + kk : 0);
+    }
   }
-  const int64_t b_step = (int64_t)BK * p.ldb;
+  const int64_t b_step = TB ? BK : (int64_t)BK * p.ldb;
 
   auto issue = [&](int t) {
     const int buf = t % STAGES;
@@ -117,25 +142,47 @@ simt_packed_kernel(GemmArgs p, int64_t k_per_split, float *__restrict__ ws, int 
 #pragma unroll
     for (int j = 0; j < A_PER_T; ++j) {
       const int e = tid + j * kThreadsP;
-      const int kk = 8 * (e / (8 * BM)) + e % 8, r = (e / 8) % BM;
-      const bool ok = a_row_ok[j] && kk < rem;
-      cp_async4(&As[buf][kk][r], ok ? a_src[j] + (int64_t)t * BK : p.A, ok);
+      const float *src = a_src[j] + (int64_t)t * a_step;
+      if (!TA) {
+        const int kk = 8 * (e / (8 * BM)) + e % 8, r = (e / 8) % BM;
+        const bool ok = a_ok[j] && kk < rem;
+        cp_async4(&As[buf][kk][r], ok ? src : p.A, ok);
+      } else {
+        const int kr = e / (BM / 4), mq = (e % (BM / 4)) * 4;
+        float *dst = &As[buf][kr][mq];
+        const bool row_ok = kr < rem;
+        if (VEC && row_ok && a_ok[j] == 4) {
+          cp_async16(dst, src);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const bool ok = row_ok && i < a_ok[j];
+            cp_async4(dst + i, ok ? src + i : p.A, ok);
+          }
+        }
+      }
     }
 #pragma unroll
     for (int s = 0; s < B_PER_T; ++s) {
-      const int slot = tid + s * kThreadsP;
-      const int kr = slot / (BN / 4), cq = (slot % (BN / 4)) * 4;
-      float *dst = &Bs[buf][kr][cq];
-      const bool row_ok = kr < rem;
+      const int e = tid + s * kThreadsP;
       const float *src = b_src[s] + (int64_t)t * b_step;
-      if (VEC && row_ok && b_cols[s] == 4) {
-        cp_async16(dst, src);
-      } else {
+      if (!TB) {
+        const int kr = e / (BN / 4), cq = (e % (BN / 4)) * 4;
+        float *dst = &Bs[buf][kr][cq];
+        const bool row_ok = kr < rem;
+        if (VEC && row_ok && b_ok[s] == 4) {
+          cp_async16(dst, src);
+        } else {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const bool ok = row_ok && i < b_cols[s];
-          cp_async4(dst + i, ok ? src + i : p.B, ok);
+          for (int i = 0; i < 4; ++i) {
+            const bool ok = row_ok && i < b_ok[s];
+            cp_async4(dst + i, ok ? src + i : p.B, ok);
+          }
         }
+      } else {
+        const int kk = 8 * (e / (8 * BN)) + e % 8, c = (e / 8) % BN;
+        const bool ok = b_ok[s] && kk < rem;
+        cp_async4(&Bs[buf][kk][c], ok ? src : p.B, ok);
       }
     }
   };
@@ -254,7 +301,7 @@ cudaError_t launch_splitk_reduce(const GemmArgs &p, const float *ws, int splits,
   return cudaGetLastError();
 }
 
-template <int BM, int BN, int BK, int STAGES>
+template <int BM, int BN, int BK, int STAGES, bool TA, bool TB>
 cudaError_t launch_packed(const gemm_plan_t &plan, const GemmArgs &p, float *ws, cudaStream_t s) {
   const int split = plan.split_k > 1 ? plan.split_k : 1;
   int64_t kps = ceil_div(p.K, split);
@@ -262,9 +309,9 @@ cudaError_t launch_packed(const gemm_plan_t &plan, const GemmArgs &p, float *ws,
   dim3 grid((unsigned)ceil_div(p.N, BN), (unsigned)ceil_div(p.M, BM), (unsigned)split);
   float *w = split > 1 ? ws : nullptr;
   const int ws_vec = (p.N % 4 == 0) ? 1 : 0;
-  constexpr int smem = STAGES * BK * ((BM + 4) + BN) * 4;
-  auto kv = simt_packed_kernel<BM, BN, BK, STAGES, true>;
-  auto ks = simt_packed_kernel<BM, BN, BK, STAGES, false>;
+  constexpr int smem = STAGES * BK * ((BM + 4) + BN + (TB ? 4 : 0)) * 4;
+  auto kv = simt_packed_kernel<BM, BN, BK, STAGES, true, TA, TB>;
+  auto ks = simt_packed_kernel<BM, BN, BK, STAGES, false, TA, TB>;
   if (smem > 48 * 1024) {
     if (cudaFuncSetAttribute(kv, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
         cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
@@ -282,9 +329,12 @@ cudaError_t launch_packed(const gemm_plan_t &plan, const GemmArgs &p, float *ws,
 }
 
 cudaError_t launch_simt(const gemm_plan_t &plan, const GemmArgs &p, float *ws, cudaStream_t s) {
-  if (plan.bm == 64 && plan.bn == 128 && plan.bk == 16 && plan.stages == 4)
-    return launch_packed<64, 128, 16, 4>(plan, p, ws, s);
-  return cudaErrorInvalidValue;
+  if (!(plan.bm == 64 && plan.bn == 128 && plan.bk == 16 && plan.stages == 4))
+    return cudaErrorInvalidValue;
+  if (!p.ta && !p.tb) return launch_packed<64, 128, 16, 4, false, false>(plan, p, ws, s);
+  if (p.ta && !p.tb) return launch_packed<64, 128, 16, 4, true, false>(plan, p, ws, s);
+  if (!p.ta && p.tb) return launch_packed<64, 128, 16, 4, false, true>(plan, p, ws, s);
+  return launch_packed<64, 128, 16, 4, true, true>(plan, p, ws, s);
 }
 
 }  // namespace gg

@@ -902,20 +902,25 @@ int launch_cfg(const gemm_plan_t &plan, const GemmArgs &a, char *ws, cudaStream_
   float *bhi = reinterpret_cast<float *>(ws + L.b_hi);
   float *blo = reinterpret_cast<float *>(ws + L.b_lo);
 
-  // split pass
-  if (!AK) {
-    int64_t groups = a.M * (L.kp / 4);
-    int64_t blocks = ceil_div(groups, 256);
+  // Split passes: each operand becomes K-major hi (and lo) planes.  An
+  // operand stored with K contiguous (A as M x K, B as N x K) is split row
+  // by row; one stored with K as its row index is split and transposed.
+  auto split_k_major = [&](const float *src, int64_t ld, int64_t rows, float *hi, float *lo) {
+    int64_t blocks = ceil_div(rows * (L.kp / 4), 256);
     if (blocks > 152 * 16) blocks = 152 * 16;
-    split_rows_kernel<<<(unsigned)blocks, 256, 0, s>>>(a.A, a.lda, a.M, a.K, L.kp, ahi,
-                                                        X3 ? alo : nullptr);
+    split_rows_kernel<<<(unsigned)blocks, 256, 0, s>>>(src, ld, rows, a.K, L.kp, hi, lo);
+  };
+  auto split_transposed = [&](const float *src, int64_t ld, int64_t cols, float *hi, float *lo) {
+    const int vec = ((ld & 3) == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0) ? 1 : 0;
+    dim3 grid((unsigned)ceil_div(cols, kTrN), (unsigned)ceil_div(L.kp, kTrK));
+    split_transpose_kernel<<<grid, 256, 0, s>>>(src, ld, a.K, cols, L.kp, vec, hi, lo);
+  };
+  if (!AK) {
+    if (a.ta) split_transposed(a.A, a.lda, a.M, ahi, X3 ? alo : nullptr);
+    else split_k_major(a.A, a.lda, a.M, ahi, X3 ? alo : nullptr);
   }
-  {
-    const int vec = ((a.ldb & 3) == 0 && (reinterpret_cast<uintptr_t>(a.B) & 15) == 0) ? 1 : 0;
-    dim3 grid((unsigned)ceil_div(a.N, kTrN), (unsigned)ceil_div(L.kp, kTrK));
-    split_transpose_kernel<<<grid, 256, 0, s>>>(a.B, a.ldb, a.K, a.N, L.kp, vec, bhi,
-                                                X3 ? blo : nullptr);
-  }
+  if (a.tb) split_k_major(a.B, a.ldb, a.N, bhi, X3 ? blo : nullptr);
+  else split_transposed(a.B, a.ldb, a.N, bhi, X3 ? blo : nullptr);
   if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_CUDA;
 
   CUtensorMap tA0, tA1, tB0, tB1;
@@ -1049,7 +1054,9 @@ int launch_tc(const gemm_plan_t &plan, const GemmArgs &a, void *ws, size_t ws_by
   if (!get_encoder()) return GEMM_ERR_UNSUPPORTED;
   if (ws_bytes < tc_workspace_bytes(plan, a.M, a.N, a.K) || ws == nullptr)
     return GEMM_ERR_WORKSPACE_TOO_SMALL;
-  if (plan.a_split_in_kernel && ((a.lda & 3) || (reinterpret_cast<uintptr_t>(a.A) & 15)))
+  // the in-kernel A split reads A by TMA as M x K rows
+  if (plan.a_split_in_kernel &&
+      (a.ta || (a.lda & 3) || (reinterpret_cast<uintptr_t>(a.A) & 15)))
     return GEMM_ERR_UNSUPPORTED;
   char *w = static_cast<char *>(ws);
   const int nprod = plan.mode == GEMM_MODE_TF32 ? 1 : 3;

@@ -28,6 +28,12 @@ MODES = {"auto": MODE_AUTO, "fp32_simt": MODE_FP32_SIMT, "tf32x3": MODE_TF32X3, 
          "naive": MODE_NAIVE, "coalesced": MODE_COALESCED, "tiled16": MODE_TILED16,
          "tiled32": MODE_TILED32}
 
+# storage order and operand ops of gemm_f32_op
+ROW_MAJOR = 0
+COL_MAJOR = 1
+OP_N = 0
+OP_T = 1
+
 OK = 0
 ERR_INVALID_ARG = -1
 ERR_UNSUPPORTED = -2
@@ -41,7 +47,8 @@ KERNELS = {0: "none", 1: "scale", 2: "naive", 3: "coalesced", 4: "tiled", 5: "si
 BOUNDS = {0: "none", 1: "fp32", 2: "tf32x3", 3: "hbm", 4: "tf32"}
 
 # Every symbol include/gb300_gemm.h declares.
-EXPORTED = ["gemm_f32", "gemm_f32_ex", "gemm_f32_plan", "hbm_copy_f32", "hbm_copy_calibrate",
+EXPORTED = ["gemm_f32", "gemm_f32_ex", "gemm_f32_plan", "gemm_f32_op", "gemm_f32_op_plan",
+            "hbm_copy_f32", "hbm_copy_calibrate",
             "gemm_device_info", "gemm_strerror", "gemm_check_status", "gemm_shutdown",
             "gemm_abi_version", "gemm_set_profile_events", "gemm_f32_splitk_noalloc",
             "fp32_fma_peak", "fp32_fma_peak_sink_floats"]
@@ -119,6 +126,12 @@ def load(path: str | None = None):
         lib.gemm_f32_plan.argtypes = [i64, i64, i64, i64, i64, i64, i32, ctypes.c_size_t, i32,
                                       ctypes.POINTER(GemmPlan)]
         lib.gemm_f32_plan.restype = i32
+        lib.gemm_f32_op.argtypes = [i32, i32, i32, i64, i64, i64, f32, vp, i64, vp, i64, f32,
+                                    vp, i64, i32, vp, ctypes.c_size_t, vp]
+        lib.gemm_f32_op.restype = i32
+        lib.gemm_f32_op_plan.argtypes = [i32, i32, i32, i64, i64, i64, i64, i64, i64, i32,
+                                         ctypes.c_size_t, i32, ctypes.POINTER(GemmPlan)]
+        lib.gemm_f32_op_plan.restype = i32
         lib.hbm_copy_f32.argtypes = [vp, vp, ctypes.c_size_t, vp]
         lib.hbm_copy_f32.restype = i32
         lib.hbm_copy_calibrate.argtypes = [vp, vp, ctypes.c_size_t, i32, vp,
@@ -168,6 +181,12 @@ def gemm_f32_ex(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, mode=MODE_AUTO,
                               workspace, ws_bytes, stream)
 
 
+def gemm_f32_op(layout, op_a, op_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                mode=MODE_AUTO, workspace=None, ws_bytes=0, stream=0) -> int:
+    return load().gemm_f32_op(layout, op_a, op_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                              _mode(mode), workspace, ws_bytes, stream)
+
+
 def gemm_f32_splitk_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, split_k=0,
                             stream=0) -> int:
     """Split-K CUDA-core GEMM whose scratch is the library's static device
@@ -186,6 +205,27 @@ def plan(M, N, K, lda=None, ldb=None, ldc=None, mode=MODE_AUTO, align_hint=0,
                               1 if beta_nonzero else 0, ctypes.byref(out))
     if rc != OK:
         raise GemmError(rc, "gemm_f32_plan")
+    return out.as_dict()
+
+
+def stored_shape(layout, op, rows, cols):
+    """(rows, cols) of the matrix as stored for a logical rows x cols
+    operand op(X), and the smallest legal leading dimension."""
+    r, c = (rows, cols) if op == OP_N else (cols, rows)
+    return (r, c), max(c if layout == ROW_MAJOR else r, 1)
+
+
+def plan_op(layout, op_a, op_b, M, N, K, lda=None, ldb=None, ldc=None, mode=MODE_AUTO,
+            align_hint=0, beta_nonzero=False) -> dict:
+    """gemm_f32_op_plan: the row-major problem a gemm_f32_op call runs."""
+    out = GemmPlan()
+    lda = stored_shape(layout, op_a, M, K)[1] if lda is None else lda
+    ldb = stored_shape(layout, op_b, K, N)[1] if ldb is None else ldb
+    ldc = stored_shape(layout, OP_N, M, N)[1] if ldc is None else ldc
+    rc = load().gemm_f32_op_plan(layout, op_a, op_b, M, N, K, lda, ldb, ldc, _mode(mode),
+                                 align_hint, 1 if beta_nonzero else 0, ctypes.byref(out))
+    if rc != OK:
+        raise GemmError(rc, "gemm_f32_op_plan")
     return out.as_dict()
 
 
@@ -229,22 +269,30 @@ def _stream_handle(stream):
     return s.cuda_stream
 
 
-def _check_matrix(t, name):
+def _operand(t, name):
+    """(op, ld) of a 2-D float32 CUDA tensor used as a GEMM operand: a
+    row-major view (unit column stride) is op N with ld = row stride; a
+    transposed view of a row-major buffer (unit row stride, e.g. ``X.t()``)
+    is op T with ld = column stride."""
     import torch
-    if not (t.is_cuda and t.dtype == torch.float32 and t.dim() == 2 and
-            (t.stride(1) == 1 or t.shape[1] <= 1)):
-        raise ValueError(f"{name} must be a 2-D float32 CUDA tensor with unit column stride")
-    return max(t.stride(0), 1)
+    if not (t.is_cuda and t.dtype == torch.float32 and t.dim() == 2):
+        raise ValueError(f"{name} must be a 2-D float32 CUDA tensor")
+    if t.stride(1) == 1 or t.shape[1] <= 1:
+        return OP_N, max(t.stride(0), 1)
+    if t.stride(0) == 1 or t.shape[0] <= 1:
+        return OP_T, max(t.stride(1), 1)
+    raise ValueError(f"{name} must have a unit row or column stride")
 
 
 def matmul(A, B, C=None, alpha=1.0, beta=0.0, mode=MODE_AUTO, stream=None,
            workspace=None):
-    """C <- alpha * A @ B + beta * C for row-major float32 CUDA tensors.
+    """C <- alpha * A @ B + beta * C for float32 CUDA tensors.
 
     A (M x K) and B (K x N) may be row slices of larger buffers (row stride =
-    leading dimension).  C is allocated when None (then beta must be 0).
-    ``workspace``: optional uint8/float CUDA tensor used as caller-owned
-    scratch.  Returns C.
+    leading dimension) or transposed views of row-major buffers (``X.t()``,
+    run as op T without a copy).  C is row-major, allocated when None (then
+    beta must be 0).  ``workspace``: optional uint8/float CUDA tensor used as
+    caller-owned scratch.  Returns C.
     """
     import torch
     M, K = A.shape
@@ -255,15 +303,26 @@ def matmul(A, B, C=None, alpha=1.0, beta=0.0, mode=MODE_AUTO, stream=None,
         if beta != 0.0:
             raise ValueError("beta != 0 needs C")
         C = torch.empty((M, N), dtype=torch.float32, device=A.device)
-    lda, ldb, ldc = _check_matrix(A, "A"), _check_matrix(B, "B"), _check_matrix(C, "C")
+    op_a, lda = _operand(A, "A")
+    op_b, ldb = _operand(B, "B")
+    op_c, ldc = _operand(C, "C")
+    if op_c != OP_N:
+        raise ValueError("C must be a 2-D float32 CUDA tensor with unit column stride")
     ws_ptr, ws_bytes = None, 0
     if workspace is not None:
         ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
-    rc = load().gemm_f32_ex(M, N, K, float(alpha), A.data_ptr(), lda, B.data_ptr(), ldb,
-                            float(beta), C.data_ptr(), ldc, _mode(mode), ws_ptr, ws_bytes,
-                            _stream_handle(stream))
+    if op_a == OP_N and op_b == OP_N:
+        rc = load().gemm_f32_ex(M, N, K, float(alpha), A.data_ptr(), lda, B.data_ptr(), ldb,
+                                float(beta), C.data_ptr(), ldc, _mode(mode), ws_ptr, ws_bytes,
+                                _stream_handle(stream))
+        what = "gemm_f32_ex"
+    else:
+        rc = load().gemm_f32_op(ROW_MAJOR, op_a, op_b, M, N, K, float(alpha), A.data_ptr(), lda,
+                                B.data_ptr(), ldb, float(beta), C.data_ptr(), ldc, _mode(mode),
+                                ws_ptr, ws_bytes, _stream_handle(stream))
+        what = "gemm_f32_op"
     if rc != OK:
-        raise GemmError(rc, "gemm_f32_ex")
+        raise GemmError(rc, what)
     return C
 
 

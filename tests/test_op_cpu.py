@@ -1,0 +1,109 @@
+"""Host-side checks of gemm_f32_op / gemm_f32_op_plan (no GPU needed): the
+storage-order and op arguments, leading-dimension rules, and the row-major
+problem each call is planned as."""
+import itertools
+
+import pytest
+
+from roofline_gb300 import build, gemm
+
+ROW, COL, N_, T_ = gemm.ROW_MAJOR, gemm.COL_MAJOR, gemm.OP_N, gemm.OP_T
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return gemm.load()
+
+
+def test_bad_layout_or_op_rejected(lib):
+    for layout, op_a, op_b in [(2, 0, 0), (-1, 0, 0), (0, 2, 0), (0, 0, -1), (1, 3, 1)]:
+        rc = gemm.gemm_f32_op(layout, op_a, op_b, 4, 4, 4, 1.0, 256, 4, 256, 4, 0.0, 256, 4,
+                              0, None, 0, 0)
+        assert rc == gemm.ERR_INVALID_ARG
+        with pytest.raises(gemm.GemmError):
+            gemm.plan_op(layout, op_a, op_b, 4, 4, 4, 4, 4, 4)
+
+
+# (layout, op_a, op_b, M, N, K) -> smallest legal (lda, ldb, ldc)
+LD_CASES = [
+    ((ROW, N_, N_, 8, 6, 4), (4, 6, 6)),
+    ((ROW, T_, N_, 8, 6, 4), (8, 6, 6)),
+    ((ROW, N_, T_, 8, 6, 4), (4, 4, 6)),
+    ((ROW, T_, T_, 8, 6, 4), (8, 4, 6)),
+    ((COL, N_, N_, 8, 6, 4), (8, 4, 8)),
+    ((COL, T_, N_, 8, 6, 4), (4, 4, 8)),
+    ((COL, N_, T_, 8, 6, 4), (8, 6, 8)),
+    ((COL, T_, T_, 8, 6, 4), (4, 6, 8)),
+]
+
+
+@pytest.mark.parametrize("case,lds", LD_CASES)
+def test_leading_dimension_rules(lib, case, lds):
+    layout, op_a, op_b, M, N, K = case
+    assert gemm.stored_shape(layout, op_a, M, K)[1] == lds[0]
+    assert gemm.stored_shape(layout, op_b, K, N)[1] == lds[1]
+    assert gemm.stored_shape(layout, N_, M, N)[1] == lds[2]
+    gemm.plan_op(layout, op_a, op_b, M, N, K, *lds, mode="fp32_simt")
+    for i in range(3):
+        bad = list(lds)
+        bad[i] -= 1
+        with pytest.raises(gemm.GemmError) as e:
+            gemm.plan_op(layout, op_a, op_b, M, N, K, *bad, mode="fp32_simt")
+        assert e.value.code == gemm.ERR_INVALID_ARG
+        rc = gemm.gemm_f32_op(layout, op_a, op_b, M, N, K, 1.0, 256, bad[0], 256, bad[1], 0.0,
+                              256, bad[2], 1, None, 0, 0)
+        assert rc == gemm.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("mode", ["fp32_simt", "tf32x3", "tf32", "auto"])
+@pytest.mark.parametrize("shape", [(4096, 4096, 4096), (1023, 515, 777), (65536, 64, 4096)])
+def test_plain_row_major_plans_equal_gemm_f32_plan(lib, mode, shape):
+    M, N, K = shape
+    assert gemm.plan_op(ROW, N_, N_, M, N, K, mode=mode) == gemm.plan(M, N, K, mode=mode)
+
+
+@pytest.mark.parametrize("mode", ["fp32_simt", "tf32x3", "auto"])
+@pytest.mark.parametrize("shape", [(4096, 2048, 1024), (1023, 515, 777), (64, 65536, 4096)])
+def test_column_major_is_the_transposed_row_major_problem(lib, mode, shape):
+    M, N, K = shape
+    # column-major A*B = row-major (B^T A^T)^T: an N x M problem
+    assert gemm.plan_op(COL, N_, N_, M, N, K, mode=mode) == \
+        gemm.plan(N, M, K, K, M, M, mode=mode)
+
+
+def test_transposed_a_uses_the_pre_split(lib):
+    p = gemm.plan_op(ROW, T_, N_, 4096, 4096, 4096, mode="tf32x3")
+    assert p["kernel_name"] == "tc_tf32x3" and p["a_split_in_kernel"] == 0
+    assert p["launches"] == 3 + p["stream_k"]
+    # B stored N x K: still one split pass for B, A split on chip
+    q = gemm.plan_op(ROW, N_, T_, 4096, 4096, 4096, mode="tf32x3")
+    assert q["a_split_in_kernel"] == 1 and q["launches"] == 2 + q["stream_k"]
+    # the tensor-core workspace then also holds A_hi / A_lo
+    assert p["workspace_bytes"] >= q["workspace_bytes"] + 2 * 4096 * 4096 * 4
+
+
+@pytest.mark.parametrize("mode", ["naive", "coalesced", "tiled16", "tiled32"])
+def test_teaching_kernels_take_plain_operands_only(lib, mode):
+    assert gemm.plan_op(ROW, N_, N_, 64, 64, 64, mode=mode)["kernel"] > 0
+    for layout, op_a, op_b in itertools.product([ROW, COL], [N_, T_], [N_, T_]):
+        if layout == ROW and op_a == N_ and op_b == N_:
+            continue
+        plain_colmajor = layout == COL and op_a == N_ and op_b == N_
+        if plain_colmajor:
+            # column-major with no ops is a plain row-major problem again
+            assert gemm.plan_op(layout, op_a, op_b, 64, 64, 64, mode=mode)["kernel"] > 0
+            continue
+        with pytest.raises(gemm.GemmError) as e:
+            gemm.plan_op(layout, op_a, op_b, 64, 64, 64, mode=mode)
+        assert e.value.code == gemm.ERR_UNSUPPORTED
+
+
+def test_empty_and_no_device(lib):
+    import torch
+    assert gemm.gemm_f32_op(COL, T_, T_, 0, 5, 5, 1.0, None, 5, None, 5, 0.0, None, 1, 0,
+                            None, 0, 0) == gemm.OK
+    if not torch.cuda.is_available():
+        rc = gemm.gemm_f32_op(COL, T_, N_, 4, 4, 4, 1.0, 256, 4, 256, 4, 0.0, 256, 4, 1,
+                              None, 0, 0)
+        assert rc == gemm.ERR_NO_DEVICE
