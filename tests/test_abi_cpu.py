@@ -158,9 +158,10 @@ def test_stream_k_plan_bounds(lib):
 def test_tf32_mode_plans(lib):
     p = gemm.plan(4096, 4096, 4096, mode="tf32")
     assert p["kernel_name"] == "tc_tf32" and p["bound_name"] == "tf32"
-    # B_hi only (no B_lo), plus stream-K partials
+    # square: A pre-split too; A_hi and B_hi only (no lo parts), plus stream-K partials
+    assert p["a_split_in_kernel"] == 0 and p["launches"] == 3 + p["stream_k"]
     extra = p["grid_ctas"] * 2 * 128 * p["bn"] * 4 if p["stream_k"] else 0
-    assert p["workspace_bytes"] == 4096 * 4096 * 4 + extra
+    assert p["workspace_bytes"] == 2 * 4096 * 4096 * 4 + extra
     s = gemm.plan(65536, 64, 4096, mode="tf32")
-    assert s["bound_name"] == "hbm" and s["ctas_per_sm"] == 2
+    assert s["bound_name"] == "hbm" and s["ctas_per_sm"] == 2 and s["a_split_in_kernel"] == 1
     assert gemm.plan(64, 64, 64, mode="tf32")["mode"] == gemm.MODE_TF32
