@@ -223,6 +223,39 @@ GEMM_API int gemm_f32_op_plan(int layout, int op_a, int op_b, int64_t M, int64_t
                               uintptr_t align_hint, int beta_nonzero, gemm_plan_t *out);
 
 /*
+ * gemm_f32_host -- C <- alpha * A * B + beta * C with A, B and C in HOST
+ * memory (row-major, leading dimensions as gemm_f32_ex).  Blocking: returns
+ * once C holds the result (or an error), with no copy still touching the
+ * caller's buffers.
+ *
+ * The course page's scaffolding copies the operands to the GPU, runs the
+ * kernel and copies the result back ("Project - tiled matrix multiply",
+ * "Starter scaffolding"); this call does the same for the caller, in row
+ * blocks, so the host-to-device copies of later blocks, the GEMM of the
+ * current block and the device-to-host copy of earlier blocks overlap.
+ * Page-locked host buffers (cudaHostAlloc / cudaMallocHost) are needed for
+ * the copies to overlap; pageable buffers give the same result, slower.
+ *
+ * mode: as gemm_f32_ex; AUTO is resolved once, for the first row block, and
+ * that mode runs every block.  blocks: number of row blocks, 1 ..
+ * GEMM_HOST_MAX_BLOCKS, or 0 for the library's choice (one block for short
+ * products, else blocks of at least 1024 rows, at most 4).  Row blocks hold
+ * whole 128-row tiles except the last.
+ * The library stages the whole problem in device memory it owns (M*K + K*N
+ * + M*N floats plus the GEMM workspace), grown on demand and freed by
+ * gemm_shutdown(); calls on one device are serialised.
+ * Returns GEMM_OK, GEMM_ERR_INVALID_ARG (size, ld, pointer, mode, blocks),
+ * GEMM_ERR_UNSUPPORTED, GEMM_ERR_CUDA (including a failed staging
+ * allocation), GEMM_ERR_DEVICE_TIMEOUT (a bounded wait in the tensor-core
+ * kernel ran out), GEMM_ERR_NO_DEVICE.
+ */
+#define GEMM_HOST_MAX_BLOCKS 64
+
+GEMM_API int gemm_f32_host(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
+                           int64_t lda, const float *B, int64_t ldb, float beta, float *C,
+                           int64_t ldc, int mode, int blocks);
+
+/*
  * hbm_copy_f32 -- dst[i] = src[i] for i < n on `stream` (the
  * device-to-device copy kernel of "Bandwidths and peak rate - exercises",
  * exercise 2: one read and one write per element).  Device pointers, must

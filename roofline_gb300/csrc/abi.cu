@@ -231,7 +231,6 @@ int gemm_f32_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int
 }  // extern "C"
 
 namespace gg {
-namespace {
 
 // One row-major GEMM (operand storage per p.ta / p.tb): checks, plan,
 // workspace, launch.
@@ -289,6 +288,8 @@ int run_gemm(const GemmArgs &p, int mode, void *workspace, size_t ws_bytes, cuda
       return GEMM_ERR_UNSUPPORTED;
   }
 }
+
+namespace {
 
 // gemm_f32_op's problem as a row-major one.  Column-major storage is the
 // row-major storage of the transpose, so C^T = op(B)^T * op(A)^T: the
@@ -430,6 +431,7 @@ int gemm_check_status(cudaStream_t stream) {
 }
 
 void gemm_shutdown(void) {
+  host_pipeline_shutdown();
   std::lock_guard<std::mutex> lk(g_ws_mu);
   for (int d = 0; d < kMaxDevices; ++d) {
     if (g_ws_ptr[d]) {

@@ -23,6 +23,12 @@ struct GemmArgs {
   // tb = 1 means B is stored N x K (B(k,j) = B[j*ldb + k]); 0 is the
   // row-major M x K / K x N storage of gemm_f32.
   int ta = 0, tb = 0;
+  // Tensor-core path only.  b_presplit = 1: the workspace already holds the
+  // B_hi / B_lo planes of this B (same N, K and mode, written by an earlier
+  // call on the same stream), so the B split pass is skipped.  plain_order =
+  // 1: launch without programmatic dependent launch (each kernel waits for
+  // everything before it in the stream).
+  int b_presplit = 0, plain_order = 0;
 };
 
 // Cached properties of one device (or the built-in GB300 figures).
@@ -60,6 +66,14 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
               int64_t ldc, int mode, uintptr_t align_hint, int beta_nonzero,
               const DeviceProps &dp, gemm_plan_t *out, int ta = 0, int tb = 0);
 bool tc_supported(const DeviceProps &dp);
+
+// One row-major GEMM through the planner and the kernels (abi.cu): the body
+// of gemm_f32_ex / gemm_f32_op.  workspace == nullptr: the library's
+// per-device buffer.  Returns a GEMM_* status.
+int run_gemm(const GemmArgs &p, int mode, void *workspace, size_t ws_bytes, cudaStream_t stream);
+
+// Host-buffer pipeline (host.cu): frees its device staging, streams and events.
+void host_pipeline_shutdown();
 
 // Kernel launchers.  Each returns cudaSuccess or the launch error.
 cudaError_t launch_scale(const GemmArgs &p, cudaStream_t s);

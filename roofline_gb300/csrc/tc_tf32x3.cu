@@ -868,21 +868,23 @@ struct WsLayout {
   int64_t kp;
 };
 
-// Workspace regions: A_hi, A_lo (unless A is split in the kernel), B_hi,
-// B_lo (transposed), then for stream-K the partial tiles (2 per CTA).
+// Workspace regions: B_hi, B_lo (K-major), A_hi, A_lo (unless A is split
+// in the kernel), then for stream-K the partial tiles (2 per CTA).  The B
+// planes come first so their place depends only on N, K and the mode: calls
+// that share B (row blocks of one product) can reuse them.
 WsLayout ws_layout(int64_t M, int64_t N, int64_t K, bool a_inkernel, int64_t streamk_ctas,
                    int bn, bool x3) {
   WsLayout w{};
   w.kp = round_up(K, 4);
-  const uint64_t a_bytes = a_inkernel ? 0 : align256((uint64_t)M * w.kp * 4);
-  const uint64_t a_lo_bytes = x3 ? a_bytes : 0;
   const uint64_t b_bytes = align256((uint64_t)N * w.kp * 4);
   const uint64_t b_lo_bytes = x3 ? b_bytes : 0;
-  w.a_hi = 0;
-  w.a_lo = a_bytes;
-  w.b_hi = a_bytes + a_lo_bytes;
-  w.b_lo = w.b_hi + b_bytes;
-  w.partial = w.b_lo + b_lo_bytes;
+  const uint64_t a_bytes = a_inkernel ? 0 : align256((uint64_t)M * w.kp * 4);
+  const uint64_t a_lo_bytes = x3 ? a_bytes : 0;
+  w.b_hi = 0;
+  w.b_lo = b_bytes;
+  w.a_hi = b_bytes + b_lo_bytes;
+  w.a_lo = w.a_hi + a_bytes;
+  w.partial = w.a_lo + a_lo_bytes;
   w.total = w.partial + (uint64_t)streamk_ctas * 2 * kBM * bn * 4;
   return w;
 }
@@ -919,8 +921,10 @@ int launch_cfg(const gemm_plan_t &plan, const GemmArgs &a, char *ws, cudaStream_
     if (a.ta) split_transposed(a.A, a.lda, a.M, ahi, X3 ? alo : nullptr);
     else split_k_major(a.A, a.lda, a.M, ahi, X3 ? alo : nullptr);
   }
-  if (a.tb) split_k_major(a.B, a.ldb, a.N, bhi, X3 ? blo : nullptr);
-  else split_transposed(a.B, a.ldb, a.N, bhi, X3 ? blo : nullptr);
+  if (!a.b_presplit) {
+    if (a.tb) split_k_major(a.B, a.ldb, a.N, bhi, X3 ? blo : nullptr);
+    else split_transposed(a.B, a.ldb, a.N, bhi, X3 ? blo : nullptr);
+  }
   if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_CUDA;
 
   CUtensorMap tA0, tA1, tB0, tB1;
@@ -962,8 +966,9 @@ int launch_cfg(const gemm_plan_t &plan, const GemmArgs &a, char *ws, cudaStream_
   // Programmatic dependent launch lets each kernel be scheduled while the one
   // before it drains (each waits for its predecessor before reading its
   // output).  With the caller's profiling events set, plain stream order is
-  // kept so the events bracket the GEMM kernel alone.
-  const bool pdl = !profile_events_set();
+  // kept so the events bracket the GEMM kernel alone; callers that chain the
+  // GEMM behind cross-stream event waits ask for plain order as well.
+  const bool pdl = !profile_events_set() && !a.plain_order;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;

@@ -48,10 +48,13 @@ BOUNDS = {0: "none", 1: "fp32", 2: "tf32x3", 3: "hbm", 4: "tf32"}
 
 # Every symbol include/gb300_gemm.h declares.
 EXPORTED = ["gemm_f32", "gemm_f32_ex", "gemm_f32_plan", "gemm_f32_op", "gemm_f32_op_plan",
-            "hbm_copy_f32", "hbm_copy_calibrate",
+            "gemm_f32_host", "hbm_copy_f32", "hbm_copy_calibrate",
             "gemm_device_info", "gemm_strerror", "gemm_check_status", "gemm_shutdown",
             "gemm_abi_version", "gemm_set_profile_events", "gemm_f32_splitk_noalloc",
             "fp32_fma_peak", "fp32_fma_peak_sink_floats"]
+
+# most row blocks gemm_f32_host pipelines
+HOST_MAX_BLOCKS = 64
 
 # size of the static scratch array behind gemm_f32_splitk_noalloc
 NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -132,6 +135,9 @@ def load(path: str | None = None):
         lib.gemm_f32_op_plan.argtypes = [i32, i32, i32, i64, i64, i64, i64, i64, i64, i32,
                                          ctypes.c_size_t, i32, ctypes.POINTER(GemmPlan)]
         lib.gemm_f32_op_plan.restype = i32
+        lib.gemm_f32_host.argtypes = [i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, i64, i32,
+                                      i32]
+        lib.gemm_f32_host.restype = i32
         lib.hbm_copy_f32.argtypes = [vp, vp, ctypes.c_size_t, vp]
         lib.hbm_copy_f32.restype = i32
         lib.hbm_copy_calibrate.argtypes = [vp, vp, ctypes.c_size_t, i32, vp,
@@ -185,6 +191,13 @@ def gemm_f32_op(layout, op_a, op_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc
                 mode=MODE_AUTO, workspace=None, ws_bytes=0, stream=0) -> int:
     return load().gemm_f32_op(layout, op_a, op_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
                               _mode(mode), workspace, ws_bytes, stream)
+
+
+def gemm_f32_host(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, mode=MODE_AUTO,
+                  blocks=0) -> int:
+    """Host-memory GEMM (raw host addresses); blocking; returns the status."""
+    return load().gemm_f32_host(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, _mode(mode),
+                                blocks)
 
 
 def gemm_f32_splitk_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, split_k=0,
@@ -323,6 +336,36 @@ def matmul(A, B, C=None, alpha=1.0, beta=0.0, mode=MODE_AUTO, stream=None,
         what = "gemm_f32_op"
     if rc != OK:
         raise GemmError(rc, what)
+    return C
+
+
+def _host_matrix(t, name):
+    import torch
+    if not (t.device.type == "cpu" and t.dtype == torch.float32 and t.dim() == 2 and
+            (t.stride(1) == 1 or t.shape[1] <= 1)):
+        raise ValueError(f"{name} must be a 2-D float32 CPU tensor with unit column stride")
+    return max(t.stride(0), 1)
+
+
+def matmul_host(A, B, C=None, alpha=1.0, beta=0.0, mode=MODE_AUTO, blocks=0):
+    """C <- alpha * A @ B + beta * C for row-major float32 CPU tensors (pin
+    them with ``.pin_memory()`` so the copies overlap the GEMM).  The library
+    moves the data to the GPU and back in row blocks and runs the GEMM there;
+    the call returns when C holds the result.  Returns C."""
+    import torch
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K:
+        raise ValueError(f"inner dimensions differ: {K} vs {K2}")
+    if C is None:
+        if beta != 0.0:
+            raise ValueError("beta != 0 needs C")
+        C = torch.empty((M, N), dtype=torch.float32, pin_memory=A.is_pinned())
+    lda, ldb, ldc = _host_matrix(A, "A"), _host_matrix(B, "B"), _host_matrix(C, "C")
+    rc = load().gemm_f32_host(M, N, K, float(alpha), A.data_ptr(), lda, B.data_ptr(), ldb,
+                              float(beta), C.data_ptr(), ldc, _mode(mode), int(blocks))
+    if rc != OK:
+        raise GemmError(rc, "gemm_f32_host")
     return C
 
 

@@ -1,0 +1,105 @@
+"""GPU parity for gemm_f32_host: host buffers in, host buffer out, the
+product pipelined in row blocks (copies of later blocks overlapping the GEMM
+of the current one).  Checked against the oracle on the same seeded inputs,
+and bit for bit against the device-pointer call when both run one block
+with the same plan."""
+import numpy as np
+import pytest
+
+import oracle
+from tests.gpu_util import TOL_E1
+from workloads import matrix, sample_entries
+
+pytestmark = pytest.mark.gpu
+
+
+def host_tensor(arr, pinned):
+    import torch
+    t = torch.from_numpy(arr)
+    return t.pin_memory() if pinned else t.clone()
+
+
+def run_host(M, N, K, alpha, beta, mode, blocks, pad=(0, 0, 0), dist="u11", pinned=True,
+             seed=900):
+    import torch
+    from roofline_gb300 import gemm
+    a = matrix(M, K, K + pad[0], seed, dist)
+    b = matrix(K, N, N + pad[1], seed + 1, dist)
+    c = matrix(M, N, N + pad[2], seed + 2, dist)
+    hA, hB, hC = host_tensor(a, pinned), host_tensor(b, pinned), host_tensor(c, pinned)
+    rc = gemm.gemm_f32_host(M, N, K, alpha, hA.data_ptr(), K + pad[0], hB.data_ptr(), N + pad[1],
+                            beta, hC.data_ptr(), N + pad[2], gemm.MODES[mode], blocks)
+    assert rc == gemm.OK, gemm.strerror(rc)
+    out = hC.numpy()
+    if pad[2]:
+        assert np.all(np.isnan(out[:, N:]))  # padding of C untouched
+    return a[:, :K], b[:, :N], c[:, :N], out[:, :N].copy()
+
+
+CASES = [
+    # (M, N, K, blocks)
+    (1000, 300, 257, 3),    # ragged last block
+    (777, 513, 129, 0),
+    (513, 64, 1000, 5),
+    (128, 200, 64, 1),
+    (1, 7, 3, 0),
+    (300, 1, 65, 4),
+]
+
+
+@pytest.mark.parametrize("case", CASES)
+@pytest.mark.parametrize("mode", ["fp32_simt", "tf32x3", "tf32", "auto"])
+@pytest.mark.parametrize("beta", [0.0, -0.75])
+def test_host_matches_oracle(case, mode, beta):
+    M, N, K, blocks = case
+    A, B, C0, got = run_host(M, N, K, 1.5, beta, mode, blocks, pad=(3, 1, 2))
+    ref, D = oracle.gemm(A, B, 1.5, beta, C0 if beta else None, with_bound=True)
+    tol = 2e-3 if mode == "tf32" else TOL_E1
+    assert oracle.err_normalised(got, ref, D) <= tol
+
+
+@pytest.mark.parametrize("mode", ["fp32_simt", "tf32x3"])
+@pytest.mark.parametrize("blocks", [1, 4, 7])
+def test_host_integer_bit_exact(mode, blocks):
+    A, B, C0, got = run_host(1100, 260, 300, 1.0, 0.0, mode, blocks, dist="int2")
+    assert oracle.mismatches(got, oracle.gemm(A, B, 1.0, 0.0, None)) == 0
+
+
+def test_host_pageable_buffers():
+    A, B, C0, got = run_host(700, 400, 300, 1.0, 0.5, "auto", 3, pinned=False)
+    ref, D = oracle.gemm(A, B, 1.0, 0.5, C0, with_bound=True)
+    assert oracle.err_normalised(got, ref, D) <= TOL_E1
+
+
+def test_host_k_zero_scales_c():
+    # lda >= max(K, 1) = 1, as in BLAS
+    A, B, C0, got = run_host(300, 200, 0, 1.0, 2.0, "auto", 2, pad=(1, 0, 0))
+    assert np.array_equal(got, np.float32(2.0) * C0)
+
+
+@pytest.mark.parametrize("mode", ["fp32_simt", "tf32x3"])
+def test_host_one_block_equals_device_call(mode):
+    import torch
+    from roofline_gb300 import gemm
+    M, N, K = 640, 384, 320
+    A, B, C0, got = run_host(M, N, K, 0.5, 0.25, mode, 1)
+    dC = torch.from_numpy(C0.copy()).cuda()
+    gemm.matmul(torch.from_numpy(A.copy()).cuda(), torch.from_numpy(B.copy()).cuda(), dC, 0.5,
+                0.25, mode)
+    torch.cuda.synchronize()
+    assert np.array_equal(got.view(np.uint32), dC.cpu().numpy().view(np.uint32))
+
+
+@pytest.mark.parametrize("blocks", [0, 8])
+def test_host_square_4096_sampled(blocks):
+    import torch
+    from roofline_gb300 import gemm
+    from workloads import WORKLOADS
+    w = WORKLOADS["sq4096"]
+    a, b, _ = w.make()
+    hA = torch.from_numpy(a).pin_memory()
+    hB = torch.from_numpy(b).pin_memory()
+    hC = gemm.matmul_host(hA[:, :w.K], hB[:, :w.N], blocks=blocks)
+    rows, cols = sample_entries(w.M, w.N)
+    ref, D = oracle.gemm_entries(a[:, :w.K], b[:, :w.N], rows, cols, 1.0, 0.0, None)
+    assert oracle.err_normalised(hC.numpy()[rows, cols], ref, D) <= TOL_E1
