@@ -101,6 +101,9 @@ struct SimtConfig {
   int bm, bn, bk, threads;
 };
 SimtConfig simt_config();
+// Built (BK, stages) pairs of the 64 x 128 CUDA-core tile; the first is the default.
+#define GG_SIMT_CONFIGS(X) X(16, 4) X(32, 2)
+bool simt_config_valid(int bk, int stages);
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 

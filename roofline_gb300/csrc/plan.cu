@@ -78,11 +78,20 @@ void plan_simt(int64_t M, int64_t N, int64_t K, bool vec, const DeviceProps &dp,
   out->bn = c.bn;
   out->bk = c.bk;
   out->stages = 4;
+  // Tuning knob: GEMM_SIMT_CONFIG="bk,stages" picks another built K depth and
+  // ring length (ignored if it names none).
+  if (const char *cfg = std::getenv("GEMM_SIMT_CONFIG")) {
+    int bk = 0, st = 0;
+    if (std::sscanf(cfg, "%d,%d", &bk, &st) == 2 && simt_config_valid(bk, st)) {
+      out->bk = bk;
+      out->stages = st;
+    }
+  }
   out->threads = c.threads;
   out->vec = vec ? 1 : 0;
   if (split > 1) {
     // round the slice depth to whole BK tiles, then recount the slices
-    int64_t kps = ceil_div(ceil_div(K, split), c.bk) * c.bk;
+    int64_t kps = ceil_div(ceil_div(K, split), out->bk) * out->bk;
     split = (int)ceil_div(K, kps);
   }
   out->split_k = split;

@@ -294,6 +294,14 @@ __global__ void splitk_reduce_kernel(GemmArgs p, const float *__restrict__ ws, i
 
 SimtConfig simt_config() { return SimtConfig{64, 128, 16, kThreadsP}; }
 
+bool simt_config_valid(int bk, int stages) {
+#define GG_SIMT(BK_, ST_) \
+  if (bk == BK_ && stages == ST_) return true;
+  GG_SIMT_CONFIGS(GG_SIMT)
+#undef GG_SIMT
+  return false;
+}
+
 cudaError_t launch_splitk_reduce(const GemmArgs &p, const float *ws, int splits, cudaStream_t s) {
   int64_t blocks = ceil_div(p.M * p.N, 256);
   if (blocks > 4096) blocks = 4096;
@@ -329,12 +337,17 @@ cudaError_t launch_packed(const gemm_plan_t &plan, const GemmArgs &p, float *ws,
 }
 
 cudaError_t launch_simt(const gemm_plan_t &plan, const GemmArgs &p, float *ws, cudaStream_t s) {
-  if (!(plan.bm == 64 && plan.bn == 128 && plan.bk == 16 && plan.stages == 4))
-    return cudaErrorInvalidValue;
-  if (!p.ta && !p.tb) return launch_packed<64, 128, 16, 4, false, false>(plan, p, ws, s);
-  if (p.ta && !p.tb) return launch_packed<64, 128, 16, 4, true, false>(plan, p, ws, s);
-  if (!p.ta && p.tb) return launch_packed<64, 128, 16, 4, false, true>(plan, p, ws, s);
-  return launch_packed<64, 128, 16, 4, true, true>(plan, p, ws, s);
+  if (plan.bm != 64 || plan.bn != 128) return cudaErrorInvalidValue;
+#define GG_SIMT(BK_, ST_)                                                              \
+  if (plan.bk == BK_ && plan.stages == ST_) {                                          \
+    if (!p.ta && !p.tb) return launch_packed<64, 128, BK_, ST_, false, false>(plan, p, ws, s); \
+    if (p.ta && !p.tb) return launch_packed<64, 128, BK_, ST_, true, false>(plan, p, ws, s);   \
+    if (!p.ta && p.tb) return launch_packed<64, 128, BK_, ST_, false, true>(plan, p, ws, s);   \
+    return launch_packed<64, 128, BK_, ST_, true, true>(plan, p, ws, s);                       \
+  }
+  GG_SIMT_CONFIGS(GG_SIMT)
+#undef GG_SIMT
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace gg

@@ -20,6 +20,11 @@ from workloads import matrix
 pytestmark = pytest.mark.gpu
 
 ROW, COL, N_, T_ = 0, 1, 0, 1
+
+
+def _dense(x):
+    """A fresh C-ordered copy (canonical strides even for 1 x 1 views)."""
+    return np.array(x, dtype=np.float32, order="C", copy=True)
 COMBOS = list(itertools.product([ROW, COL], [N_, T_], [N_, T_]))
 
 
@@ -36,17 +41,17 @@ def stored(layout, op, rows, cols, pad, seed, dist):
         buf = matrix(sc, sr, ld, seed, dist)
         S = buf[:, :sr].T
     X = S if op == N_ else S.T
-    return buf, ld, np.ascontiguousarray(X)
+    return buf, ld, _dense(X)
 
 
 def c_buffer(layout, M, N, pad, seed, dist):
     if layout == ROW:
         ld = N + pad
         buf = matrix(M, N, ld, seed, dist)
-        return buf, ld, np.ascontiguousarray(buf[:, :N])
+        return buf, ld, _dense(buf[:, :N])
     ld = M + pad
     buf = matrix(N, M, ld, seed, dist)
-    return buf, ld, np.ascontiguousarray(buf[:, :M].T)
+    return buf, ld, _dense(buf[:, :M].T)
 
 
 def c_logical(layout, buf, M, N):
@@ -69,7 +74,7 @@ def run_op(layout, op_a, op_b, M, N, K, alpha, beta, dist, mode, pad=3, seed=700
     if pad:  # padding of C is never written
         pad_part = out[:, N:] if layout == ROW else out[:, M:]
         assert np.all(np.isnan(pad_part))
-    return A, B, C0, np.ascontiguousarray(c_logical(layout, out, M, N))
+    return A, B, C0, _dense(c_logical(layout, out, M, N))
 
 
 def run_plain(A, B, C0, alpha, beta, mode, transpose_problem=False):
@@ -78,7 +83,7 @@ def run_plain(A, B, C0, alpha, beta, mode, transpose_problem=False):
     import torch
     from roofline_gb300 import gemm
     if transpose_problem:
-        A, B, C0 = np.ascontiguousarray(B.T), np.ascontiguousarray(A.T), np.ascontiguousarray(C0.T)
+        A, B, C0 = _dense(B.T), _dense(A.T), _dense(C0.T)
     dA, dB, dC = (torch.from_numpy(x).cuda() for x in (A, B, C0))
     gemm.matmul(dA, dB, dC, alpha, beta, mode)
     torch.cuda.synchronize()
@@ -133,8 +138,8 @@ def test_op_bitwise_equals_plain_storage(layout, op_a, op_b, mode, monkeypatch):
     M, N, K = 333, 270, 161
     A, B, C0, got = run_op(layout, op_a, op_b, M, N, K, 0.75, 0.5, "u11", mode)
     want = run_plain(A, B, C0, 0.75, 0.5, mode, transpose_problem=(layout == COL))
-    assert np.array_equal(np.ascontiguousarray(got).view(np.uint32),
-                          np.ascontiguousarray(want).view(np.uint32))
+    assert np.array_equal(_dense(got).view(np.uint32),
+                          _dense(want).view(np.uint32))
 
 
 def test_matmul_takes_transposed_views():
@@ -145,8 +150,8 @@ def test_matmul_takes_transposed_views():
     Bt = torch.from_numpy(matrix(N, K, K, 12, "u11")).cuda()   # B^T stored row-major
     C = gemm.matmul(At.t(), Bt.t(), mode="fp32_simt")
     torch.cuda.synchronize()
-    A = np.ascontiguousarray(At.cpu().numpy().T)
-    B = np.ascontiguousarray(Bt.cpu().numpy().T)
+    A = _dense(At.cpu().numpy().T)
+    B = _dense(Bt.cpu().numpy().T)
     ref, D = oracle.gemm(A, B, 1.0, 0.0, None, with_bound=True)
     assert oracle.err_normalised(C.cpu().numpy(), ref, D) <= TOL_E1
 
@@ -164,8 +169,27 @@ def test_op_large_transposed_sampled(mode):
     C = gemm.matmul(dAt.t(), dBt.t(), mode=mode)
     torch.cuda.synchronize()
     rows, cols = sample_entries(M, N, n=2048)
-    A = np.ascontiguousarray(At.T)
-    B = np.ascontiguousarray(Bt.T)
+    A = _dense(At.T)
+    B = _dense(Bt.T)
     ref, D = oracle.gemm_entries(A, B, rows, cols, 1.0, 0.0, None)
     got = C.cpu().numpy()[rows, cols]
     assert oracle.err_normalised(got, ref, D) <= TOL_E1
+
+
+SIMT_BUILT = ["16,4", "32,2"]
+
+
+@pytest.mark.parametrize("cfg", SIMT_BUILT)
+@pytest.mark.parametrize("op_a,op_b", [(N_, N_), (T_, N_), (N_, T_), (T_, T_)])
+@pytest.mark.parametrize("shape", [(333, 270, 161), (64, 128, 32), (1, 1, 1), (200, 131, 1003)])
+def test_simt_every_built_configuration(cfg, op_a, op_b, shape, monkeypatch):
+    from roofline_gb300 import gemm
+    monkeypatch.setenv("GEMM_SIMT_CONFIG", cfg)
+    M, N, K = shape
+    p = gemm.plan_op(ROW, op_a, op_b, M, N, K, mode="fp32_simt")
+    assert "%d,%d" % (p["bk"], p["stages"]) == cfg
+    A, B, C0, got = run_op(ROW, op_a, op_b, M, N, K, 1.25, 0.5, "u11", "fp32_simt")
+    ref, D = oracle.gemm(A, B, 1.25, 0.5, C0, with_bound=True)
+    assert oracle.err_normalised(got, ref, D) <= TOL_E1
+    A, B, C0, got = run_op(ROW, op_a, op_b, M, N, K, 1.0, 0.0, "int2", "fp32_simt")
+    assert oracle.mismatches(got, oracle.gemm(A, B, 1.0, 0.0, None)) == 0
