@@ -91,8 +91,8 @@ cudaError_t launch_fma_peak(int64_t iters, int packed, int sm_count, float *sink
 int launch_tc(const gemm_plan_t &plan, const GemmArgs &p, void *ws, size_t ws_bytes,
               cudaStream_t s);
 uint64_t tc_workspace_bytes(const gemm_plan_t &plan, int64_t M, int64_t N, int64_t K);
-bool tc_config_valid(int bn, int bk, int stages, int a_inkernel, int concat, int nprod);
-int tc_ctas_per_sm(int bn, int bk, int stages, int a_inkernel, int concat, int nprod,
+bool tc_config_valid(int bm, int bn, int bk, int stages, int a_inkernel, int concat, int nprod);
+int tc_ctas_per_sm(int bm, int bn, int bk, int stages, int a_inkernel, int concat, int nprod,
                    int smem_per_sm);
 int tc_read_and_clear_status(cudaStream_t s);
 

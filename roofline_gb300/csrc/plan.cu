@@ -201,22 +201,37 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
       const bool wide = N > 128 && tiles256 >= 2 * sms;
       p.a_split_in_kernel = a_aligned ? 1 : 0;
       p.launches = a_aligned ? 2 : 3;
-      auto set = [&](int bn, int bk, int st, int cc) {
-        p.bn = bn; p.bk = bk; p.stages = st; p.b_concat = cc;
+      auto set = [&](int bn, int bk, int st, int cc, int bm = 128) {
+        p.bm = bm; p.bn = bn; p.bk = bk; p.stages = st; p.b_concat = cc;
+      };
+      // 256 x 256 tiles (two 128-row accumulators sharing each B tile) halve
+      // the operand bytes per MMA; they take pre-split operands.
+      const int64_t tiles_m2 = ceil_div(M, 256) * ceil_div(N, 256);
+      auto pre_split = [&]() {
+        p.a_split_in_kernel = 0;
+        p.launches = 3;
       };
       if (!x3) {
-        // 1xTF32: no A_lo / B_lo, so more stages fit.  Narrow B (HBM-bound on
-        // A): split A on chip so it is read once.  Otherwise pre-split A as
-        // well: with one MMA per K step the on-chip split is the slower
-        // stage (GB300, 4096^3: 388 us on chip against 338 us with the
-        // pre-pass; 8192^3: 2.85 ms against 2.00 ms).
+        // 1xTF32: one MMA per K step, so feeding operands is the limit.
+        // Narrow B (HBM-bound on A): 128-row tiles with A split on chip, so A
+        // is read once.  Wide: 256 x 256 tiles (GB300: 4096^3 kernel 176 us
+        // against 241 us with 128 x 256 tiles, 8192^3 1.15 ms against
+        // 1.87 ms).  Otherwise 128 x 256 tiles, pre-split (the on-chip split
+        // is the slower stage with a single MMA per K step).
         if (a_aligned && N <= 64) {
           set(64, 32, 4, 0);
+        } else if (wide) {
+          set(256, 32, 3, 0, 256);
+          pre_split();
         } else {
           set(256, 16, 8, 0);
-          p.a_split_in_kernel = 0;
-          p.launches = 3;
+          pre_split();
         }
+      } else if (wide && tiles_m2 >= 4 * sms) {
+        // many tiles: 256 x 256 tiles, pre-split A (GB300, 8192^3: kernel
+        // 3.03 ms against 3.31 ms for 128 x 256 tiles with A split on chip)
+        set(256, 16, 3, 0, 256);
+        pre_split();
       } else if (a_aligned) {
         if (N <= 64) set(64, 32, 3, 1);        // narrow: 2 CTAs per SM stream A
         else if (wide) set(256, 16, 5, 0);
@@ -226,19 +241,24 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
         else set(128, 16, 3, 1);
       }
       // Tuning knob: GEMM_TC_CONFIG="bn,bk,stages,a_split_in_kernel,b_concat"
-      // picks one of the built configurations (ignored if it names none, or
-      // asks for the in-kernel split with a misaligned A).
+      // (128-row tile) or "bm,bn,bk,stages,a_split_in_kernel,b_concat" picks
+      // one of the built configurations (ignored if it names none, or asks
+      // for the in-kernel split with a misaligned A).
       if (const char *cfg = std::getenv("GEMM_TC_CONFIG")) {
-        int bn = 0, bk = 0, st = 0, ak = 0, cc = 0;
-        if (std::sscanf(cfg, "%d,%d,%d,%d,%d", &bn, &bk, &st, &ak, &cc) == 5 &&
-            tc_config_valid(bn, bk, st, ak, cc, nprod) && (!ak || a_aligned)) {
-          set(bn, bk, st, cc);
-          p.a_split_in_kernel = ak;
-          p.launches = ak ? 2 : 3;
+        int v[6] = {0, 0, 0, 0, 0, 0};
+        const int n = std::sscanf(cfg, "%d,%d,%d,%d,%d,%d", &v[0], &v[1], &v[2], &v[3], &v[4],
+                                  &v[5]);
+        const int *c = n == 6 ? v + 1 : v;
+        const int bm = n == 6 ? v[0] : 128;
+        if ((n == 5 || n == 6) && tc_config_valid(bm, c[0], c[1], c[2], c[3], c[4], nprod) &&
+            (!c[3] || a_aligned)) {
+          set(c[0], c[1], c[2], c[4], bm);
+          p.a_split_in_kernel = c[3];
+          p.launches = c[3] ? 2 : 3;
         }
       }
-      p.ctas_per_sm = tc_ctas_per_sm(p.bn, p.bk, p.stages, p.a_split_in_kernel, p.b_concat, nprod,
-                                     dp.smem_per_sm > 0 ? dp.smem_per_sm : 233472);
+      p.ctas_per_sm = tc_ctas_per_sm(p.bm, p.bn, p.bk, p.stages, p.a_split_in_kernel, p.b_concat,
+                                     nprod, dp.smem_per_sm > 0 ? dp.smem_per_sm : 233472);
       // Stream-K: when the tiles do not fill whole waves of resident CTAs,
       // launch one wave of persistent CTAs that split the (tile, K block)
       // work evenly (each at least 4 K blocks); a fix-up kernel sums the

@@ -47,7 +47,6 @@ namespace {
 
 __device__ int g_tc_status;  // 0 = ok, else a GEMM_ERR_* code
 
-constexpr int kBM = 128;
 constexpr int kThreadsTC = 192;
 constexpr int kConvThreads = 128;  // warps 2..5
 
@@ -262,33 +261,58 @@ struct TcParams {
   int64_t ldc;
   int num_kb;        // K blocks per output tile
   int tiles_n;       // output tiles along N (tile t = m_tile * tiles_n + n_tile)
-  int64_t total;     // tiles * num_kb: the (tile, K block) work units
+  int waves;         // whole tiles per CTA before the stream-K part
+  int64_t dp_tiles;  // waves * G: tiles done whole, in waves
+  int64_t sk_units;  // (tiles - dp_tiles) * num_kb: units shared out stream-K
   float *partial;    // stream-K partial tiles: 2 slots of 128 x BN per CTA
   uint64_t timeout_ns;
   int stall_producer;  // test hook: the producer issues nothing
 };
 
-// Work split (stream-K): CTA c of G owns the work units [c*total/G,
-// (c+1)*total/G), walked tile by tile.  With G = tiles each CTA owns exactly
-// one whole tile.
+// Work split.  CTA c of G first takes `waves` whole tiles, c, c + G, ...:
+// the CTAs of one wave start their tiles together and walk K in step, so the
+// operand slices of a wave are shared through L2.  The (tile, K block) units
+// of the tiles left over are then split evenly (stream-K): CTA c owns units
+// [c*S/G, (c+1)*S/G) of them, walked tile by tile.  Without stream-K,
+// G = tiles: one wave of one tile per CTA.
 struct Segment {
   int tile, kb0, kb1;  // K blocks [kb0, kb1) of output tile `tile`
+  int slot;            // stream-K partial slot: 0 first stream-K segment, 1 later ones
 };
 
 __host__ __device__ __forceinline__ int64_t unit_begin(int64_t total, int64_t c, int64_t G) {
   return total * c / G;
 }
 
-// Segment `i` of the walk [u0, u1) (valid while the returned kb1 > kb0).
-__device__ __forceinline__ bool next_segment(int64_t &u, int64_t u1, int num_kb, Segment &sg) {
-  if (u >= u1) return false;
-  sg.tile = (int)(u / num_kb);
-  sg.kb0 = (int)(u % num_kb);
-  const int64_t left = u1 - u;
-  sg.kb1 = (int)(sg.kb0 + left < num_kb ? sg.kb0 + left : num_kb);
-  u += sg.kb1 - sg.kb0;
-  return true;
-}
+struct Walk {
+  int64_t c, G, u, u1;
+  int w;
+  bool first_sk;
+
+  __device__ __forceinline__ Walk(const TcParams &p, int64_t cta, int64_t grid)
+      : c(cta), G(grid), u(unit_begin(p.sk_units, cta, grid)),
+        u1(unit_begin(p.sk_units, cta + 1, grid)), w(0), first_sk(true) {}
+
+  __device__ __forceinline__ bool next(const TcParams &p, Segment &sg) {
+    if (w < p.waves) {
+      sg.tile = (int)((int64_t)w * G + c);
+      sg.kb0 = 0;
+      sg.kb1 = p.num_kb;
+      sg.slot = 0;
+      ++w;
+      return true;
+    }
+    if (u >= u1) return false;
+    sg.tile = (int)(p.dp_tiles + u / p.num_kb);
+    sg.kb0 = (int)(u % p.num_kb);
+    const int64_t left = u1 - u;
+    sg.kb1 = (int)(sg.kb0 + left < p.num_kb ? sg.kb0 + left : p.num_kb);
+    u += sg.kb1 - sg.kb0;
+    sg.slot = first_sk ? 0 : 1;
+    first_sk = false;
+    return true;
+  }
+};
 
 // BN: output columns per CTA.  BK: K depth of one stage (16 -> 64-byte
 // swizzle, 32 -> 128-byte swizzle).  AK: A arrives raw (FP32) and the
@@ -297,12 +321,16 @@ __device__ __forceinline__ bool next_segment(int64_t &u, int64_t u1, int num_kb,
 // and A_lo come pre-split from the workspace.  CONCAT: B_hi and B_lo sit
 // next to each other in the stage, so A_hi*[B_hi | B_lo] is one MMA of width
 // 2*BN into two accumulators that the epilogue adds.
-template <int BN, int BK, int STAGES, bool AK, bool CONCAT, int NPROD>
+template <int BM, int BN, int BK, int STAGES, bool AK, bool CONCAT, int NPROD>
 struct TcCfg {
   static_assert(NPROD == 3 || NPROD == 1, "3xTF32 or 1xTF32");
   static_assert(NPROD == 3 || !CONCAT, "1xTF32 has no B_lo to concatenate");
+  static_assert(BM == 128 || (BM == 256 && !AK && !CONCAT),
+                "a 256-row tile takes pre-split operands and separate B planes");
   static constexpr bool X3 = NPROD == 3;
-  static constexpr int A_BYTES = kBM * BK * 4;
+  static constexpr int MH = BM / 128;  // 128-row halves, one accumulator each
+  static constexpr int A_BYTES = BM * BK * 4;
+  static constexpr int A_HALF_BYTES = 128 * BK * 4;
   static constexpr int B_BYTES = BN * BK * 4;
   static constexpr int A_SMEM = (AK || !X3) ? A_BYTES : 2 * A_BYTES;  // A (raw/hi) [+ A_lo]
   static constexpr int B_SMEM = X3 ? 2 * B_BYTES : B_BYTES;           // B_hi [+ B_lo]
@@ -311,7 +339,7 @@ struct TcCfg {
   static constexpr int ROW_BYTES = BK * 4;              // 64 or 128
   static constexpr uint32_t LAYOUT = ROW_BYTES == 128 ? 2u : 4u;
   static constexpr uint32_t SBO = 8 * ROW_BYTES;        // 8-row group stride
-  static constexpr int ACC_COLS = CONCAT ? 2 * BN : BN;
+  static constexpr int ACC_COLS = MH * (CONCAT ? 2 * BN : BN);
   static constexpr int LO_COL0 = ACC_COLS;
   static constexpr int LO_COLS = (AK && X3) ? STAGES * BK : 0;
   static constexpr int TMEM_NEED = ACC_COLS + LO_COLS;
@@ -327,13 +355,13 @@ struct TcCfg {
   static_assert(TMEM_NEED <= 512, "tensor memory");
 };
 
-template <int BN, int BK, int STAGES, bool AK, bool CONCAT, int NPROD>
+template <int BM, int BN, int BK, int STAGES, bool AK, bool CONCAT, int NPROD>
 __global__ void __launch_bounds__(kThreadsTC, 1)
 tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
                  const __grid_constant__ CUtensorMap tmA_lo,
                  const __grid_constant__ CUtensorMap tmB_hi,
                  const __grid_constant__ CUtensorMap tmB_lo, TcParams p) {
-  using Cfg = TcCfg<BN, BK, STAGES, AK, CONCAT, NPROD>;
+  using Cfg = TcCfg<BM, BN, BK, STAGES, AK, CONCAT, NPROD>;
   constexpr bool X3 = Cfg::X3;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -355,8 +383,6 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t G = gridDim.x;
-  const int64_t u_begin = unit_begin(p.total, blockIdx.x, G);
-  const int64_t u_end = unit_begin(p.total, blockIdx.x + 1, G);
   const uint64_t deadline = globaltimer() + p.timeout_ns;
 
   if (threadIdx.x == 0) {
@@ -393,10 +419,10 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
     // ---------------- TMA producer: every stage of every segment, in order
     int issued = 0;
     if (lane == 0 && !p.stall_producer) {
-      int64_t u = u_begin;
+      Walk walk(p, blockIdx.x, G);
       Segment sg;
-      while (ok && next_segment(u, u_end, p.num_kb, sg)) {
-        const int32_t m0 = (sg.tile / p.tiles_n) * kBM;
+      while (ok && walk.next(p, sg)) {
+        const int32_t m0 = (sg.tile / p.tiles_n) * BM;
         const int32_t n0 = (sg.tile % p.tiles_n) * BN;
         for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
           const int s = issued % STAGES;
@@ -424,13 +450,13 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
   } else if (warp == 1) {
     // ---------------- MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_tf32(kBM, BN);
-      constexpr uint32_t idesc2 = idesc_tf32(kBM, CONCAT ? 2 * BN : BN);
+      constexpr uint32_t idesc = idesc_tf32(128, BN);
+      constexpr uint32_t idesc2 = idesc_tf32(128, CONCAT ? 2 * BN : BN);
       bool any = false;
       int it = 0, si = 0;
-      int64_t u = u_begin;
+      Walk walk(p, blockIdx.x, G);
       Segment sg;
-      while (ok && next_segment(u, u_end, p.num_kb, sg)) {
+      while (ok && walk.next(p, sg)) {
         if (si > 0) {
           // the epilogue must have drained the previous segment's accumulator
           if (!mbar_wait(acc_empty, (uint32_t)(si - 1) & 1u, deadline, abort_flag)) {
@@ -453,26 +479,33 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
 #pragma unroll
           for (int kk = 0; kk < BK / 8; ++kk) {
             const uint32_t off = kk * 32;  // 8 TF32 values = 32 bytes along K
-            const uint64_t dah = smem_desc(ah + off, Cfg::SBO, Cfg::LAYOUT);
             const uint64_t dbh = smem_desc(bh + off, Cfg::SBO, Cfg::LAYOUT);
             const uint32_t acc = (kb > sg.kb0 || kk > 0) ? 1u : 0u;
-            if (!X3) {
-              mma_tf32(tmem_base, dah, dbh, idesc, acc);  // 1xTF32: A_hi * B_hi only
-            } else if (CONCAT) {
-              // columns [0, BN): A_hi*B_hi (+ A_lo*B_hi); [BN, 2BN): A_hi*B_lo
-              mma_tf32(tmem_base, dah, dbh, idesc2, acc);
-              if (AK)
-                mma_tf32_ts(tmem_base, lo_t + kk * 8, dbh, idesc, 1u);
-              else
-                mma_tf32(tmem_base, smem_desc(al + off, Cfg::SBO, Cfg::LAYOUT), dbh, idesc, 1u);
-            } else {
-              const uint64_t dbl = smem_desc(bl + off, Cfg::SBO, Cfg::LAYOUT);
-              mma_tf32(tmem_base, dah, dbl, idesc, acc);  // small terms first
-              if (AK)
-                mma_tf32_ts(tmem_base, lo_t + kk * 8, dbh, idesc, 1u);
-              else
-                mma_tf32(tmem_base, smem_desc(al + off, Cfg::SBO, Cfg::LAYOUT), dbh, idesc, 1u);
-              mma_tf32(tmem_base, dah, dbh, idesc, 1u);
+            // each 128-row half of the A tile feeds its own accumulator
+#pragma unroll
+            for (int h = 0; h < Cfg::MH; ++h) {
+              const uint32_t ah_h = ah + h * Cfg::A_HALF_BYTES + off;
+              const uint32_t al_h = al + h * Cfg::A_HALF_BYTES + off;
+              const uint32_t d = tmem_base + (uint32_t)(h * BN);
+              const uint64_t dah = smem_desc(ah_h, Cfg::SBO, Cfg::LAYOUT);
+              if (!X3) {
+                mma_tf32(d, dah, dbh, idesc, acc);  // 1xTF32: A_hi * B_hi only
+              } else if (CONCAT) {
+                // columns [0, BN): A_hi*B_hi (+ A_lo*B_hi); [BN, 2BN): A_hi*B_lo
+                mma_tf32(d, dah, dbh, idesc2, acc);
+                if (AK)
+                  mma_tf32_ts(d, lo_t + kk * 8, dbh, idesc, 1u);
+                else
+                  mma_tf32(d, smem_desc(al_h, Cfg::SBO, Cfg::LAYOUT), dbh, idesc, 1u);
+              } else {
+                const uint64_t dbl = smem_desc(bl + off, Cfg::SBO, Cfg::LAYOUT);
+                mma_tf32(d, dah, dbl, idesc, acc);  // small terms first
+                if (AK)
+                  mma_tf32_ts(d, lo_t + kk * 8, dbh, idesc, 1u);
+                else
+                  mma_tf32(d, smem_desc(al_h, Cfg::SBO, Cfg::LAYOUT), dbh, idesc, 1u);
+                mma_tf32(d, dah, dbh, idesc, 1u);
+              }
             }
           }
           mma_commit(&empty[s]);
@@ -499,9 +532,9 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
     const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16);
     const bool vec = ((p.ldc & 3) == 0) && ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0);
     int it = 0, si = 0;
-    int64_t u = u_begin;
+    Walk walk(p, blockIdx.x, G);
     Segment sg;
-    while (ok && next_segment(u, u_end, p.num_kb, sg)) {
+    while (ok && walk.next(p, sg)) {
       if (AK) {
         for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++it) {
           const int s = it % STAGES;
@@ -567,57 +600,63 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
       }
       tc_fence_after();
       const bool whole = sg.kb0 == 0 && sg.kb1 == p.num_kb;
-      const int64_t m0 = (int64_t)(sg.tile / p.tiles_n) * kBM;
+      const int64_t m0 = (int64_t)(sg.tile / p.tiles_n) * BM;
       const int64_t n0 = (int64_t)(sg.tile % p.tiles_n) * BN;
-      const int64_t grow = m0 + row;
-      // partial tiles: slot 0 for this CTA's first segment, 1 for its last
-      float *prow = p.partial + ((int64_t)(blockIdx.x * 2 + (si == 0 ? 0 : 1)) * kBM + row) * BN;
+      // each 128-row half of the tile sits in its own accumulator columns
 #pragma unroll 1
-      for (int c = 0; c < BN; c += 32) {
-        uint32_t r[32];
-        tmem_ld32(lane_base + (uint32_t)c, r);
-        if (CONCAT) {
-          uint32_t r2[32];
-          tmem_ld32(lane_base + (uint32_t)(BN + c), r2);
-          tmem_ld_wait();
+      for (int h = 0; h < Cfg::MH; ++h) {
+        const int tr = h * 128 + row;  // row within the tile
+        const int64_t grow = m0 + tr;
+        const uint32_t lane_acc = lane_base + (uint32_t)(h * BN);
+        // partial tiles: slot 0 for this CTA's first stream-K segment, 1 for its last
+        float *prow = p.partial + ((int64_t)(blockIdx.x * 2 + sg.slot) * BM + tr) * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t r[32];
+          tmem_ld32(lane_acc + (uint32_t)c, r);
+          if (CONCAT) {
+            uint32_t r2[32];
+            tmem_ld32(lane_acc + (uint32_t)(BN + c), r2);
+            tmem_ld_wait();
 #pragma unroll
-          for (int q = 0; q < 32; ++q)
-            r[q] = __float_as_uint(__uint_as_float(r[q]) + __uint_as_float(r2[q]));
-        } else {
-          tmem_ld_wait();
-        }
-        if (!whole) {
-#pragma unroll
-          for (int q = 0; q < 32; q += 4)
-            *reinterpret_cast<float4 *>(prow + c + q) =
-                make_float4(__uint_as_float(r[q]), __uint_as_float(r[q + 1]),
-                            __uint_as_float(r[q + 2]), __uint_as_float(r[q + 3]));
-        } else if (grow < p.M) {
-          float *dst = p.C + grow * p.ldc + n0 + c;
-          const int64_t left = p.N - (n0 + c);
-          if (vec && left >= 32) {
-#pragma unroll
-            for (int q = 0; q < 32; q += 4) {
-              float4 o = make_float4(p.alpha * __uint_as_float(r[q]),
-                                     p.alpha * __uint_as_float(r[q + 1]),
-                                     p.alpha * __uint_as_float(r[q + 2]),
-                                     p.alpha * __uint_as_float(r[q + 3]));
-              if (p.beta != 0.0f) {
-                const float4 old = *reinterpret_cast<const float4 *>(dst + q);
-                o.x = fmaf(p.beta, old.x, o.x);
-                o.y = fmaf(p.beta, old.y, o.y);
-                o.z = fmaf(p.beta, old.z, o.z);
-                o.w = fmaf(p.beta, old.w, o.w);
-              }
-              *reinterpret_cast<float4 *>(dst + q) = o;
-            }
+            for (int q = 0; q < 32; ++q)
+              r[q] = __float_as_uint(__uint_as_float(r[q]) + __uint_as_float(r2[q]));
           } else {
+            tmem_ld_wait();
+          }
+          if (!whole) {
 #pragma unroll
-            for (int q = 0; q < 32; ++q) {
-              if (q < left) {
-                float o = p.alpha * __uint_as_float(r[q]);
-                if (p.beta != 0.0f) o = fmaf(p.beta, dst[q], o);
-                dst[q] = o;
+            for (int q = 0; q < 32; q += 4)
+              *reinterpret_cast<float4 *>(prow + c + q) =
+                  make_float4(__uint_as_float(r[q]), __uint_as_float(r[q + 1]),
+                              __uint_as_float(r[q + 2]), __uint_as_float(r[q + 3]));
+          } else if (grow < p.M) {
+            float *dst = p.C + grow * p.ldc + n0 + c;
+            const int64_t left = p.N - (n0 + c);
+            if (vec && left >= 32) {
+#pragma unroll
+              for (int q = 0; q < 32; q += 4) {
+                float4 o = make_float4(p.alpha * __uint_as_float(r[q]),
+                                       p.alpha * __uint_as_float(r[q + 1]),
+                                       p.alpha * __uint_as_float(r[q + 2]),
+                                       p.alpha * __uint_as_float(r[q + 3]));
+                if (p.beta != 0.0f) {
+                  const float4 old = *reinterpret_cast<const float4 *>(dst + q);
+                  o.x = fmaf(p.beta, old.x, o.x);
+                  o.y = fmaf(p.beta, old.y, o.y);
+                  o.z = fmaf(p.beta, old.z, o.z);
+                  o.w = fmaf(p.beta, old.w, o.w);
+                }
+                *reinterpret_cast<float4 *>(dst + q) = o;
+              }
+            } else {
+#pragma unroll
+              for (int q = 0; q < 32; ++q) {
+                if (q < left) {
+                  float o = p.alpha * __uint_as_float(r[q]);
+                  if (p.beta != 0.0f) o = fmaf(p.beta, dst[q], o);
+                  dst[q] = o;
+                }
               }
             }
           }
@@ -639,38 +678,41 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
 
 // Stream-K fix-up: an output tile whose K blocks were split between CTAs
 // gets C = alpha * (sum of its partial tiles, in CTA order) + beta * C.
-// Block j looks at the boundary between CTAs j and j+1; the block whose
-// boundary is the first one strictly inside a tile handles that tile, all
-// other blocks return at once (whole tiles were written by the GEMM).
+// Block j looks at the boundary between CTAs j and j+1 in the stream-K unit
+// space; the block whose boundary is the first one strictly inside a tile
+// handles that tile, all other blocks return at once (whole tiles were
+// written by the GEMM).
 constexpr int kFixMaxParts = 256;
 
 __global__ void __launch_bounds__(256)
-streamk_fixup_kernel(TcParams p, int BN, int64_t G) {
+streamk_fixup_kernel(TcParams p, int BM, int BN, int64_t G) {
   __shared__ int64_t part_off[kFixMaxParts];
   __shared__ int nparts;
   grid_dependency_wait();  // the GEMM's partial tiles
   const int64_t c = (int64_t)blockIdx.x + 1;  // boundary between CTAs c-1 and c
-  const int64_t b = unit_begin(p.total, c, G);
-  const int64_t t = b / p.num_kb;
-  const int64_t first = t * p.num_kb, last = first + p.num_kb - 1;
-  if (b == first || b > last) return;                    // not strictly inside a tile
-  if (unit_begin(p.total, c - 1, G) > first) return;     // an earlier boundary owns it
+  // boundaries live in the stream-K unit space (tiles after the whole-tile waves)
+  const int64_t b = unit_begin(p.sk_units, c, G);
+  const int64_t tl = b / p.num_kb;
+  const int64_t t = p.dp_tiles + tl;
+  const int64_t first = tl * p.num_kb, last = first + p.num_kb - 1;
+  if (b == first || b > last) return;                       // not strictly inside a tile
+  if (unit_begin(p.sk_units, c - 1, G) > first) return;     // an earlier boundary owns it
   if (threadIdx.x == 0) {
     int n = 0;
-    for (int64_t cta = c - 1; cta < G && unit_begin(p.total, cta, G) <= last; ++cta) {
-      const int64_t ub = unit_begin(p.total, cta, G), ue = unit_begin(p.total, cta + 1, G);
+    for (int64_t cta = c - 1; cta < G && unit_begin(p.sk_units, cta, G) <= last; ++cta) {
+      const int64_t ub = unit_begin(p.sk_units, cta, G), ue = unit_begin(p.sk_units, cta + 1, G);
       if (ub == ue) continue;  // no work
       // the tile is this CTA's first segment (slot 0) or its last (slot 1)
       const int slot = (ub >= first) ? 0 : 1;
-      if (n < kFixMaxParts) part_off[n++] = (cta * 2 + slot) * (int64_t)kBM * BN;
+      if (n < kFixMaxParts) part_off[n++] = (cta * 2 + slot) * (int64_t)BM * BN;
     }
     nparts = n;
   }
   __syncthreads();
   const int n = nparts;
-  // blockIdx.y picks 32 of the tile's 128 rows; each thread keeps four
+  // blockIdx.y picks 32 of the tile's BM rows; each thread keeps four
   // independent 16-byte sums so several loads are in flight
-  const int64_t m0 = (t / p.tiles_n) * kBM + blockIdx.y * 32;
+  const int64_t m0 = (t / p.tiles_n) * BM + blockIdx.y * 32;
   const int64_t n0 = (t % p.tiles_n) * BN;
   const int64_t row0 = (int64_t)blockIdx.y * 32 * BN;  // offset of these rows in a part
   const bool vec = ((p.ldc & 3) == 0) && ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0);
@@ -873,7 +915,7 @@ struct WsLayout {
 // planes come first so their place depends only on N, K and the mode: calls
 // that share B (row blocks of one product) can reuse them.
 WsLayout ws_layout(int64_t M, int64_t N, int64_t K, bool a_inkernel, int64_t streamk_ctas,
-                   int bn, bool x3) {
+                   int bm, int bn, bool x3) {
   WsLayout w{};
   w.kp = round_up(K, 4);
   const uint64_t b_bytes = align256((uint64_t)N * w.kp * 4);
@@ -885,20 +927,20 @@ WsLayout ws_layout(int64_t M, int64_t N, int64_t K, bool a_inkernel, int64_t str
   w.a_hi = b_bytes + b_lo_bytes;
   w.a_lo = w.a_hi + a_bytes;
   w.partial = w.a_lo + a_lo_bytes;
-  w.total = w.partial + (uint64_t)streamk_ctas * 2 * kBM * bn * 4;
+  w.total = w.partial + (uint64_t)streamk_ctas * 2 * bm * bn * 4;
   return w;
 }
 
-template <int BN, int BK, int STAGES, bool AK, bool CONCAT, int NPROD>
+template <int BM, int BN, int BK, int STAGES, bool AK, bool CONCAT, int NPROD>
 int launch_cfg(const gemm_plan_t &plan, const GemmArgs &a, char *ws, cudaStream_t s) {
-  using Cfg = TcCfg<BN, BK, STAGES, AK, CONCAT, NPROD>;
+  using Cfg = TcCfg<BM, BN, BK, STAGES, AK, CONCAT, NPROD>;
   constexpr bool X3 = Cfg::X3;
-  const int64_t tiles_m = ceil_div(a.M, kBM), tiles_n = ceil_div(a.N, BN);
+  const int64_t tiles_m = ceil_div(a.M, BM), tiles_n = ceil_div(a.N, BN);
   const int64_t tiles = tiles_m * tiles_n;
   const int num_kb = (int)ceil_div(a.K, BK);
   const int64_t G = plan.stream_k ? plan.grid_ctas : tiles;
   if (G < 1 || G > 0x7fffffff || tiles > 0x7fffffff) return GEMM_ERR_UNSUPPORTED;
-  const WsLayout L = ws_layout(a.M, a.N, a.K, AK, plan.stream_k ? G : 0, BN, X3);
+  const WsLayout L = ws_layout(a.M, a.N, a.K, AK, plan.stream_k ? G : 0, BM, BN, X3);
   float *ahi = reinterpret_cast<float *>(ws + L.a_hi);
   float *alo = reinterpret_cast<float *>(ws + L.a_lo);
   float *bhi = reinterpret_cast<float *>(ws + L.b_hi);
@@ -930,12 +972,12 @@ int launch_cfg(const gemm_plan_t &plan, const GemmArgs &a, char *ws, cudaStream_
   CUtensorMap tA0, tA1, tB0, tB1;
   bool ok;
   if (AK) {
-    ok = encode_2d(&tA0, a.A, a.K, a.M, a.lda, BK, kBM);
+    ok = encode_2d(&tA0, a.A, a.K, a.M, a.lda, BK, BM);
     tA1 = tA0;
   } else {
-    ok = encode_2d(&tA0, ahi, L.kp, a.M, L.kp, BK, kBM);
+    ok = encode_2d(&tA0, ahi, L.kp, a.M, L.kp, BK, BM);
     tA1 = tA0;
-    if (X3) ok = ok && encode_2d(&tA1, alo, L.kp, a.M, L.kp, BK, kBM);
+    if (X3) ok = ok && encode_2d(&tA1, alo, L.kp, a.M, L.kp, BK, BM);
   }
   ok = ok && encode_2d(&tB0, bhi, L.kp, a.N, L.kp, BK, BN);
   tB1 = tB0;
@@ -952,12 +994,24 @@ int launch_cfg(const gemm_plan_t &plan, const GemmArgs &a, char *ws, cudaStream_
   p.ldc = a.ldc;
   p.num_kb = num_kb;
   p.tiles_n = (int)tiles_n;
-  p.total = tiles * num_kb;
+  // Whole-tile waves first, the rest of the tiles stream-K (G == tiles
+  // without stream-K: one wave).  A short stream-K part would give each CTA
+  // only a few K blocks and the fix-up many parts per tile, so the last whole
+  // wave is folded into it until each CTA gets at least 4 K blocks and a
+  // tile at most ~250 parts (the fix-up sums up to 256).
+  int64_t waves = tiles / G, rest = tiles - waves * G;
+  while (rest > 0 && waves > 0 && (rest * num_kb < 4 * G || G > 250 * rest)) {
+    --waves;
+    rest += G;
+  }
+  p.waves = (int)waves;
+  p.dp_tiles = waves * G;
+  p.sk_units = rest * num_kb;
   p.partial = reinterpret_cast<float *>(ws + L.partial);
   p.timeout_ns = env_u64("GEMM_DEBUG_WAIT_LIMIT_NS", 2000000000ull);
   p.stall_producer = (int)env_u64("GEMM_DEBUG_STALL_PRODUCER", 0);
 
-  auto kern = tc_tf32x3_kernel<BN, BK, STAGES, AK, CONCAT, NPROD>;
+  auto kern = tc_tf32x3_kernel<BM, BN, BK, STAGES, AK, CONCAT, NPROD>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Cfg::SMEM_BYTES) != cudaSuccess) {
     cudaGetLastError();
@@ -988,12 +1042,12 @@ int launch_cfg(const gemm_plan_t &plan, const GemmArgs &a, char *ws, cudaStream_
   }
   if (plan.stream_k) {
     cudaLaunchConfig_t fc = {};
-    fc.gridDim = dim3((unsigned)(G - 1), kBM / 32);
+    fc.gridDim = dim3((unsigned)(G - 1), BM / 32);
     fc.blockDim = dim3(256);
     fc.stream = s;
     fc.attrs = attr;
     fc.numAttrs = pdl ? 1 : 0;
-    e = cudaLaunchKernelEx(&fc, streamk_fixup_kernel, p, (int)BN, G);
+    e = cudaLaunchKernelEx(&fc, streamk_fixup_kernel, p, (int)BM, (int)BN, G);
     if (e != cudaSuccess) {
       cudaGetLastError();
       return GEMM_ERR_CUDA;
@@ -1007,41 +1061,45 @@ int launch_cfg(const gemm_plan_t &plan, const GemmArgs &a, char *ws, cudaStream_
 // The tcgen05 kernels are built for sm_103a only.
 bool tc_supported(const DeviceProps &dp) { return dp.cc_major == 10 && dp.cc_minor == 3; }
 
-// Tile configurations the planner may pick: (bn, bk, stages, A split in
+// Tile configurations the planner may pick: (bm, bn, bk, stages, A split in
 // kernel, concatenated B MMA, TF32 products per FP32 product).
-#define GG_TC_CONFIGS(X)             \
-  X(256, 16, 5, true, false, 3)      \
-  X(128, 32, 4, true, true, 3)       \
-  X(64, 32, 6, true, true, 3)        \
-  X(64, 32, 3, true, true, 3)        \
-  X(64, 32, 2, true, false, 3)       \
-  X(64, 16, 4, true, false, 3)       \
-  X(256, 16, 4, false, false, 3)     \
-  X(128, 16, 3, false, true, 3)      \
-  X(256, 16, 8, true, false, 1)      \
-  X(64, 32, 4, true, false, 1)       \
-  X(256, 16, 8, false, false, 1)
+#define GG_TC_CONFIGS(X)                  \
+  X(128, 256, 16, 5, true, false, 3)      \
+  X(128, 128, 32, 4, true, true, 3)       \
+  X(128, 64, 32, 6, true, true, 3)        \
+  X(128, 64, 32, 3, true, true, 3)        \
+  X(128, 64, 32, 2, true, false, 3)       \
+  X(128, 64, 16, 4, true, false, 3)       \
+  X(128, 256, 16, 4, false, false, 3)     \
+  X(128, 128, 16, 3, false, true, 3)      \
+  X(256, 256, 16, 3, false, false, 3)     \
+  X(128, 256, 16, 8, true, false, 1)      \
+  X(128, 64, 32, 4, true, false, 1)       \
+  X(128, 256, 16, 8, false, false, 1)     \
+  X(256, 256, 16, 6, false, false, 1)     \
+  X(256, 256, 32, 3, false, false, 1)
 
-bool tc_config_valid(int bn, int bk, int stages, int a_inkernel, int concat, int nprod) {
-#define GG_MATCH(BN_, BK_, ST_, AK_, CC_, NP_)                                       \
-  if (bn == BN_ && bk == BK_ && stages == ST_ && (a_inkernel != 0) == AK_ &&   \
-      (concat != 0) == CC_ && nprod == NP_)                                          \
-    return true;
+#define GG_TC_MATCH(BM_, BN_, BK_, ST_, AK_, CC_, NP_)                                  \
+  (bm == BM_ && bn == BN_ && bk == BK_ && stages == ST_ && (a_inkernel != 0) == AK_ && \
+   (concat != 0) == CC_ && nprod == NP_)
+
+bool tc_config_valid(int bm, int bn, int bk, int stages, int a_inkernel, int concat, int nprod) {
+#define GG_MATCH(BM_, BN_, BK_, ST_, AK_, CC_, NP_) \
+  if (GG_TC_MATCH(BM_, BN_, BK_, ST_, AK_, CC_, NP_)) return true;
   GG_TC_CONFIGS(GG_MATCH)
 #undef GG_MATCH
   return false;
 }
 
 // CTAs of one configuration that fit on an SM (shared memory and TMEM).
-int tc_ctas_per_sm(int bn, int bk, int stages, int a_inkernel, int concat, int nprod,
+int tc_ctas_per_sm(int bm, int bn, int bk, int stages, int a_inkernel, int concat, int nprod,
                    int smem_per_sm) {
-#define GG_OCC(BN_, BK_, ST_, AK_, CC_, NP_)                                         \
-  if (bn == BN_ && bk == BK_ && stages == ST_ && (a_inkernel != 0) == AK_ &&   \
-      (concat != 0) == CC_ && nprod == NP_) {                                        \
-    using C = TcCfg<BN_, BK_, ST_, AK_, CC_, NP_>;                                   \
-    int by_smem = smem_per_sm / (C::SMEM_BYTES + 1024);                              \
-    int by_tmem = 512 / C::TMEM_COLS;                                                \
-    return by_smem < by_tmem ? by_smem : by_tmem;                                    \
+#define GG_OCC(BM_, BN_, BK_, ST_, AK_, CC_, NP_)              \
+  if (GG_TC_MATCH(BM_, BN_, BK_, ST_, AK_, CC_, NP_)) {         \
+    using C = TcCfg<BM_, BN_, BK_, ST_, AK_, CC_, NP_>;         \
+    int by_smem = smem_per_sm / (C::SMEM_BYTES + 1024);         \
+    int by_tmem = 512 / C::TMEM_COLS;                           \
+    return by_smem < by_tmem ? by_smem : by_tmem;               \
   }
   GG_TC_CONFIGS(GG_OCC)
 #undef GG_OCC
@@ -1050,7 +1108,7 @@ int tc_ctas_per_sm(int bn, int bk, int stages, int a_inkernel, int concat, int n
 
 uint64_t tc_workspace_bytes(const gemm_plan_t &plan, int64_t M, int64_t N, int64_t K) {
   return ws_layout(M, N, K, plan.a_split_in_kernel != 0, plan.stream_k ? plan.grid_ctas : 0,
-                   plan.bn, plan.mode != GEMM_MODE_TF32)
+                   plan.bm, plan.bn, plan.mode != GEMM_MODE_TF32)
       .total;
 }
 
@@ -1065,10 +1123,11 @@ int launch_tc(const gemm_plan_t &plan, const GemmArgs &a, void *ws, size_t ws_by
     return GEMM_ERR_UNSUPPORTED;
   char *w = static_cast<char *>(ws);
   const int nprod = plan.mode == GEMM_MODE_TF32 ? 1 : 3;
-#define GG_LAUNCH(BN_, BK_, ST_, AK_, CC_, NP_)                                          \
-  if (plan.bn == BN_ && plan.bk == BK_ && plan.stages == ST_ &&                          \
-      (plan.a_split_in_kernel != 0) == AK_ && (plan.b_concat != 0) == CC_ && nprod == NP_) \
-    return launch_cfg<BN_, BK_, ST_, AK_, CC_, NP_>(plan, a, w, s);
+  const int bm = plan.bm, bn = plan.bn, bk = plan.bk, stages = plan.stages;
+  const int a_inkernel = plan.a_split_in_kernel, concat = plan.b_concat;
+#define GG_LAUNCH(BM_, BN_, BK_, ST_, AK_, CC_, NP_)  \
+  if (GG_TC_MATCH(BM_, BN_, BK_, ST_, AK_, CC_, NP_)) \
+    return launch_cfg<BM_, BN_, BK_, ST_, AK_, CC_, NP_>(plan, a, w, s);
   GG_TC_CONFIGS(GG_LAUNCH)
 #undef GG_LAUNCH
   return GEMM_ERR_UNSUPPORTED;

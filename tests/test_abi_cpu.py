@@ -139,6 +139,8 @@ def test_tc_plans_on_cpu(lib):
     r = gemm.plan(1023, 1025, 777, 777, 1025, 1025, mode="tf32x3")
     assert r["a_split_in_kernel"] == 0 and r["launches"] == 3 + r["stream_k"]
     assert gemm.plan(4096, 4096, 4096)["kernel_name"] == "tc_tf32x3"  # auto
+    big = gemm.plan(8192, 8192, 8192, mode="tf32x3")  # many tiles: 256 x 256, A pre-split
+    assert (big["bm"], big["bn"], big["a_split_in_kernel"]) == (256, 256, 0)
     assert gemm.plan(512, 512, 512)["kernel_name"] == "simt"  # auto, small
 
 
@@ -160,8 +162,9 @@ def test_tf32_mode_plans(lib):
     assert p["kernel_name"] == "tc_tf32" and p["bound_name"] == "tf32"
     # square: A pre-split too; A_hi and B_hi only (no lo parts), plus stream-K partials
     assert p["a_split_in_kernel"] == 0 and p["launches"] == 3 + p["stream_k"]
-    extra = p["grid_ctas"] * 2 * 128 * p["bn"] * 4 if p["stream_k"] else 0
+    extra = p["grid_ctas"] * 2 * p["bm"] * p["bn"] * 4 if p["stream_k"] else 0
     assert p["workspace_bytes"] == 2 * 4096 * 4096 * 4 + extra
+    assert (p["bm"], p["bn"], p["bk"]) == (256, 256, 32)  # wide: 256 x 256 tiles
     s = gemm.plan(65536, 64, 4096, mode="tf32")
     assert s["bound_name"] == "hbm" and s["ctas_per_sm"] == 2 and s["a_split_in_kernel"] == 1
     assert gemm.plan(64, 64, 64, mode="tf32")["mode"] == gemm.MODE_TF32

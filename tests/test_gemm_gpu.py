@@ -59,7 +59,11 @@ EDGE_SHAPES = [(1, 1, 1), (2, 3, 5), (17, 31, 33), (33, 17, 1), (127, 129, 64),
                (513, 65, 129), (1000, 3, 77)]
 
 
-def _run_shape(M, N, K, mode, alpha, beta, pad=(0, 0, 0), offset=0, seed=0, dist="u11"):
+def _run_shape(M, N, K, mode, alpha, beta, pad=(0, 0, 0), offset=0, seed=0, dist="u11",
+               sampled=False):
+    """Runs one GEMM with guard bands checked; returns (C, C_ref, D), or with
+    ``sampled`` ({"C": C, "inputs": (A, B, C_old)}, None, None) for the
+    caller to check sampled entries."""
     import torch
     from roofline_gb300 import gemm
     lda, ldb, ldc = K + pad[0], N + pad[1], N + pad[2]
@@ -91,6 +95,8 @@ def _run_shape(M, N, K, mode, alpha, beta, pad=(0, 0, 0), offset=0, seed=0, dist
         assert np.array_equal(np.isnan(full[1:M + 1, N:]), np.isnan(C0[:, N:]))
     assert np.all(out[offset + cbuf.size:] == sentinel)
     assert np.all(out[:offset] == sentinel)
+    if sampled:
+        return {"C": full[1:M + 1, :N], "inputs": (A[:, :K], B[:, :N], C0[:, :N])}, None, None
     ref, D = oracle.gemm(A[:, :K], B[:, :N], alpha, beta, C0[:, :N], with_bound=True)
     return full[1:M + 1, :N], ref, D
 
@@ -212,11 +218,12 @@ def test_status_clear_after_normal_runs():
 # The planner's own choice for representative shapes:
 # (M, N, K, lda) -> (bn, bk, stages, A split in kernel, concatenated B)
 TC_PLANS = [
-    ((1000, 64, 96, 96), (64, 32, 3, 1, 1)),
-    ((512, 512, 512, 512), (128, 32, 4, 1, 1)),
-    ((2432, 8192, 128, 128), (256, 16, 5, 1, 0)),
-    ((1023, 1025, 777, 777), (128, 16, 3, 0, 1)),
-    ((2432, 8192, 129, 129), (256, 16, 4, 0, 0)),
+    ((1000, 64, 96, 96), (128, 64, 32, 3, 1, 1)),
+    ((512, 512, 512, 512), (128, 128, 32, 4, 1, 1)),
+    ((2432, 8192, 128, 128), (128, 256, 16, 5, 1, 0)),
+    ((1023, 1025, 777, 777), (128, 128, 16, 3, 0, 1)),
+    ((2432, 8192, 129, 129), (128, 256, 16, 4, 0, 0)),
+    ((5120, 8192, 64, 64), (256, 256, 16, 3, 0, 0)),   # many tiles: 256 x 256
 ]
 
 
@@ -227,7 +234,7 @@ def test_tf32x3_planner_choices(shape, cfg):
     from workloads import sample_entries
     M, N, K, lda = shape
     p = gemm.plan(M, N, K, lda, N, N, mode="tf32x3")
-    assert (p["bn"], p["bk"], p["stages"], p["a_split_in_kernel"], p["b_concat"]) == cfg
+    assert (p["bm"], p["bn"], p["bk"], p["stages"], p["a_split_in_kernel"], p["b_concat"]) == cfg
     assert p["ctas_per_sm"] >= 1
     A = matrix(M, K, lda, 4000 + K, "u11")
     B = matrix(K, N, None, 4100 + K, "u11")
@@ -244,19 +251,25 @@ def test_tf32x3_planner_choices(shape, cfg):
 # Every tensor-core configuration the library is built with, forced through
 # the GEMM_TC_CONFIG knob, on one ragged shape (full check).
 TC_BUILT = ["256,16,5,1,0", "128,32,4,1,1", "64,32,6,1,1", "64,32,3,1,1", "64,32,2,1,0",
-            "64,16,4,1,0", "256,16,4,0,0", "128,16,3,0,1"]
+            "64,16,4,1,0", "256,16,4,0,0", "128,16,3,0,1", "256,256,16,3,0,0"]
+
+
+def _cfg(cfg):
+    """(bm, bn, bk, stages, a_split_in_kernel, b_concat) of a GEMM_TC_CONFIG string."""
+    v = list(map(int, cfg.split(",")))
+    return tuple(v) if len(v) == 6 else (128, *v)
 
 
 @pytest.mark.parametrize("cfg", TC_BUILT)
 def test_tf32x3_every_built_configuration(cfg, monkeypatch):
     from roofline_gb300 import gemm
-    bn, bk, st, ak, cc = map(int, cfg.split(","))
+    bm, bn, bk, st, ak, cc = _cfg(cfg)
     monkeypatch.setenv("GEMM_TC_CONFIG", cfg)
     M, N, K = 777, 200, 300
     pad = (0 if ak else 1, 0, 0)
     p = gemm.plan(M, N, K, K + pad[0], N, N, mode="tf32x3")
-    assert (p["bn"], p["bk"], p["stages"], p["a_split_in_kernel"], p["b_concat"]) == \
-        (bn, bk, st, ak, cc)
+    assert (p["bm"], p["bn"], p["bk"], p["stages"], p["a_split_in_kernel"], p["b_concat"]) == \
+        (bm, bn, bk, st, ak, cc)
     got, ref, D = _run_shape(M, N, K, "tf32x3", 1.5, 0.5, pad=pad, offset=0, seed=st + bn)
     assert oracle.err_normalised(got, ref, D) <= TOL_E1
 
@@ -313,21 +326,22 @@ def test_fma_peak_probe():
 # about 2^-10 of |a||b| and the normalised error stays below 2^-10 plus the
 # FP32 accumulation error; 2e-3 bounds both for the shapes here.
 TOL_TF32 = 2e-3
-TF32_BUILT = ["256,16,8,1,0", "64,32,4,1,0", "256,16,8,0,0"]
+TF32_BUILT = ["256,16,8,1,0", "64,32,4,1,0", "256,16,8,0,0", "256,256,16,6,0,0",
+              "256,256,32,3,0,0"]
 
 
 @pytest.mark.parametrize("cfg", TF32_BUILT)
 @pytest.mark.parametrize("streamk", ["0", "1"])
 def test_tf32_mode_every_configuration(cfg, streamk, monkeypatch):
     from roofline_gb300 import gemm
-    bn, bk, st, ak, cc = map(int, cfg.split(","))
+    bm, bn, bk, st, ak, cc = _cfg(cfg)
     monkeypatch.setenv("GEMM_TC_CONFIG", cfg)
     monkeypatch.setenv("GEMM_TC_STREAMK", streamk)
     M, N, K = 777, 200, 300
     pad = (0 if ak else 1, 0, 0)
     p = gemm.plan(M, N, K, K + pad[0], N, N, mode="tf32")
     assert p["kernel_name"] == "tc_tf32"
-    assert (p["bn"], p["bk"], p["stages"], p["a_split_in_kernel"]) == (bn, bk, st, ak)
+    assert (p["bm"], p["bn"], p["bk"], p["stages"], p["a_split_in_kernel"]) == (bm, bn, bk, st, ak)
     got, ref, D = _run_shape(M, N, K, "tf32", 1.5, 0.5, pad=pad, offset=0, seed=st + bn)
     e1 = oracle.err_normalised(got, ref, D)
     assert e1 <= TOL_TF32, e1
@@ -344,3 +358,35 @@ def test_tf32_mode_workloads(name):
         assert r["mismatches"] == 0, r
     else:
         assert r["e1"] <= TOL_TF32, r
+
+
+def _waves(tiles, num_kb, G):
+    """Whole-tile waves and stream-K tiles of the tensor-core work split."""
+    waves, rest = tiles // G, tiles % G
+    while rest > 0 and waves > 0 and (rest * num_kb < 4 * G or G > 250 * rest):
+        waves, rest = waves - 1, rest + G
+    return waves, rest
+
+
+@pytest.mark.parametrize("mode,cfg", [("tf32x3", None), ("tf32x3", "256,256,16,3,0,0"),
+                                      ("tf32", "256,16,8,0,0"), ("tf32", "256,256,16,6,0,0")])
+def test_tc_whole_waves_then_stream_k(mode, cfg, monkeypatch):
+    # 168 tiles x 64 K blocks (2688 or 5376 rows, 2048 columns, K = 1024): one
+    # wave of whole tiles, then a stream-K remainder whose partial tiles the
+    # fix-up sums
+    from roofline_gb300 import gemm
+    from workloads import sample_entries
+    if cfg:
+        monkeypatch.setenv("GEMM_TC_CONFIG", cfg)
+    monkeypatch.setenv("GEMM_TC_STREAMK", "1")
+    M, N, K = 2688 * (2 if cfg and cfg.startswith("256,256") else 1), 2048, 1024
+    p = gemm.plan(M, N, K, K, N, N, mode=mode)
+    tiles = -(-M // p["bm"]) * -(-N // p["bn"])
+    waves, rest = _waves(tiles, -(-K // p["bk"]), p["grid_ctas"])
+    assert p["stream_k"] == 1 and waves >= 1 and rest > 0, (p, waves, rest)
+    got_full, _, _ = _run_shape(M, N, K, mode, 0.75, 0.25, seed=31, sampled=True)
+    A, B, C0 = got_full["inputs"]
+    rows, cols = sample_entries(M, N, n=30000, seed=77)
+    ref, D = oracle.gemm_entries(A, B, rows, cols, 0.75, 0.25, C0)
+    tol = TOL_TF32 if mode == "tf32" else TOL_E1
+    assert oracle.err_normalised(got_full["C"][rows, cols], ref, D) <= tol

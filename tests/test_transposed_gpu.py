@@ -25,6 +25,8 @@ ROW, COL, N_, T_ = 0, 1, 0, 1
 def _dense(x):
     """A fresh C-ordered copy (canonical strides even for 1 x 1 views)."""
     return np.array(x, dtype=np.float32, order="C", copy=True)
+
+
 COMBOS = list(itertools.product([ROW, COL], [N_, T_], [N_, T_]))
 
 
