@@ -57,6 +57,23 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(x: float, world: int, dev) -> float:
+    """The largest of every rank's `x` (a time), identical on all ranks."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_step: float, steps: int, world: int, ms_max: float) -> float:
+    """Aggregate throughput: every rank ran `steps` steps of `flops_per_step`
+    (replicas, weak scaling), timed by the slowest rank."""
+    return world * steps * flops_per_step / (ms_max * 1e-3) / 1e12
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -320,13 +337,9 @@ def run_ours(args):
     torch.cuda.synchronize()
     main_ms = [ev_b[i].elapsed_time(ev_a[i]) for i in range(nk)]
 
-    t_max = ms_total
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_max = float(t.item())
+    t_max = max_over_ranks(ms_total, world, dev)
     flops = float(w.flops)
-    value = world * args.steps * flops / (t_max * 1e-3) / 1e12
+    value = whole_job_tflops(flops, args.steps, world, t_max)
     ms_step = t_max / args.steps
 
     # roofline of the dominant (main GEMM) kernel
@@ -403,13 +416,9 @@ def e2e(args, w, A, B, C0, dset, dev, world):
     t0 = time.perf_counter()
     for _ in range(steps):
         one()
-    ms = (time.perf_counter() - t0) * 1e3
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks((time.perf_counter() - t0) * 1e3, world, dev)
     h2d = 4 * (w.M * w.K + w.K * w.N + (w.M * w.N if w.beta != 0 else 0))
-    return {"value": world * steps * float(w.flops) / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+    return {"value": whole_job_tflops(float(w.flops), steps, world, ms), "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4 * w.M * w.N, "steps": steps,
             "ms_per_step": ms / steps,
             "path": "pinned host -> gemm_f32_host (row blocks: H2D copy stream, GEMM stream, "
