@@ -45,6 +45,8 @@ def parse_args():
     ap.add_argument("--no-extras", action="store_true", help="skip per-mode and reference points")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--calibrate-only", action="store_true",
+                    help="run only the HBM copy calibration (2 x 1 GiB buffers) and print GB/s")
     return ap.parse_args()
 
 
@@ -593,10 +595,34 @@ def extras(args, w, sets, info, peaks, peaks_src):
     return out
 
 
+def run_calibration(args):
+    """The C1 copy calibration alone: out[i] = in[i] over 256M floats, one
+    untimed copy, then `args.steps` (at least 50) timed copies between CUDA
+    events; GB/s = 2 * n * 4 * iterations / time."""
+    import torch
+
+    from roofline_gb300 import gemm
+    rank, _, local = dist_env()
+    torch.cuda.set_device(local)
+    n = 256 << 20
+    src = torch.ones(n, dtype=torch.float32, device="cuda")
+    dst = torch.empty_like(src)
+    iters = max(50, args.steps)
+    gbs = gemm.hbm_copy_calibrate(src, dst, iters=iters)
+    ok = bool(torch.equal(src, dst))
+    if rank == 0:
+        print(json.dumps({"metric": "HBM copy bandwidth (2 x n x 4 bytes / t)", "value": gbs,
+                          "unit": "GB/s", "n_floats": n, "iterations": iters,
+                          "copy_exact": ok}), flush=True)
+    return 0 if ok else 1
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.calibrate_only:
+        return run_calibration(args)
     return run_ours(args)
 
 

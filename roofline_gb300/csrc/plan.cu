@@ -103,8 +103,12 @@ void plan_simt(int64_t M, int64_t N, int64_t K, bool vec, const DeviceProps &dp,
 
 }  // namespace
 
-// The split pre-passes tile K in 32-deep rows of a grid's y dimension.
-static bool tc_k_fits(int64_t K) { return ceil_div(K, 32) <= 65535; }
+// Shapes the tensor-core path takes: the split pre-passes tile K in 32-deep
+// rows of a grid's y dimension, and TMA tile coordinates are 32-bit.
+static bool tc_shape_fits(int64_t M, int64_t N, int64_t K) {
+  const int64_t lim = ((int64_t)1 << 31) - 512;
+  return ceil_div(K, 32) <= 65535 && M < lim && N < lim && K < lim;
+}
 
 int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
               int mode, uintptr_t align_hint, int beta_nonzero, const DeviceProps &dp,
@@ -129,7 +133,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
     // Tensor cores (3xTF32) once the problem is large enough to amortise the
     // split pass; the CUDA-core kernel otherwise.
     const bool big = (double)M * N * K >= 64.0 * 1024 * 1024 * 64;
-    resolved = (tc_supported(dp) && big && tc_k_fits(K)) ? GEMM_MODE_TF32X3
+    resolved = (tc_supported(dp) && big && tc_shape_fits(M, N, K)) ? GEMM_MODE_TF32X3
                                                          : GEMM_MODE_FP32_SIMT;
   }
   p.mode = resolved;
@@ -184,7 +188,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
     case GEMM_MODE_TF32X3:
     case GEMM_MODE_TF32: {
       if (!tc_supported(dp)) return GEMM_ERR_UNSUPPORTED;
-      if (ceil_div(M, 128) > 65535 || !tc_k_fits(K)) return GEMM_ERR_UNSUPPORTED;
+      if (ceil_div(M, 128) > 65535 || !tc_shape_fits(M, N, K)) return GEMM_ERR_UNSUPPORTED;
       const bool x3 = resolved == GEMM_MODE_TF32X3;
       const int nprod = x3 ? 3 : 1;
       p.kernel = x3 ? GEMM_KERNEL_TC_TF32X3 : GEMM_KERNEL_TC_TF32;

@@ -168,3 +168,19 @@ def test_tf32_mode_plans(lib):
     s = gemm.plan(65536, 64, 4096, mode="tf32")
     assert s["bound_name"] == "hbm" and s["ctas_per_sm"] == 2 and s["a_split_in_kernel"] == 1
     assert gemm.plan(64, 64, 64, mode="tf32")["mode"] == gemm.MODE_TF32
+
+
+def test_tensor_core_shape_limits(lib):
+    # TMA tile coordinates are 32-bit and the split passes tile K on a grid's
+    # y dimension: such shapes are refused in tensor-core modes, and AUTO
+    # keeps them on the CUDA cores
+    n_big = 1 << 31
+    for mode in ("tf32x3", "tf32"):
+        with pytest.raises(gemm.GemmError) as e:
+            gemm.plan(1, n_big, 8, 8, n_big, n_big, mode=mode)
+        assert e.value.code == gemm.ERR_UNSUPPORTED
+        with pytest.raises(gemm.GemmError) as e:
+            gemm.plan(128, 128, 65535 * 32 + 1, mode=mode)
+        assert e.value.code == gemm.ERR_UNSUPPORTED
+    assert gemm.plan(1, n_big, 8, 8, n_big, n_big)["kernel_name"] == "simt"
+    assert gemm.plan(4096, 4096, 65535 * 32 + 1)["kernel_name"] == "simt"

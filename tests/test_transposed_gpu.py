@@ -195,3 +195,14 @@ def test_simt_every_built_configuration(cfg, op_a, op_b, shape, monkeypatch):
     assert oracle.err_normalised(got, ref, D) <= TOL_E1
     A, B, C0, got = run_op(ROW, op_a, op_b, M, N, K, 1.0, 0.0, "int2", "fp32_simt")
     assert oracle.mismatches(got, oracle.gemm(A, B, 1.0, 0.0, None)) == 0
+
+
+@pytest.mark.parametrize("group", ["1", "3", "8", "40"])
+@pytest.mark.parametrize("op_b", [N_, T_])
+def test_simt_tile_orders(group, op_b, monkeypatch):
+    # the tile order is a bijection of the grid for any group size, ragged
+    # row-tile counts included (1000 rows = 15.6 row-tiles)
+    monkeypatch.setenv("GEMM_SIMT_GROUP", group)
+    M, N, K = 1000, 1100, 96
+    A, B, C0, got = run_op(ROW, N_, op_b, M, N, K, 1.0, 0.0, "int2", "fp32_simt")
+    assert oracle.mismatches(got, oracle.gemm(A, B, 1.0, 0.0, None)) == 0
