@@ -18,6 +18,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -147,11 +148,19 @@ class ClockSampler:
                 "power_w_max": max(power) if power else None}
 
 
+def code_only(text: str) -> str:
+    """C/CUDA source with comments and blank lines removed, so that editing
+    a comment does not mark a kernel's counters stale."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*$", "", l).rstrip() for l in text.splitlines())
+    return "\n".join(l for l in lines if l)
+
+
 def source_hash(paths):
     h = hashlib.sha256()
     for p in paths:
-        with open(os.path.join(ROOT, p), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, p), encoding="utf-8") as f:
+            h.update(code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -13,17 +13,25 @@
 //     A*B ~= A_hi*B_lo + A_lo*B_hi + A_hi*B_hi
 // (the dropped A_lo*B_lo term is below 2^-20 of |A||B|).
 //
-// Kernel structure (one 128 x BN output tile per CTA, 192 threads):
+// 1xTF32 mode issues only A_hi*B_hi.
+//
+// Kernel structure (192 threads per CTA; output tiles of BM = 128 or 256
+// rows by BN columns; a 256-row tile is two 128-row halves, each with its
+// own accumulator, sharing every B tile):
 //   warp 0      TMA producer: one lane streams K-blocks of the operand tiles
 //               into a STAGES-deep shared-memory ring (cp.async.bulk.tensor,
 //               completion counted on per-stage mbarriers);
-//   warp 1      allocates the TMEM accumulator (BN fp32 columns x 128 lanes)
-//               and one lane issues tcgen05.mma kind::tf32, committing each
-//               stage back to the producer when its MMAs retire;
+//   warp 1      allocates TMEM (the accumulators, plus the A_lo ring when A
+//               is split on chip) and one lane issues tcgen05.mma
+//               kind::tf32, committing each stage back to the producer when
+//               its MMAs retire;
 //   warps 2-5   (a) when A is split inside the kernel: convert each landed
 //               FP32 A tile into its hi part (in place) and lo part, then
 //               release it to the MMA warp; (b) epilogue: tcgen05.ld the
 //               accumulator rows, apply C = alpha*acc + beta*C, store.
+// A CTA walks a list of (tile, K-range) segments: whole tiles in waves, then
+// an even share of the remaining tiles' K blocks (stream-K; see Walk), with
+// the pipeline running across segment boundaries.
 // Operands live in shared memory K-major with the TMA swizzle (64 B rows for
 // BK = 16, 128 B rows for BK = 32), which is the layout the MMA's smem
 // descriptors describe.  B is row-major (N contiguous) in global memory, so

@@ -62,3 +62,32 @@ def test_gemm_bytes():
     # ragged shape with beta != 0 reads C as well
     assert rf.gemm_bytes(1023, 1025, 777, True) == 4 * (1023 * 777 + 777 * 1025 + 2 * 1023 * 1025)
     assert rf.gemm_bytes(65536, 64, 4096) == 1_091_567_616
+
+
+def test_traffic_entries_match_current_sources():
+    # every committed ncu traffic figure belongs to the kernel source as it
+    # is now (comments aside); a stale entry would make bench.py report null
+    import json
+    import os
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    sys.path.insert(0, root)
+    import bench
+    with open(os.path.join(root, "profiles", "traffic.json")) as f:
+        entries = json.load(f)
+    assert entries
+    for key, e in entries.items():
+        assert e["source_hash"] == bench.source_hash(e["sources"]), key
+        assert e["dram_bytes_per_launch"] > 0
+
+
+def test_source_hash_ignores_comments_only():
+    import os
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+    a = "int f() {  // one\n  return 1; /* two\n three */\n}\n"
+    b = "int f() {\n\n  return 1;   // changed comment\n}\n"
+    c = "int f() {\n  return 2;\n}\n"
+    assert bench.code_only(a) == bench.code_only(b)
+    assert bench.code_only(a) != bench.code_only(c)
