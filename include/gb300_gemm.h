@@ -100,7 +100,7 @@ typedef struct gemm_plan {
   int32_t stages;          /* shared-memory pipeline depth */
   int32_t split_k;         /* K slices; > 1 uses the workspace and a reduction */
   int32_t vec;             /* 1: 128-bit global access path, 0: scalar path */
-  int32_t a_split_in_kernel; /* TF32X3: A split inside the GEMM kernel (1) or by a pre-pass (0) */
+  int32_t a_split_in_kernel; /* tensor-core modes: A split inside the GEMM kernel (1) or by a pre-pass (0) */
   int32_t bound;           /* GEMM_BOUND_* */
   int32_t threads;         /* threads per CTA */
   int32_t launches;        /* kernels one call launches (split pass, main, reduction) */
@@ -111,8 +111,9 @@ typedef struct gemm_plan {
   double intensity;        /* flops / bytes */
   int32_t b_concat;        /* TF32X3: A_hi*[B_hi|B_lo] issued as one MMA of width 2*bn (1) or two MMAs (0) */
   int32_t ctas_per_sm;     /* CTAs of the main kernel resident per SM (shared memory and TMEM budget) */
-  int32_t stream_k;        /* TF32X3: grid_ctas persistent CTAs share the (tile, K block) work evenly;
-                              a fix-up kernel sums the parts of tiles shared between CTAs */
+  int32_t stream_k;        /* tensor-core modes: grid_ctas persistent CTAs take whole tiles in
+                              waves, then share the remaining tiles' K blocks evenly; a fix-up
+                              kernel sums the parts of tiles shared between CTAs */
   int32_t reserved;
 } gemm_plan_t;
 
