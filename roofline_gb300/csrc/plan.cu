@@ -8,6 +8,7 @@
 // ("Bandwidths and peak rate - exercises", exercise 3).  The planner does
 // both per call: it sizes the grid against the SM count read from the
 // device and classifies the shape with the ridge point of the mode's roof.
+#include <cmath>
 #include <cstdio>
 #include <cstdlib>
 
@@ -202,7 +203,10 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
       const bool a_aligned = !ta && (lda % 4 == 0) && ((align_hint & 15) == 0);
       const int64_t sms = dp.sm_count > 0 ? dp.sm_count : 152;
       const int64_t tiles256 = ceil_div(M, 128) * ceil_div(N, 256);
-      const bool wide = N > 128 && tiles256 >= 2 * sms;
+      // 128 x 256 tiles once there are at least half a wave of them
+      // (GB300, 3xTF32, N = K = 4096: M = 1024 150 us against 195 us with
+      // 128 x 128 tiles, M = 2048 266 us against 336 us)
+      const bool wide = N > 128 && tiles256 * 2 >= sms;
       p.a_split_in_kernel = a_aligned ? 1 : 0;
       p.launches = a_aligned ? 2 : 3;
       auto set = [&](int bn, int bk, int st, int cc, int bm = 128) {
@@ -264,9 +268,17 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
       p.ctas_per_sm = tc_ctas_per_sm(p.bm, p.bn, p.bk, p.stages, p.a_split_in_kernel, p.b_concat,
                                      nprod, dp.smem_per_sm > 0 ? dp.smem_per_sm : 233472);
       // Stream-K: when the tiles do not fill whole waves of resident CTAs,
-      // launch one wave of persistent CTAs that split the (tile, K block)
-      // work evenly (each at least 4 K blocks); a fix-up kernel sums the
-      // parts of tiles shared between CTAs, in CTA order.
+      // launch one wave of persistent CTAs that take whole tiles in waves and
+      // split the rest of the (tile, K block) work evenly (each at least 4 K
+      // blocks); a fix-up kernel sums the parts of tiles shared between
+      // CTAs, in CTA order.  The split part costs about half a wave (its
+      // CTAs sit at unrelated K positions, and the fix-up runs after), so it
+      // is taken when the last partial wave would leave more than ~45 % of
+      // the CTAs idle, or there are 4 to 8 waves (where it measured 2 %
+      // faster), or the shape is HBM-bound (idle SMs are lost bandwidth).
+      // GB300, 3xTF32 step times with / without: 4096^3 464 / 501 us;
+      // 2048 x 4096 x 4096 293 / 266 us; 8192^3 3.39 / 3.46 ms; M = 65536,
+      // N = 64, K = 4096 222 / 236 us; 1xTF32 4096^3 243 / 223 us.
       {
         const int64_t tiles = ceil_div(M, p.bm) * ceil_div(N, p.bn);
         const int64_t slots = (int64_t)(p.ctas_per_sm > 0 ? p.ctas_per_sm : 1) * sms;
@@ -276,7 +288,12 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
         int64_t g = slots < total / 4 ? slots : total / 4;
         if (g > 250 * tiles) g = 250 * tiles;
         const char *sk = std::getenv("GEMM_TC_STREAMK");  // tuning knob: 0 off, 1 on
-        bool want = (tiles % slots) != 0 && tiles < 8 * slots;
+        const double waves = (double)tiles / (double)slots;
+        const double idle = std::ceil(waves) - waves;  // of the last wave
+        const double roof = x3 ? kPlanTf32DenseFlops / 3.0 : kPlanTf32DenseFlops;
+        const bool hbm_bound = p.intensity < roof / kPlanHbmBytesPerSec;
+        bool want = (tiles % slots) != 0 && tiles < 8 * slots &&
+                    (hbm_bound || idle > 0.45 || waves >= 4.0);
         if (sk) want = std::atoi(sk) != 0;
         p.stream_k = (want && g >= 2 && g < tiles * 64) ? 1 : 0;
         p.grid_ctas = p.stream_k ? g : tiles;
