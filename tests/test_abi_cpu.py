@@ -184,3 +184,24 @@ def test_tensor_core_shape_limits(lib):
         assert e.value.code == gemm.ERR_UNSUPPORTED
     assert gemm.plan(1, n_big, 8, 8, n_big, n_big)["kernel_name"] == "simt"
     assert gemm.plan(4096, 4096, 65535 * 32 + 1)["kernel_name"] == "simt"
+
+
+def test_stream_k_choice(lib):
+    # stream-K when the last wave of 128 x 256 tiles would leave many CTAs
+    # idle (4096^3: 512 tiles on 152 SMs, 3.37 waves), not for 1.68 waves
+    # (2048 x 4096 x 4096) where its cost outweighs the idle SMs; always for
+    # HBM-bound shapes
+    assert gemm.plan(4096, 4096, 4096, mode="tf32x3")["stream_k"] == 1
+    p = gemm.plan(2048, 4096, 4096, mode="tf32x3")
+    assert (p["bn"], p["stream_k"], p["grid_ctas"]) == (256, 0, 256)
+    assert gemm.plan(65536, 64, 4096, mode="tf32x3")["stream_k"] == 1
+    assert gemm.plan(4096, 4096, 4096, mode="tf32")["stream_k"] == 0
+    # whole waves only: no stream-K
+    q = gemm.plan(152 * 128, 256, 4096, mode="tf32x3")
+    assert q["stream_k"] == 0
+
+
+def test_wide_tiles_from_half_a_wave(lib):
+    # 128 x 256 tiles once there are at least 76 of them (half of 152 SMs)
+    assert gemm.plan(1024, 4096, 4096, mode="tf32x3")["bn"] == 256
+    assert gemm.plan(512, 512, 512, mode="tf32x3")["bn"] == 128
