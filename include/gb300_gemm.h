@@ -157,7 +157,10 @@ GEMM_API int gemm_f32(int64_t M, int64_t N, int64_t K, const float *A, int64_t l
  * (gemm_f32_plan), 256-byte aligned, owned by the caller and not used by
  * any other work in flight on the GPU during this call.  workspace == NULL
  * lets the library use its own per-device buffer, grown with cudaMalloc
- * when needed (which synchronises the device) and freed by gemm_shutdown().
+ * when needed (which synchronises the device) and freed by gemm_shutdown();
+ * that buffer is shared by every call on the device, so calls that use it
+ * must not run at the same time on the GPU (issue them on one stream, or
+ * give each concurrent stream its own workspace).
  * A non-NULL workspace smaller than the plan needs returns
  * GEMM_ERR_WORKSPACE_TOO_SMALL.
  */

@@ -305,7 +305,9 @@ def matmul(A, B, C=None, alpha=1.0, beta=0.0, mode=MODE_AUTO, stream=None,
     leading dimension) or transposed views of row-major buffers (``X.t()``,
     run as op T without a copy).  C is row-major, allocated when None (then
     beta must be 0).  ``workspace``: optional uint8/float CUDA tensor used as
-    caller-owned scratch.  Returns C.
+    caller-owned scratch; without one the library's per-device buffer is
+    used, which calls running at the same time on different streams must not
+    share.  Returns C.
     """
     import torch
     M, K = A.shape

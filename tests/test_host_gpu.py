@@ -103,3 +103,36 @@ def test_host_square_4096_sampled(blocks):
     rows, cols = sample_entries(w.M, w.N)
     ref, D = oracle.gemm_entries(a[:, :w.K], b[:, :w.N], rows, cols, 1.0, 0.0, None)
     assert oracle.err_normalised(hC.numpy()[rows, cols], ref, D) <= TOL_E1
+
+
+def test_host_calls_from_two_threads():
+    # calls on one device are serialised by the library; results stay exact
+    import threading
+
+    import torch
+    from roofline_gb300 import gemm
+    M, N, K = 700, 520, 300
+    jobs = []
+    for seed in (1, 2):
+        a = matrix(M, K, None, 100 * seed, "int2")
+        b = matrix(K, N, None, 100 * seed + 1, "int2")
+        jobs.append((torch.from_numpy(a).pin_memory(), torch.from_numpy(b).pin_memory(),
+                     oracle.gemm(a, b, 1.0, 0.0, None)))
+    out = [None, None]
+    errs = []
+
+    def work(i):
+        try:
+            for _ in range(5):
+                out[i] = gemm.matmul_host(jobs[i][0], jobs[i][1], mode="auto", blocks=3).numpy()
+        except Exception as e:  # pragma: no cover - reported below
+            errs.append(e)
+
+    ts = [threading.Thread(target=work, args=(i,)) for i in range(2)]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    assert not errs, errs
+    for i in range(2):
+        assert oracle.mismatches(out[i], jobs[i][2]) == 0
