@@ -250,7 +250,7 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(w, args.mode, None),
+        "config": workload_config(w, args.mode, rotation_of(w)[2]),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": f"each step: first {rows} of {w.M} output rows of {w.name} "
                                    f"(all N, all K), fp64 accumulation"},
@@ -292,7 +292,7 @@ def run_ours(args):
     A, B, C0 = w.make()
     sets, set_bytes = device_sets(w, dev, (A, B, C0))
     nsets = len(sets)
-    rotation = f"inputs rotated over {nsets} buffer sets ({nsets * set_bytes / 2**20:.0f} MiB > L2)"
+    rotation = rotation_of(w)[2]
 
     plan = gemm.plan(w.M, w.N, w.K, lda, ldb, ldc, args.mode, 0, w.beta != 0.0)
     stream = torch.cuda.current_stream()
@@ -513,13 +513,22 @@ def measure(w, mode, sets, steps, warmup=3):
     return step_ms, kernel_ms, plan
 
 
+def rotation_of(w, min_sets=2):
+    """(input sets, bytes per set, description) of the L2 rotation the timed
+    loop uses: enough sets to exceed L2 three times (2 to 8)."""
+    lda, ldb, ldc = w.lds()
+    set_bytes = 4 * (w.M * lda + w.K * ldb + w.M * ldc)
+    nsets = max(min_sets, min(8, -(-3 * L2_BYTES // set_bytes)))
+    return nsets, set_bytes, (f"inputs rotated over {nsets} buffer sets "
+                              f"({nsets * set_bytes / 2**20:.0f} MiB > L2)")
+
+
 def device_sets(w, dev, arrays=None, min_sets=2):
     """Device copies of the workload's inputs, enough sets to exceed L2 three times."""
     import torch
     A, B, C0 = arrays if arrays is not None else w.make()
     lda, ldb, ldc = w.lds()
-    set_bytes = 4 * (w.M * lda + w.K * ldb + w.M * ldc)
-    nsets = max(min_sets, min(8, -(-3 * L2_BYTES // set_bytes)))
+    nsets, set_bytes, _ = rotation_of(w, min_sets)
     hA, hB = torch.from_numpy(A), torch.from_numpy(B)
     hC = torch.from_numpy(C0) if C0 is not None else None
     sets = []

@@ -68,3 +68,14 @@ def test_reference_arm_under_torchrun_prints_once():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_reference_arm_config_matches_ours():
+    # both arms name the same workload configuration
+    sys.path.insert(0, ROOT)
+    import bench
+    from workloads import WORKLOADS
+    w = WORKLOADS["sq4096"]
+    cfg = bench.workload_config(w, "auto", bench.rotation_of(w)[2])
+    assert cfg["M"] == cfg["N"] == cfg["K"] == 4096
+    assert cfg["l2"] == "inputs rotated over 3 buffer sets (576 MiB > L2)"
