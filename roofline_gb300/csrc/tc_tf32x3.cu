@@ -268,7 +268,8 @@ struct TcParams {
   float *C;
   int64_t ldc;
   int num_kb;        // K blocks per output tile
-  int tiles_n;       // output tiles along N (tile t = m_tile * tiles_n + n_tile)
+  int tiles_m, tiles_n;  // output tiles along M and N
+  int col_order;     // tile t = n_tile * tiles_m + m_tile (1) or m_tile * tiles_n + n_tile (0)
   int waves;         // whole tiles per CTA before the stream-K part
   int64_t dp_tiles;  // waves * G: tiles done whole, in waves
   int64_t sk_units;  // (tiles - dp_tiles) * num_kb: units shared out stream-K
@@ -283,6 +284,18 @@ struct TcParams {
 // of the tiles left over are then split evenly (stream-K): CTA c owns units
 // [c*S/G, (c+1)*S/G) of them, walked tile by tile.  Without stream-K,
 // G = tiles: one wave of one tile per CTA.
+// Row-tile and column-tile of output tile t.
+__host__ __device__ __forceinline__ void tile_coords(const TcParams &p, int64_t t, int64_t &mt,
+                                                     int64_t &nt) {
+  if (p.col_order) {
+    mt = t % p.tiles_m;
+    nt = t / p.tiles_m;
+  } else {
+    mt = t / p.tiles_n;
+    nt = t % p.tiles_n;
+  }
+}
+
 struct Segment {
   int tile, kb0, kb1;  // K blocks [kb0, kb1) of output tile `tile`
   int slot;            // stream-K partial slot: 0 first stream-K segment, 1 later ones
@@ -430,8 +443,10 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
       Walk walk(p, blockIdx.x, G);
       Segment sg;
       while (ok && walk.next(p, sg)) {
-        const int32_t m0 = (sg.tile / p.tiles_n) * BM;
-        const int32_t n0 = (sg.tile % p.tiles_n) * BN;
+        int64_t mt, nt;
+        tile_coords(p, sg.tile, mt, nt);
+        const int32_t m0 = (int32_t)(mt * BM);
+        const int32_t n0 = (int32_t)(nt * BN);
         for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
           const int s = issued % STAGES;
           const uint32_t ph = (uint32_t)(issued / STAGES) & 1u;
@@ -608,8 +623,10 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
       }
       tc_fence_after();
       const bool whole = sg.kb0 == 0 && sg.kb1 == p.num_kb;
-      const int64_t m0 = (int64_t)(sg.tile / p.tiles_n) * BM;
-      const int64_t n0 = (int64_t)(sg.tile % p.tiles_n) * BN;
+      int64_t mt, nt;
+      tile_coords(p, sg.tile, mt, nt);
+      const int64_t m0 = mt * BM;
+      const int64_t n0 = nt * BN;
       // each 128-row half of the tile sits in its own accumulator columns
 #pragma unroll 1
       for (int h = 0; h < Cfg::MH; ++h) {
@@ -720,8 +737,10 @@ streamk_fixup_kernel(TcParams p, int BM, int BN, int64_t G) {
   const int n = nparts;
   // blockIdx.y picks 32 of the tile's BM rows; each thread keeps four
   // independent 16-byte sums so several loads are in flight
-  const int64_t m0 = (t / p.tiles_n) * BM + blockIdx.y * 32;
-  const int64_t n0 = (t % p.tiles_n) * BN;
+  int64_t mt, nt;
+  tile_coords(p, t, mt, nt);
+  const int64_t m0 = mt * BM + blockIdx.y * 32;
+  const int64_t n0 = nt * BN;
   const int64_t row0 = (int64_t)blockIdx.y * 32 * BN;  // offset of these rows in a part
   const bool vec = ((p.ldc & 3) == 0) && ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0);
   const int span = 32 * BN;
@@ -1001,7 +1020,24 @@ int launch_cfg(const gemm_plan_t &plan, const GemmArgs &a, char *ws, cudaStream_
   p.C = a.C;
   p.ldc = a.ldc;
   p.num_kb = num_kb;
+  p.tiles_m = (int)tiles_m;
   p.tiles_n = (int)tiles_n;
+  // Tile order.  The tiles left for the stream-K part come last; their CTAs
+  // sit at unrelated K positions, so whichever operand they share must stay
+  // in L2.  Numbering tiles down the columns puts them in a few column
+  // blocks (sharing B's planes); along the rows, in a few row blocks
+  // (sharing A).  Take the order that shares the operand with more bytes in
+  // the GEMM: B (hi + lo, 8 bytes a value in 3xTF32) against A (4 bytes raw
+  // when split on chip, 8 pre-split; 1xTF32: 4 and 4).  GB300, 3xTF32 with
+  // 128 x 256 tiles, rows / columns: 4096^3 460 / 445 us, 3072 x 4096 x 4096
+  // 399 / 367 us, 6144^3 1.54 / 1.48 ms, 2048 x 8192 x 4096 513 / 491 us,
+  // 8192 x 2048 x 4096 457 / 469 us; even for 256 x 256 tiles.
+  // Tuning knob: GEMM_TC_ORDER = 0 (rows) / 1 (columns).
+  {
+    const double a_bytes = (double)a.M * (AK || !X3 ? 4.0 : 8.0);
+    const double b_bytes = (double)a.N * (X3 ? 8.0 : 4.0);
+    p.col_order = (int)env_u64("GEMM_TC_ORDER", a_bytes < b_bytes ? 1 : 0);
+  }
   // Whole-tile waves first, the rest of the tiles stream-K (G == tiles
   // without stream-K: one wave).  A short stream-K part would give each CTA
   // only a few K blocks and the fix-up many parts per tile, so the last whole

@@ -368,9 +368,10 @@ def _waves(tiles, num_kb, G):
     return waves, rest
 
 
+@pytest.mark.parametrize("order", ["0", "1"])
 @pytest.mark.parametrize("mode,cfg", [("tf32x3", None), ("tf32x3", "256,256,16,3,0,0"),
                                       ("tf32", "256,16,8,0,0"), ("tf32", "256,256,16,6,0,0")])
-def test_tc_whole_waves_then_stream_k(mode, cfg, monkeypatch):
+def test_tc_whole_waves_then_stream_k(mode, cfg, order, monkeypatch):
     # 168 tiles x 64 K blocks (2688 or 5376 rows, 2048 columns, K = 1024): one
     # wave of whole tiles, then a stream-K remainder whose partial tiles the
     # fix-up sums
@@ -379,6 +380,7 @@ def test_tc_whole_waves_then_stream_k(mode, cfg, monkeypatch):
     if cfg:
         monkeypatch.setenv("GEMM_TC_CONFIG", cfg)
     monkeypatch.setenv("GEMM_TC_STREAMK", "1")
+    monkeypatch.setenv("GEMM_TC_ORDER", order)  # tiles numbered along rows (0) or columns (1)
     M, N, K = 2688 * (2 if cfg and cfg.startswith("256,256") else 1), 2048, 1024
     p = gemm.plan(M, N, K, K, N, N, mode=mode)
     tiles = -(-M // p["bm"]) * -(-N // p["bn"])
