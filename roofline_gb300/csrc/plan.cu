@@ -271,14 +271,14 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
       // launch one wave of persistent CTAs that take whole tiles in waves and
       // split the rest of the (tile, K block) work evenly (each at least 4 K
       // blocks); a fix-up kernel sums the parts of tiles shared between
-      // CTAs, in CTA order.  The split part costs about half a wave (its
-      // CTAs sit at unrelated K positions, and the fix-up runs after), so it
-      // is taken when the last partial wave would leave more than ~45 % of
-      // the CTAs idle, or there are 4 to 8 waves (where it measured 2 %
-      // faster), or the shape is HBM-bound (idle SMs are lost bandwidth).
-      // GB300, 3xTF32 step times with / without: 4096^3 464 / 501 us;
-      // 2048 x 4096 x 4096 293 / 266 us; 8192^3 3.39 / 3.46 ms; M = 65536,
-      // N = 64, K = 4096 222 / 236 us; 1xTF32 4096^3 243 / 223 us.
+      // CTAs, in CTA order.  For 3xTF32 (tiles ordered so the split part
+      // shares the larger operand in L2) it always paid on GB300 (step times
+      // with / without: 2560 x 2560 x 4096 207 / 262 us, 2048 x 4096 x 4096
+      // 260 / 264 us, 4096^3 459 / 510 us, 6144^3 1.42 / 1.52 ms).  For
+      // 1xTF32's 256 x 256 tiles the split part and its larger fix-up cost
+      // about half a wave (4096^3: 243 / 222 us), so there it is taken when
+      // the last wave would leave more than ~45 % of the CTAs idle, for 4 to
+      // 8 waves, or for an HBM-bound shape (idle SMs are lost bandwidth).
       {
         const int64_t tiles = ceil_div(M, p.bm) * ceil_div(N, p.bn);
         const int64_t slots = (int64_t)(p.ctas_per_sm > 0 ? p.ctas_per_sm : 1) * sms;
@@ -293,7 +293,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
         const double roof = x3 ? kPlanTf32DenseFlops / 3.0 : kPlanTf32DenseFlops;
         const bool hbm_bound = p.intensity < roof / kPlanHbmBytesPerSec;
         bool want = (tiles % slots) != 0 && tiles < 8 * slots &&
-                    (hbm_bound || idle > 0.45 || waves >= 4.0);
+                    (x3 || hbm_bound || idle > 0.45 || waves >= 4.0);
         if (sk) want = std::atoi(sk) != 0;
         p.stream_k = (want && g >= 2 && g < tiles * 64) ? 1 : 0;
         p.grid_ctas = p.stream_k ? g : tiles;

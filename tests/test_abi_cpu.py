@@ -187,13 +187,12 @@ def test_tensor_core_shape_limits(lib):
 
 
 def test_stream_k_choice(lib):
-    # stream-K when the last wave of 128 x 256 tiles would leave many CTAs
-    # idle (4096^3: 512 tiles on 152 SMs, 3.37 waves), not for 1.68 waves
-    # (2048 x 4096 x 4096) where its cost outweighs the idle SMs; always for
-    # HBM-bound shapes
+    # 3xTF32: stream-K whenever the tiles leave a partial last wave (fewer
+    # than 8 waves); 1xTF32's 256 x 256 tiles: only when the last wave would
+    # leave many CTAs idle, for 4-8 waves, or HBM-bound shapes
     assert gemm.plan(4096, 4096, 4096, mode="tf32x3")["stream_k"] == 1
     p = gemm.plan(2048, 4096, 4096, mode="tf32x3")
-    assert (p["bn"], p["stream_k"], p["grid_ctas"]) == (256, 0, 256)
+    assert (p["bn"], p["stream_k"], p["grid_ctas"]) == (256, 1, 152)
     assert gemm.plan(65536, 64, 4096, mode="tf32x3")["stream_k"] == 1
     assert gemm.plan(4096, 4096, 4096, mode="tf32")["stream_k"] == 0
     # whole waves only: no stream-K
