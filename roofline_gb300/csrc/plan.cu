@@ -274,7 +274,9 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
       // CTAs, in CTA order.  For 3xTF32 (tiles ordered so the split part
       // shares the larger operand in L2) it always paid on GB300 (step times
       // with / without: 2560 x 2560 x 4096 207 / 262 us, 2048 x 4096 x 4096
-      // 260 / 264 us, 4096^3 459 / 510 us, 6144^3 1.42 / 1.52 ms).  For
+      // 260 / 264 us, 4096^3 459 / 510 us, 6144^3 1.42 / 1.52 ms) once there
+      // is more than one wave of tiles; under one wave nearly every tile would
+      // be shared by two CTAs, so it waits for many idle SMs.  For
       // 1xTF32's 256 x 256 tiles the split part and its larger fix-up cost
       // about half a wave (4096^3: 243 / 222 us), so there it is taken when
       // the last wave would leave more than ~45 % of the CTAs idle, for 4 to
@@ -293,7 +295,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
         const double roof = x3 ? kPlanTf32DenseFlops / 3.0 : kPlanTf32DenseFlops;
         const bool hbm_bound = p.intensity < roof / kPlanHbmBytesPerSec;
         bool want = (tiles % slots) != 0 && tiles < 8 * slots &&
-                    (x3 || hbm_bound || idle > 0.45 || waves >= 4.0);
+                    ((x3 && waves > 1.0) || hbm_bound || idle > 0.45 || waves >= 4.0);
         if (sk) want = std::atoi(sk) != 0;
         p.stream_k = (want && g >= 2 && g < tiles * 64) ? 1 : 0;
         p.grid_ctas = p.stream_k ? g : tiles;

@@ -193,6 +193,11 @@ def test_stream_k_choice(lib):
     assert gemm.plan(4096, 4096, 4096, mode="tf32x3")["stream_k"] == 1
     p = gemm.plan(2048, 4096, 4096, mode="tf32x3")
     assert (p["bn"], p["stream_k"], p["grid_ctas"]) == (256, 1, 152)
+    # under one wave (128 tiles on 152 SMs): one CTA per tile
+    q = gemm.plan(1024, 4096, 4096, mode="tf32x3")
+    assert (q["bn"], q["stream_k"], q["grid_ctas"]) == (256, 0, 128)
+    # few tiles for the SMs (512^3: 16 tiles): split K across them
+    assert gemm.plan(512, 512, 512, mode="tf32x3")["stream_k"] == 1
     assert gemm.plan(65536, 64, 4096, mode="tf32x3")["stream_k"] == 1
     assert gemm.plan(4096, 4096, 4096, mode="tf32")["stream_k"] == 0
     # whole waves only: no stream-K
