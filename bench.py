@@ -540,6 +540,43 @@ def device_sets(w, dev, arrays=None, min_sets=2):
     return sets, set_bytes
 
 
+def graph_replay(w, reps=50):
+    """Per-call time of workload `w` (mode AUTO, caller workspace) issued one
+    call at a time and replayed from a CUDA graph holding one call per input
+    set; both timed with CUDA events over the same calls."""
+    import torch
+
+    from roofline_gb300 import gemm
+    sets, _ = device_sets(w, torch.device("cuda"))
+    p = gemm.plan(w.M, w.N, w.K, *w.lds(), "auto", 0, w.beta != 0.0)
+    ws = torch.empty(max(int(p["workspace_bytes"]), 256), dtype=torch.uint8, device="cuda")
+
+    def calls():
+        for a, b, c in sets:
+            gemm.matmul(a, b, c, w.alpha, w.beta, "auto", workspace=ws)
+
+    calls()
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        calls()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    res = {"calls_per_replay": len(sets), "kernel": p["kernel_name"], "launches": p["launches"]}
+    for tag, fn in [("eager_us", calls), ("graph_us", g.replay)]:
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        res[tag] = e0.elapsed_time(e1) * 1e3 / (reps * len(sets))
+    res["graph_tflops"] = float(w.flops) / (res["graph_us"] * 1e-6) / 1e12
+    return res
+
+
 def extras(args, w, sets, info, peaks, peaks_src):
     """Both modes on the same workload, the other large workloads, the FMA and
     HBM copy roofs, and cuBLAS reference points (timed beside the library,
@@ -580,6 +617,12 @@ def extras(args, w, sets, info, peaks, peaks_src):
             torch.cuda.empty_cache()
         except Exception as e:  # pragma: no cover
             out[name] = {"failed": str(e)}
+    # launch overhead: 512^3 calls one by one against the same calls replayed
+    # from a CUDA graph (one capture of one call per input set)
+    try:
+        out["sq512_graph"] = graph_replay(WORKLOADS["sq512"])
+    except Exception as e:  # pragma: no cover
+        out["sq512_graph"] = {"failed": str(e)}
     # FP32 FMA roof, measured ("Bandwidths and peak rate - exercises", exercise 5)
     try:
         out["fp32_fma_peak_tflops"] = {"scalar": gemm.fp32_fma_peak(1 << 16, False),

@@ -161,6 +161,9 @@ GEMM_API int gemm_f32(int64_t M, int64_t N, int64_t K, const float *A, int64_t l
  * that buffer is shared by every call on the device, so calls that use it
  * must not run at the same time on the GPU (issue them on one stream, or
  * give each concurrent stream its own workspace).
+ * A call allocates nothing, synchronises nothing and reads nothing back to
+ * the host when the workspace is given (or the library buffer is already
+ * large enough), so it can be captured into a CUDA graph and replayed.
  * A non-NULL workspace smaller than the plan needs returns
  * GEMM_ERR_WORKSPACE_TOO_SMALL.
  */

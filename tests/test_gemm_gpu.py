@@ -392,3 +392,30 @@ def test_tc_whole_waves_then_stream_k(mode, cfg, order, monkeypatch):
     ref, D = oracle.gemm_entries(A, B, rows, cols, 0.75, 0.25, C0)
     tol = TOL_TF32 if mode == "tf32" else TOL_E1
     assert oracle.err_normalised(got_full["C"][rows, cols], ref, D) <= tol
+
+
+@pytest.mark.parametrize("mode,shape", [("fp32_simt", (512, 512, 512)), ("tf32x3", (1000, 520, 300)),
+                                        ("tf32x3", (4096, 4096, 512)), ("tf32", (1024, 1024, 256))])
+def test_calls_capture_into_a_cuda_graph(mode, shape):
+    # with a caller workspace (no allocation inside the call) a GEMM can be
+    # captured in a CUDA graph and replayed; every replay recomputes C
+    import torch
+    from roofline_gb300 import gemm
+    M, N, K = shape
+    A = torch.from_numpy(matrix(M, K, None, 61, "int2")).cuda()
+    B = torch.from_numpy(matrix(K, N, None, 62, "int2")).cuda()
+    C = torch.full((M, N), float("nan"), device="cuda")
+    p = gemm.plan(M, N, K, mode=mode)
+    ws = torch.empty(max(p["workspace_bytes"], 256), dtype=torch.uint8, device="cuda")
+    gemm.matmul(A, B, C, mode=mode, workspace=ws)  # warm-up outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.graph(g, stream=s):
+        gemm.matmul(A, B, C, mode=mode, workspace=ws)
+    ref = oracle.gemm(A.cpu().numpy(), B.cpu().numpy(), 1.0, 0.0, None)
+    for _ in range(3):
+        C.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert oracle.mismatches(C.cpu().numpy(), ref) == 0
