@@ -179,11 +179,6 @@ def ncu_traffic(kernel_key: str):
         return None, "absent"
 
 
-KERNEL_SOURCES = {
-    "simt": ["roofline_gb300/csrc/simt.cu"],
-    "tc_tf32x3": ["roofline_gb300/csrc/tc_tf32x3.cu"],
-}
-
 
 # --------------------------------------------------------------- oracle timing
 

@@ -1,0 +1,229 @@
+// Passes around the tensor-core GEMM kernel: the TF32 hi/lo split of an
+// operand into the workspace (row by row, or transposed so that it becomes
+// K-major), and the stream-K fix-up that sums the parts of tiles shared
+// between CTAs.  All are HBM-bound copies.
+#include "tc_common.cuh"
+
+namespace gg {
+namespace tc {
+namespace {
+
+// Stream-K fix-up: an output tile whose K blocks were split between CTAs
+// gets C = alpha * (sum of its partial tiles, in CTA order) + beta * C.
+// Block j looks at the boundary between CTAs j and j+1 in the stream-K unit
+// space; the block whose boundary is the first one strictly inside a tile
+// handles that tile, all other blocks return at once (whole tiles were
+// written by the GEMM).
+constexpr int kFixMaxParts = 256;
+constexpr int kFixRows = 16;  // tile rows per fix-up block
+
+__global__ void __launch_bounds__(256)
+streamk_fixup_kernel(TcParams p, int BM, int BN, int64_t G) {
+  __shared__ int64_t part_off[kFixMaxParts];
+  __shared__ int nparts;
+  grid_dependency_wait();  // the GEMM's partial tiles
+  const int64_t c = (int64_t)blockIdx.x + 1;  // boundary between CTAs c-1 and c
+  // boundaries live in the stream-K unit space (tiles after the whole-tile waves)
+  const int64_t b = unit_begin(p.sk_units, c, G);
+  const int64_t tl = b / p.num_kb;
+  const int64_t t = p.dp_tiles + tl;
+  const int64_t first = tl * p.num_kb, last = first + p.num_kb - 1;
+  if (b == first || b > last) return;                       // not strictly inside a tile
+  if (unit_begin(p.sk_units, c - 1, G) > first) return;     // an earlier boundary owns it
+  if (threadIdx.x == 0) {
+    int n = 0;
+    for (int64_t cta = c - 1; cta < G && unit_begin(p.sk_units, cta, G) <= last; ++cta) {
+      const int64_t ub = unit_begin(p.sk_units, cta, G), ue = unit_begin(p.sk_units, cta + 1, G);
+      if (ub == ue) continue;  // no work
+      // the tile is this CTA's first segment (slot 0) or its last (slot 1)
+      const int slot = (ub >= first) ? 0 : 1;
+      if (n < kFixMaxParts) part_off[n++] = (cta * 2 + slot) * (int64_t)BM * BN;
+    }
+    nparts = n;
+  }
+  __syncthreads();
+  const int n = nparts;
+  // blockIdx.y picks 32 of the tile's BM rows; each thread keeps four
+  // independent 16-byte sums so several loads are in flight
+  int64_t mt, nt;
+  tile_coords(p, t, mt, nt);
+  const int64_t m0 = mt * BM + blockIdx.y * kFixRows;
+  const int64_t n0 = nt * BN;
+  const int64_t row0 = (int64_t)blockIdx.y * kFixRows * BN;  // offset of these rows in a part
+  const bool vec = ((p.ldc & 3) == 0) && ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0);
+  const int span = kFixRows * BN;
+  for (int e0 = threadIdx.x * 4; e0 < span; e0 += blockDim.x * 16) {
+    float4 acc[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = 0; i < n; ++i) {
+      const float *base = p.partial + part_off[i] + row0;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int e = e0 + u * blockDim.x * 4;
+        if (e < span) {
+          const float4 v = *reinterpret_cast<const float4 *>(base + e);
+          acc[u].x += v.x;
+          acc[u].y += v.y;
+          acc[u].z += v.z;
+          acc[u].w += v.w;
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int e = e0 + u * blockDim.x * 4;
+      if (e >= span) continue;
+      const int r = e / BN, col = e % BN;
+      const int64_t gr = m0 + r, gc = n0 + col;
+      if (gr >= p.M || gc >= p.N) continue;
+      float *dst = p.C + gr * p.ldc + gc;
+      const float a4[4] = {acc[u].x, acc[u].y, acc[u].z, acc[u].w};
+      if (vec && gc + 4 <= p.N) {
+        float4 o = make_float4(p.alpha * a4[0], p.alpha * a4[1], p.alpha * a4[2], p.alpha * a4[3]);
+        if (p.beta != 0.0f) {
+          const float4 old = *reinterpret_cast<const float4 *>(dst);
+          o.x = fmaf(p.beta, old.x, o.x);
+          o.y = fmaf(p.beta, old.y, o.y);
+          o.z = fmaf(p.beta, old.z, o.z);
+          o.w = fmaf(p.beta, old.w, o.w);
+        }
+        *reinterpret_cast<float4 *>(dst) = o;
+      } else {
+        for (int q = 0; q < 4 && gc + q < p.N; ++q) {
+          float o = p.alpha * a4[q];
+          if (p.beta != 0.0f) o = fmaf(p.beta, dst[q], o);
+          dst[q] = o;
+        }
+      }
+    }
+  }
+}
+
+// dst_hi/dst_lo (rows x kp, row-major) <- split of src (rows x k, ld), zero for k <= c < kp
+// (lo == nullptr: the hi part only, for 1xTF32).
+__global__ void split_rows_kernel(const float *__restrict__ src, int64_t ld, int64_t rows,
+                                  int64_t k, int64_t kp, float *__restrict__ hi,
+                                  float *__restrict__ lo) {
+  grid_launch_dependents();
+  const int64_t groups = rows * (kp / 4);
+  for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < groups;
+       g += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = g / (kp / 4);
+    const int64_t c = (g % (kp / 4)) * 4;
+    const float *s = src + r * ld + c;
+    float v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = (c + i < k) ? __ldg(s + i) : 0.0f;
+    float4 h, l;
+    h.x = tf32_rna(v[0]); l.x = v[0] - h.x;
+    h.y = tf32_rna(v[1]); l.y = v[1] - h.y;
+    h.z = tf32_rna(v[2]); l.z = v[2] - h.z;
+    h.w = tf32_rna(v[3]); l.w = v[3] - h.w;
+    *reinterpret_cast<float4 *>(hi + r * kp + c) = h;
+    if (lo) *reinterpret_cast<float4 *>(lo + r * kp + c) = l;
+  }
+}
+
+// B (k x n, ld, row-major) -> Bt_hi/Bt_lo (n x kp, row-major), columns
+// k <= c < kp zero.  One CTA of 256 threads moves a 32 (k) x 128 (n) tile:
+// each thread loads four 16-byte pieces along n (all in flight at once),
+// the tile goes through shared memory, and each thread then stores four
+// 16-byte pieces of hi and of lo along k.  `vec` (ld % 4 == 0 and a 16-byte
+// aligned B) enables the 16-byte loads; the stores are 16-byte aligned
+// because kp is a multiple of 4.
+constexpr int kTrK = 32, kTrN = 128;
+
+__global__ void __launch_bounds__(256)
+split_transpose_kernel(const float *__restrict__ src, int64_t ld, int64_t k, int64_t n,
+                       int64_t kp, int vec, float *__restrict__ hi, float *__restrict__ lo) {
+  __shared__ float tile[kTrK][kTrN + 1];
+  grid_dependency_wait();   // A_hi/A_lo pass before this one (if any) is done
+  grid_launch_dependents();  // the GEMM may launch; it waits for this grid to finish
+  const int64_t k0 = (int64_t)blockIdx.y * kTrK;
+  const int64_t n0 = (int64_t)blockIdx.x * kTrN;
+  const int t = threadIdx.x;
+  // loads: piece p = t + 256 * i covers row p / 32, columns 4 * (p % 32) .. +3
+  float4 v[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int p = t + 256 * i;
+    const int64_t kk = k0 + p / 32, nn = n0 + 4 * (p % 32);
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (kk < k) {
+      const float *s = src + kk * ld + nn;
+      if (vec && nn + 4 <= n) {
+        x = __ldg(reinterpret_cast<const float4 *>(s));
+      } else {
+        if (nn + 0 < n) x.x = __ldg(s + 0);
+        if (nn + 1 < n) x.y = __ldg(s + 1);
+        if (nn + 2 < n) x.z = __ldg(s + 2);
+        if (nn + 3 < n) x.w = __ldg(s + 3);
+      }
+    }
+    v[i] = x;
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int p = t + 256 * i;
+    float *row = &tile[p / 32][4 * (p % 32)];
+    row[0] = v[i].x;
+    row[1] = v[i].y;
+    row[2] = v[i].z;
+    row[3] = v[i].w;
+  }
+  __syncthreads();
+  // stores: piece q = t + 256 * i covers output row n0 + q / 8, k quad q % 8
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int q = t + 256 * i;
+    const int nl = q / 8, kq = 4 * (q % 8);
+    const int64_t nn = n0 + nl, kk = k0 + kq;
+    if (nn < n && kk < kp) {
+      float4 h, l;
+      const float a0 = tile[kq + 0][nl], a1 = tile[kq + 1][nl];
+      const float a2 = tile[kq + 2][nl], a3 = tile[kq + 3][nl];
+      h.x = tf32_rna(a0); l.x = a0 - h.x;
+      h.y = tf32_rna(a1); l.y = a1 - h.y;
+      h.z = tf32_rna(a2); l.z = a2 - h.z;
+      h.w = tf32_rna(a3); l.w = a3 - h.w;
+      *reinterpret_cast<float4 *>(hi + nn * kp + kk) = h;
+      if (lo) *reinterpret_cast<float4 *>(lo + nn * kp + kk) = l;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_split_rows(const float *src, int64_t ld, int64_t rows, int64_t k, int64_t kp,
+                              float *hi, float *lo, cudaStream_t s) {
+  int64_t blocks = ceil_div(rows * (kp / 4), 256);
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  if (blocks < 1) blocks = 1;
+  split_rows_kernel<<<(unsigned)blocks, 256, 0, s>>>(src, ld, rows, k, kp, hi, lo);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_split_transposed(const float *src, int64_t ld, int64_t k, int64_t cols,
+                                    int64_t kp, float *hi, float *lo, cudaStream_t s) {
+  const int vec = ((ld & 3) == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0) ? 1 : 0;
+  dim3 grid((unsigned)ceil_div(cols, kTrN), (unsigned)ceil_div(kp, kTrK));
+  split_transpose_kernel<<<grid, 256, 0, s>>>(src, ld, k, cols, kp, vec, hi, lo);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fixup(const TcParams &p, int bm, int bn, int64_t G, bool pdl, cudaStream_t s) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t fc = {};
+  fc.gridDim = dim3((unsigned)(G - 1), (unsigned)(bm / kFixRows));
+  fc.blockDim = dim3(256);
+  fc.stream = s;
+  fc.attrs = attr;
+  fc.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&fc, streamk_fixup_kernel, p, bm, bn, G);
+}
+
+}  // namespace tc
+}  // namespace gg

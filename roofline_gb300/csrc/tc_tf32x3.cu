@@ -41,299 +41,20 @@
 // kernel records GEMM_ERR_DEVICE_TIMEOUT in a device status word, stops
 // issuing work, waits (bounded) for the copies and MMAs it already issued,
 // frees its TMEM and returns.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
 #include <cstdlib>
 #include <mutex>
 
-#include "common.cuh"
+#include "tc_common.cuh"
 
 namespace gg {
+
+using namespace tc;
 
 namespace {
 
 __device__ int g_tc_status;  // 0 = ok, else a GEMM_ERR_* code
 
-constexpr int kThreadsTC = 192;
-constexpr int kConvThreads = 128;  // warps 2..5
-
-// ------------------------------------------------------------------ PTX helpers
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ uint64_t globaltimer() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-               "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Waits for the phase of `bar` with the given parity.  Gives up when the
-// deadline passes or another role has raised the CTA's abort flag.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t deadline,
-                                          volatile int *abort_flag) {
-  uint32_t spins = 0;
-  while (!mbar_try_wait(bar, parity)) {
-    if ((++spins & 63u) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer() > deadline) return false;
-    }
-  }
-  return true;
-}
-
-__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar,
-                                            int32_t x, int32_t y) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
-      : "memory");
-}
-
-__device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
-  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_alloc(uint32_t *dst, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                   smem_u32(dst)),
-               "r"(ncols)
-               : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-               : "memory");
-}
-
-// D(tmem) (+)= A(smem) * B(smem)^T, both K-major, kind::tf32.
-__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                         uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Arrives on `bar` once every previously issued tcgen05 op of this thread completes.
-__device__ __forceinline__ void mma_commit(uint64_t *bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_u32(bar))
-      : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-}
-
-__device__ __forceinline__ void tmem_ld_wait() {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void fence_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// Programmatic dependent launch: wait for the previous kernel in the stream
-// (no-op when launched without the attribute), and let the next one launch.
-__device__ __forceinline__ void grid_dependency_wait() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-__device__ __forceinline__ void grid_launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-__device__ __forceinline__ float tf32_rna(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return __uint_as_float(r);
-}
-
-// Shared-memory matrix descriptor of a K-major, swizzled operand tile whose
-// 8-row groups are `sbo` bytes apart.  layout: 2 = 128 B swizzle, 4 = 64 B.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t sbo, uint32_t layout) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-  d |= (uint64_t)1u << 16;                            // leading byte offset (unused here)
-  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;        // stride byte offset
-  d |= (uint64_t)1u << 46;                            // descriptor version for tcgen05
-  d |= (uint64_t)layout << 61;
-  return d;
-}
-
-// Instruction descriptor: D = F32, A = B = TF32, both K-major, M x N.
-__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
-  return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) |
-         ((uint32_t)(M >> 4) << 24);
-}
-
-// D(tmem) (+)= A(tmem) * B(smem)^T, kind::tf32 (A read from tensor memory).
-__device__ __forceinline__ void mma_tf32_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
-                                            uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-template <int N>
-__device__ __forceinline__ void tmem_st(uint32_t taddr, const uint32_t (&r)[N]);
-
-template <>
-__device__ __forceinline__ void tmem_st<16>(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-      : "memory");
-}
-
-template <>
-__device__ __forceinline__ void tmem_st<32>(uint32_t taddr, const uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
-      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(
-          taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
-      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
-      "r"(r[29]), "r"(r[30]), "r"(r[31])
-      : "memory");
-}
-
-__device__ __forceinline__ void tmem_st_wait() {
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
 // ------------------------------------------------------------------ the GEMM kernel
-
-struct TcParams {
-  int64_t M, N, K;
-  float alpha, beta;
-  float *C;
-  int64_t ldc;
-  int num_kb;        // K blocks per output tile
-  int tiles_m, tiles_n;  // output tiles along M and N
-  int col_order;     // tile t = n_tile * tiles_m + m_tile (1) or m_tile * tiles_n + n_tile (0)
-  int waves;         // whole tiles per CTA before the stream-K part
-  int64_t dp_tiles;  // waves * G: tiles done whole, in waves
-  int64_t sk_units;  // (tiles - dp_tiles) * num_kb: units shared out stream-K
-  float *partial;    // stream-K partial tiles: 2 slots of 128 x BN per CTA
-  uint64_t timeout_ns;
-  int stall_producer;  // test hook: the producer issues nothing
-};
-
-// Work split.  CTA c of G first takes `waves` whole tiles, c, c + G, ...:
-// the CTAs of one wave start their tiles together and walk K in step, so the
-// operand slices of a wave are shared through L2.  The (tile, K block) units
-// of the tiles left over are then split evenly (stream-K): CTA c owns units
-// [c*S/G, (c+1)*S/G) of them, walked tile by tile.  Without stream-K,
-// G = tiles: one wave of one tile per CTA.
-// Row-tile and column-tile of output tile t.
-__host__ __device__ __forceinline__ void tile_coords(const TcParams &p, int64_t t, int64_t &mt,
-                                                     int64_t &nt) {
-  if (p.col_order) {
-    mt = t % p.tiles_m;
-    nt = t / p.tiles_m;
-  } else {
-    mt = t / p.tiles_n;
-    nt = t % p.tiles_n;
-  }
-}
-
-struct Segment {
-  int tile, kb0, kb1;  // K blocks [kb0, kb1) of output tile `tile`
-  int slot;            // stream-K partial slot: 0 first stream-K segment, 1 later ones
-};
-
-__host__ __device__ __forceinline__ int64_t unit_begin(int64_t total, int64_t c, int64_t G) {
-  return total * c / G;
-}
-
-struct Walk {
-  int64_t c, G, u, u1;
-  int w;
-  bool first_sk;
-
-  __device__ __forceinline__ Walk(const TcParams &p, int64_t cta, int64_t grid)
-      : c(cta), G(grid), u(unit_begin(p.sk_units, cta, grid)),
-        u1(unit_begin(p.sk_units, cta + 1, grid)), w(0), first_sk(true) {}
-
-  __device__ __forceinline__ bool next(const TcParams &p, Segment &sg) {
-    if (w < p.waves) {
-      sg.tile = (int)((int64_t)w * G + c);
-      sg.kb0 = 0;
-      sg.kb1 = p.num_kb;
-      sg.slot = 0;
-      ++w;
-      return true;
-    }
-    if (u >= u1) return false;
-    sg.tile = (int)(p.dp_tiles + u / p.num_kb);
-    sg.kb0 = (int)(u % p.num_kb);
-    const int64_t left = u1 - u;
-    sg.kb1 = (int)(sg.kb0 + left < p.num_kb ? sg.kb0 + left : p.num_kb);
-    u += sg.kb1 - sg.kb0;
-    sg.slot = first_sk ? 0 : 1;
-    first_sk = false;
-    return true;
-  }
-};
 
 // BN: output columns per CTA.  BK: K depth of one stage (16 -> 64-byte
 // swizzle, 32 -> 128-byte swizzle).  AK: A arrives raw (FP32) and the
@@ -701,192 +422,6 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
   if (warp == 1) tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
 }
 
-// Stream-K fix-up: an output tile whose K blocks were split between CTAs
-// gets C = alpha * (sum of its partial tiles, in CTA order) + beta * C.
-// Block j looks at the boundary between CTAs j and j+1 in the stream-K unit
-// space; the block whose boundary is the first one strictly inside a tile
-// handles that tile, all other blocks return at once (whole tiles were
-// written by the GEMM).
-constexpr int kFixMaxParts = 256;
-
-__global__ void __launch_bounds__(256)
-streamk_fixup_kernel(TcParams p, int BM, int BN, int64_t G) {
-  __shared__ int64_t part_off[kFixMaxParts];
-  __shared__ int nparts;
-  grid_dependency_wait();  // the GEMM's partial tiles
-  const int64_t c = (int64_t)blockIdx.x + 1;  // boundary between CTAs c-1 and c
-  // boundaries live in the stream-K unit space (tiles after the whole-tile waves)
-  const int64_t b = unit_begin(p.sk_units, c, G);
-  const int64_t tl = b / p.num_kb;
-  const int64_t t = p.dp_tiles + tl;
-  const int64_t first = tl * p.num_kb, last = first + p.num_kb - 1;
-  if (b == first || b > last) return;                       // not strictly inside a tile
-  if (unit_begin(p.sk_units, c - 1, G) > first) return;     // an earlier boundary owns it
-  if (threadIdx.x == 0) {
-    int n = 0;
-    for (int64_t cta = c - 1; cta < G && unit_begin(p.sk_units, cta, G) <= last; ++cta) {
-      const int64_t ub = unit_begin(p.sk_units, cta, G), ue = unit_begin(p.sk_units, cta + 1, G);
-      if (ub == ue) continue;  // no work
-      // the tile is this CTA's first segment (slot 0) or its last (slot 1)
-      const int slot = (ub >= first) ? 0 : 1;
-      if (n < kFixMaxParts) part_off[n++] = (cta * 2 + slot) * (int64_t)BM * BN;
-    }
-    nparts = n;
-  }
-  __syncthreads();
-  const int n = nparts;
-  // blockIdx.y picks 32 of the tile's BM rows; each thread keeps four
-  // independent 16-byte sums so several loads are in flight
-  int64_t mt, nt;
-  tile_coords(p, t, mt, nt);
-  const int64_t m0 = mt * BM + blockIdx.y * 32;
-  const int64_t n0 = nt * BN;
-  const int64_t row0 = (int64_t)blockIdx.y * 32 * BN;  // offset of these rows in a part
-  const bool vec = ((p.ldc & 3) == 0) && ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0);
-  const int span = 32 * BN;
-  for (int e0 = threadIdx.x * 4; e0 < span; e0 += blockDim.x * 16) {
-    float4 acc[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int i = 0; i < n; ++i) {
-      const float *base = p.partial + part_off[i] + row0;
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int e = e0 + u * blockDim.x * 4;
-        if (e < span) {
-          const float4 v = *reinterpret_cast<const float4 *>(base + e);
-          acc[u].x += v.x;
-          acc[u].y += v.y;
-          acc[u].z += v.z;
-          acc[u].w += v.w;
-        }
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int e = e0 + u * blockDim.x * 4;
-      if (e >= span) continue;
-      const int r = e / BN, col = e % BN;
-      const int64_t gr = m0 + r, gc = n0 + col;
-      if (gr >= p.M || gc >= p.N) continue;
-      float *dst = p.C + gr * p.ldc + gc;
-      const float a4[4] = {acc[u].x, acc[u].y, acc[u].z, acc[u].w};
-      if (vec && gc + 4 <= p.N) {
-        float4 o = make_float4(p.alpha * a4[0], p.alpha * a4[1], p.alpha * a4[2], p.alpha * a4[3]);
-        if (p.beta != 0.0f) {
-          const float4 old = *reinterpret_cast<const float4 *>(dst);
-          o.x = fmaf(p.beta, old.x, o.x);
-          o.y = fmaf(p.beta, old.y, o.y);
-          o.z = fmaf(p.beta, old.z, o.z);
-          o.w = fmaf(p.beta, old.w, o.w);
-        }
-        *reinterpret_cast<float4 *>(dst) = o;
-      } else {
-        for (int q = 0; q < 4 && gc + q < p.N; ++q) {
-          float o = p.alpha * a4[q];
-          if (p.beta != 0.0f) o = fmaf(p.beta, dst[q], o);
-          dst[q] = o;
-        }
-      }
-    }
-  }
-}
-
-// ------------------------------------------------------------------ split pass
-
-// dst_hi/dst_lo (rows x kp, row-major) <- split of src (rows x k, ld), zero for k <= c < kp
-// (lo == nullptr: the hi part only, for 1xTF32).
-__global__ void split_rows_kernel(const float *__restrict__ src, int64_t ld, int64_t rows,
-                                  int64_t k, int64_t kp, float *__restrict__ hi,
-                                  float *__restrict__ lo) {
-  grid_launch_dependents();
-  const int64_t groups = rows * (kp / 4);
-  for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < groups;
-       g += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = g / (kp / 4);
-    const int64_t c = (g % (kp / 4)) * 4;
-    const float *s = src + r * ld + c;
-    float v[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) v[i] = (c + i < k) ? __ldg(s + i) : 0.0f;
-    float4 h, l;
-    h.x = tf32_rna(v[0]); l.x = v[0] - h.x;
-    h.y = tf32_rna(v[1]); l.y = v[1] - h.y;
-    h.z = tf32_rna(v[2]); l.z = v[2] - h.z;
-    h.w = tf32_rna(v[3]); l.w = v[3] - h.w;
-    *reinterpret_cast<float4 *>(hi + r * kp + c) = h;
-    if (lo) *reinterpret_cast<float4 *>(lo + r * kp + c) = l;
-  }
-}
-
-// B (k x n, ld, row-major) -> Bt_hi/Bt_lo (n x kp, row-major), columns
-// k <= c < kp zero.  One CTA of 256 threads moves a 32 (k) x 128 (n) tile:
-// each thread loads four 16-byte pieces along n (all in flight at once),
-// the tile goes through shared memory, and each thread then stores four
-// 16-byte pieces of hi and of lo along k.  `vec` (ld % 4 == 0 and a 16-byte
-// aligned B) enables the 16-byte loads; the stores are 16-byte aligned
-// because kp is a multiple of 4.
-constexpr int kTrK = 32, kTrN = 128;
-
-__global__ void __launch_bounds__(256)
-split_transpose_kernel(const float *__restrict__ src, int64_t ld, int64_t k, int64_t n,
-                       int64_t kp, int vec, float *__restrict__ hi, float *__restrict__ lo) {
-  __shared__ float tile[kTrK][kTrN + 1];
-  grid_dependency_wait();   // A_hi/A_lo pass before this one (if any) is done
-  grid_launch_dependents();  // the GEMM may launch; it waits for this grid to finish
-  const int64_t k0 = (int64_t)blockIdx.y * kTrK;
-  const int64_t n0 = (int64_t)blockIdx.x * kTrN;
-  const int t = threadIdx.x;
-  // loads: piece p = t + 256 * i covers row p / 32, columns 4 * (p % 32) .. +3
-  float4 v[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int p = t + 256 * i;
-    const int64_t kk = k0 + p / 32, nn = n0 + 4 * (p % 32);
-    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (kk < k) {
-      const float *s = src + kk * ld + nn;
-      if (vec && nn + 4 <= n) {
-        x = __ldg(reinterpret_cast<const float4 *>(s));
-      } else {
-        if (nn + 0 < n) x.x = __ldg(s + 0);
-        if (nn + 1 < n) x.y = __ldg(s + 1);
-        if (nn + 2 < n) x.z = __ldg(s + 2);
-        if (nn + 3 < n) x.w = __ldg(s + 3);
-      }
-    }
-    v[i] = x;
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int p = t + 256 * i;
-    float *row = &tile[p / 32][4 * (p % 32)];
-    row[0] = v[i].x;
-    row[1] = v[i].y;
-    row[2] = v[i].z;
-    row[3] = v[i].w;
-  }
-  __syncthreads();
-  // stores: piece q = t + 256 * i covers output row n0 + q / 8, k quad q % 8
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int q = t + 256 * i;
-    const int nl = q / 8, kq = 4 * (q % 8);
-    const int64_t nn = n0 + nl, kk = k0 + kq;
-    if (nn < n && kk < kp) {
-      float4 h, l;
-      const float a0 = tile[kq + 0][nl], a1 = tile[kq + 1][nl];
-      const float a2 = tile[kq + 2][nl], a3 = tile[kq + 3][nl];
-      h.x = tf32_rna(a0); l.x = a0 - h.x;
-      h.y = tf32_rna(a1); l.y = a1 - h.y;
-      h.z = tf32_rna(a2); l.z = a2 - h.z;
-      h.w = tf32_rna(a3); l.w = a3 - h.w;
-      *reinterpret_cast<float4 *>(hi + nn * kp + kk) = h;
-      if (lo) *reinterpret_cast<float4 *>(lo + nn * kp + kk) = l;
-    }
-  }
-}
-
 // ------------------------------------------------------------------ host side
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -976,25 +511,19 @@ int launch_cfg(const gemm_plan_t &plan, const GemmArgs &a, char *ws, cudaStream_
   // Split passes: each operand becomes K-major hi (and lo) planes.  An
   // operand stored with K contiguous (A as M x K, B as N x K) is split row
   // by row; one stored with K as its row index is split and transposed.
-  auto split_k_major = [&](const float *src, int64_t ld, int64_t rows, float *hi, float *lo) {
-    int64_t blocks = ceil_div(rows * (L.kp / 4), 256);
-    if (blocks > 152 * 16) blocks = 152 * 16;
-    split_rows_kernel<<<(unsigned)blocks, 256, 0, s>>>(src, ld, rows, a.K, L.kp, hi, lo);
-  };
-  auto split_transposed = [&](const float *src, int64_t ld, int64_t cols, float *hi, float *lo) {
-    const int vec = ((ld & 3) == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0) ? 1 : 0;
-    dim3 grid((unsigned)ceil_div(cols, kTrN), (unsigned)ceil_div(L.kp, kTrK));
-    split_transpose_kernel<<<grid, 256, 0, s>>>(src, ld, a.K, cols, L.kp, vec, hi, lo);
-  };
+  cudaError_t se = cudaSuccess;
   if (!AK) {
-    if (a.ta) split_transposed(a.A, a.lda, a.M, ahi, X3 ? alo : nullptr);
-    else split_k_major(a.A, a.lda, a.M, ahi, X3 ? alo : nullptr);
+    se = a.ta ? launch_split_transposed(a.A, a.lda, a.K, a.M, L.kp, ahi, X3 ? alo : nullptr, s)
+              : launch_split_rows(a.A, a.lda, a.M, a.K, L.kp, ahi, X3 ? alo : nullptr, s);
   }
-  if (!a.b_presplit) {
-    if (a.tb) split_k_major(a.B, a.ldb, a.N, bhi, X3 ? blo : nullptr);
-    else split_transposed(a.B, a.ldb, a.N, bhi, X3 ? blo : nullptr);
+  if (se == cudaSuccess && !a.b_presplit) {
+    se = a.tb ? launch_split_rows(a.B, a.ldb, a.N, a.K, L.kp, bhi, X3 ? blo : nullptr, s)
+              : launch_split_transposed(a.B, a.ldb, a.K, a.N, L.kp, bhi, X3 ? blo : nullptr, s);
   }
-  if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_CUDA;
+  if (se != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
 
   CUtensorMap tA0, tA1, tB0, tB1;
   bool ok;
@@ -1085,13 +614,7 @@ int launch_cfg(const gemm_plan_t &plan, const GemmArgs &a, char *ws, cudaStream_
     return GEMM_ERR_CUDA;
   }
   if (plan.stream_k) {
-    cudaLaunchConfig_t fc = {};
-    fc.gridDim = dim3((unsigned)(G - 1), BM / 32);
-    fc.blockDim = dim3(256);
-    fc.stream = s;
-    fc.attrs = attr;
-    fc.numAttrs = pdl ? 1 : 0;
-    e = cudaLaunchKernelEx(&fc, streamk_fixup_kernel, p, (int)BM, (int)BN, G);
+    e = launch_fixup(p, BM, BN, G, pdl, s);
     if (e != cudaSuccess) {
       cudaGetLastError();
       return GEMM_ERR_CUDA;
