@@ -291,16 +291,18 @@ struct Walk {
 };
 
 // Passes around the GEMM kernel (tc_split.cu).  Each returns the launch error.
+// pdl: launched with programmatic dependent launch, so it may be scheduled
+// while the kernel before it drains; it waits for that kernel before touching
+// memory.
 // dst hi/lo (rows x kp, row-major) <- split of src (rows x k, row stride ld);
 // columns k..kp-1 zero; lo == nullptr: the hi part only (1xTF32).
 cudaError_t launch_split_rows(const float *src, int64_t ld, int64_t rows, int64_t k, int64_t kp,
-                              float *hi, float *lo, cudaStream_t s);
+                              float *hi, float *lo, bool pdl, cudaStream_t s);
 // dst hi/lo (cols x kp, row-major) <- split of the transpose of src (k x cols,
 // row stride ld); columns k..kp-1 zero.
 cudaError_t launch_split_transposed(const float *src, int64_t ld, int64_t k, int64_t cols,
-                                    int64_t kp, float *hi, float *lo, cudaStream_t s);
-// Sums the parts of the tiles shared between stream-K CTAs into C.  pdl: may
-// be scheduled while the GEMM kernel drains (it waits for it before reading).
+                                    int64_t kp, float *hi, float *lo, bool pdl, cudaStream_t s);
+// Sums the parts of the tiles shared between stream-K CTAs into C.
 cudaError_t launch_fixup(const TcParams &p, int bm, int bn, int64_t G, bool pdl, cudaStream_t s);
 
 }  // namespace tc

@@ -105,6 +105,7 @@ streamk_fixup_kernel(TcParams p, int BM, int BN, int64_t G) {
 __global__ void split_rows_kernel(const float *__restrict__ src, int64_t ld, int64_t rows,
                                   int64_t k, int64_t kp, float *__restrict__ hi,
                                   float *__restrict__ lo) {
+  grid_dependency_wait();     // the kernel before this one is done
   grid_launch_dependents();
   const int64_t groups = rows * (kp / 4);
   for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < groups;
@@ -138,7 +139,7 @@ __global__ void __launch_bounds__(256)
 split_transpose_kernel(const float *__restrict__ src, int64_t ld, int64_t k, int64_t n,
                        int64_t kp, int vec, float *__restrict__ hi, float *__restrict__ lo) {
   __shared__ float tile[kTrK][kTrN + 1];
-  grid_dependency_wait();   // A_hi/A_lo pass before this one (if any) is done
+  grid_dependency_wait();   // the kernel before this one is done
   grid_launch_dependents();  // the GEMM may launch; it waits for this grid to finish
   const int64_t k0 = (int64_t)blockIdx.y * kTrK;
   const int64_t n0 = (int64_t)blockIdx.x * kTrN;
@@ -195,34 +196,42 @@ split_transpose_kernel(const float *__restrict__ src, int64_t ld, int64_t k, int
 
 }  // namespace
 
-cudaError_t launch_split_rows(const float *src, int64_t ld, int64_t rows, int64_t k, int64_t kp,
-                              float *hi, float *lo, cudaStream_t s) {
-  int64_t blocks = ceil_div(rows * (kp / 4), 256);
-  if (blocks > 152 * 16) blocks = 152 * 16;
-  if (blocks < 1) blocks = 1;
-  split_rows_kernel<<<(unsigned)blocks, 256, 0, s>>>(src, ld, rows, k, kp, hi, lo);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_split_transposed(const float *src, int64_t ld, int64_t k, int64_t cols,
-                                    int64_t kp, float *hi, float *lo, cudaStream_t s) {
-  const int vec = ((ld & 3) == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0) ? 1 : 0;
-  dim3 grid((unsigned)ceil_div(cols, kTrN), (unsigned)ceil_div(kp, kTrK));
-  split_transpose_kernel<<<grid, 256, 0, s>>>(src, ld, k, cols, kp, vec, hi, lo);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_fixup(const TcParams &p, int bm, int bn, int64_t G, bool pdl, cudaStream_t s) {
+// One launch with the programmatic-dependent-launch attribute when `pdl`.
+template <typename... Args>
+cudaError_t launch(void (*kern)(Args...), dim3 grid, dim3 block, bool pdl, cudaStream_t s,
+                   Args... args) {
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t fc = {};
-  fc.gridDim = dim3((unsigned)(G - 1), (unsigned)(bm / kFixRows));
-  fc.blockDim = dim3(256);
-  fc.stream = s;
-  fc.attrs = attr;
-  fc.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&fc, streamk_fixup_kernel, p, bm, bn, G);
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = grid;
+  lc.blockDim = block;
+  lc.stream = s;
+  lc.attrs = attr;
+  lc.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&lc, kern, args...);
+}
+
+cudaError_t launch_split_rows(const float *src, int64_t ld, int64_t rows, int64_t k, int64_t kp,
+                              float *hi, float *lo, bool pdl, cudaStream_t s) {
+  int64_t blocks = ceil_div(rows * (kp / 4), 256);
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  if (blocks < 1) blocks = 1;
+  return launch(split_rows_kernel, dim3((unsigned)blocks), dim3(256), pdl, s, src, ld, rows, k,
+                kp, hi, lo);
+}
+
+cudaError_t launch_split_transposed(const float *src, int64_t ld, int64_t k, int64_t cols,
+                                    int64_t kp, float *hi, float *lo, bool pdl, cudaStream_t s) {
+  const int vec = ((ld & 3) == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0) ? 1 : 0;
+  dim3 grid((unsigned)ceil_div(cols, kTrN), (unsigned)ceil_div(kp, kTrK));
+  return launch(split_transpose_kernel, grid, dim3(256), pdl, s, src, ld, k, cols, kp, vec, hi,
+                lo);
+}
+
+cudaError_t launch_fixup(const TcParams &p, int bm, int bn, int64_t G, bool pdl, cudaStream_t s) {
+  return launch(streamk_fixup_kernel, dim3((unsigned)(G - 1), (unsigned)(bm / kFixRows)),
+                dim3(256), pdl, s, p, bm, bn, G);
 }
 
 }  // namespace tc

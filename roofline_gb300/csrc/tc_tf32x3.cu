@@ -511,14 +511,21 @@ int launch_cfg(const gemm_plan_t &plan, const GemmArgs &a, char *ws, cudaStream_
   // Split passes: each operand becomes K-major hi (and lo) planes.  An
   // operand stored with K contiguous (A as M x K, B as N x K) is split row
   // by row; one stored with K as its row index is split and transposed.
+  // Programmatic dependent launch lets each kernel be scheduled while the one
+  // before it drains (each waits for its predecessor before touching
+  // memory).  With the caller's profiling events set, plain stream order is
+  // kept so the events bracket the GEMM kernel alone; callers that chain the
+  // GEMM behind cross-stream event waits ask for plain order as well.
+  const bool pdl = !profile_events_set() && !a.plain_order;
   cudaError_t se = cudaSuccess;
   if (!AK) {
-    se = a.ta ? launch_split_transposed(a.A, a.lda, a.K, a.M, L.kp, ahi, X3 ? alo : nullptr, s)
-              : launch_split_rows(a.A, a.lda, a.M, a.K, L.kp, ahi, X3 ? alo : nullptr, s);
+    se = a.ta ? launch_split_transposed(a.A, a.lda, a.K, a.M, L.kp, ahi, X3 ? alo : nullptr, pdl, s)
+              : launch_split_rows(a.A, a.lda, a.M, a.K, L.kp, ahi, X3 ? alo : nullptr, pdl, s);
   }
   if (se == cudaSuccess && !a.b_presplit) {
-    se = a.tb ? launch_split_rows(a.B, a.ldb, a.N, a.K, L.kp, bhi, X3 ? blo : nullptr, s)
-              : launch_split_transposed(a.B, a.ldb, a.K, a.N, L.kp, bhi, X3 ? blo : nullptr, s);
+    se = a.tb ? launch_split_rows(a.B, a.ldb, a.N, a.K, L.kp, bhi, X3 ? blo : nullptr, pdl, s)
+              : launch_split_transposed(a.B, a.ldb, a.K, a.N, L.kp, bhi, X3 ? blo : nullptr, pdl,
+                                        s);
   }
   if (se != cudaSuccess) {
     cudaGetLastError();
@@ -590,12 +597,6 @@ int launch_cfg(const gemm_plan_t &plan, const GemmArgs &a, char *ws, cudaStream_
     cudaGetLastError();
     return GEMM_ERR_CUDA;
   }
-  // Programmatic dependent launch lets each kernel be scheduled while the one
-  // before it drains (each waits for its predecessor before reading its
-  // output).  With the caller's profiling events set, plain stream order is
-  // kept so the events bracket the GEMM kernel alone; callers that chain the
-  // GEMM behind cross-stream event waits ask for plain order as well.
-  const bool pdl = !profile_events_set() && !a.plain_order;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
