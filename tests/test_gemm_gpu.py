@@ -1,4 +1,6 @@
 """GPU parity: the CUDA path through the C ABI against the CPU oracle."""
+import functools
+
 import numpy as np
 import pytest
 
@@ -419,3 +421,46 @@ def test_calls_capture_into_a_cuda_graph(mode, shape):
         g.replay()
         torch.cuda.synchronize()
         assert oracle.mismatches(C.cpu().numpy(), ref) == 0
+
+
+@functools.lru_cache(maxsize=1)
+def _extreme_inputs(M, N, K):
+    A = matrix(M, K, None, 91, "int2")
+    B = matrix(K, N, None, 92, "int2")
+    if K > (1 << 20):
+        # keep |partial sums| below 2^24: entries in {-1, 0, 1}
+        A = np.clip(A, -1, 1)
+        B = np.clip(B, -1, 1)
+    return A, B
+
+
+EXTREME = [
+    (1, 1, 1 << 22),          # one dot product of 4M terms (split K)
+    (1 << 20, 1, 16),         # a million rows, one column
+    (2, 1 << 20, 8),          # two rows, a million columns
+    (128, 128, (65535 * 32) - 32),  # the longest K the tensor-core split passes take
+]
+
+
+@pytest.mark.parametrize("mode", ["auto", "fp32_simt", "tf32x3"])
+@pytest.mark.parametrize("shape", EXTREME, ids=lambda s: "x".join(map(str, s)))
+def test_extreme_shapes_sampled(shape, mode):
+    # extreme aspect ratios and the longest K, integer inputs so every
+    # sampled entry must equal the oracle exactly (|partial sums| < 2^24)
+    import torch
+    from roofline_gb300 import gemm
+    from workloads import sample_entries
+    M, N, K = shape
+    try:
+        gemm.plan(M, N, K, mode=mode)
+    except gemm.GemmError as e:
+        assert e.code == gemm.ERR_UNSUPPORTED
+        pytest.skip("K beyond what the tensor-core split passes take")
+    A, B = _extreme_inputs(M, N, K)
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    C = gemm.matmul(dA, dB, mode=mode)
+    torch.cuda.synchronize()
+    rows, cols = sample_entries(M, N, n=min(2048, M * N), seed=5)
+    ref, _ = oracle.gemm_entries(A, B, rows, cols, 1.0, 0.0, None)
+    got = C.cpu().numpy()[rows, cols]
+    assert np.array_equal(got, ref)
