@@ -114,7 +114,8 @@ typedef struct gemm_plan {
   int32_t stream_k;        /* tensor-core modes: grid_ctas persistent CTAs take whole tiles in
                               waves, then share the remaining tiles' K blocks evenly; a fix-up
                               kernel sums the parts of tiles shared between CTAs */
-  int32_t reserved;
+  int32_t a_hi_tmem;       /* tensor-core modes with A split on chip: A_hi kept in tensor memory (1)
+                              or written back to shared memory (0) */
 } gemm_plan_t;
 
 typedef struct gemm_device_info {

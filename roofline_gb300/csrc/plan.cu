@@ -241,17 +241,26 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
         set(256, 16, 3, 0, 256);
         pre_split();
       } else if (a_aligned) {
-        if (N <= 64) set(64, 32, 3, 1);        // narrow: 2 CTAs per SM stream A
-        else if (wide) set(256, 16, 5, 0);
-        else set(128, 32, 4, 1);
+        // One CTA per SM leaves tensor memory for A_hi next to A_lo, so the
+        // MMAs read only B from shared memory (GB300, interleaved runs: 4096^3
+        // 469 vs 471 us, 6144^3 1.51 vs 1.53 ms; 128 x 128 tiles, where
+        // shared memory is the limit: 1024 x 1024 x 8192 97 vs 117 us).
+        if (N <= 64) {
+          set(64, 32, 3, 1);                   // narrow: 2 CTAs per SM stream A
+        } else {
+          if (wide) set(256, 16, 5, 0);
+          else set(128, 32, 4, 1);
+          p.a_hi_tmem = 1;
+        }
       } else {
         if (wide) set(256, 16, 4, 0);
         else set(128, 16, 3, 1);
       }
-      // Tuning knob: GEMM_TC_CONFIG="bn,bk,stages,a_split_in_kernel,b_concat"
-      // (128-row tile) or "bm,bn,bk,stages,a_split_in_kernel,b_concat" picks
-      // one of the built configurations (ignored if it names none, or asks
-      // for the in-kernel split with a misaligned A).
+      // Tuning knob: GEMM_TC_CONFIG="bn,bk,stages,a_split,b_concat" (128-row
+      // tile) or "bm,bn,bk,stages,a_split,b_concat" picks one of the built
+      // configurations (ignored if it names none, or asks for the in-kernel
+      // split with a misaligned A).  a_split: 0 pre-split, 1 on chip, 2 on
+      // chip with A_hi kept in tensor memory.
       if (const char *cfg = std::getenv("GEMM_TC_CONFIG")) {
         int v[6] = {0, 0, 0, 0, 0, 0};
         const int n = std::sscanf(cfg, "%d,%d,%d,%d,%d,%d", &v[0], &v[1], &v[2], &v[3], &v[4],
@@ -261,11 +270,13 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
         if ((n == 5 || n == 6) && tc_config_valid(bm, c[0], c[1], c[2], c[3], c[4], nprod) &&
             (!c[3] || a_aligned)) {
           set(c[0], c[1], c[2], c[4], bm);
-          p.a_split_in_kernel = c[3];
+          p.a_split_in_kernel = c[3] != 0;
+          p.a_hi_tmem = c[3] == 2;
           p.launches = c[3] ? 2 : 3;
         }
       }
-      p.ctas_per_sm = tc_ctas_per_sm(p.bm, p.bn, p.bk, p.stages, p.a_split_in_kernel, p.b_concat,
+      p.ctas_per_sm = tc_ctas_per_sm(p.bm, p.bn, p.bk, p.stages,
+                                     p.a_split_in_kernel ? (p.a_hi_tmem ? 2 : 1) : 0, p.b_concat,
                                      nprod, dp.smem_per_sm > 0 ? dp.smem_per_sm : 233472);
       // Stream-K: when the tiles do not fill whole waves of resident CTAs,
       // launch one wave of persistent CTAs that take whole tiles in waves and

@@ -26,9 +26,12 @@
 //               kind::tf32, committing each stage back to the producer when
 //               its MMAs retire;
 //   warps 2-5   (a) when A is split inside the kernel: convert each landed
-//               FP32 A tile into its hi part (in place) and lo part, then
-//               release it to the MMA warp; (b) epilogue: tcgen05.ld the
-//               accumulator rows, apply C = alpha*acc + beta*C, store.
+//               FP32 A tile into its hi part and lo part (lo into a
+//               tensor-memory ring read by the [a_tmem] form of the MMA; hi
+//               in place in shared memory, or into a second ring when the
+//               CTA owns enough tensor memory), then release it to the MMA
+//               warp; (b) epilogue: tcgen05.ld the accumulator rows, apply
+//               C = alpha*acc + beta*C, store.
 // A CTA walks a list of (tile, K-range) segments: whole tiles in waves, then
 // an even share of the remaining tiles' K blocks (stream-K; see Walk), with
 // the pipeline running across segment boundaries.
@@ -63,12 +66,13 @@ __device__ int g_tc_status;  // 0 = ok, else a GEMM_ERR_* code
 // and A_lo come pre-split from the workspace.  CONCAT: B_hi and B_lo sit
 // next to each other in the stage, so A_hi*[B_hi | B_lo] is one MMA of width
 // 2*BN into two accumulators that the epilogue adds.
-template <int BM, int BN, int BK, int STAGES, bool AK, bool CONCAT, int NPROD>
+template <int BM, int BN, int BK, int STAGES, int AK, bool CONCAT, int NPROD>
 struct TcCfg {
   static_assert(NPROD == 3 || NPROD == 1, "3xTF32 or 1xTF32");
   static_assert(NPROD == 3 || !CONCAT, "1xTF32 has no B_lo to concatenate");
   static_assert(BM == 128 || (BM == 256 && !AK && !CONCAT),
                 "a 256-row tile takes pre-split operands and separate B planes");
+  static_assert(AK >= 0 && AK <= 2 && (AK != 2 || NPROD == 3), "A_hi in TMEM is a 3xTF32 form");
   static constexpr bool X3 = NPROD == 3;
   static constexpr int MH = BM / 128;  // 128-row halves, one accumulator each
   static constexpr int A_BYTES = BM * BK * 4;
@@ -84,7 +88,12 @@ struct TcCfg {
   static constexpr int ACC_COLS = MH * (CONCAT ? 2 * BN : BN);
   static constexpr int LO_COL0 = ACC_COLS;
   static constexpr int LO_COLS = (AK && X3) ? STAGES * BK : 0;
-  static constexpr int TMEM_NEED = ACC_COLS + LO_COLS;
+  // AK == 2: the converters also put A_hi in a tensor-memory ring (the MMAs
+  // read both A parts from TMEM; shared memory then carries only B)
+  static constexpr bool HI_TMEM = AK == 2;
+  static constexpr int HI_COL0 = LO_COL0 + LO_COLS;
+  static constexpr int HI_COLS = HI_TMEM ? STAGES * BK : 0;
+  static constexpr int TMEM_NEED = ACC_COLS + LO_COLS + HI_COLS;
   static constexpr int TMEM_COLS = TMEM_NEED <= 32    ? 32
                                    : TMEM_NEED <= 64  ? 64
                                    : TMEM_NEED <= 128 ? 128
@@ -97,7 +106,7 @@ struct TcCfg {
   static_assert(TMEM_NEED <= 512, "tensor memory");
 };
 
-template <int BM, int BN, int BK, int STAGES, bool AK, bool CONCAT, int NPROD>
+template <int BM, int BN, int BK, int STAGES, int AK, bool CONCAT, int NPROD>
 __global__ void __launch_bounds__(kThreadsTC, 1)
 tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
                  const __grid_constant__ CUtensorMap tmA_lo,
@@ -220,6 +229,7 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
           const uint32_t ah = smem_u32(a_hi(s)), al = smem_u32(a_lo(s));
           const uint32_t bh = smem_u32(b_hi(s)), bl = smem_u32(b_lo(s));
           const uint32_t lo_t = tmem_base + (uint32_t)(Cfg::LO_COL0 + s * BK);
+          const uint32_t hi_t = tmem_base + (uint32_t)(Cfg::HI_COL0 + s * BK);
 #pragma unroll
           for (int kk = 0; kk < BK / 8; ++kk) {
             const uint32_t off = kk * 32;  // 8 TF32 values = 32 bytes along K
@@ -236,19 +246,28 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
                 mma_tf32(d, dah, dbh, idesc, acc);  // 1xTF32: A_hi * B_hi only
               } else if (CONCAT) {
                 // columns [0, BN): A_hi*B_hi (+ A_lo*B_hi); [BN, 2BN): A_hi*B_lo
-                mma_tf32(d, dah, dbh, idesc2, acc);
+                if (Cfg::HI_TMEM)
+                  mma_tf32_ts(d, hi_t + kk * 8, dbh, idesc2, acc);
+                else
+                  mma_tf32(d, dah, dbh, idesc2, acc);
                 if (AK)
                   mma_tf32_ts(d, lo_t + kk * 8, dbh, idesc, 1u);
                 else
                   mma_tf32(d, smem_desc(al_h, Cfg::SBO, Cfg::LAYOUT), dbh, idesc, 1u);
               } else {
                 const uint64_t dbl = smem_desc(bl + off, Cfg::SBO, Cfg::LAYOUT);
-                mma_tf32(d, dah, dbl, idesc, acc);  // small terms first
+                if (Cfg::HI_TMEM)  // small terms first
+                  mma_tf32_ts(d, hi_t + kk * 8, dbl, idesc, acc);
+                else
+                  mma_tf32(d, dah, dbl, idesc, acc);
                 if (AK)
                   mma_tf32_ts(d, lo_t + kk * 8, dbh, idesc, 1u);
                 else
                   mma_tf32(d, smem_desc(al_h, Cfg::SBO, Cfg::LAYOUT), dbh, idesc, 1u);
-                mma_tf32(d, dah, dbh, idesc, 1u);
+                if (Cfg::HI_TMEM)
+                  mma_tf32_ts(d, hi_t + kk * 8, dbh, idesc, 1u);
+                else
+                  mma_tf32(d, dah, dbh, idesc, 1u);
               }
             }
           }
@@ -311,6 +330,7 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
             continue;
           }
           uint32_t lo[BK];
+          uint32_t hi[BK];  // used (and kept in registers) only with A_hi in TMEM
 #pragma unroll
           for (int c = 0; c < BK / 4; ++c) {
             const int phys = (BK == 32) ? (c ^ (row & 7)) : (c ^ ((row >> 1) & 3));
@@ -325,11 +345,20 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
             lo[4 * c + 1] = __float_as_uint(x.y - h.y);
             lo[4 * c + 2] = __float_as_uint(x.z - h.z);
             lo[4 * c + 3] = __float_as_uint(x.w - h.w);
-            *ptr = h;
+            if constexpr (Cfg::HI_TMEM) {
+              hi[4 * c + 0] = __float_as_uint(h.x);
+              hi[4 * c + 1] = __float_as_uint(h.y);
+              hi[4 * c + 2] = __float_as_uint(h.z);
+              hi[4 * c + 3] = __float_as_uint(h.w);
+            } else {
+              *ptr = h;
+            }
           }
           tmem_st<BK>(lane_base + (uint32_t)(Cfg::LO_COL0 + s * BK), lo);
+          if constexpr (Cfg::HI_TMEM)
+            tmem_st<BK>(lane_base + (uint32_t)(Cfg::HI_COL0 + s * BK), hi);
           tmem_st_wait();
-          fence_async_smem();  // A_hi written by this thread -> visible to the MMA
+          if (!Cfg::HI_TMEM) fence_async_smem();  // A_hi written in shared memory -> visible to the MMA
           tc_fence_before();
           mbar_arrive(&conv[s]);
         }
@@ -493,7 +522,7 @@ WsLayout ws_layout(int64_t M, int64_t N, int64_t K, bool a_inkernel, int64_t str
   return w;
 }
 
-template <int BM, int BN, int BK, int STAGES, bool AK, bool CONCAT, int NPROD>
+template <int BM, int BN, int BK, int STAGES, int AK, bool CONCAT, int NPROD>
 int launch_cfg(const gemm_plan_t &plan, const GemmArgs &a, char *ws, cudaStream_t s) {
   using Cfg = TcCfg<BM, BN, BK, STAGES, AK, CONCAT, NPROD>;
   constexpr bool X3 = Cfg::X3;
@@ -630,25 +659,30 @@ int launch_cfg(const gemm_plan_t &plan, const GemmArgs &a, char *ws, cudaStream_
 bool tc_supported(const DeviceProps &dp) { return dp.cc_major == 10 && dp.cc_minor == 3; }
 
 // Tile configurations the planner may pick: (bm, bn, bk, stages, A split in
-// kernel, concatenated B MMA, TF32 products per FP32 product).
+// kernel (0 no, 1 with A_hi in shared memory, 2 with A_hi in tensor memory),
+// concatenated B MMA, TF32 products per FP32 product).
 #define GG_TC_CONFIGS(X)                  \
-  X(128, 256, 16, 5, true, false, 3)      \
-  X(128, 128, 32, 4, true, true, 3)       \
-  X(128, 64, 32, 6, true, true, 3)        \
-  X(128, 64, 32, 3, true, true, 3)        \
-  X(128, 64, 32, 2, true, false, 3)       \
-  X(128, 64, 16, 4, true, false, 3)       \
-  X(128, 256, 16, 4, false, false, 3)     \
-  X(128, 128, 16, 3, false, true, 3)      \
-  X(256, 256, 16, 3, false, false, 3)     \
-  X(128, 256, 16, 8, true, false, 1)      \
-  X(128, 64, 32, 4, true, false, 1)       \
-  X(128, 256, 16, 8, false, false, 1)     \
-  X(256, 256, 16, 6, false, false, 1)     \
-  X(256, 256, 32, 3, false, false, 1)
+  X(128, 256, 16, 5, 1, false, 3)       \
+  X(128, 256, 16, 5, 2, false, 3)       \
+  X(128, 128, 32, 4, 2, true, 3)        \
+  X(128, 128, 32, 4, 1, true, 3)        \
+  X(128, 64, 32, 6, 1, true, 3)         \
+  X(128, 64, 32, 3, 1, true, 3)         \
+  X(128, 64, 32, 2, 1, false, 3)        \
+  X(128, 64, 16, 4, 1, false, 3)        \
+  X(128, 256, 16, 4, 0, false, 3)       \
+  X(128, 128, 16, 3, 0, true, 3)        \
+  X(256, 256, 16, 3, 0, false, 3)       \
+  X(128, 256, 16, 8, 1, false, 1)       \
+  X(128, 64, 32, 4, 1, false, 1)        \
+  X(128, 256, 16, 8, 0, false, 1)       \
+  X(256, 256, 16, 6, 0, false, 1)       \
+  X(256, 256, 32, 3, 0, false, 1)       
 
+// a_inkernel: 0 A pre-split, 1 split on chip (A_hi in shared memory), 2 split
+// on chip with A_hi in tensor memory.
 #define GG_TC_MATCH(BM_, BN_, BK_, ST_, AK_, CC_, NP_)                                  \
-  (bm == BM_ && bn == BN_ && bk == BK_ && stages == ST_ && (a_inkernel != 0) == AK_ && \
+  (bm == BM_ && bn == BN_ && bk == BK_ && stages == ST_ && a_inkernel == (AK_) && \
    (concat != 0) == CC_ && nprod == NP_)
 
 bool tc_config_valid(int bm, int bn, int bk, int stages, int a_inkernel, int concat, int nprod) {
@@ -692,7 +726,8 @@ int launch_tc(const gemm_plan_t &plan, const GemmArgs &a, void *ws, size_t ws_by
   char *w = static_cast<char *>(ws);
   const int nprod = plan.mode == GEMM_MODE_TF32 ? 1 : 3;
   const int bm = plan.bm, bn = plan.bn, bk = plan.bk, stages = plan.stages;
-  const int a_inkernel = plan.a_split_in_kernel, concat = plan.b_concat;
+  const int a_inkernel = plan.a_split_in_kernel ? (plan.a_hi_tmem ? 2 : 1) : 0;
+  const int concat = plan.b_concat;
 #define GG_LAUNCH(BM_, BN_, BK_, ST_, AK_, CC_, NP_)  \
   if (GG_TC_MATCH(BM_, BN_, BK_, ST_, AK_, CC_, NP_)) \
     return launch_cfg<BM_, BN_, BK_, ST_, AK_, CC_, NP_>(plan, a, w, s);

@@ -70,7 +70,7 @@ class GemmPlan(ctypes.Structure):
                 ("workspace_bytes", ctypes.c_uint64), ("flops", ctypes.c_double),
                 ("bytes", ctypes.c_double), ("intensity", ctypes.c_double),
                 ("b_concat", ctypes.c_int32), ("ctas_per_sm", ctypes.c_int32),
-                ("stream_k", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("stream_k", ctypes.c_int32), ("a_hi_tmem", ctypes.c_int32)]
 
     def as_dict(self):
         d = {name: getattr(self, name) for name, _ in self._fields_}

@@ -253,7 +253,8 @@ def test_tf32x3_planner_choices(shape, cfg):
 # Every tensor-core configuration the library is built with, forced through
 # the GEMM_TC_CONFIG knob, on one ragged shape (full check).
 TC_BUILT = ["256,16,5,1,0", "128,32,4,1,1", "64,32,6,1,1", "64,32,3,1,1", "64,32,2,1,0",
-            "64,16,4,1,0", "256,16,4,0,0", "128,16,3,0,1", "256,256,16,3,0,0"]
+            "64,16,4,1,0", "256,16,4,0,0", "128,16,3,0,1", "256,256,16,3,0,0",
+            "256,16,5,2,0", "128,32,4,2,1"]
 
 
 def _cfg(cfg):
@@ -271,7 +272,8 @@ def test_tf32x3_every_built_configuration(cfg, monkeypatch):
     pad = (0 if ak else 1, 0, 0)
     p = gemm.plan(M, N, K, K + pad[0], N, N, mode="tf32x3")
     assert (p["bm"], p["bn"], p["bk"], p["stages"], p["a_split_in_kernel"], p["b_concat"]) == \
-        (bm, bn, bk, st, ak, cc)
+        (bm, bn, bk, st, min(ak, 1), cc)
+    assert p["a_hi_tmem"] == (1 if ak == 2 else 0)
     got, ref, D = _run_shape(M, N, K, "tf32x3", 1.5, 0.5, pad=pad, offset=0, seed=st + bn)
     assert oracle.err_normalised(got, ref, D) <= TOL_E1
 
