@@ -63,7 +63,7 @@ bool query_props(int dev, DeviceProps *d) {
   cudaDeviceProp prop;
   if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return false;
   p.hbm_bytes = (int64_t)prop.totalGlobalMem;
-  std::snprintf(p.name, sizeof(p.name), "%s", prop.name);
+  std::snprintf(p.name, sizeof(p.name), "%.127s", prop.name);
   p.from_device = 1;
   *d = p;
   return true;

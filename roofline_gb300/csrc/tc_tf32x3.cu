@@ -310,7 +310,7 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
           // Row `row` of the landed tile: 16-byte chunk c sits at chunk
           // c ^ f(row) of its 64- or 128-byte line (the TMA swizzle).
           uint8_t *line = a_hi(s) + row * Cfg::ROW_BYTES;
-          if (!X3) {
+          if constexpr (!X3) {
             // 1xTF32: round in place, nothing goes to tensor memory.  Chunks
             // are visited in swizzled order so a warp's 32 rows hit 32
             // different banks.
@@ -327,40 +327,40 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
             }
             fence_async_smem();
             mbar_arrive(&conv[s]);
-            continue;
-          }
-          uint32_t lo[BK];
-          uint32_t hi[BK];  // used (and kept in registers) only with A_hi in TMEM
+          } else {
+            uint32_t lo[BK];
+            uint32_t hi[BK];  // used (and kept in registers) only with A_hi in TMEM
 #pragma unroll
-          for (int c = 0; c < BK / 4; ++c) {
-            const int phys = (BK == 32) ? (c ^ (row & 7)) : (c ^ ((row >> 1) & 3));
-            float4 *ptr = reinterpret_cast<float4 *>(line + phys * 16);
-            const float4 x = *ptr;
-            float4 h;
-            h.x = tf32_rna(x.x);
-            h.y = tf32_rna(x.y);
-            h.z = tf32_rna(x.z);
-            h.w = tf32_rna(x.w);
-            lo[4 * c + 0] = __float_as_uint(x.x - h.x);
-            lo[4 * c + 1] = __float_as_uint(x.y - h.y);
-            lo[4 * c + 2] = __float_as_uint(x.z - h.z);
-            lo[4 * c + 3] = __float_as_uint(x.w - h.w);
-            if constexpr (Cfg::HI_TMEM) {
-              hi[4 * c + 0] = __float_as_uint(h.x);
-              hi[4 * c + 1] = __float_as_uint(h.y);
-              hi[4 * c + 2] = __float_as_uint(h.z);
-              hi[4 * c + 3] = __float_as_uint(h.w);
-            } else {
-              *ptr = h;
+            for (int c = 0; c < BK / 4; ++c) {
+              const int phys = (BK == 32) ? (c ^ (row & 7)) : (c ^ ((row >> 1) & 3));
+              float4 *ptr = reinterpret_cast<float4 *>(line + phys * 16);
+              const float4 x = *ptr;
+              float4 h;
+              h.x = tf32_rna(x.x);
+              h.y = tf32_rna(x.y);
+              h.z = tf32_rna(x.z);
+              h.w = tf32_rna(x.w);
+              lo[4 * c + 0] = __float_as_uint(x.x - h.x);
+              lo[4 * c + 1] = __float_as_uint(x.y - h.y);
+              lo[4 * c + 2] = __float_as_uint(x.z - h.z);
+              lo[4 * c + 3] = __float_as_uint(x.w - h.w);
+              if constexpr (Cfg::HI_TMEM) {
+                hi[4 * c + 0] = __float_as_uint(h.x);
+                hi[4 * c + 1] = __float_as_uint(h.y);
+                hi[4 * c + 2] = __float_as_uint(h.z);
+                hi[4 * c + 3] = __float_as_uint(h.w);
+              } else {
+                *ptr = h;
+              }
             }
+            tmem_st<BK>(lane_base + (uint32_t)(Cfg::LO_COL0 + s * BK), lo);
+            if constexpr (Cfg::HI_TMEM)
+              tmem_st<BK>(lane_base + (uint32_t)(Cfg::HI_COL0 + s * BK), hi);
+            tmem_st_wait();
+            if (!Cfg::HI_TMEM) fence_async_smem();  // A_hi in shared memory -> visible to the MMA
+            tc_fence_before();
+            mbar_arrive(&conv[s]);
           }
-          tmem_st<BK>(lane_base + (uint32_t)(Cfg::LO_COL0 + s * BK), lo);
-          if constexpr (Cfg::HI_TMEM)
-            tmem_st<BK>(lane_base + (uint32_t)(Cfg::HI_COL0 + s * BK), hi);
-          tmem_st_wait();
-          if (!Cfg::HI_TMEM) fence_async_smem();  // A_hi written in shared memory -> visible to the MMA
-          tc_fence_before();
-          mbar_arrive(&conv[s]);
         }
         if (!ok) break;
       }
