@@ -235,16 +235,19 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
           set(256, 16, 8, 0);
           pre_split();
         }
-      } else if (wide && tiles_m2 >= 4 * sms) {
-        // many tiles: 256 x 256 tiles, pre-split A (GB300, 8192^3: kernel
-        // 3.03 ms against 3.31 ms for 128 x 256 tiles with A split on chip)
+      } else if (!a_aligned && wide && tiles_m2 >= 4 * sms) {
+        // A pre-split anyway and many tiles: 256 x 256 tiles (GB300, 8192^3:
+        // kernel 3.03 ms against 3.31 ms for 128 x 256 tiles)
         set(256, 16, 3, 0, 256);
         pre_split();
       } else if (a_aligned) {
         // One CTA per SM leaves tensor memory for A_hi next to A_lo, so the
         // MMAs read only B from shared memory (GB300, interleaved runs: 4096^3
         // 469 vs 471 us, 6144^3 1.51 vs 1.53 ms; 128 x 128 tiles, where
-        // shared memory is the limit: 1024 x 1024 x 8192 97 vs 117 us).
+        // shared memory is the limit: 1024 x 1024 x 8192 97 vs 117 us).  With
+        // it the 128 x 256 tile also beats 256 x 256 tiles (pre-split A) at
+        // every size measured: 8192^3 3.35 vs 3.54 ms, 6144^3 1.44 vs
+        // 1.61 ms, 8192 x 4096 x 4096 902 vs 978 us.
         if (N <= 64) {
           set(64, 32, 3, 1);                   // narrow: 2 CTAs per SM stream A
         } else {

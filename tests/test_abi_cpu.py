@@ -139,8 +139,11 @@ def test_tc_plans_on_cpu(lib):
     r = gemm.plan(1023, 1025, 777, 777, 1025, 1025, mode="tf32x3")
     assert r["a_split_in_kernel"] == 0 and r["launches"] == 3 + r["stream_k"]
     assert gemm.plan(4096, 4096, 4096)["kernel_name"] == "tc_tf32x3"  # auto
-    big = gemm.plan(8192, 8192, 8192, mode="tf32x3")  # many tiles: 256 x 256, A pre-split
-    assert (big["bm"], big["bn"], big["a_split_in_kernel"]) == (256, 256, 0)
+    big = gemm.plan(8192, 8192, 8192, mode="tf32x3")  # A split on chip, A_hi and A_lo in TMEM
+    assert (big["bm"], big["bn"], big["a_split_in_kernel"], big["a_hi_tmem"]) == (128, 256, 1, 1)
+    # A pre-split anyway (leading dimension not a multiple of 4) and many tiles: 256 x 256
+    big2 = gemm.plan(8192, 8192, 8191, 8191, 8192, 8192, mode="tf32x3")
+    assert (big2["bm"], big2["bn"], big2["a_split_in_kernel"]) == (256, 256, 0)
     assert gemm.plan(512, 512, 512)["kernel_name"] == "simt"  # auto, small
 
 

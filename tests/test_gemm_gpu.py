@@ -225,7 +225,8 @@ TC_PLANS = [
     ((2432, 8192, 128, 128), (128, 256, 16, 5, 1, 0)),
     ((1023, 1025, 777, 777), (128, 128, 16, 3, 0, 1)),
     ((2432, 8192, 129, 129), (128, 256, 16, 4, 0, 0)),
-    ((5120, 8192, 64, 64), (256, 256, 16, 3, 0, 0)),   # many tiles: 256 x 256
+    ((5120, 8192, 64, 64), (128, 256, 16, 5, 1, 0)),   # many tiles, aligned A: split on chip
+    ((5120, 8192, 65, 65), (256, 256, 16, 3, 0, 0)),   # many tiles, A pre-split: 256 x 256
 ]
 
 
