@@ -131,9 +131,16 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
 
   int resolved = mode;
   if (mode == GEMM_MODE_AUTO) {
-    // Tensor cores (3xTF32) once the problem is large enough to amortise the
-    // split pass; the CUDA-core kernel otherwise.
-    const bool big = (double)M * N * K >= 64.0 * 1024 * 1024 * 64;
+    // Tensor cores (3xTF32) once the problem amortises the split pass and
+    // the extra launches; the CUDA-core kernel for small problems, short K
+    // (both paths are then bound by writing C and within a few percent) and
+    // fewer than 128 rows (half of every 128-row tile would idle).  GB300
+    // step times, CUDA cores / 3xTF32 (us): 512^3 16.5 / 15.6-19.1, 576^3
+    // 20.6 / 19.8, 640^3 22.4 / 17.3, 1023 x 1025 x 777 55.4 / 29.3, 1024^3
+    // 61.9 / 26.0, 2048 x 2048 x 512 100.5 / 32.0, 4096 x 64 x 4096
+    // 100.5 / 33.3; 4096^2 x 64 71.8 / 75.8, 1024^2 x 128 14.4 / 15.9,
+    // 64 x 4096 x 4096 53.3 / 65.2.
+    const bool big = (double)M * N * K >= 2.0e8 && K >= 128 && M >= 128;
     resolved = (tc_supported(dp) && big && tc_shape_fits(M, N, K)) ? GEMM_MODE_TF32X3
                                                          : GEMM_MODE_FP32_SIMT;
   }
@@ -285,33 +292,44 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
       // launch one wave of persistent CTAs that take whole tiles in waves and
       // split the rest of the (tile, K block) work evenly (each at least 4 K
       // blocks); a fix-up kernel sums the parts of tiles shared between
-      // CTAs, in CTA order.  For 3xTF32 (tiles ordered so the split part
-      // shares the larger operand in L2) it always paid on GB300 (step times
-      // with / without: 2560 x 2560 x 4096 207 / 262 us, 2048 x 4096 x 4096
-      // 260 / 264 us, 4096^3 459 / 510 us, 6144^3 1.42 / 1.52 ms) once there
-      // is more than one wave of tiles; under one wave nearly every tile would
-      // be shared by two CTAs, so it waits for many idle SMs.  For
-      // 1xTF32's 256 x 256 tiles the split part and its larger fix-up cost
-      // about half a wave (4096^3: 243 / 222 us), so there it is taken when
-      // the last wave would leave more than ~45 % of the CTAs idle, for 4 to
-      // 8 waves, or for an HBM-bound shape (idle SMs are lost bandwidth).
+      // CTAs, in CTA order.  Taken for HBM-bound shapes (idle SMs are lost
+      // bandwidth), when the tiles fill at most half the SMs (one CTA per
+      // tile is then bound by the latency of its own TMA loads, and more CTAs
+      // per tile keep more loads in flight), and otherwise when a time model
+      // says it pays.  Model: the tensor pipe of an SM at its dense rate,
+      // CTAs sharing an SM sharing it; one CTA per tile takes
+      // ceil(tiles / SMs) tile times, stream-K spreads all K blocks over the
+      // SMs but writes and re-reads one partial tile per part (about G +
+      // shared tiles parts, ~3 TB/s through L2) and launches the fix-up
+      // (~3 us).  GB300 step times, one CTA per tile / stream-K (us), 3xTF32:
+      // 1023 x 1025 x 777 (lda 777) 54.7 / 43.5, (lda 780) 37.2 / 28.0,
+      // 640^3 18.9 / 17.9, 1024^3 26.3 / 25.2, 256 x 4096 x 4096
+      // 105.8 / 85.3, 128 x 128 x 16384 254 / 53, 1536^3 41.0 / 46.4,
+      // 2048 x 2048 x 512 34.0 / 40.1, 2048^3 75.7 / 80.1, 3000^3 (lda 3003)
+      // 258 / 284, 2560 x 2560 x 4096 256 / 192, 4096^3 513 / 460; 1xTF32:
+      // 2048^3 74.5 / 64.7, 4096^3 244 / 249.
       {
         const int64_t tiles = ceil_div(M, p.bm) * ceil_div(N, p.bn);
         const int64_t slots = (int64_t)(p.ctas_per_sm > 0 ? p.ctas_per_sm : 1) * sms;
-        const int64_t total = tiles * ceil_div(K, p.bk);
-        // at least 4 K blocks per CTA, and at most 250 CTAs per tile (the
-        // fix-up sums up to 256 parts)
+        const int64_t nkb = ceil_div(K, p.bk);
+        const int64_t total = tiles * nkb;
+        // at least 4 K blocks per CTA, and at most 64 CTAs per tile (the
+        // fix-up sums up to 256 parts; a few tiles with a very long K, such
+        // as 128 x 128 x 16384, then still spread over 64 SMs per tile)
         int64_t g = slots < total / 4 ? slots : total / 4;
-        if (g > 250 * tiles) g = 250 * tiles;
+        if (g > 64 * tiles) g = 64 * tiles;
         const char *sk = std::getenv("GEMM_TC_STREAMK");  // tuning knob: 0 off, 1 on
-        const double waves = (double)tiles / (double)slots;
-        const double idle = std::ceil(waves) - waves;  // of the last wave
         const double roof = x3 ? kPlanTf32DenseFlops / 3.0 : kPlanTf32DenseFlops;
         const bool hbm_bound = p.intensity < roof / kPlanHbmBytesPerSec;
+        const double t_kb = 2.0 * p.bm * p.bn * p.bk * nprod / (kPlanTf32DenseFlops / (double)sms);
+        const double t_dp = (double)ceil_div(tiles, sms) * (double)nkb * t_kb;
+        const int64_t shared = g > 0 && tiles > g ? tiles % g : tiles;
+        const double t_sk = (double)ceil_div(total, sms) * t_kb +
+                            2.0 * (double)(g + shared) * p.bm * p.bn * 4.0 / 3.0e12 + 3.0e-6;
         bool want = (tiles % slots) != 0 && tiles < 8 * slots &&
-                    ((x3 && waves > 1.0) || hbm_bound || idle > 0.45 || waves >= 4.0);
+                    (hbm_bound || 2 * tiles <= sms || t_sk < t_dp);
         if (sk) want = std::atoi(sk) != 0;
-        p.stream_k = (want && g >= 2 && g < tiles * 64) ? 1 : 0;
+        p.stream_k = (want && g >= 2) ? 1 : 0;
         p.grid_ctas = p.stream_k ? g : tiles;
         if (p.stream_k) p.launches += 1;
       }

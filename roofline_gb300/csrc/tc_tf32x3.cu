@@ -99,12 +99,85 @@ struct TcCfg {
                                    : TMEM_NEED <= 128 ? 128
                                    : TMEM_NEED <= 256 ? 256
                                                       : 512;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+  // epilogue staging: 32 rows x 16 floats per epilogue warp
+  static constexpr int EPI_BYTES = 4 * 32 * 16 * 4;
+  static constexpr int SMEM_BYTES =
+      STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/ + EPI_BYTES;
   static_assert(ROW_BYTES == 64 || ROW_BYTES == 128, "BK must be 16 or 32");
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN");
   static_assert(!CONCAT || 2 * BN <= 256, "concatenated B must fit one MMA");
   static_assert(TMEM_NEED <= 512, "tensor memory");
 };
+
+// Epilogue store of one warp's 32 x 16 block: lane r holds v[0..15], row r,
+// columns col0..col0+15, and dst points at row 0, column col0 of the block
+// (row stride ld; rows and cols: how many of them lie inside the matrix).
+// The block goes through the warp's 2 KB of shared memory (row r's 16-byte
+// chunk k stored at chunk k ^ ((r >> 1) & 3), so both the row-per-lane
+// writes and the reads below hit 32 distinct banks) and comes back out
+// along rows: each store instruction covers 8 rows x 64 contiguous bytes
+// (16-byte accesses) or 2 rows x 64 bytes (4-byte accesses, for an
+// unaligned or clipped block), instead of 32 rows x 16 bytes.
+// dst = alpha * v + beta * dst (beta == 0: dst is not read).
+__device__ __forceinline__ void epi_store16(float4 *st, const float *v, float *dst, int64_t ld,
+                                            int rows, int cols, bool vec, float alpha,
+                                            float beta) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    st[lane * 4 + (k ^ ((lane >> 1) & 3))] =
+        make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+  __syncwarp();
+  if (vec && cols >= 16) {
+    float4 x[4], old[4];
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+      const int r = it * 8 + (lane >> 2), k = lane & 3;
+      x[it] = st[r * 4 + (k ^ ((r >> 1) & 3))];
+      old[it] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (beta != 0.0f && r < rows)
+        old[it] = *reinterpret_cast<const float4 *>(dst + (int64_t)r * ld + 4 * k);
+    }
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+      const int r = it * 8 + (lane >> 2), k = lane & 3;
+      if (r < rows) {
+        float4 o = make_float4(alpha * x[it].x, alpha * x[it].y, alpha * x[it].z, alpha * x[it].w);
+        if (beta != 0.0f) {
+          o.x = fmaf(beta, old[it].x, o.x);
+          o.y = fmaf(beta, old[it].y, o.y);
+          o.z = fmaf(beta, old[it].z, o.z);
+          o.w = fmaf(beta, old[it].w, o.w);
+        }
+        *reinterpret_cast<float4 *>(dst + (int64_t)r * ld + 4 * k) = o;
+      }
+    }
+  } else {
+    const float *sf = reinterpret_cast<const float *>(st);
+    const int j = lane & 15;
+#pragma unroll 1
+    for (int it0 = 0; it0 < 16; it0 += 4) {
+      float x[4], old[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int r = (it0 + u) * 2 + (lane >> 4);
+        x[u] = sf[r * 16 + (((j >> 2) ^ ((r >> 1) & 3)) << 2) + (j & 3)];
+        old[u] = 0.0f;
+        if (beta != 0.0f && r < rows && j < cols) old[u] = dst[(int64_t)r * ld + j];
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int r = (it0 + u) * 2 + (lane >> 4);
+        if (r < rows && j < cols) {
+          float o = alpha * x[u];
+          if (beta != 0.0f) o = fmaf(beta, old[u], o);
+          dst[(int64_t)r * ld + j] = o;
+        }
+      }
+    }
+  }
+  __syncwarp();  // the buffer is rewritten by the next block
+}
 
 template <int BM, int BN, int BK, int STAGES, int AK, bool CONCAT, int NPROD>
 __global__ void __launch_bounds__(kThreadsTC, 1)
@@ -292,6 +365,8 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
     // ---------------- converters (AK) and epilogue, warps 2..5
     const int quarter = warp & 3;  // TMEM lanes this warp may touch
     const int row = quarter * 32 + lane;
+    // this warp's epilogue staging buffer (after the barriers)
+    float4 *epi = reinterpret_cast<float4 *>(reinterpret_cast<uint8_t *>(full) + 256) + quarter * 128;
     const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16);
     const bool vec = ((p.ldc & 3) == 0) && ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0);
     int it = 0, si = 0;
@@ -380,11 +455,22 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
       // each 128-row half of the tile sits in its own accumulator columns
 #pragma unroll 1
       for (int h = 0; h < Cfg::MH; ++h) {
-        const int tr = h * 128 + row;  // row within the tile
-        const int64_t grow = m0 + tr;
+        const int tr0 = h * 128 + quarter * 32;  // this warp's first row within the tile
         const uint32_t lane_acc = lane_base + (uint32_t)(h * BN);
-        // partial tiles: slot 0 for this CTA's first stream-K segment, 1 for its last
-        float *prow = p.partial + ((int64_t)(blockIdx.x * 2 + sg.slot) * BM + tr) * BN;
+        // whole tiles go to C; partial tiles (stream-K) to this CTA's slot,
+        // 0 for its first stream-K segment, 1 for its last
+        float *dst_row0;
+        int64_t ld, rows_in;
+        if (whole) {
+          dst_row0 = p.C + (m0 + tr0) * p.ldc + n0;
+          ld = p.ldc;
+          rows_in = p.M - (m0 + tr0);
+        } else {
+          dst_row0 = p.partial + ((int64_t)(blockIdx.x * 2 + sg.slot) * BM + tr0) * BN;
+          ld = BN;
+          rows_in = 32;
+        }
+        const int rows = rows_in < 0 ? 0 : (rows_in > 32 ? 32 : (int)rows_in);
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
           uint32_t r[32];
@@ -399,40 +485,17 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
           } else {
             tmem_ld_wait();
           }
-          if (!whole) {
+          const float *v = reinterpret_cast<const float *>(r);
 #pragma unroll
-            for (int q = 0; q < 32; q += 4)
-              *reinterpret_cast<float4 *>(prow + c + q) =
-                  make_float4(__uint_as_float(r[q]), __uint_as_float(r[q + 1]),
-                              __uint_as_float(r[q + 2]), __uint_as_float(r[q + 3]));
-          } else if (grow < p.M) {
-            float *dst = p.C + grow * p.ldc + n0 + c;
-            const int64_t left = p.N - (n0 + c);
-            if (vec && left >= 32) {
-#pragma unroll
-              for (int q = 0; q < 32; q += 4) {
-                float4 o = make_float4(p.alpha * __uint_as_float(r[q]),
-                                       p.alpha * __uint_as_float(r[q + 1]),
-                                       p.alpha * __uint_as_float(r[q + 2]),
-                                       p.alpha * __uint_as_float(r[q + 3]));
-                if (p.beta != 0.0f) {
-                  const float4 old = *reinterpret_cast<const float4 *>(dst + q);
-                  o.x = fmaf(p.beta, old.x, o.x);
-                  o.y = fmaf(p.beta, old.y, o.y);
-                  o.z = fmaf(p.beta, old.z, o.z);
-                  o.w = fmaf(p.beta, old.w, o.w);
-                }
-                *reinterpret_cast<float4 *>(dst + q) = o;
-              }
+          for (int hh = 0; hh < 2; ++hh) {
+            const int col = c + 16 * hh;
+            if (whole) {
+              const int64_t left = p.N - (n0 + col);
+              const int cols = left < 0 ? 0 : (left > 16 ? 16 : (int)left);
+              epi_store16(epi, v + 16 * hh, dst_row0 + col, ld, rows, cols, vec, p.alpha,
+                          p.beta);
             } else {
-#pragma unroll
-              for (int q = 0; q < 32; ++q) {
-                if (q < left) {
-                  float o = p.alpha * __uint_as_float(r[q]);
-                  if (p.beta != 0.0f) o = fmaf(p.beta, dst[q], o);
-                  dst[q] = o;
-                }
-              }
+              epi_store16(epi, v + 16 * hh, dst_row0 + col, ld, 32, 16, true, 1.0f, 0.0f);
             }
           }
         }

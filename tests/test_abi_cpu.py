@@ -148,7 +148,7 @@ def test_tc_plans_on_cpu(lib):
 
 
 def test_stream_k_plan_bounds(lib):
-    # each CTA owns at least 4 K blocks and a tile is split among at most ~250 CTAs
+    # each CTA owns at least 4 K blocks and a tile is split among at most 64 CTAs
     for shape in [(128, 128, 65536), (65536, 64, 4096), (4096, 4096, 4096), (256, 256, 256)]:
         p = gemm.plan(*shape, mode="tf32x3")
         if not p["stream_k"]:
@@ -157,7 +157,23 @@ def test_stream_k_plan_bounds(lib):
         tiles = -(-M // 128) * -(-N // p["bn"])
         total = tiles * -(-K // p["bk"])
         assert 2 <= p["grid_ctas"] <= total // 4
-        assert p["grid_ctas"] <= 250 * tiles
+        assert p["grid_ctas"] <= 64 * tiles
+    # one tile with a very long K still spreads over 64 CTAs
+    p = gemm.plan(128, 128, 16384, mode="tf32x3")
+    assert p["stream_k"] == 1 and p["grid_ctas"] == 64
+
+
+def test_auto_choice(lib):
+    """AUTO takes the tensor cores once a problem amortises the split pass
+    (about 2e8 multiply-adds), with K >= 128 and M >= 128."""
+    tc = [(1023, 1025, 777, 777, 1025, 1025), (640, 640, 640), (1024, 1024, 1024),
+          (2048, 2048, 512), (4096, 64, 4096), (512, 512, 1024), (128, 2048, 1024)]
+    simt = [(512, 512, 512), (576, 576, 576), (4096, 4096, 64), (8192, 8192, 32),
+            (64, 4096, 4096), (1024, 1024, 128), (300, 300, 2000)]
+    for shape in tc:
+        assert gemm.plan(*shape)["kernel_name"] == "tc_tf32x3", shape
+    for shape in simt:
+        assert gemm.plan(*shape)["kernel_name"] == "simt", shape
 
 
 def test_tf32_mode_plans(lib):
@@ -190,10 +206,17 @@ def test_tensor_core_shape_limits(lib):
 
 
 def test_stream_k_choice(lib):
-    # 3xTF32: stream-K whenever the tiles leave a partial last wave (fewer
-    # than 8 waves); 1xTF32's 256 x 256 tiles: only when the last wave would
-    # leave many CTAs idle, for 4-8 waves, or HBM-bound shapes
+    # stream-K for HBM-bound shapes, for tiles filling at most half the SMs,
+    # and where the time model says spreading K over the SMs beats the
+    # partial tiles and the fix-up (the measured GB300 choices)
     assert gemm.plan(4096, 4096, 4096, mode="tf32x3")["stream_k"] == 1
+    assert gemm.plan(2560, 2560, 4096, mode="tf32x3")["stream_k"] == 1
+    assert gemm.plan(1023, 1025, 777, 777, 1025, 1025, mode="tf32x3")["stream_k"] == 1
+    assert gemm.plan(1024, 1024, 1024, mode="tf32x3")["stream_k"] == 1
+    assert gemm.plan(2048, 2048, 2048, mode="tf32")["stream_k"] == 1
+    for shape in [(1536, 1536, 1536), (2048, 2048, 512), (2048, 2048, 2048),
+                  (3000, 3000, 3000, 3003, 3000, 3000)]:
+        assert gemm.plan(*shape, mode="tf32x3")["stream_k"] == 0, shape
     p = gemm.plan(2048, 4096, 4096, mode="tf32x3")
     assert (p["bn"], p["stream_k"], p["grid_ctas"]) == (256, 1, 152)
     # under one wave (128 tiles on 152 SMs): one CTA per tile

@@ -317,6 +317,42 @@ def test_tf32x3_stream_k_deterministic():
         assert np.array_equal(o.view(np.uint32), outs[0].view(np.uint32))
 
 
+@pytest.mark.parametrize("cfg", [None, "256,256,16,3,0,0"])
+@pytest.mark.parametrize("shape", [(129, 300, 4000), (2100, 900, 1000)])
+def test_stream_k_parts_summed_in_cta_order(cfg, shape, monkeypatch):
+    """Tiles shared by many CTAs (up to ~40 parts a tile for 129 x 300 x 4000):
+    the fix-up sums a tile's parts in CTA order, so repeated calls agree to
+    the bit; integer inputs are exact."""
+    import torch
+    from roofline_gb300 import gemm
+    from workloads import matrix
+    monkeypatch.setenv("GEMM_TC_STREAMK", "1")
+    if cfg:
+        monkeypatch.setenv("GEMM_TC_CONFIG", cfg)
+    M, N, K = shape
+    pad = 1 if cfg else 0  # the 256-row configuration takes a pre-split A
+    p = gemm.plan(M, N, K, K + pad, N, N, mode="tf32x3")
+    assert p["stream_k"] == 1 and p["grid_ctas"] >= 2
+    for dist, seed in (("u11", 5), ("int2", 6)):
+        A = matrix(M, K, K + pad, seed, dist)
+        B = matrix(K, N, None, seed + 1, dist)
+        C0 = matrix(M, N, None, seed + 2, dist)
+        dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+        outs = []
+        for _ in range(4):
+            dC = torch.from_numpy(C0).cuda()
+            gemm.matmul(dA[:, :K], dB, dC, 1.0, 1.0 if dist == "int2" else 0.5, "tf32x3")
+            outs.append(dC.cpu().numpy())
+        for o in outs[1:]:
+            assert np.array_equal(o.view(np.uint32), outs[0].view(np.uint32))
+        if dist == "int2":
+            assert oracle.mismatches(outs[0], oracle.gemm(A[:, :K], B, 1.0, 1.0, C0)) == 0
+        else:
+            ref, D = oracle.gemm(A[:, :K], B, 1.0, 0.5, C0, with_bound=True)
+            assert oracle.err_normalised(outs[0], ref, D) <= TOL_E1
+    assert gemm.check_status() == gemm.OK
+
+
 def test_fma_peak_probe():
     from roofline_gb300 import gemm
     d = gemm.device_info(0)
