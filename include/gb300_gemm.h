@@ -238,20 +238,24 @@ GEMM_API int gemm_f32_op_plan(int layout, int op_a, int op_b, int64_t M, int64_t
  *
  * The course page's scaffolding copies the operands to the GPU, runs the
  * kernel and copies the result back ("Project - tiled matrix multiply",
- * "Starter scaffolding"); this call does the same for the caller, in row
- * blocks, so the host-to-device copies of later blocks, the GEMM of the
- * current block and the device-to-host copy of earlier blocks overlap.
+ * "Starter scaffolding"); this call does the same for the caller, cutting
+ * the product into row blocks of A (and C) and column blocks of B (and C).
+ * A and B blocks are copied in alternately, each GEMM starts as soon as its
+ * two blocks are on the device, and each block of C is copied back as soon
+ * as its GEMM is done, so copies in, GEMMs and copies out overlap.
  * Page-locked host buffers (cudaHostAlloc / cudaMallocHost) are needed for
  * the copies to overlap; pageable buffers give the same result, slower.
  *
- * mode: as gemm_f32_ex; AUTO is resolved once, for the first row block, and
+ * mode: as gemm_f32_ex; AUTO is resolved once, for the whole product, and
  * that mode runs every block.  blocks: number of row blocks, 1 ..
- * GEMM_HOST_MAX_BLOCKS, or 0 for the library's choice (one block for short
- * products, else blocks of at least 1024 rows, at most 4).  Row blocks hold
- * whole 128-row tiles except the last.
+ * GEMM_HOST_MAX_BLOCKS, with B in one column block; or 0 for the library's
+ * choice (one block for short products; else for K >= 2048 up to 3 x 3
+ * blocks of at least 1024 rows and 1024 columns, for shallower products up
+ * to 4 row blocks).  Row blocks hold whole 128-row tiles and column blocks
+ * whole 256-column tiles, except the last ones.
  * The library stages the whole problem in device memory it owns (M*K + K*N
- * + M*N floats plus the GEMM workspace), grown on demand and freed by
- * gemm_shutdown(); calls on one device are serialised.
+ * + M*N floats plus a GEMM workspace per column block), grown on demand and
+ * freed by gemm_shutdown(); calls on one device are serialised.
  * Returns GEMM_OK, GEMM_ERR_INVALID_ARG (size, ld, pointer, mode, blocks),
  * GEMM_ERR_UNSUPPORTED, GEMM_ERR_CUDA (including a failed staging
  * allocation), GEMM_ERR_DEVICE_TIMEOUT (a bounded wait in the tensor-core

@@ -7,21 +7,28 @@
 // events, cudaMemcpy out).  A caller whose data lives on the host pays for
 // those copies too, and on GB300 they take longer than the GEMM: about
 // 196 GB/s host-to-device and 180 GB/s device-to-host were measured on this
-// machine's host link, against 137 GFLOP in 0.47 ms for a 4096^3 product
+// machine's host link, against 137 GFLOP in 0.45 ms for a 4096^3 product
 // whose 192 MB of operands and result take about 1 ms to move.  So the
-// product is pipelined in row blocks over three library streams:
+// product is cut into a grid of row blocks of A (and C) and column blocks
+// of B (and C), and three library streams overlap the copies with the GEMMs:
 //
-//   h2d:  B, then A rows [r0, r1) (and C rows when beta != 0), block by block
-//   comp: GEMM of block i once its rows have arrived
-//   d2h:  C rows [r0, r1) of block i once its GEMM is done
+//   h2d:  B column block 0, A row block 0, then A row blocks and B column
+//         blocks alternately, keeping the arrived fraction of A and of B
+//         about equal (C row blocks travel with A's when beta != 0)
+//   comp: as soon as a block arrives, the GEMMs it completes: a new A row
+//         block against every B column block already there, a new B column
+//         block against all the A rows already there (one GEMM)
+//   d2h:  each GEMM's block of C, once that GEMM is done
 //
-// so the copies of later blocks, the GEMM of the current one and the copy
-// back of earlier ones run at the same time.  The whole problem is staged in
-// device memory owned by the library (grown on demand, freed by
-// gemm_shutdown()).  Every block runs in the mode resolved for the first
-// block; on the tensor-core path the first block splits B into its TF32
-// planes and the later blocks reuse them.
+// so the first GEMM starts once two blocks have arrived instead of after
+// all of B.  The whole problem is staged in device memory owned by the
+// library (grown on demand, freed by gemm_shutdown()).  Every GEMM runs in
+// the mode resolved for the whole product; on the tensor-core path each B
+// column block is split into its TF32 planes by its first GEMM, in a
+// workspace of its own, and its later GEMMs reuse them.
+#include <cstdlib>
 #include <mutex>
+#include <vector>
 
 #include "common.cuh"
 
@@ -31,11 +38,14 @@ namespace {
 constexpr int kMaxDev = 64;
 constexpr int kMaxBlocks = GEMM_HOST_MAX_BLOCKS;
 
+constexpr int kMaxColBlocks = 8;
+
+// Events are re-recorded freely: a stream wait takes the event's most recent
+// record at the time the wait is enqueued.
 struct HostPipe {
   bool ready = false;
   cudaStream_t h2d = nullptr, comp = nullptr, d2h = nullptr;
-  cudaEvent_t in[kMaxBlocks] = {};
-  cudaEvent_t out[kMaxBlocks] = {};
+  cudaEvent_t in = nullptr, out = nullptr;
   void *buf = nullptr;
   size_t bytes = 0;
 };
@@ -47,10 +57,8 @@ void destroy(HostPipe &p) {
   if (p.h2d) cudaStreamDestroy(p.h2d);
   if (p.comp) cudaStreamDestroy(p.comp);
   if (p.d2h) cudaStreamDestroy(p.d2h);
-  for (int i = 0; i < kMaxBlocks; ++i) {
-    if (p.in[i]) cudaEventDestroy(p.in[i]);
-    if (p.out[i]) cudaEventDestroy(p.out[i]);
-  }
+  if (p.in) cudaEventDestroy(p.in);
+  if (p.out) cudaEventDestroy(p.out);
   if (p.buf) cudaFree(p.buf);
   cudaGetLastError();
   p = HostPipe{};
@@ -61,9 +69,8 @@ int setup(HostPipe &p) {
   bool ok = cudaStreamCreateWithFlags(&p.h2d, cudaStreamNonBlocking) == cudaSuccess &&
             cudaStreamCreateWithFlags(&p.comp, cudaStreamNonBlocking) == cudaSuccess &&
             cudaStreamCreateWithFlags(&p.d2h, cudaStreamNonBlocking) == cudaSuccess;
-  for (int i = 0; ok && i < kMaxBlocks; ++i)
-    ok = cudaEventCreateWithFlags(&p.in[i], cudaEventDisableTiming) == cudaSuccess &&
-         cudaEventCreateWithFlags(&p.out[i], cudaEventDisableTiming) == cudaSuccess;
+  ok = ok && cudaEventCreateWithFlags(&p.in, cudaEventDisableTiming) == cudaSuccess &&
+       cudaEventCreateWithFlags(&p.out, cudaEventDisableTiming) == cudaSuccess;
   if (!ok) {
     destroy(p);
     return GEMM_ERR_CUDA;
@@ -89,18 +96,30 @@ int reserve(HostPipe &p, size_t need) {
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Row blocks for a product: one block while the GEMM is short (under
-// ~8 GFLOP the copies dominate and a single launch has the least overhead),
-// else blocks of at least 1024 rows, at most 4 of them.  Measured on GB300
-// with pinned buffers (ms per call for 1 / 2 / 4 / 8 blocks): 4096^3 1.49 /
-// 1.35 / 1.23 / 1.22, 8192^3 7.39 / 6.12 / 5.45 / 6.50, M = 65536, N = 64,
-// K = 4096: 5.42 / 5.59 / 5.24 / 5.33.
-int auto_blocks(int64_t M, int64_t N, int64_t K) {
-  if (2.0 * (double)M * (double)N * (double)K < 8e9) return 1;
-  int64_t b = M / 1024;
-  if (b < 1) b = 1;
-  if (b > 4) b = 4;
-  return (int)b;
+// Blocking for a product (rows x columns).  One block while the GEMM is
+// short (under ~8 GFLOP the copies dominate and a single launch has the
+// least overhead).  Else, for a deep product (K >= 2048, where B is large
+// and waiting for all of it delays the first GEMM), up to 3 x 3 blocks of at
+// least 1024 rows and columns; otherwise row blocks only, up to 4.
+// Measured on GB300 with pinned buffers (ms per call; rows x columns):
+// 4096^3 1x1 1.46, 4x1 1.03, 2x2 1.14, 3x3 1.03, 4x4 1.07, 8x8 1.60;
+// 8192^3 1x1 7.13, 4x1 5.14, 2x2 5.31, 3x3 4.78, 4x4 5.54, 4x8 4.92;
+// 2048^3 4x1 0.321, 2x2 0.307, 3x3 0.342; 65536 x 64 x 4096 (rows only)
+// 1 / 2 / 4 / 8 blocks: 5.42 / 5.59 / 5.24 / 5.33.  The copies in run at
+// ~207 GB/s alone, ~275 GB/s in total with copies out at the same time;
+// smaller blocks start the GEMMs earlier but each GEMM then carries its own
+// fixed costs (4096^3 as 4x4: 613 us of GEMMs against 420 us for one call).
+void auto_grid(int64_t M, int64_t N, int64_t K, int &nb, int &nc) {
+  nb = nc = 1;
+  if (2.0 * (double)M * (double)N * (double)K < 8e9) return;
+  auto clamp = [](int64_t v, int64_t hi) { return (int)(v < 1 ? 1 : (v > hi ? hi : v)); };
+  nc = K >= 2048 ? clamp(N / 1024, 3) : 1;
+  nb = clamp(M / 1024, nc > 1 ? 3 : 4);
+}
+
+int64_t env_int(const char *name, int64_t dflt) {
+  const char *v = std::getenv(name);
+  return (v && *v) ? std::atoll(v) : dflt;
 }
 
 // Waits for all three streams, so no copy touches the caller's buffers
@@ -166,26 +185,71 @@ extern "C" int gemm_f32_host(int64_t M, int64_t N, int64_t K, float alpha, const
   if (dev < 0 || dev >= kMaxDev) return GEMM_ERR_UNSUPPORTED;
   const DeviceProps &dp = props_of(dev);
 
-  // row blocks: whole 128-row tiles except the last
-  int nb = blocks > 0 ? blocks : auto_blocks(M, N, K);
+  // Row blocks hold whole 128-row tiles and column blocks whole 256-column
+  // tiles, except the last of each.  Column blocks only when the library
+  // picks the blocking (blocks == 0); tuning knob GEMM_HOST_COL_BLOCKS.
+  int auto_nb, auto_nc;
+  auto_grid(M, N, K, auto_nb, auto_nc);
+  int nb = blocks > 0 ? blocks : auto_nb;
   int64_t rows = ceil_div(M, nb);
   if (M > 128) rows = ceil_div(rows, 128) * 128;
   nb = (int)ceil_div(M, rows);
-  const int64_t last = M - (int64_t)(nb - 1) * rows;
+  int nc = (int)env_int("GEMM_HOST_COL_BLOCKS", blocks > 0 ? 1 : auto_nc);
+  if (nc < 1) nc = 1;
+  if (nc > kMaxColBlocks) nc = kMaxColBlocks;
+  int64_t cols = ceil_div(N, nc);
+  if (N > 256) cols = ceil_div(cols, 256) * 256;
+  nc = (int)ceil_div(N, cols);
   const int64_t kld = K > 1 ? K : 1, nld = N > 1 ? N : 1;
+  auto rows_of = [&](int64_t i) { return i + 1 < nb ? rows : M - i * rows; };
+  auto cols_of = [&](int64_t j) { return j + 1 < nc ? cols : N - j * cols; };
 
-  // one mode for every block: the one the first block resolves to
-  gemm_plan_t p0, p1;
-  st = make_plan(rows, N, K, kld, nld, nld, mode, 0, beta != 0.0f, dp, &p0);
+  // Arrival order: B column block 0, A row block 0, then whichever of A and
+  // B has the smaller arrived fraction.  Each arrival enables GEMMs: a new A
+  // row block i against each arrived column block, a new column block j
+  // against rows [0, i_arrived * rows) in one call.
+  struct Gemm {
+    int64_t r0, nr;
+    int j;
+  };
+  struct Arrival {
+    bool is_a;
+    int idx;
+    std::vector<Gemm> gemms;
+  };
+  std::vector<Arrival> order;
+  {
+    int ia = 0, jb = 0;
+    while (ia < nb || jb < nc) {
+      const bool take_a = jb > 0 && ia < nb && (jb >= nc || (double)ia / nb <= (double)jb / nc);
+      Arrival ar{take_a, take_a ? ia : jb, {}};
+      if (take_a) {
+        for (int j = 0; j < jb; ++j) ar.gemms.push_back(Gemm{ia * rows, rows_of(ia), j});
+        ++ia;
+      } else {
+        if (ia > 0) ar.gemms.push_back(Gemm{0, (int64_t)ia * rows < M ? (int64_t)ia * rows : M, jb});
+        ++jb;
+      }
+      order.push_back(ar);
+    }
+  }
+
+  // one mode for every GEMM: the one the whole product resolves to
+  gemm_plan_t whole;
+  st = make_plan(M, N, K, kld, nld, nld, mode, 0, beta != 0.0f, dp, &whole);
   if (st != GEMM_OK) return st;
-  const int bmode = (mode == GEMM_MODE_AUTO && K > 0) ? p0.mode : mode;
-  st = make_plan(rows, N, K, kld, nld, nld, bmode, 0, beta != 0.0f, dp, &p0);
-  if (st == GEMM_OK) st = make_plan(last, N, K, kld, nld, nld, bmode, 0, beta != 0.0f, dp, &p1);
-  if (st != GEMM_OK) return st;
-  const size_t ws_bytes = align256((size_t)(p0.workspace_bytes > p1.workspace_bytes
-                                                ? p0.workspace_bytes
-                                                : p1.workspace_bytes));
-  const bool tc = p0.kernel == GEMM_KERNEL_TC_TF32X3 || p0.kernel == GEMM_KERNEL_TC_TF32;
+  const int bmode = (mode == GEMM_MODE_AUTO && K > 0) ? whole.mode : mode;
+  size_t ws_bytes = 0;
+  bool tc = false;
+  for (const Arrival &ar : order)
+    for (const Gemm &g : ar.gemms) {
+      gemm_plan_t pg;
+      st = make_plan(g.nr, cols_of(g.j), K, kld, nld, nld, bmode, 0, beta != 0.0f, dp, &pg);
+      if (st != GEMM_OK) return st;
+      if ((size_t)pg.workspace_bytes > ws_bytes) ws_bytes = (size_t)pg.workspace_bytes;
+      tc = tc || pg.kernel == GEMM_KERNEL_TC_TF32X3 || pg.kernel == GEMM_KERNEL_TC_TF32;
+    }
+  ws_bytes = align256(ws_bytes);
 
   const size_t a_bytes = align256((size_t)M * K * 4), b_bytes = align256((size_t)K * N * 4);
   const size_t c_bytes = align256((size_t)M * N * 4);
@@ -193,34 +257,51 @@ extern "C" int gemm_f32_host(int64_t M, int64_t N, int64_t K, float alpha, const
   std::lock_guard<std::mutex> lk(g_host_mu[dev]);
   HostPipe &pp = g_pipe[dev];
   st = setup(pp);
-  if (st == GEMM_OK) st = reserve(pp, a_bytes + b_bytes + c_bytes + ws_bytes);
+  if (st == GEMM_OK) st = reserve(pp, a_bytes + b_bytes + c_bytes + (size_t)nc * ws_bytes);
   if (st != GEMM_OK) return st;
   char *base = static_cast<char *>(pp.buf);
   float *dA = reinterpret_cast<float *>(base);
   float *dB = reinterpret_cast<float *>(base + a_bytes);
   float *dC = reinterpret_cast<float *>(base + a_bytes + b_bytes);
-  void *ws = ws_bytes ? base + a_bytes + b_bytes + c_bytes : nullptr;
+  char *ws0 = base + a_bytes + b_bytes + c_bytes;  // column block j: ws0 + j * ws_bytes
 
-  cudaError_t e = K > 0 ? copy_rows(dB, nld, B, ldb, N, K, cudaMemcpyHostToDevice, pp.h2d)
-                        : cudaSuccess;
-  for (int i = 0; i < nb && e == cudaSuccess && st == GEMM_OK; ++i) {
-    const int64_t r0 = (int64_t)i * rows, nr = i + 1 < nb ? rows : last;
-    if (K > 0)
-      e = copy_rows(dA + r0 * kld, kld, A + r0 * lda, lda, K, nr, cudaMemcpyHostToDevice, pp.h2d);
-    if (e == cudaSuccess && beta != 0.0f)
-      e = copy_rows(dC + r0 * nld, nld, C + r0 * ldc, ldc, N, nr, cudaMemcpyHostToDevice, pp.h2d);
-    if (e == cudaSuccess) e = cudaEventRecord(pp.in[i], pp.h2d);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(pp.comp, pp.in[i], 0);
-    if (e != cudaSuccess) break;
-    GemmArgs g{nr, N, K, alpha, beta, dA + r0 * kld, kld, dB, nld, dC + r0 * nld, nld};
-    g.b_presplit = (tc && i > 0) ? 1 : 0;
-    g.plain_order = 1;
-    st = run_gemm(g, bmode, ws, ws_bytes, pp.comp);
-    if (st != GEMM_OK) break;
-    e = cudaEventRecord(pp.out[i], pp.comp);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(pp.d2h, pp.out[i], 0);
-    if (e == cudaSuccess)
-      e = copy_rows(C + r0 * ldc, ldc, dC + r0 * nld, nld, N, nr, cudaMemcpyDeviceToHost, pp.d2h);
+  cudaError_t e = cudaSuccess;
+  bool split_done[kMaxColBlocks] = {};
+  for (const Arrival &ar : order) {
+    if (e != cudaSuccess || st != GEMM_OK) break;
+    if (ar.is_a) {
+      const int64_t r0 = (int64_t)ar.idx * rows, nr = rows_of(ar.idx);
+      if (K > 0)
+        e = copy_rows(dA + r0 * kld, kld, A + r0 * lda, lda, K, nr, cudaMemcpyHostToDevice,
+                      pp.h2d);
+      if (e == cudaSuccess && beta != 0.0f)
+        e = copy_rows(dC + r0 * nld, nld, C + r0 * ldc, ldc, N, nr, cudaMemcpyHostToDevice,
+                      pp.h2d);
+    } else if (K > 0) {
+      const int64_t c0 = (int64_t)ar.idx * cols;
+      e = copy_rows(dB + c0, nld, B + c0, ldb, cols_of(ar.idx), K, cudaMemcpyHostToDevice,
+                    pp.h2d);
+    }
+    if (ar.gemms.empty()) continue;
+    if (e == cudaSuccess) e = cudaEventRecord(pp.in, pp.h2d);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(pp.comp, pp.in, 0);
+    for (const Gemm &gm : ar.gemms) {
+      if (e != cudaSuccess || st != GEMM_OK) break;
+      const int64_t c0 = (int64_t)gm.j * cols, w = cols_of(gm.j);
+      GemmArgs g{gm.nr, w, K, alpha, beta, dA + gm.r0 * kld, kld, dB + c0, nld,
+                 dC + gm.r0 * nld + c0, nld};
+      g.b_presplit = (tc && split_done[gm.j]) ? 1 : 0;
+      g.plain_order = 1;
+      st = run_gemm(g, bmode, ws_bytes ? ws0 + (size_t)gm.j * ws_bytes : nullptr, ws_bytes,
+                    pp.comp);
+      if (st != GEMM_OK) break;
+      split_done[gm.j] = true;
+      e = cudaEventRecord(pp.out, pp.comp);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(pp.d2h, pp.out, 0);
+      if (e == cudaSuccess)
+        e = copy_rows(C + gm.r0 * ldc + c0, ldc, dC + gm.r0 * nld + c0, nld, w, gm.nr,
+                      cudaMemcpyDeviceToHost, pp.d2h);
+    }
   }
   if (e != cudaSuccess) {
     cudaGetLastError();

@@ -352,7 +352,8 @@ def _host_matrix(t, name):
 def matmul_host(A, B, C=None, alpha=1.0, beta=0.0, mode=MODE_AUTO, blocks=0):
     """C <- alpha * A @ B + beta * C for row-major float32 CPU tensors (pin
     them with ``.pin_memory()`` so the copies overlap the GEMM).  The library
-    moves the data to the GPU and back in row blocks and runs the GEMM there;
+    moves the data to the GPU and back in blocks (row blocks of A and C,
+    column blocks of B and C) and runs the GEMMs there as the blocks arrive;
     the call returns when C holds the result.  Returns C."""
     import torch
     M, K = A.shape

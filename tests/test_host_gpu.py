@@ -65,6 +65,46 @@ def test_host_integer_bit_exact(mode, blocks):
     assert oracle.mismatches(got, oracle.gemm(A, B, 1.0, 0.0, None)) == 0
 
 
+GRID_CASES = [
+    # (M, N, K, row blocks, column blocks): A row blocks and B column blocks
+    # arrive alternately; ragged last blocks both ways
+    (1000, 700, 257, 3, 3),
+    (777, 1300, 129, 2, 5),
+    (300, 2000, 96, 1, 4),   # one row block: each B column block is one GEMM
+    (1100, 513, 300, 4, 2),
+]
+
+
+@pytest.mark.parametrize("case", GRID_CASES)
+@pytest.mark.parametrize("mode", ["fp32_simt", "tf32x3", "auto"])
+@pytest.mark.parametrize("beta", [0.0, 0.5])
+def test_host_grid_of_blocks(case, mode, beta, monkeypatch):
+    M, N, K, nb, nc = case
+    monkeypatch.setenv("GEMM_HOST_COL_BLOCKS", str(nc))
+    A, B, C0, got = run_host(M, N, K, -1.25, beta, mode, nb, pad=(1, 3, 2))
+    ref, D = oracle.gemm(A, B, -1.25, beta, C0 if beta else None, with_bound=True)
+    assert oracle.err_normalised(got, ref, D) <= TOL_E1
+    # integer inputs: exact whatever the blocking
+    A, B, C0, got = run_host(M, N, K, 1.0, 1.0, mode, nb, dist="int2", seed=77)
+    assert oracle.mismatches(got, oracle.gemm(A, B, 1.0, 1.0, C0)) == 0
+
+
+def test_host_auto_grid_2048():
+    """2048 x 2048 x 1024 (8.6 GFLOP): the library's blocking is 2 x 2."""
+    import torch
+    from roofline_gb300 import gemm
+    M, N, K = 2048, 2048, 1024
+    a = matrix(M, K, None, 5, "u11")
+    b = matrix(K, N, None, 6, "u11")
+    c = matrix(M, N, None, 7, "u11")
+    hC = torch.from_numpy(c.copy()).pin_memory()
+    gemm.matmul_host(torch.from_numpy(a).pin_memory(), torch.from_numpy(b).pin_memory(), hC,
+                     0.75, -0.5, blocks=0)
+    rows, cols = sample_entries(M, N, n=20000, seed=3)
+    ref, D = oracle.gemm_entries(a, b, rows, cols, 0.75, -0.5, c)
+    assert oracle.err_normalised(hC.numpy()[rows, cols], ref, D) <= TOL_E1
+
+
 def test_host_pageable_buffers():
     A, B, C0, got = run_host(700, 400, 300, 1.0, 0.5, "auto", 3, pinned=False)
     ref, D = oracle.gemm(A, B, 1.0, 0.5, C0, with_bound=True)
