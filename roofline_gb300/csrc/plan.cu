@@ -215,17 +215,14 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
       // 128 x 128 tiles, M = 2048 266 us against 336 us)
       const bool wide = N > 128 && tiles256 * 2 >= sms;
       p.a_split_in_kernel = a_aligned ? 1 : 0;
-      p.launches = a_aligned ? 2 : 3;
+      p.launches = 2;  // the split pass (A and B in one launch when both are split) and the GEMM
       auto set = [&](int bn, int bk, int st, int cc, int bm = 128) {
         p.bm = bm; p.bn = bn; p.bk = bk; p.stages = st; p.b_concat = cc;
       };
       // 256 x 256 tiles (two 128-row accumulators sharing each B tile) halve
       // the operand bytes per MMA; they take pre-split operands.
       const int64_t tiles_m2 = ceil_div(M, 256) * ceil_div(N, 256);
-      auto pre_split = [&]() {
-        p.a_split_in_kernel = 0;
-        p.launches = 3;
-      };
+      auto pre_split = [&]() { p.a_split_in_kernel = 0; };
       if (!x3) {
         // 1xTF32: one MMA per K step, so feeding operands is the limit.
         // Narrow B (HBM-bound on A): 128-row tiles with A split on chip, so A
@@ -282,7 +279,6 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
           set(c[0], c[1], c[2], c[4], bm);
           p.a_split_in_kernel = c[3] != 0;
           p.a_hi_tmem = c[3] == 2;
-          p.launches = c[3] ? 2 : 3;
         }
       }
       p.ctas_per_sm = tc_ctas_per_sm(p.bm, p.bn, p.bk, p.stages,

@@ -294,14 +294,24 @@ struct Walk {
 // pdl: launched with programmatic dependent launch, so it may be scheduled
 // while the kernel before it drains; it waits for that kernel before touching
 // memory.
-// dst hi/lo (rows x kp, row-major) <- split of src (rows x k, row stride ld);
-// columns k..kp-1 zero; lo == nullptr: the hi part only (1xTF32).
-cudaError_t launch_split_rows(const float *src, int64_t ld, int64_t rows, int64_t k, int64_t kp,
-                              float *hi, float *lo, bool pdl, cudaStream_t s);
-// dst hi/lo (cols x kp, row-major) <- split of the transpose of src (k x cols,
-// row stride ld); columns k..kp-1 zero.
-cudaError_t launch_split_transposed(const float *src, int64_t ld, int64_t k, int64_t cols,
-                                    int64_t kp, float *hi, float *lo, bool pdl, cudaStream_t s);
+// One operand's TF32 split into hi (and lo) planes, K-major.  transposed =
+// 0: dst (a = rows x kp) <- src (rows x b = k, row stride ld); transposed =
+// 1: dst (b = cols x kp) <- the transpose of src (a = k x cols, row stride
+// ld).  Columns k..kp-1 are zero; lo == nullptr: the hi part only (1xTF32).
+struct SplitJob {
+  const float *src;
+  int64_t ld, a, b, kp;
+  float *hi, *lo;
+  int transposed, vec;
+  int64_t blocks;  // thread blocks of this job
+  int64_t grid_x;  // transposed: blocks along cols
+};
+SplitJob split_rows_job(const float *src, int64_t ld, int64_t rows, int64_t k, int64_t kp,
+                        float *hi, float *lo);
+SplitJob split_transposed_job(const float *src, int64_t ld, int64_t k, int64_t cols, int64_t kp,
+                              float *hi, float *lo);
+// One launch running job a, then (b != nullptr) job b, in separate blocks.
+cudaError_t launch_splits(const SplitJob &a, const SplitJob *b, bool pdl, cudaStream_t s);
 // Sums the parts of the tiles shared between stream-K CTAs into C.
 cudaError_t launch_fixup(const TcParams &p, int bm, int bn, int64_t G, bool pdl, cudaStream_t s);
 

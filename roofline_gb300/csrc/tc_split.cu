@@ -16,6 +16,7 @@ namespace {
 // written by the GEMM).
 constexpr int kFixMaxParts = 256;
 constexpr int kFixRows = 16;  // tile rows per fix-up block
+constexpr int kTrK = 32, kTrN = 128;  // transposed split: k x n tile per block
 
 __global__ void __launch_bounds__(256)
 streamk_fixup_kernel(TcParams p, int BM, int BN, int64_t G) {
@@ -100,19 +101,18 @@ streamk_fixup_kernel(TcParams p, int BM, int BN, int64_t G) {
   }
 }
 
-// dst_hi/dst_lo (rows x kp, row-major) <- split of src (rows x k, ld), zero for k <= c < kp
-// (lo == nullptr: the hi part only, for 1xTF32).
-__global__ void split_rows_kernel(const float *__restrict__ src, int64_t ld, int64_t rows,
-                                  int64_t k, int64_t kp, float *__restrict__ hi,
-                                  float *__restrict__ lo) {
-  grid_dependency_wait();     // the kernel before this one is done
-  grid_launch_dependents();
+// Row split: dst_hi/dst_lo (rows x kp, row-major) <- split of src (rows x
+// k, ld), zero for k <= c < kp (lo == nullptr: the hi part only, for
+// 1xTF32).  Block `blk` of the job's `blocks` walks the 4-float groups
+// grid-stride.
+__device__ __forceinline__ void split_rows_block(const SplitJob &j, int64_t blk) {
+  const int64_t rows = j.a, k = j.b, kp = j.kp;
   const int64_t groups = rows * (kp / 4);
-  for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < groups;
-       g += (int64_t)gridDim.x * blockDim.x) {
+  for (int64_t g = blk * (int64_t)blockDim.x + threadIdx.x; g < groups;
+       g += j.blocks * (int64_t)blockDim.x) {
     const int64_t r = g / (kp / 4);
     const int64_t c = (g % (kp / 4)) * 4;
-    const float *s = src + r * ld + c;
+    const float *s = j.src + r * j.ld + c;
     float v[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) v[i] = (c + i < k) ? __ldg(s + i) : 0.0f;
@@ -121,28 +121,23 @@ __global__ void split_rows_kernel(const float *__restrict__ src, int64_t ld, int
     h.y = tf32_rna(v[1]); l.y = v[1] - h.y;
     h.z = tf32_rna(v[2]); l.z = v[2] - h.z;
     h.w = tf32_rna(v[3]); l.w = v[3] - h.w;
-    *reinterpret_cast<float4 *>(hi + r * kp + c) = h;
-    if (lo) *reinterpret_cast<float4 *>(lo + r * kp + c) = l;
+    *reinterpret_cast<float4 *>(j.hi + r * kp + c) = h;
+    if (j.lo) *reinterpret_cast<float4 *>(j.lo + r * kp + c) = l;
   }
 }
 
-// B (k x n, ld, row-major) -> Bt_hi/Bt_lo (n x kp, row-major), columns
-// k <= c < kp zero.  One CTA of 256 threads moves a 32 (k) x 128 (n) tile:
-// each thread loads four 16-byte pieces along n (all in flight at once),
-// the tile goes through shared memory, and each thread then stores four
-// 16-byte pieces of hi and of lo along k.  `vec` (ld % 4 == 0 and a 16-byte
-// aligned B) enables the 16-byte loads; the stores are 16-byte aligned
-// because kp is a multiple of 4.
-constexpr int kTrK = 32, kTrN = 128;
-
-__global__ void __launch_bounds__(256)
-split_transpose_kernel(const float *__restrict__ src, int64_t ld, int64_t k, int64_t n,
-                       int64_t kp, int vec, float *__restrict__ hi, float *__restrict__ lo) {
-  __shared__ float tile[kTrK][kTrN + 1];
-  grid_dependency_wait();   // the kernel before this one is done
-  grid_launch_dependents();  // the GEMM may launch; it waits for this grid to finish
-  const int64_t k0 = (int64_t)blockIdx.y * kTrK;
-  const int64_t n0 = (int64_t)blockIdx.x * kTrN;
+// Transposed split: src (k x n, ld, row-major) -> hi/lo (n x kp, row-major),
+// columns k <= c < kp zero.  One block of 256 threads moves a 32 (k) x 128
+// (n) tile: each thread loads four 16-byte pieces along n (all in flight at
+// once), the tile goes through shared memory, and each thread then stores
+// four 16-byte pieces of hi and of lo along k.  `vec` (ld % 4 == 0 and a
+// 16-byte aligned source) enables the 16-byte loads; the stores are 16-byte
+// aligned because kp is a multiple of 4.
+__device__ __forceinline__ void split_transpose_block(const SplitJob &j, int64_t blk,
+                                                      float (*tile)[kTrN + 1]) {
+  const int64_t k = j.a, n = j.b, kp = j.kp;
+  const int64_t k0 = (blk / j.grid_x) * kTrK;
+  const int64_t n0 = (blk % j.grid_x) * kTrN;
   const int t = threadIdx.x;
   // loads: piece p = t + 256 * i covers row p / 32, columns 4 * (p % 32) .. +3
   float4 v[4];
@@ -152,8 +147,8 @@ split_transpose_kernel(const float *__restrict__ src, int64_t ld, int64_t k, int
     const int64_t kk = k0 + p / 32, nn = n0 + 4 * (p % 32);
     float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
     if (kk < k) {
-      const float *s = src + kk * ld + nn;
-      if (vec && nn + 4 <= n) {
+      const float *s = j.src + kk * j.ld + nn;
+      if (j.vec && nn + 4 <= n) {
         x = __ldg(reinterpret_cast<const float4 *>(s));
       } else {
         if (nn + 0 < n) x.x = __ldg(s + 0);
@@ -188,10 +183,26 @@ split_transpose_kernel(const float *__restrict__ src, int64_t ld, int64_t k, int
       h.y = tf32_rna(a1); l.y = a1 - h.y;
       h.z = tf32_rna(a2); l.z = a2 - h.z;
       h.w = tf32_rna(a3); l.w = a3 - h.w;
-      *reinterpret_cast<float4 *>(hi + nn * kp + kk) = h;
-      if (lo) *reinterpret_cast<float4 *>(lo + nn * kp + kk) = l;
+      *reinterpret_cast<float4 *>(j.hi + nn * kp + kk) = h;
+      if (j.lo) *reinterpret_cast<float4 *>(j.lo + nn * kp + kk) = l;
     }
   }
+}
+
+// One launch for one or two split jobs (A's and B's): the first job's
+// blocks come first, then the second's.
+__global__ void __launch_bounds__(256) split_kernel(SplitJob j0, SplitJob j1) {
+  __shared__ float tile[kTrK][kTrN + 1];
+  grid_dependency_wait();   // the kernel before this one is done
+  grid_launch_dependents();  // the GEMM may launch; it waits for this grid to finish
+  int64_t blk = blockIdx.x;
+  const bool second = blk >= j0.blocks;
+  const SplitJob j = second ? j1 : j0;
+  if (second) blk -= j0.blocks;
+  if (j.transposed)
+    split_transpose_block(j, blk, tile);
+  else
+    split_rows_block(j, blk);
 }
 
 }  // namespace
@@ -212,21 +223,30 @@ cudaError_t launch(void (*kern)(Args...), dim3 grid, dim3 block, bool pdl, cudaS
   return cudaLaunchKernelEx(&lc, kern, args...);
 }
 
-cudaError_t launch_split_rows(const float *src, int64_t ld, int64_t rows, int64_t k, int64_t kp,
-                              float *hi, float *lo, bool pdl, cudaStream_t s) {
-  int64_t blocks = ceil_div(rows * (kp / 4), 256);
-  if (blocks > 152 * 16) blocks = 152 * 16;
-  if (blocks < 1) blocks = 1;
-  return launch(split_rows_kernel, dim3((unsigned)blocks), dim3(256), pdl, s, src, ld, rows, k,
-                kp, hi, lo);
+SplitJob split_rows_job(const float *src, int64_t ld, int64_t rows, int64_t k, int64_t kp,
+                        float *hi, float *lo) {
+  SplitJob j{src, ld, rows, k, kp, hi, lo, 0, 0, 0, 1};
+  j.blocks = ceil_div(rows * (kp / 4), 256);
+  if (j.blocks > 152 * 16) j.blocks = 152 * 16;
+  if (j.blocks < 1) j.blocks = 1;
+  return j;
 }
 
-cudaError_t launch_split_transposed(const float *src, int64_t ld, int64_t k, int64_t cols,
-                                    int64_t kp, float *hi, float *lo, bool pdl, cudaStream_t s) {
-  const int vec = ((ld & 3) == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0) ? 1 : 0;
-  dim3 grid((unsigned)ceil_div(cols, kTrN), (unsigned)ceil_div(kp, kTrK));
-  return launch(split_transpose_kernel, grid, dim3(256), pdl, s, src, ld, k, cols, kp, vec, hi,
-                lo);
+SplitJob split_transposed_job(const float *src, int64_t ld, int64_t k, int64_t cols, int64_t kp,
+                              float *hi, float *lo) {
+  SplitJob j{src, ld, k, cols, kp, hi, lo, 1, 0, 0, 1};
+  j.vec = ((ld & 3) == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0) ? 1 : 0;
+  j.grid_x = ceil_div(cols, kTrN);
+  j.blocks = j.grid_x * ceil_div(kp, kTrK);
+  return j;
+}
+
+cudaError_t launch_splits(const SplitJob &a, const SplitJob *b, bool pdl, cudaStream_t s) {
+  SplitJob none{};
+  const SplitJob &second = b ? *b : none;
+  const int64_t blocks = a.blocks + second.blocks;
+  if (blocks < 1 || blocks > 0x7fffffff) return cudaErrorInvalidValue;
+  return launch(split_kernel, dim3((unsigned)blocks), dim3(256), pdl, s, a, second);
 }
 
 cudaError_t launch_fixup(const TcParams &p, int bm, int bn, int64_t G, bool pdl, cudaStream_t s) {

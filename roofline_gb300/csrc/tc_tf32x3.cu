@@ -609,16 +609,17 @@ int launch_cfg(const gemm_plan_t &plan, const GemmArgs &a, char *ws, cudaStream_
   // kept so the events bracket the GEMM kernel alone; callers that chain the
   // GEMM behind cross-stream event waits ask for plain order as well.
   const bool pdl = !profile_events_set() && !a.plain_order;
-  cudaError_t se = cudaSuccess;
-  if (!AK) {
-    se = a.ta ? launch_split_transposed(a.A, a.lda, a.K, a.M, L.kp, ahi, X3 ? alo : nullptr, pdl, s)
-              : launch_split_rows(a.A, a.lda, a.M, a.K, L.kp, ahi, X3 ? alo : nullptr, pdl, s);
-  }
-  if (se == cudaSuccess && !a.b_presplit) {
-    se = a.tb ? launch_split_rows(a.B, a.ldb, a.N, a.K, L.kp, bhi, X3 ? blo : nullptr, pdl, s)
-              : launch_split_transposed(a.B, a.ldb, a.K, a.N, L.kp, bhi, X3 ? blo : nullptr, pdl,
-                                        s);
-  }
+  // Both passes, when both run, are one launch.
+  SplitJob jobs[2];
+  int njobs = 0;
+  if (!AK)
+    jobs[njobs++] = a.ta ? split_transposed_job(a.A, a.lda, a.K, a.M, L.kp, ahi, X3 ? alo : nullptr)
+                         : split_rows_job(a.A, a.lda, a.M, a.K, L.kp, ahi, X3 ? alo : nullptr);
+  if (!a.b_presplit)
+    jobs[njobs++] = a.tb ? split_rows_job(a.B, a.ldb, a.N, a.K, L.kp, bhi, X3 ? blo : nullptr)
+                         : split_transposed_job(a.B, a.ldb, a.K, a.N, L.kp, bhi, X3 ? blo : nullptr);
+  const cudaError_t se =
+      njobs ? launch_splits(jobs[0], njobs > 1 ? &jobs[1] : nullptr, pdl, s) : cudaSuccess;
   if (se != cudaSuccess) {
     cudaGetLastError();
     return GEMM_ERR_CUDA;
