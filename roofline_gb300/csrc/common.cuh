@@ -23,11 +23,12 @@ struct GemmArgs {
   // tb = 1 means B is stored N x K (B(k,j) = B[j*ldb + k]); 0 is the
   // row-major M x K / K x N storage of gemm_f32.
   int ta = 0, tb = 0;
-  // Tensor-core path only.  b_presplit = 1: the workspace already holds the
+  // b_presplit = 1 (tensor-core path only): the workspace already holds the
   // B_hi / B_lo planes of this B (same N, K and mode, written by an earlier
   // call on the same stream), so the B split pass is skipped.  plain_order =
   // 1: launch without programmatic dependent launch (each kernel waits for
-  // everything before it in the stream).
+  // everything before it in the stream), for callers that chain the GEMM
+  // behind cross-stream event waits.
   int b_presplit = 0, plain_order = 0;
 };
 
