@@ -259,8 +259,16 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
           else set(128, 32, 4, 1);
           p.a_hi_tmem = 1;
         }
+      } else if (wide) {
+        set(256, 16, 4, 0);
       } else {
-        if (wide) set(256, 16, 4, 0);
+        // Tiles filling at most half the SMs go stream-K (below); there one
+        // CTA per SM with 6 stages beats two with 3 (the same bytes in
+        // flight, half the partial tiles to sum): GB300, 1023 x 1025 x 777
+        // (lda 777) 35.5 against 39.7 us.  More tiles keep two CTAs per SM,
+        // so one CTA's epilogue overlaps the other's MMAs.
+        const int64_t tiles128 = ceil_div(M, 128) * ceil_div(N, 128);
+        if (2 * tiles128 <= sms) set(128, 16, 6, 1);
         else set(128, 16, 3, 1);
       }
       // Tuning knob: GEMM_TC_CONFIG="bn,bk,stages,a_split,b_concat" (128-row

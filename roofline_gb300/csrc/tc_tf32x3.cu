@@ -736,6 +736,7 @@ bool tc_supported(const DeviceProps &dp) { return dp.cc_major == 10 && dp.cc_min
   X(128, 64, 16, 4, 1, false, 3)        \
   X(128, 256, 16, 4, 0, false, 3)       \
   X(128, 128, 16, 3, 0, true, 3)        \
+  X(128, 128, 16, 6, 0, true, 3)        \
   X(256, 256, 16, 3, 0, false, 3)       \
   X(128, 256, 16, 8, 1, false, 1)       \
   X(128, 64, 32, 4, 1, false, 1)        \

@@ -223,7 +223,8 @@ TC_PLANS = [
     ((1000, 64, 96, 96), (128, 64, 32, 3, 1, 1)),
     ((512, 512, 512, 512), (128, 128, 32, 4, 1, 1)),
     ((2432, 8192, 128, 128), (128, 256, 16, 5, 1, 0)),
-    ((1023, 1025, 777, 777), (128, 128, 16, 3, 0, 1)),
+    ((1023, 1025, 777, 777), (128, 128, 16, 6, 0, 1)),   # A pre-split, under half a wave: 6 stages
+    ((5000, 250, 777, 777), (128, 128, 16, 3, 0, 1)),    # A pre-split, more tiles: 3 stages, 2 CTAs/SM
     ((2432, 8192, 129, 129), (128, 256, 16, 4, 0, 0)),
     ((5120, 8192, 64, 64), (128, 256, 16, 5, 1, 0)),   # many tiles, aligned A: split on chip
     ((5120, 8192, 65, 65), (256, 256, 16, 3, 0, 0)),   # many tiles, A pre-split: 256 x 256
@@ -254,7 +255,7 @@ def test_tf32x3_planner_choices(shape, cfg):
 # Every tensor-core configuration the library is built with, forced through
 # the GEMM_TC_CONFIG knob, on one ragged shape (full check).
 TC_BUILT = ["256,16,5,1,0", "128,32,4,1,1", "64,32,6,1,1", "64,32,3,1,1", "64,32,2,1,0",
-            "64,16,4,1,0", "256,16,4,0,0", "128,16,3,0,1", "256,256,16,3,0,0",
+            "64,16,4,1,0", "256,16,4,0,0", "128,16,3,0,1", "128,16,6,0,1", "256,256,16,3,0,0",
             "256,16,5,2,0", "128,32,4,2,1"]
 
 
