@@ -253,7 +253,12 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
         // every size measured: 8192^3 3.35 vs 3.54 ms, 6144^3 1.44 vs
         // 1.61 ms, 8192 x 4096 x 4096 902 vs 978 us.
         if (N <= 64) {
-          set(64, 32, 3, 1);                   // narrow: 2 CTAs per SM stream A
+          // narrow: 2 CTAs per SM stream A; with few tiles (stream-K) one CTA
+          // per SM with 6 stages halves the partial tiles (GB300, 1024 x 64 x
+          // 8192: 38.2 -> 29.7 us, 2048 x 64 x 4096: 29.6 -> 25.7 us; equal
+          // at 32-64 tiles, 204 against 271 us on 65536 x 64 x 4096)
+          if (4 * ceil_div(M, 128) <= sms) set(64, 32, 6, 1);
+          else set(64, 32, 3, 1);
         } else {
           if (wide) set(256, 16, 5, 0);
           else set(128, 32, 4, 1);

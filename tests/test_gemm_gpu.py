@@ -220,7 +220,8 @@ def test_status_clear_after_normal_runs():
 # The planner's own choice for representative shapes:
 # (M, N, K, lda) -> (bn, bk, stages, A split in kernel, concatenated B)
 TC_PLANS = [
-    ((1000, 64, 96, 96), (128, 64, 32, 3, 1, 1)),
+    ((1000, 64, 96, 96), (128, 64, 32, 6, 1, 1)),       # narrow, few tiles: 6 stages, 1 CTA/SM
+    ((9000, 64, 96, 96), (128, 64, 32, 3, 1, 1)),       # narrow, more tiles: 3 stages, 2 CTAs/SM
     ((512, 512, 512, 512), (128, 128, 32, 4, 1, 1)),
     ((2432, 8192, 128, 128), (128, 256, 16, 5, 1, 0)),
     ((1023, 1025, 777, 777), (128, 128, 16, 6, 0, 1)),   # A pre-split, under half a wave: 6 stages
