@@ -213,7 +213,12 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
       // 128 x 256 tiles once there are at least half a wave of them
       // (GB300, 3xTF32, N = K = 4096: M = 1024 150 us against 195 us with
       // 128 x 128 tiles, M = 2048 266 us against 336 us)
-      const bool wide = N > 128 && tiles256 * 2 >= sms;
+      // and for a long K, where the stream-K CTAs, at unrelated K positions,
+      // stream their operands mostly from HBM and the larger tile moves
+      // fewer bytes per product (1024 x 1024 x 16384: 154 us against 208 us;
+      // at K = 8192 it is a wash: 1024 x 1024 x 8192 80 / 83 us, 512 x 2048
+      // x 8192 130 / 116 us)
+      const bool wide = N > 128 && (tiles256 * 2 >= sms || K >= 16384);
       p.a_split_in_kernel = a_aligned ? 1 : 0;
       p.launches = 2;  // the split pass (A and B in one launch when both are split) and the GEMM
       auto set = [&](int bn, int bk, int st, int cc, int bm = 128) {
@@ -307,16 +312,19 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
       // per tile keep more loads in flight), and otherwise when a time model
       // says it pays.  Model: the tensor pipe of an SM at its dense rate,
       // CTAs sharing an SM sharing it; one CTA per tile takes
-      // ceil(tiles / SMs) tile times, stream-K spreads all K blocks over the
-      // SMs but writes and re-reads one partial tile per part (about G +
-      // shared tiles parts, ~3 TB/s through L2) and launches the fix-up
-      // (~3 us).  GB300 step times, one CTA per tile / stream-K (us), 3xTF32:
+      // ceil(tiles / SMs) tile times (K blocks plus one epilogue), stream-K
+      // spreads all K blocks over the SMs but drains up to two more partial
+      // tiles per CTA, writes and re-reads one partial tile per part (about
+      // G + shared tiles parts, ~6 TB/s, mostly through L2) and launches the
+      // fix-up (~3 us).  GB300 step times, one CTA per tile / stream-K (us), 3xTF32:
       // 1023 x 1025 x 777 (lda 777) 54.7 / 43.5, (lda 780) 37.2 / 28.0,
       // 640^3 18.9 / 17.9, 1024^3 26.3 / 25.2, 256 x 4096 x 4096
       // 105.8 / 85.3, 128 x 128 x 16384 254 / 53, 1536^3 41.0 / 46.4,
       // 2048 x 2048 x 512 34.0 / 40.1, 2048^3 75.7 / 80.1, 3000^3 (lda 3003)
-      // 258 / 284, 2560 x 2560 x 4096 256 / 192, 4096^3 513 / 460; 1xTF32:
-      // 2048^3 74.5 / 64.7, 4096^3 244 / 249.
+      // 258 / 284, 2560 x 2560 x 4096 256 / 192, 4096^3 513 / 460,
+      // 2560 x 2560 x 1024 73.4 / 66.2, 6144 x 6144 x 2048 497 / 482,
+      // 1024 x 4096 x 4096 143 / 169;
+      // 1xTF32: 2048^3 74.5 / 64.7, 4096^3 244 / 249.
       {
         const int64_t tiles = ceil_div(M, p.bm) * ceil_div(N, p.bn);
         const int64_t slots = (int64_t)(p.ctas_per_sm > 0 ? p.ctas_per_sm : 1) * sms;
@@ -331,10 +339,14 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
         const double roof = x3 ? kPlanTf32DenseFlops / 3.0 : kPlanTf32DenseFlops;
         const bool hbm_bound = p.intensity < roof / kPlanHbmBytesPerSec;
         const double t_kb = 2.0 * p.bm * p.bn * p.bk * nprod / (kPlanTf32DenseFlops / (double)sms);
-        const double t_dp = (double)ceil_div(tiles, sms) * (double)nkb * t_kb;
+        // draining one tile of accumulators to global memory (~32 GB/s an SM)
+        const double t_epi = (double)p.bm * p.bn * 4.0 / 32.0e9;
+        const int64_t waves_dp = ceil_div(tiles, sms);
+        const double t_dp = (double)waves_dp * ((double)nkb * t_kb + t_epi);
         const int64_t shared = g > 0 && tiles > g ? tiles % g : tiles;
         const double t_sk = (double)ceil_div(total, sms) * t_kb +
-                            2.0 * (double)(g + shared) * p.bm * p.bn * 4.0 / 3.0e12 + 3.0e-6;
+                            (double)(tiles / (g > 0 ? g : 1) + 2) * t_epi +
+                            2.0 * (double)(g + shared) * p.bm * p.bn * 4.0 / 6.0e12 + 3.0e-6;
         bool want = (tiles % slots) != 0 && tiles < 8 * slots &&
                     (hbm_bound || 2 * tiles <= sms || t_sk < t_dp);
         if (sk) want = std::atoi(sk) != 0;
