@@ -40,14 +40,20 @@ bool mode_known(int mode) {
 // CTA-slices (1/split of the K loop each), in pairs at the full per-SM rate
 // (about 70% of the FP32 peak) and a leftover single CTA at about 60% of
 // it.  A split adds a reduction that reads the slices and writes C once
-// (at ~6 TB/s, plus a launch).
+// (at ~6 TB/s, plus a launch and one L2 round trip per 8 slices).
 double simt_time_estimate(int64_t M, int64_t N, int64_t K, int64_t tiles, int split, int64_t sms,
                           double fp32_peak, const SimtConfig &c) {
   const double rate = 0.7 * fp32_peak / (double)sms;
   const double slice_flops = 2.0 * c.bm * c.bn * (double)K / split;
   const int64_t u = ceil_div(tiles * split, sms);
   double t = (double)(u / 2) * 2.0 * slice_flops / rate + (double)(u % 2) * slice_flops / (0.6 * rate);
-  if (split > 1) t += (split + 1.0) * (double)M * (double)N * 4.0 / 6.0e12 + 2e-6;
+  // the reduction: its traffic, its launch, and for a small C ~0.75 us per
+  // 8 slices (eight chains in flight per thread; fitted on GB300 to the best
+  // slice counts of 32 x 32 x 65536, 64 x 64 x 8192, 128 x 128 x 4096 and
+  // 128 x 128 x 16384)
+  if (split > 1)
+    t += (split + 1.0) * (double)M * (double)N * 4.0 / 6.0e12 + 2e-6 +
+         std::ceil(split / 8.0) * 0.75e-6;
   return t;
 }
 
@@ -56,9 +62,12 @@ void plan_simt(int64_t M, int64_t N, int64_t K, bool vec, const DeviceProps &dp,
   const int64_t sms = dp.sm_count > 0 ? dp.sm_count : 152;
   const SimtConfig c = simt_config();
   const int64_t tiles = ceil_div(M, c.bm) * ceil_div(N, c.bn);
-  // slices of at least 64 along K, at most 16
+  // Slices of at least 64 along K, at most 256: a small output with a long
+  // K needs many slices to occupy the SMs (GB300, 32 x 32 x 65536: 16
+  // slices 238 us, 128 slices 39 us; 64 x 64 x 8192: 37.0 -> 14.7 us), and
+  // the reduction's cost in the estimate keeps large outputs at few slices.
   int64_t max_split = K / 64;
-  if (max_split > 16) max_split = 16;
+  if (max_split > 256) max_split = 256;
   if (max_split < 1) max_split = 1;
   int split = 1;
   double best = simt_time_estimate(M, N, K, tiles, 1, sms, fp32_peak, c);

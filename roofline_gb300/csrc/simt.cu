@@ -301,17 +301,32 @@ simt_packed_kernel(GemmArgs p, int64_t k_per_split, float *__restrict__ ws, int 
   }
 }
 
-// C <- alpha * sum_{z < splits} ws[z] + beta * C, slices summed in order z = 0..splits-1.
+// C <- alpha * sum_{z < splits} ws[z] + beta * C.  Slice z goes to chain
+// z % 8 (each chain summed in z order), then the chains are combined in a
+// fixed tree, so the result does not depend on timing; the eight chains keep
+// eight loads in flight per thread, which matters with many slices and a
+// small C (32 x 32 x 65536 uses 241 slices).
 __global__ void splitk_reduce_kernel(GemmArgs p, const float *__restrict__ ws, int splits) {
   pdl_wait();  // the GEMM's slices
   pdl_trigger();
   const int64_t total = p.M * p.N;
   for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total;
        t += (int64_t)gridDim.x * blockDim.x) {
-    float s = ws[t];
-    for (int z = 1; z < splits; ++z) s += ws[(int64_t)z * total + t];
-    const int64_t r = t / p.N, c = t % p.N;
-    float *dst = p.C + r * p.ldc + c;
+    float c[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    int z = 0;
+    for (; z + 8 <= splits; z += 8) {
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = ws[(int64_t)(z + u) * total + t];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) c[u] += v[u];
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (z + u < splits) c[u] += ws[(int64_t)(z + u) * total + t];
+    const float s = ((c[0] + c[1]) + (c[2] + c[3])) + ((c[4] + c[5]) + (c[6] + c[7]));
+    const int64_t r = t / p.N, col = t % p.N;
+    float *dst = p.C + r * p.ldc + col;
     float o = p.alpha * s;
     if (p.beta != 0.0f) o = fmaf(p.beta, *dst, o);
     *dst = o;
