@@ -148,8 +148,14 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
     // 20.6 / 19.8, 640^3 22.4 / 17.3, 1023 x 1025 x 777 55.4 / 29.3, 1024^3
     // 61.9 / 26.0, 2048 x 2048 x 512 100.5 / 32.0, 4096 x 64 x 4096
     // 100.5 / 33.3; 4096^2 x 64 71.8 / 75.8, 1024^2 x 128 14.4 / 15.9,
-    // 64 x 4096 x 4096 53.3 / 65.2.
-    const bool big = (double)M * N * K >= 2.0e8 && K >= 128 && M >= 128;
+    // 64 x 4096 x 4096 53.3 / 65.2.  A tiny C (at most 256 x 256) with K up
+    // to 16384 stays on the CUDA cores too: split K across ~70 slices there
+    // fills the SMs where stream-K has only a few tiles to share (128 x 128 x
+    // 16384 22.6 / 51.2, 256 x 256 x 4096 18.6 / 32.9, 128 x 512 x 8192
+    // 28.8 / 42.9; 128 x 1024 x 8192 47.3 / 43.0, 256 x 256 x 65536
+    // 172 / 123).
+    const bool tiny_c = (double)M * (double)N <= 65536.0 && K <= 16384;
+    const bool big = (double)M * N * K >= 2.0e8 && K >= 128 && M >= 128 && !tiny_c;
     resolved = (tc_supported(dp) && big && tc_shape_fits(M, N, K)) ? GEMM_MODE_TF32X3
                                                          : GEMM_MODE_FP32_SIMT;
   }

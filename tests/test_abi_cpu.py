@@ -165,11 +165,14 @@ def test_stream_k_plan_bounds(lib):
 
 def test_auto_choice(lib):
     """AUTO takes the tensor cores once a problem amortises the split pass
-    (about 2e8 multiply-adds), with K >= 128 and M >= 128."""
+    (about 2e8 multiply-adds), with K >= 128, M >= 128 and a C larger than
+    256 x 256 (or K > 16384)."""
     tc = [(1023, 1025, 777, 777, 1025, 1025), (640, 640, 640), (1024, 1024, 1024),
-          (2048, 2048, 512), (4096, 64, 4096), (512, 512, 1024), (128, 2048, 1024)]
+          (2048, 2048, 512), (4096, 64, 4096), (512, 512, 1024), (128, 2048, 1024),
+          (128, 1024, 8192), (256, 256, 65536)]
     simt = [(512, 512, 512), (576, 576, 576), (4096, 4096, 64), (8192, 8192, 32),
-            (64, 4096, 4096), (1024, 1024, 128), (300, 300, 2000)]
+            (64, 4096, 4096), (1024, 1024, 128), (300, 300, 2000), (128, 128, 16384),
+            (256, 256, 4096), (128, 512, 8192)]
     for shape in tc:
         assert gemm.plan(*shape)["kernel_name"] == "tc_tf32x3", shape
     for shape in simt:
