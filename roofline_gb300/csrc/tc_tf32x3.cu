@@ -758,7 +758,12 @@ bool tc_config_valid(int bm, int bn, int bk, int stages, int a_inkernel, int con
   return false;
 }
 
-// CTAs of one configuration that fit on an SM (shared memory and TMEM).
+// Every configuration needs more than 113 registers a thread (134-156), so
+// at most two CTAs of 192 threads share an SM's 65536 registers.
+constexpr int kMaxCtasPerSm = 2;
+
+// CTAs of one configuration that fit on an SM (shared memory, TMEM and
+// registers).
 int tc_ctas_per_sm(int bm, int bn, int bk, int stages, int a_inkernel, int concat, int nprod,
                    int smem_per_sm) {
 #define GG_OCC(BM_, BN_, BK_, ST_, AK_, CC_, NP_)              \
@@ -766,7 +771,8 @@ int tc_ctas_per_sm(int bm, int bn, int bk, int stages, int a_inkernel, int conca
     using C = TcCfg<BM_, BN_, BK_, ST_, AK_, CC_, NP_>;         \
     int by_smem = smem_per_sm / (C::SMEM_BYTES + 1024);         \
     int by_tmem = 512 / C::TMEM_COLS;                           \
-    return by_smem < by_tmem ? by_smem : by_tmem;               \
+    int n = by_smem < by_tmem ? by_smem : by_tmem;              \
+    return n < kMaxCtasPerSm ? n : kMaxCtasPerSm;               \
   }
   GG_TC_CONFIGS(GG_OCC)
 #undef GG_OCC
