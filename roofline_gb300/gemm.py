@@ -290,10 +290,15 @@ def _operand(t, name):
     import torch
     if not (t.is_cuda and t.dtype == torch.float32 and t.dim() == 2):
         raise ValueError(f"{name} must be a 2-D float32 CUDA tensor")
+    # A stride along a dimension of length 1 is never used (torch may report
+    # any value there), so the leading dimension is then at least the row
+    # length of the stored matrix.
     if t.stride(1) == 1 or t.shape[1] <= 1:
-        return OP_N, max(t.stride(0), 1)
+        ld = t.stride(0) if t.shape[0] > 1 else max(t.stride(0), t.shape[1])
+        return OP_N, max(ld, 1)
     if t.stride(0) == 1 or t.shape[0] <= 1:
-        return OP_T, max(t.stride(1), 1)
+        ld = t.stride(1) if t.shape[1] > 1 else max(t.stride(1), t.shape[0])
+        return OP_T, max(ld, 1)
     raise ValueError(f"{name} must have a unit row or column stride")
 
 
@@ -346,7 +351,9 @@ def _host_matrix(t, name):
     if not (t.device.type == "cpu" and t.dtype == torch.float32 and t.dim() == 2 and
             (t.stride(1) == 1 or t.shape[1] <= 1)):
         raise ValueError(f"{name} must be a 2-D float32 CPU tensor with unit column stride")
-    return max(t.stride(0), 1)
+    # the row stride of a one-row matrix is never used (torch may report any value)
+    ld = t.stride(0) if t.shape[0] > 1 else max(t.stride(0), t.shape[1])
+    return max(ld, 1)
 
 
 def matmul_host(A, B, C=None, alpha=1.0, beta=0.0, mode=MODE_AUTO, blocks=0):

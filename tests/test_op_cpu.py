@@ -107,3 +107,34 @@ def test_empty_and_no_device(lib):
         rc = gemm.gemm_f32_op(COL, T_, N_, 4, 4, 4, 1.0, 256, 4, 256, 4, 0.0, 256, 4, 1,
                               None, 0, 0)
         assert rc == gemm.ERR_NO_DEVICE
+
+
+class _View:
+    """Shape and strides of a 2-D float32 CUDA tensor, for the binding's
+    operand classification (no device needed)."""
+
+    def __init__(self, shape, strides):
+        import torch
+        self.shape, self._strides = shape, strides
+        self.is_cuda, self.dtype = True, torch.float32
+
+    def stride(self, i):
+        return self._strides[i]
+
+    def dim(self):
+        return 2
+
+
+@pytest.mark.parametrize("shape,strides,want", [
+    ((5, 7), (7, 1), (gemm.OP_N, 7)),       # row-major rows of 7
+    ((5, 7), (9, 1), (gemm.OP_N, 9)),       # row slice of a wider buffer
+    ((7, 5), (1, 7), (gemm.OP_T, 7)),       # transposed view X.t()
+    ((1, 449), (1, 1), (gemm.OP_N, 449)),   # one row: its row stride is never used
+    ((1, 449), (3, 1), (gemm.OP_N, 449)),
+    ((449, 1), (1, 1), (gemm.OP_N, 1)),     # one column
+    ((449, 1), (1, 3), (gemm.OP_N, 1)),
+    ((1, 1), (1, 1), (gemm.OP_N, 1)),
+])
+def test_operand_leading_dimension(shape, strides, want):
+    assert gemm._operand(_View(shape, strides), "X") == want
+

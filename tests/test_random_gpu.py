@@ -84,3 +84,28 @@ def test_cases_cover_every_mode_and_layout():
     assert {c[7] for c in cases} == {False, True} and {c[8] for c in cases} == {False, True}
     assert {c[5] == 0.0 for c in cases} == {False, True}
     assert any(max(c[0], c[1], c[2]) >= 640 for c in cases)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("shape", [(1, 99, 449), (77, 1, 300), (1, 1, 513), (200, 150, 1),
+                                   (1, 300, 1)], ids=lambda v: "x".join(map(str, v)))
+@pytest.mark.parametrize("ta", [False, True])
+@pytest.mark.parametrize("tb", [False, True])
+@pytest.mark.parametrize("mode", ["fp32_simt", "tf32x3", "auto"])
+def test_single_row_or_column_operands(shape, ta, tb, mode):
+    """Operands with one row or one column, stored either way: torch reports
+    arbitrary strides along a length-1 dimension, which the binding must not
+    take for a leading dimension (a 1 x 449 transposed view has row stride 1)."""
+    import torch
+    from roofline_gb300 import gemm
+    M, N, K = shape
+    A = matrix(K, M, None, 61, "u11") if ta else matrix(M, K, None, 61, "u11")
+    B = matrix(N, K, None, 62, "u11") if tb else matrix(K, N, None, 62, "u11")
+    dA = torch.from_numpy(A).cuda()
+    dB = torch.from_numpy(B).cuda()
+    dA, dB = (dA.t() if ta else dA), (dB.t() if tb else dB)
+    C = gemm.matmul(dA, dB, mode=mode)
+    torch.cuda.synchronize()
+    ref, D = oracle.gemm(_dense(A.T if ta else A), _dense(B.T if tb else B), with_bound=True)
+    assert oracle.err_normalised(C.cpu().numpy(), ref, D) <= TOL_E1
+
