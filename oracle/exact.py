@@ -50,7 +50,7 @@ def gemm_exact(A, B, alpha=1.0, beta=0.0, C0=None, M=None, N=None, K=None):
         for j in range(N):
             s = Fraction(0)
             sa = Fraction(0)
-            for k in range(K):
+            for k in range(K if alpha != 0.0 else 0):  # alpha == 0: A, B not read
                 p = Fraction(float(A[i, k])) * Fraction(float(B[k, j]))
                 s += p
                 sa += abs(p)

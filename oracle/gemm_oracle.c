@@ -18,7 +18,8 @@
  * float), generalised from N x N to M x N x K, leading dimensions, and the
  * alpha/beta scaling of the cuBLAS SGEMM call in section "Stage 3 - the
  * reference ceiling: cuBLAS".  When beta == 0, C_old is not read (BLAS
- * convention), so NaN in C_old does not propagate.
+ * convention), so NaN in C_old does not propagate; likewise when alpha == 0
+ * A and B are not read (S is taken as 0), so C_ref = float_rn(beta * C_old).
  *
  * Each product of two floats is exact in double (24 + 24 < 53 significand
  * bits); the only roundings are the double additions, the alpha/beta
@@ -45,6 +46,7 @@ static float oracle_entry(int64_t i, int64_t j, int64_t K, double alpha,
                           int64_t ldc, double *bound) {
   double s = 0.0, sa = 0.0;
   const float *a = A + i * lda;
+  if (alpha == 0.0) K = 0; /* A and B are not read */
   for (int64_t k = 0; k < K; ++k) {
     double p = (double)a[k] * (double)B[k * ldb + j];
     s += p;

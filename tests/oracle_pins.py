@@ -112,6 +112,22 @@ def check_beta_zero_ignores_c(orc):
     return [] if np.all(np.isfinite(got)) else ["beta=0 read C_old (NaN propagated)"]
 
 
+def check_alpha_zero_ignores_ab(orc):
+    """BLAS reading of alpha == 0 (as of beta == 0): A and B are not read, so
+    C = float_rn(beta * C_old) exactly (a product of two floats rounds once),
+    and beta == 0 gives zeros, even with NaN in A and B."""
+    A = np.full((4, 3), np.nan, dtype=np.float32)
+    B = np.full((3, 5), np.inf, dtype=np.float32)
+    C0 = matrix(4, 5, None, 602, "u11")
+    fails = []
+    got = orc.gemm(A, B, alpha=0.0, beta=-1.5, C0=C0)
+    if not np.array_equal(got, np.float32(-1.5) * C0):
+        fails.append("alpha=0 read A or B, or did not give beta*C_old")
+    if not np.array_equal(orc.gemm(A, B, alpha=0.0, beta=0.0, C0=C0), np.zeros((4, 5), np.float32)):
+        fails.append("alpha=0, beta=0 did not give zeros")
+    return fails
+
+
 def check_numpy_f64_512(orc):
     A = matrix(512, 512, None, 700, "u11")
     B = matrix(512, 512, None, 701, "u11")
@@ -143,7 +159,8 @@ def check_entries_match_full(orc):
 
 
 ALL = [check_identity, check_all_ones, check_rank1, check_integer_bruteforce,
-       check_rational_bruteforce, check_beta_zero_ignores_c, check_numpy_f64_512,
+       check_rational_bruteforce, check_beta_zero_ignores_c, check_alpha_zero_ignores_ab,
+       check_numpy_f64_512,
        check_entries_match_full]
 
 

@@ -108,6 +108,7 @@ MUTANTS = {
     "float_accumulator": ("double s = 0.0, sa = 0.0;", "float s = 0.0f; double sa = 0.0;"),
     "bound_without_beta": ("d += fabs(beta) * fabs(c);", "(void)d;"),
     "reads_c_when_beta_zero": ("if (beta != 0.0) {", "if (Cin) {"),
+    "reads_ab_when_alpha_zero": ("if (alpha == 0.0) K = 0;", ";"),
 }
 
 _RUNNER = r"""
