@@ -79,7 +79,7 @@ extern "C" {
 
 /* kernel identifiers reported by gemm_f32_plan */
 #define GEMM_KERNEL_NONE 0          /* nothing to launch (M or N is 0) */
-#define GEMM_KERNEL_SCALE 1         /* K == 0: C <- beta*C only */
+#define GEMM_KERNEL_SCALE 1         /* K == 0 (or a call with alpha == 0): C <- beta*C only */
 #define GEMM_KERNEL_NAIVE 2
 #define GEMM_KERNEL_COALESCED 3
 #define GEMM_KERNEL_TILED 4
@@ -153,7 +153,9 @@ GEMM_API int gemm_f32(int64_t M, int64_t N, int64_t K, const float *A, int64_t l
 
 /*
  * gemm_f32_ex -- C <- alpha * A * B + beta * C (BLAS semantics).
- * When beta == 0, C is not read (NaN/Inf in C do not propagate).
+ * When beta == 0, C is not read (NaN/Inf in C do not propagate); when
+ * alpha == 0, A and B are not read and C <- beta * C (one scaling kernel;
+ * gemm_f32_plan describes the alpha != 0 call).
  * workspace/ws_bytes: device scratch of at least plan.workspace_bytes
  * (gemm_f32_plan), 256-byte aligned, owned by the caller and not used by
  * any other work in flight on the GPU during this call.  workspace == NULL

@@ -176,6 +176,7 @@ extern "C" int gemm_f32_host(int64_t M, int64_t N, int64_t K, float alpha, const
   if (st == GEMM_ERR_INVALID_ARG) return st;
   if (M == 0 || N == 0) return GEMM_OK;
   if (!C || (K > 0 && (!A || !B))) return GEMM_ERR_INVALID_ARG;
+  if (alpha == 0.0f) K = 0;  // BLAS: A and B are not read, C <- beta * C
 
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) {

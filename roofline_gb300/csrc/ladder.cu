@@ -14,7 +14,7 @@ __device__ __forceinline__ void store_out(const GemmArgs &p, int64_t r, int64_t 
   *dst = v;
 }
 
-// K == 0: C <- beta*C (beta == 0 writes zeros without reading C).
+// K == 0 or alpha == 0: C <- beta*C (beta == 0 writes zeros without reading C).
 __global__ void scale_kernel(GemmArgs p) {
   int64_t total = p.M * p.N;
   for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total;

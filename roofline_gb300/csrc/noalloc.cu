@@ -69,7 +69,9 @@ extern "C" int gemm_f32_splitk_noalloc(int64_t M, int64_t N, int64_t K, float al
   if (dev < 0 || dev >= kMaxDev) return GEMM_ERR_UNSUPPORTED;
   const DeviceProps &dp = props_of(dev);
   GemmArgs p{M, N, K, alpha, beta, A, lda, B, ldb, C, ldc};
-  if (K == 0) return launch_scale(p, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+  // K == 0, or alpha == 0 (BLAS: A and B are not read): C <- beta * C
+  if (K == 0 || alpha == 0.0f)
+    return launch_scale(p, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 
   gemm_plan_t plan;
   int st = make_plan(M, N, K, lda, ldb, ldc, GEMM_MODE_FP32_SIMT,

@@ -505,3 +505,32 @@ def test_extreme_shapes_sampled(shape, mode):
     ref, _ = oracle.gemm_entries(A, B, rows, cols, 1.0, 0.0, None)
     got = C.cpu().numpy()[rows, cols]
     assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("mode", ["fp32_simt", "tf32x3", "tf32", "auto", "tiled16"])
+@pytest.mark.parametrize("beta", [0.0, -1.5])
+def test_alpha_zero_reads_neither_a_nor_b(mode, beta):
+    """BLAS semantics of alpha == 0: A and B are not read (NaN and Inf there
+    do not reach C) and C <- beta * C, bit for bit with the oracle."""
+    import torch
+    from roofline_gb300 import gemm
+    M, N, K = 300, 200, 129
+    A = np.full((M, K), np.nan, dtype=np.float32)
+    B = np.full((K, N), np.inf, dtype=np.float32)
+    C0 = matrix(M, N, None, 77, "u11")
+    want = oracle.gemm(A, B, 0.0, beta, C0)
+    dC = torch.from_numpy(C0.copy()).cuda()
+    gemm.matmul(torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda(), dC, 0.0, beta, mode)
+    torch.cuda.synchronize()
+    assert np.array_equal(dC.cpu().numpy(), want)
+    # host buffers, and the no-allocation split-K entry point
+    hC = torch.from_numpy(C0.copy())
+    gemm.matmul_host(torch.from_numpy(A), torch.from_numpy(B), hC, 0.0, beta, mode)
+    assert np.array_equal(hC.numpy(), want)
+    dC = torch.from_numpy(C0.copy()).cuda()
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    rc = gemm.gemm_f32_splitk_noalloc(M, N, K, 0.0, dA.data_ptr(), K, dB.data_ptr(), N, beta,
+                                      dC.data_ptr(), N)
+    torch.cuda.synchronize()
+    assert rc == gemm.OK and np.array_equal(dC.cpu().numpy(), want)
+
