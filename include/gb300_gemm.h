@@ -64,7 +64,10 @@ extern "C" {
  * accuracy; not bitwise equal to FP32_SIMT).  TF32 is one TF32 MMA per
  * product (operands rounded to TF32, 11 significant bits; FP32
  * accumulation): about three times the 3xTF32 rate, TF32-accurate only
- * (error up to about 2^-10 of sum |A||B|).  The remaining modes are the
+ * (error up to about 2^-10 of sum |A||B|).  Non-finite inputs: NaN
+ * propagates in every mode; an Inf gives the IEEE +-Inf on the CUDA cores
+ * but NaN in the TF32 modes (the split puts Inf against a zero part of the
+ * other operand, and Inf * 0 = NaN).  The remaining modes are the
  * course page's ladder kernels ("Stage 0" naive with x -> row, "Stage 1"
  * coalesced with x -> column, "Stage 2" shared-memory tiles of 16 or 32),
  * kept for comparison. */

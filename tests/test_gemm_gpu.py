@@ -534,3 +534,33 @@ def test_alpha_zero_reads_neither_a_nor_b(mode, beta):
     torch.cuda.synchronize()
     assert rc == gemm.OK and np.array_equal(dC.cpu().numpy(), want)
 
+
+@pytest.mark.parametrize("mode", ["fp32_simt", "tf32x3", "tf32", "auto"])
+def test_non_finite_inputs(mode):
+    """A NaN in A makes its row of C NaN in every mode.  An Inf in A gives the
+    oracle's +-Inf row on the CUDA cores; the TF32 split modes give NaN there
+    (tf32(Inf) = Inf, and the Inf meets a zero part of the other operand in a
+    cross product, Inf * 0 = NaN).  Every other row stays within tolerance."""
+    import torch
+    from roofline_gb300 import gemm
+    M, N, K = 260, 300, 200
+    A = matrix(M, K, None, 81, "u11")
+    B = matrix(K, N, None, 82, "u11")
+    A[3, 17] = np.nan
+    A[200, 5] = np.inf
+    C = gemm.matmul(torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda(), mode=mode)
+    torch.cuda.synchronize()
+    got = C.cpu().numpy()
+    ref = oracle.gemm(A, B)
+    assert np.all(np.isnan(got[3]))
+    if mode == "fp32_simt":
+        assert np.array_equal(got[200], ref[200])  # +-Inf, signs from B
+    else:
+        assert np.all(~np.isfinite(got[200]))
+    rest = np.ones(M, bool)
+    rest[[3, 200]] = False
+    Af = A[rest]
+    ref_r, D = oracle.gemm(Af, B, with_bound=True)
+    tol = 2e-3 if mode == "tf32" else TOL_E1
+    assert oracle.err_normalised(got[rest], ref_r, D) <= tol
+
