@@ -1,6 +1,6 @@
-"""Seeded random parity sweep: shapes, padded leading dimensions, alpha/beta,
-storage order of each operand, mode and the stream-K switch drawn from a
-fixed-seed generator, each case checked against the oracle (normalised error
+"""Seeded random parity sweep: shapes, padded leading dimensions, base
+offsets, alpha/beta, storage order of each operand, mode and the stream-K
+switch drawn from a fixed-seed generator, each case checked against the oracle (normalised error
 for the FP32 and 3xTF32 modes, the TF32 bound for 1xTF32) with C's padding
 columns left untouched."""
 import numpy as np
@@ -64,6 +64,18 @@ def test_random_case(i, monkeypatch):
         dB = torch.from_numpy(Bs).cuda()[:, :N]
     Cs = matrix(M, N, N + pads[2], seed + 2, "u11")
     dCs = torch.from_numpy(Cs).cuda()
+    # each operand at a random float offset inside a larger buffer, so base
+    # addresses are 4-byte aligned only (no TMA on the operand itself)
+    offs = [int(x) for x in np.random.default_rng(999 + i).integers(0, 4, size=3)]
+
+    def shift(t, off):
+        buf = torch.empty(t.numel() + 8, dtype=torch.float32, device="cuda")
+        buf[off:off + t.numel()] = t.reshape(-1)
+        return buf[off:off + t.numel()].view(t.shape)
+    dA = shift(dAs, offs[0])[:, :M].t() if ta else shift(torch.from_numpy(As).cuda(), offs[0])[:, :K]
+    dB = (shift(torch.from_numpy(Bt).cuda(), offs[1])[:, :K].t() if tb
+          else shift(torch.from_numpy(Bs).cuda(), offs[1])[:, :N])
+    dCs = shift(dCs, offs[2])
     gemm.matmul(dA, dB, dCs[:, :N], alpha, beta, mode)
     torch.cuda.synchronize()
     out = dCs.cpu().numpy()
