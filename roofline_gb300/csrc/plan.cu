@@ -248,11 +248,14 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
         // Narrow B (HBM-bound on A): 128-row tiles with A split on chip, so A
         // is read once.  Wide: 256 x 256 tiles (GB300: 4096^3 kernel 176 us
         // against 241 us with 128 x 256 tiles, 8192^3 1.15 ms against
-        // 1.87 ms).  Otherwise 128 x 256 tiles, pre-split (the on-chip split
-        // is the slower stage with a single MMA per K step).
+        // 1.87 ms) once there are half a wave of them; fewer go to 128 x 256
+        // tiles (2048^3: 48.6 us against 60.1 us for 64 tiles of 256 x 256
+        // shared out stream-K).  Otherwise 128 x 256 tiles, pre-split (the
+        // on-chip split is the slower stage with a single MMA per K step:
+        // 4096^3 380 us against 277 us).
         if (a_aligned && N <= 64) {
           set(64, 32, 4, 0);
-        } else if (wide) {
+        } else if (wide && 2 * tiles_m2 >= sms) {
           set(256, 32, 3, 0, 256);
           pre_split();
         } else {

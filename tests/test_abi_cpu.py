@@ -216,7 +216,10 @@ def test_stream_k_choice(lib):
     assert gemm.plan(2560, 2560, 4096, mode="tf32x3")["stream_k"] == 1
     assert gemm.plan(1023, 1025, 777, 777, 1025, 1025, mode="tf32x3")["stream_k"] == 1
     assert gemm.plan(1024, 1024, 1024, mode="tf32x3")["stream_k"] == 1
-    assert gemm.plan(2048, 2048, 2048, mode="tf32")["stream_k"] == 1
+    # 1xTF32 2048^3: 64 tiles of 256 x 256 are under half a wave, so 128 x 256
+    # tiles, one CTA each (48.6 us against 60.1 us stream-K on 256 x 256)
+    p = gemm.plan(2048, 2048, 2048, mode="tf32")
+    assert (p["bm"], p["bn"], p["stream_k"]) == (128, 256, 0)
     for shape in [(1536, 1536, 1536), (2048, 2048, 512), (2048, 2048, 2048),
                   (3000, 3000, 3000, 3003, 3000, 3000)]:
         assert gemm.plan(*shape, mode="tf32x3")["stream_k"] == 0, shape
