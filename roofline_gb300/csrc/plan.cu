@@ -256,7 +256,12 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
         if (a_aligned && N <= 64) {
           set(64, 32, 4, 0);
         } else if (wide && 2 * tiles_m2 >= sms) {
-          set(256, 32, 3, 0, 256);
+          // BK = 16 with 6 stages is 1-3 % ahead of BK = 32 with 3 for K up
+          // to ~6144 (4096^3 212-218 against 217-225 us, 8192 x 8192 x 2048
+          // 382 against 392 us, 6144^3 equal), 10 % behind at 8192^3 (1468
+          // against 1337 us)
+          if (K >= 8192) set(256, 32, 3, 0, 256);
+          else set(256, 16, 6, 0, 256);
           pre_split();
         } else {
           set(256, 16, 8, 0);
@@ -365,8 +370,11 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
         const double t_sk = (double)ceil_div(total, sms) * t_kb +
                             (double)(tiles / (g > 0 ? g : 1) + 2) * t_epi +
                             2.0 * (double)(g + shared) * p.bm * p.bn * 4.0 / 6.0e12 + 3.0e-6;
+        // (the half-a-wave shortcut is measured for 3xTF32; with a third of
+        // the MMA work per tile, 1xTF32 follows the model: 1024^3 one CTA per
+        // tile 25.6 us against 27.1 us, 1024 x 1024 x 4096 stream-K)
         bool want = (tiles % slots) != 0 && tiles < 8 * slots &&
-                    (hbm_bound || 2 * tiles <= sms || t_sk < t_dp);
+                    (hbm_bound || (x3 && 2 * tiles <= sms) || t_sk < t_dp);
         if (sk) want = std::atoi(sk) != 0;
         p.stream_k = (want && g >= 2) ? 1 : 0;
         p.grid_ctas = p.stream_k ? g : tiles;

@@ -186,7 +186,9 @@ def test_tf32_mode_plans(lib):
     assert p["a_split_in_kernel"] == 0 and p["launches"] == 2 + p["stream_k"]
     extra = p["grid_ctas"] * 2 * p["bm"] * p["bn"] * 4 if p["stream_k"] else 0
     assert p["workspace_bytes"] == 2 * 4096 * 4096 * 4 + extra
-    assert (p["bm"], p["bn"], p["bk"]) == (256, 256, 32)  # wide: 256 x 256 tiles
+    assert (p["bm"], p["bn"], p["bk"]) == (256, 256, 16)  # wide: 256 x 256 tiles
+    big = gemm.plan(8192, 8192, 8192, mode="tf32")
+    assert (big["bm"], big["bn"], big["bk"], big["stages"]) == (256, 256, 32, 3)  # long K
     s = gemm.plan(65536, 64, 4096, mode="tf32")
     assert s["bound_name"] == "hbm" and s["ctas_per_sm"] == 2 and s["a_split_in_kernel"] == 1
     assert gemm.plan(64, 64, 64, mode="tf32")["mode"] == gemm.MODE_TF32
