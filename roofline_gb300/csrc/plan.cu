@@ -233,7 +233,12 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
       // fewer bytes per product (1024 x 1024 x 16384: 154 us against 208 us;
       // at K = 8192 it is a wash: 1024 x 1024 x 8192 80 / 83 us, 512 x 2048
       // x 8192 130 / 116 us)
-      const bool wide = N > 128 && (tiles256 * 2 >= sms || K >= 16384);
+      // ... unless 256-column tiles would cover N with more than 1.25x the
+      // columns 128-column tiles do (8192 x 384 x 8192: 512 columns of MMA
+      // work for 384, 206 us against 185 us; 6144 x 640 x 2048 at 1.2x still
+      // prefers the wide tile, 70.0 against 72.8 us).
+      const bool wide = N > 128 && (tiles256 * 2 >= sms || K >= 16384) &&
+                        4 * ceil_div(N, 256) * 256 <= 5 * ceil_div(N, 128) * 128;
       p.a_split_in_kernel = a_aligned ? 1 : 0;
       p.launches = 2;  // the split pass (A and B in one launch when both are split) and the GEMM
       auto set = [&](int bn, int bk, int st, int cc, int bm = 128) {
