@@ -564,3 +564,35 @@ def test_non_finite_inputs(mode):
     tol = 2e-3 if mode == "tf32" else TOL_E1
     assert oracle.err_normalised(got[rest], ref_r, D) <= tol
 
+
+@pytest.mark.parametrize("mode,shape", [("tf32x3", (1000, 900, 700)), ("fp32_simt", (300, 260, 2000)),
+                                        ("auto", (1023, 1025, 777))])
+def test_concurrent_streams_with_own_workspaces(mode, shape):
+    """Calls running at the same time on two streams, each with its own
+    workspace (split planes, stream-K partial tiles, split-K slices), do not
+    disturb each other: integer inputs give exact results on both."""
+    import torch
+    from roofline_gb300 import gemm
+    M, N, K = shape
+    p = gemm.plan(M, N, K, mode=mode)
+    jobs = []
+    for seed in (11, 12):
+        A = matrix(M, K, None, seed, "int2")
+        B = matrix(K, N, None, seed + 100, "int2")
+        ws = torch.empty(max(p["workspace_bytes"], 256), dtype=torch.uint8, device="cuda")
+        jobs.append((torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda(), ws,
+                     oracle.gemm(A, B), torch.cuda.Stream()))
+    torch.cuda.synchronize()
+    outs = [[], []]
+    for rep in range(6):
+        for i, (dA, dB, ws, _, st) in enumerate(jobs):
+            with torch.cuda.stream(st):
+                C = torch.empty(M, N, device="cuda")
+                gemm.matmul(dA, dB, C, 1.0, 0.0, mode, stream=st, workspace=ws)
+                outs[i].append(C)
+    torch.cuda.synchronize()
+    for i in range(2):
+        for C in outs[i]:
+            assert oracle.mismatches(C.cpu().numpy(), jobs[i][3]) == 0
+    assert gemm.check_status() == gemm.OK
+
