@@ -164,20 +164,72 @@ def source_hash(paths):
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel_key: str):
-    """DRAM bytes per launch from the committed ncu summary, or None when the
-    kernel's source changed after the counters were taken."""
+# Sources whose change invalidates a kernel's recorded DRAM counters: the
+# kernel itself, what it includes, and the planner that picks its launch.
+TRAFFIC_SOURCES = {
+    "tc": ["roofline_gb300/csrc/tc_tf32x3.cu", "roofline_gb300/csrc/tc_common.cuh",
+           "roofline_gb300/csrc/common.cuh", "roofline_gb300/csrc/plan.cu"],
+    "simt": ["roofline_gb300/csrc/simt.cu", "roofline_gb300/csrc/common.cuh",
+             "roofline_gb300/csrc/plan.cu"],
+}
+
+
+def kernel_instance(plan) -> str:
+    """The template instantiation and launch shape a plan runs, e.g.
+    ``tc_tf32x3_kernel<128,256,16,5,2,0,3> grid=152 stream_k=1``."""
+    k = plan["kernel_name"]
+    if k in ("tc_tf32x3", "tc_tf32"):
+        ak = 0 if not plan["a_split_in_kernel"] else (2 if plan["a_hi_tmem"] else 1)
+        nprod = 1 if k == "tc_tf32" else 3
+        inst = (f"tc_tf32x3_kernel<{plan['bm']},{plan['bn']},{plan['bk']},{plan['stages']},"
+                f"{ak},{int(plan['b_concat'])},{nprod}>")
+    elif k == "simt":
+        inst = (f"simt_packed_kernel<{plan['bm']},{plan['bn']},{plan['bk']},{plan['stages']},"
+                f"{int(plan['vec'])},0,0>")
+    else:
+        inst = k
+    return f"{inst} grid={plan['grid_ctas']} split_k={plan['split_k']} stream_k={plan['stream_k']}"
+
+
+def ncu_traffic(plan, workload: str):
+    """DRAM bytes per launch of exactly this instantiation and launch shape on
+    this workload, from the committed ncu summaries, or None when absent or
+    when a source it depends on changed after the counters were taken."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
+    key = f"{kernel_instance(plan)} @ {workload}"
     try:
         with open(path) as f:
             d = json.load(f)
-        e = d[kernel_key]
-        if e.get("source_hash") != source_hash(e["sources"]):
-            return None, "stale"
-        return float(e["dram_bytes_per_launch"]), e.get("note", "")
     except Exception:
-        return None, "absent"
+        return None, f"no profiles/traffic.json entry for {key}"
+    e = d.get(key)
+    if e is None:
+        return None, f"no profiles/traffic.json entry for {key}"
+    if e.get("source_hash") != source_hash(e["sources"]):
+        return None, f"stale: sources of {key} changed after the capture"
+    return float(e["dram_bytes_per_launch"]), e.get("note", "")
 
+
+class Stamps:
+    """Device int64 pairs for gemm_set_profile_stamps: pair i receives the
+    earliest start and latest end (GPU %globaltimer, ns) of the main kernel
+    of the call made while it was set."""
+
+    def __init__(self, n, dev):
+        import torch
+        self.t = torch.empty((n, 2), dtype=torch.int64, device=dev)
+        self.reset()
+
+    def reset(self):
+        self.t[:, 0] = -1  # all ones: the atomic minimum's identity
+        self.t[:, 1] = 0
+
+    def ptr(self, i):
+        return self.t.data_ptr() + 16 * i
+
+    def ms(self, n=None):
+        v = self.t[:n].cpu().numpy().view("uint64").astype("float64")
+        return [(e - b) * 1e-6 for b, e in v]
 
 
 # --------------------------------------------------------------- oracle timing
@@ -258,12 +310,76 @@ def run_reference(args):
 
 # --------------------------------------------------------------- our arm
 
+# Main-kernel durations averaged for each roofline entry (at least this many
+# launches whatever --steps is).
+KERNEL_SAMPLES = 50
+
+
 def workload_config(w, mode, rotation):
     cfg = {"workload": f"{w.name}: {w.description}", "M": w.M, "N": w.N, "K": w.K,
            "alpha": w.alpha, "beta": w.beta, "layout": "row-major", "mode": mode}
     if rotation is not None:
         cfg["l2"] = rotation
     return cfg
+
+
+class Caller:
+    """One library call per step on rotating device input sets, through the
+    C ABI with the pointers and stream resolved once (gemm_f32_ex)."""
+
+    def __init__(self, w, mode, sets):
+        import torch
+
+        from roofline_gb300 import gemm
+        self.gemm = gemm
+        self.lib = gemm.load()
+        self.w = w
+        self.mode = gemm._mode(mode)
+        lda, ldb, ldc = w.lds()
+        self.args = [(a.data_ptr(), b.data_ptr(), c.data_ptr()) for a, b, c in sets]
+        self.lds = (lda, ldb, ldc)
+        self.stream = torch.cuda.current_stream()
+        self.handle = self.stream.cuda_stream
+
+    def __call__(self, i):
+        a, b, c = self.args[i % len(self.args)]
+        lda, ldb, ldc = self.lds
+        w = self.w
+        rc = self.lib.gemm_f32_ex(w.M, w.N, w.K, w.alpha, a, lda, b, ldb, w.beta, c, ldc,
+                                  self.mode, None, 0, self.handle)
+        if rc != 0:
+            raise self.gemm.GemmError(rc, "gemm_f32_ex")
+
+
+def stamped_run(call, stamps, first, count):
+    """Calls first .. first+count-1, main kernel of call i stamped into pair i."""
+    from roofline_gb300 import gemm
+    lib = gemm.load()
+    for i in range(first, first + count):
+        lib.gemm_set_profile_stamps(stamps.ptr(i))
+        call(i)
+    lib.gemm_set_profile_stamps(None)
+
+
+def event_kernel_ms(call, n):
+    """Cross-check in another launch mode: CUDA events recorded by the library
+    around the main kernel (which puts that kernel in plain stream order),
+    mean over n calls."""
+    import torch
+
+    from roofline_gb300 import gemm
+    s = torch.cuda.current_stream()
+    eb = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    ea = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    for e in eb + ea:  # torch creates the underlying cudaEvent on first record
+        e.record(s)
+    torch.cuda.synchronize()
+    for i in range(n):
+        gemm.set_profile_events(eb[i], ea[i])
+        call(i)
+    gemm.set_profile_events(None, None)
+    torch.cuda.synchronize()
+    return statistics.mean(eb[i].elapsed_time(ea[i]) for i in range(n))
 
 
 def run_ours(args):
@@ -286,15 +402,11 @@ def run_ours(args):
     lda, ldb, ldc = w.lds()
     A, B, C0 = w.make()
     sets, set_bytes = device_sets(w, dev, (A, B, C0))
-    nsets = len(sets)
     rotation = rotation_of(w)[2]
 
     plan = gemm.plan(w.M, w.N, w.K, lda, ldb, ldc, args.mode, 0, w.beta != 0.0)
     stream = torch.cuda.current_stream()
-
-    def step(i):
-        a, b, c = sets[i % nsets]
-        gemm.matmul(a, b, c, w.alpha, w.beta, args.mode)
+    step = Caller(w, args.mode, sets)
 
     for i in range(args.warmup):
         step(i)
@@ -312,36 +424,30 @@ def run_ours(args):
             torch.cuda.synchronize()
     torch.cuda.synchronize()
 
+    # The timed region: K steps in the library's production launch order.
+    # Each step's main kernel also stamps its start and end into its own pair
+    # (%globaltimer, atomics in the kernel; the launch order is unchanged),
+    # and the stamping continues, untimed, for the steps that follow until
+    # there are KERNEL_SAMPLES pairs, all in one back-to-back stream of calls.
+    n_stamped = max(args.steps, KERNEL_SAMPLES)
+    stamps = Stamps(n_stamped, dev)
+    torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     start.record(stream)
-    for i in range(args.steps):
-        step(i)
+    stamped_run(step, stamps, 0, args.steps)
     end.record(stream)
+    stamped_run(step, stamps, args.steps, n_stamped - args.steps)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
     ms_total = start.elapsed_time(end)
     if gemm.check_status() != gemm.OK:
-        raise RuntimeError("device status reported a timeout during the timed region")
-
-    # Separate pass for the roofline: the library records events around its
-    # main kernel (plain stream order for these calls), one pair per step.
-    nk = max(3, min(args.steps, 50))
-    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(nk)]
-    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(nk)]
-    for e in ev_b + ev_a:  # torch creates the underlying cudaEvent on first record
-        e.record(stream)
-    torch.cuda.synchronize()
-    for i in range(nk):
-        gemm.set_profile_events(ev_b[i], ev_a[i])
-        step(i)
-    gemm.set_profile_events(None, None)
-    torch.cuda.synchronize()
-    main_ms = [ev_b[i].elapsed_time(ev_a[i]) for i in range(nk)]
+        raise RuntimeError("device status reported an error during the timed region")
+    main_ms = stamps.ms()
 
     t_max = max_over_ranks(ms_total, world, dev)
     flops = float(w.flops)
@@ -351,9 +457,15 @@ def run_ours(args):
     # roofline of the dominant (main GEMM) kernel
     main_avg = statistics.mean(main_ms)
     roof = roofline_for(plan, w, main_avg, info, peaks, peaks_src)
-    roof["kernel_timing"] = f"mean of {nk} launches, CUDA events recorded around the kernel on its stream"
+    roof["kernel_timing"] = (
+        f"mean of {len(main_ms)} launches: the main kernel's first-CTA start to last-CTA end "
+        f"(%globaltimer stamps written by the kernel) in the {args.steps} timed steps and the "
+        f"{n_stamped - args.steps} steps issued right after them, same launch order "
+        f"(programmatic dependent launch on)")
+    roof["kernel_ms_timed_steps"] = statistics.mean(main_ms[:args.steps])
     roof["kernel_ms_best"] = min(main_ms)
     roof["achieved_best"] = roof["achieved"] * main_avg / min(main_ms)
+    roof["kernel_ms_events_plain_order"] = event_kernel_ms(step, KERNEL_SAMPLES)
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -379,7 +491,7 @@ def run_ours(args):
 
     # end to end: host buffers in, result back to the host, every step
     if not args.no_e2e:
-        line["e2e"] = e2e(args, w, A, B, C0, sets[0], dev, world)
+        line["e2e"] = e2e(args, w, A, B, C0, dev, world)
 
     if rank == 0 and not args.no_extras:
         line["extras"] = extras(args, w, sets, info, peaks, peaks_src)
@@ -393,11 +505,56 @@ def run_ours(args):
     return 0
 
 
-def e2e(args, w, A, B, C0, dset, dev, world):
+def link_ms(h2d_bytes, d2h_bytes, dev, reps=5):
+    """Time to move h2d_bytes host->device and d2h_bytes device->host between
+    pinned host buffers and device memory, the two directions concurrently on
+    two streams (the copy engines the library's host call uses): best of
+    `reps`, CUDA events.  Also each direction alone."""
+    import torch
+    hi = torch.empty(h2d_bytes // 4, dtype=torch.float32).pin_memory()
+    di = torch.empty_like(hi, device=dev)
+    do = torch.empty(d2h_bytes // 4, dtype=torch.float32, device=dev)
+    ho = torch.empty(do.numel(), dtype=torch.float32).pin_memory()
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    cur = torch.cuda.current_stream(dev)
+
+    def timed(fn):
+        best = None
+        for _ in range(reps + 1):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(dev)
+            e0.record(cur)
+            fn()
+            e1.record(cur)
+            torch.cuda.synchronize(dev)
+            t = e0.elapsed_time(e1)
+            best = t if best is None else min(best, t)
+        return best
+
+    def both():
+        s_in.wait_stream(cur)
+        s_out.wait_stream(cur)
+        with torch.cuda.stream(s_in):
+            di.copy_(hi, non_blocking=True)
+        with torch.cuda.stream(s_out):
+            ho.copy_(do, non_blocking=True)
+        cur.wait_stream(s_in)
+        cur.wait_stream(s_out)
+
+    res = {"both_ms": timed(both),
+           "h2d_ms": timed(lambda: di.copy_(hi, non_blocking=True)),
+           "d2h_ms": timed(lambda: ho.copy_(do, non_blocking=True))}
+    del hi, di, do, ho
+    return res
+
+
+def e2e(args, w, A, B, C0, dev, world):
     """The metric measured through the host-buffer C-ABI call gemm_f32_host:
     A, B (and C when beta != 0) in pinned host memory, copied in, multiplied
-    and copied back inside the call (row blocks pipelined over copy and
-    compute streams).  Timed on the host around whole blocking calls."""
+    and copied back inside the call (blocks pipelined over copy and compute
+    streams).  Timed on the host around whole blocking calls.  Its roof is the
+    host link: the same bytes moved in both directions at once, measured in
+    the same run."""
     import torch
     import torch.distributed as dist
 
@@ -424,11 +581,27 @@ def e2e(args, w, A, B, C0, dset, dev, world):
         one()
     ms = max_over_ranks((time.perf_counter() - t0) * 1e3, world, dev)
     h2d = 4 * (w.M * w.K + w.K * w.N + (w.M * w.N if w.beta != 0 else 0))
-    return {"value": whole_job_tflops(float(w.flops), steps, world, ms), "unit": "TFLOP/s",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4 * w.M * w.N, "steps": steps,
-            "ms_per_step": ms / steps,
-            "path": "pinned host -> gemm_f32_host (row blocks: H2D copy stream, GEMM stream, "
-                    "D2H copy stream) -> pinned host; host wall clock around blocking calls"}
+    d2h = 4 * w.M * w.N
+    out = {"value": whole_job_tflops(float(w.flops), steps, world, ms), "unit": "TFLOP/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+           "ms_per_step": ms / steps,
+           "path": "pinned host -> gemm_f32_host (blocks: H2D copy stream, GEMM stream, "
+                   "D2H copy stream) -> pinned host; host wall clock around blocking calls"}
+    try:
+        lk = link_ms(h2d, d2h, dev)
+        call_ms = ms / steps
+        out["roofline"] = {
+            "bound": "host_link", "achieved": (h2d + d2h) / (call_ms * 1e-3) / 1e9,
+            "peak": (h2d + d2h) / (lk["both_ms"] * 1e-3) / 1e9, "unit": "GB/s",
+            "frac": lk["both_ms"] / call_ms,
+            "link_ms": lk["both_ms"], "h2d_alone_gbs": h2d / (lk["h2d_ms"] * 1e-3) / 1e9,
+            "d2h_alone_gbs": d2h / (lk["d2h_ms"] * 1e-3) / 1e9,
+            "peak_source": "the call's own input and output bytes copied between pinned host "
+                           "buffers and device memory, both directions at once on two streams, "
+                           "measured in this run (best of 5)"}
+    except Exception as e:  # pragma: no cover
+        out["roofline"] = {"failed": str(e)}
+    return out
 
 
 def time_steps(fn, steps, warmup):
@@ -465,9 +638,10 @@ def roofline_for(plan, w, kernel_ms, info, peaks, peaks_src):
         roof = {"bound": "alu", "achieved": rf.tflops(flops, kernel_ms),
                 "peak": info["fp32_peak_tflops"], "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    traffic, tnote = ncu_traffic(f"{kname}:{w.name}")
+    traffic, tnote = ncu_traffic(plan, w.name)
     roof["traffic"] = traffic
     roof["kernel"] = kname
+    roof["instance"] = kernel_instance(plan)
     roof["kernel_ms"] = kernel_ms
     roof["algorithmic"] = (f"{alg_bytes} B" if roof["unit"] == "GB/s" else f"{flops:.0f} FLOP") + \
         " per launch"
@@ -481,39 +655,35 @@ def roofline_for(plan, w, kernel_ms, info, peaks, peaks_src):
     return roof
 
 
-def measure(w, mode, sets, steps, warmup=3):
-    """(mean step ms, mean main-kernel ms, plan) for `steps` library calls."""
+def measure(w, mode, sets, info, peaks, peaks_src, steps=KERNEL_SAMPLES, warmup=3):
+    """One config: mean step time over `steps` back-to-back calls (CUDA events
+    on the launching stream), then the same calls again with the main kernel
+    stamped (same launch order) for its mean duration and roofline."""
     import torch
 
     from roofline_gb300 import gemm
-    n = len(sets)
     plan = gemm.plan(w.M, w.N, w.K, *w.lds(), mode, 0, w.beta != 0.0)
-
-    def fn(i):
-        a, b, c = sets[i % n]
-        gemm.matmul(a, b, c, w.alpha, w.beta, mode)
-    step_ms = time_steps(fn, steps, warmup)
-    s = torch.cuda.current_stream()
-    eb = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    ea = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    for e in eb + ea:
-        e.record(s)
+    call = Caller(w, mode, sets)
+    step_ms = time_steps(call, steps, warmup)
+    stamps = Stamps(steps, torch.device("cuda"))
+    stamped_run(call, stamps, 0, steps)
     torch.cuda.synchronize()
-    for i in range(steps):
-        gemm.set_profile_events(eb[i], ea[i])
-        fn(i)
-    gemm.set_profile_events(None, None)
-    torch.cuda.synchronize()
-    kernel_ms = statistics.mean(eb[i].elapsed_time(ea[i]) for i in range(steps))
-    return step_ms, kernel_ms, plan
+    kernel_ms = statistics.mean(stamps.ms())
+    r = roofline_for(plan, w, kernel_ms, info, peaks, peaks_src)
+    return {"tflops": float(w.flops) / (step_ms * 1e-3) / 1e12, "ms": step_ms,
+            "kernel": plan["kernel_name"], "kernel_ms": kernel_ms, "calls": steps,
+            "plan": {k: plan[k] for k in ("bm", "bn", "bk", "stages", "split_k", "stream_k",
+                                          "grid_ctas", "launches")},
+            "roofline": {k: r[k] for k in ("bound", "achieved", "peak", "unit", "frac",
+                                           "traffic", "instance", "peak_source")}}
 
 
 def rotation_of(w, min_sets=2):
     """(input sets, bytes per set, description) of the L2 rotation the timed
-    loop uses: enough sets to exceed L2 three times (2 to 8)."""
+    loop uses: enough sets to exceed L2 three times (2 to 64)."""
     lda, ldb, ldc = w.lds()
     set_bytes = 4 * (w.M * lda + w.K * ldb + w.M * ldc)
-    nsets = max(min_sets, min(8, -(-3 * L2_BYTES // set_bytes)))
+    nsets = max(min_sets, min(64, -(-3 * L2_BYTES // set_bytes)))
     return nsets, set_bytes, (f"inputs rotated over {nsets} buffer sets "
                               f"({nsets * set_bytes / 2**20:.0f} MiB > L2)")
 
@@ -543,6 +713,7 @@ def graph_replay(w, reps=50):
 
     from roofline_gb300 import gemm
     sets, _ = device_sets(w, torch.device("cuda"))
+    sets = sets[:8]
     p = gemm.plan(w.M, w.N, w.K, *w.lds(), "auto", 0, w.beta != 0.0)
     ws = torch.empty(max(int(p["workspace_bytes"]), 256), dtype=torch.uint8, device="cuda")
 
@@ -572,46 +743,42 @@ def graph_replay(w, reps=50):
     return res
 
 
+# Every workload of the measured configuration list, with the modes timed for
+# each (the headline workload's AUTO line is the main result).
+EXTRA_CONFIGS = [("sq4096", ["fp32_simt", "tf32x3", "tf32"]),
+                 ("sq8192", ["auto", "fp32_simt"]),
+                 ("skinny", ["auto"]),
+                 ("ragged", ["auto", "fp32_simt"]),
+                 ("sq512", ["auto", "tf32x3"]),
+                 ("sq512_int", ["auto"])]
+
+
 def extras(args, w, sets, info, peaks, peaks_src):
-    """Both modes on the same workload, the other large workloads, the FMA and
-    HBM copy roofs, and cuBLAS reference points (timed beside the library,
-    never inside it)."""
+    """Every config with its roofline (mean of KERNEL_SAMPLES calls each), the
+    FMA and HBM copy roofs, and cuBLAS reference points (timed beside the
+    library, never inside it)."""
     import torch
 
     from roofline_gb300 import gemm
     from workloads import WORKLOADS
-    out = {}
+    out = {"configs": {}}
     n = len(sets)
-    for mode in ["fp32_simt", "tf32x3"]:
-        try:
-            step_ms, kernel_ms, p = measure(w, mode, sets, 20)
-        except gemm.GemmError as e:
-            out[mode] = {"unavailable": str(e)}
-            continue
-        out[mode] = {"tflops": float(w.flops) / (step_ms * 1e-3) / 1e12, "ms": step_ms,
-                     "kernel": p["kernel_name"], "kernel_ms": kernel_ms,
-                     "roofline_frac": roofline_for(p, w, kernel_ms, info, peaks, peaks_src)["frac"]}
-    # the other large workloads: a short timing per mode
-    for name, modes in [("sq8192", ["auto", "fp32_simt"]), ("skinny", ["auto"])]:
-        if name == w.name:
-            continue
+    for name, modes in EXTRA_CONFIGS:
         wl = WORKLOADS[name]
         try:
-            wsets, _ = device_sets(wl, torch.device("cuda"))
+            wsets = sets if name == w.name else device_sets(wl, torch.device("cuda"))[0]
             res = {}
             for mode in modes:
-                steps = 5 if (name == "sq8192" and mode == "fp32_simt") else 20
-                step_ms, kernel_ms, p = measure(wl, mode, wsets, steps)
-                r = roofline_for(p, wl, kernel_ms, info, peaks, peaks_src)
-                res[mode] = {"tflops": float(wl.flops) / (step_ms * 1e-3) / 1e12, "ms": step_ms,
-                             "kernel": p["kernel_name"], "kernel_ms": kernel_ms,
-                             "roofline": {k: r[k] for k in ("bound", "achieved", "peak", "unit",
-                                                            "frac")}}
-            out[name] = res
-            del wsets
-            torch.cuda.empty_cache()
+                try:
+                    res[mode] = measure(wl, mode, wsets, info, peaks, peaks_src)
+                except gemm.GemmError as e:
+                    res[mode] = {"unavailable": str(e)}
+            out["configs"][name] = res
+            if name != w.name:
+                del wsets
+                torch.cuda.empty_cache()
         except Exception as e:  # pragma: no cover
-            out[name] = {"failed": str(e)}
+            out["configs"][name] = {"failed": str(e)}
     # launch overhead: 512^3 calls one by one against the same calls replayed
     # from a CUDA graph (one capture of one call per input set)
     try:

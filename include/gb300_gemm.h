@@ -180,11 +180,31 @@ GEMM_API int gemm_f32_ex(int64_t M, int64_t N, int64_t K, float alpha, const flo
 
 /*
  * gemm_f32_plan -- what gemm_f32/gemm_f32_ex would run for this shape, with
- * no launch and no allocation.  align_hint: the bitwise OR of the A, B and C
- * addresses the call will use (0 = assume 16-byte aligned); it decides
- * between the 128-bit and the scalar path.  beta_nonzero only changes the
- * algorithmic byte count.  Uses the current device's properties when a
- * device is visible, else built-in GB300 figures (152 SMs).
+ * no launch and no allocation.
+ *
+ * The course page picks each rung's launch by hand: 16 x 16 thread blocks
+ * and a grid that covers N x N for the naive and coalesced kernels, TILE x
+ * TILE blocks for the shared-memory kernel, with TILE = 16 and 32 measured
+ * side by side ("Project - tiled matrix multiply", sections "Stage 0 - the
+ * naive baseline", "Stage 1 - global memory coalescing" and "Stage 2").  The
+ * plan is that choice made by the library for any M, N, K: kernel, CTA tile,
+ * pipeline depth, K slices, stream-K grid and workspace.  It also places the
+ * shape on the roofline: arithmetic intensity = 2*M*N*K / algorithmic bytes,
+ * compared with the ridge point = arithmetic rate / memory bandwidth of the
+ * resolved mode ("Bandwidths and peak rate - exercises", exercise 3), which
+ * gives plan.bound.
+ *
+ * Arguments: M, N, K >= 0 and the leading dimensions as gemm_f32_ex would
+ * get them (row-major; a too-small ld returns GEMM_ERR_INVALID_ARG).
+ * align_hint: the bitwise OR of the A, B and C addresses the call will use
+ * (0 = assume 16-byte aligned); it decides between the 128-bit and the
+ * scalar path.  beta_nonzero only changes the algorithmic byte count.  out:
+ * caller-owned, written only on GEMM_OK.  Uses the current device's
+ * properties when a device is visible, else built-in GB300 figures (152
+ * SMs).  Host only: launches nothing, allocates nothing.  Returns GEMM_OK,
+ * GEMM_ERR_INVALID_ARG (sizes, ld, mode, out == NULL) or
+ * GEMM_ERR_UNSUPPORTED (a tensor-core mode on a device without sm_103a, or a
+ * shape beyond its limits).
  */
 GEMM_API int gemm_f32_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
                   int64_t ldc, int mode, uintptr_t align_hint,
@@ -318,14 +338,27 @@ GEMM_API int64_t fp32_fma_peak_sink_floats(void);
  */
 GEMM_API int gemm_device_info(int dev, gemm_device_info_t *out);
 
-/* Static string for a status code (never NULL). */
+/*
+ * gemm_strerror -- a static, NUL-terminated description of a status code
+ * (never NULL; unknown codes get "unknown status code"); the caller must not
+ * free it.  The course page's scaffolding wraps every CUDA call in a
+ * CUDA_CHECK macro that prints the error string and exits the process
+ * ("Project - tiled matrix multiply", section "Starter scaffolding"); a
+ * library must leave that decision to its caller, so every call returns a
+ * code and this gives the text that macro would have printed.
+ */
 GEMM_API const char *gemm_strerror(int code);
 
 /*
- * gemm_check_status -- synchronises `stream`, then reads and clears the
- * device status word that the tensor-core kernel sets when one of its
- * bounded waits runs out.  Returns GEMM_ERR_DEVICE_TIMEOUT if it was set,
- * GEMM_ERR_CUDA if the synchronisation reported an error, else GEMM_OK.
+ * gemm_check_status -- the deferred half of that same CUDA_CHECK step
+ * ("Starter scaffolding" checks cudaGetLastError and cudaDeviceSynchronize
+ * after a launch): synchronises `stream`, then reads and clears the
+ * library's device status words, set by the tensor-core kernel when one of
+ * its bounded waits runs out and by the stream-K fix-up when a tile has more
+ * parts than it can sum.  Returns GEMM_ERR_DEVICE_TIMEOUT or
+ * GEMM_ERR_UNSUPPORTED if one was set (the result of the call that set it is
+ * not valid), GEMM_ERR_CUDA if the synchronisation reported an error, else
+ * GEMM_OK.  Blocking; not for use during stream capture.
  */
 GEMM_API int gemm_check_status(cudaStream_t stream);
 
@@ -340,6 +373,26 @@ GEMM_API int gemm_check_status(cudaStream_t stream);
 GEMM_API int gemm_set_profile_events(cudaEvent_t before_main, cudaEvent_t after_main);
 
 /*
+ * gemm_set_profile_stamps -- measurement aid that keeps the launch order of
+ * a call unchanged (gemm_set_profile_events puts the main kernel in plain
+ * stream order, which the events need; the split pass, GEMM kernel and
+ * fix-up otherwise overlap their launches).  For the calling host thread,
+ * the next GEMM calls' main kernel (the CUDA-core or tensor-core GEMM
+ * kernel) reads the GPU's nanosecond clock (%globaltimer) and folds it into
+ * stamps[0] with an atomic minimum when each of its CTAs starts work (past
+ * its wait for the kernel before it), and into stamps[1] with an atomic
+ * maximum when each CTA has finished, so stamps[1] - stamps[0] is that
+ * launch's duration in ns.  stamps: DEVICE memory on the current device, 8-byte
+ * aligned, owned by the caller, who sets stamps[0] = ~0 and stamps[1] = 0
+ * before the call and passes a fresh pair for each launch it wants timed
+ * separately.  NULL stops.  The course page times with cudaEvent pairs
+ * ("Project - tiled matrix multiply", "Starter scaffolding"); these stamps
+ * time one kernel inside a chain of launches that events would serialise.
+ * Returns GEMM_ERR_INVALID_ARG for a misaligned pointer, else GEMM_OK.
+ */
+GEMM_API int gemm_set_profile_stamps(unsigned long long *stamps);
+
+/*
  * gemm_f32_splitk_noalloc -- C <- alpha * A * B + beta * C on the CUDA cores
  * (the FP32_SIMT kernel), allocating no device memory at all.  The course
  * pages have no counterpart to this call; it exists for callers that cannot
@@ -352,11 +405,16 @@ GEMM_API int gemm_set_profile_events(cudaEvent_t before_main, cudaEvent_t after_
  *
  * Arguments and layout are those of gemm_f32_ex (device pointers, row-major,
  * lda >= K, ldb >= N, ldc >= N).  split_k = 0 takes the planner's slice
- * count for FP32_SIMT; split_k >= 1 asks for that many K slices (rounded to
- * whole 8- or 16-deep tiles).  When the slices' partial sums,
- * split_k * M * N * 4 bytes, exceed GEMM_NOALLOC_SCRATCH_BYTES the call
- * returns GEMM_ERR_WORKSPACE_TOO_SMALL and launches nothing; one slice needs
- * no scratch.  Other errors as gemm_f32_ex.
+ * count for FP32_SIMT, reduced if need be to the most slices whose partial
+ * sums fit the array (at worst one slice, which needs no scratch), so it
+ * never fails for want of scratch.  1 <= split_k <= GEMM_NOALLOC_MAX_SPLIT
+ * asks for that many K slices (rounded to whole K tiles of the kernel, 16
+ * deep by default, which can only lower the count); when their partial
+ * sums, split_k * M * N * 4 bytes, exceed GEMM_NOALLOC_SCRATCH_BYTES the
+ * call returns
+ * GEMM_ERR_WORKSPACE_TOO_SMALL and launches nothing.  split_k < 0 or above
+ * GEMM_NOALLOC_MAX_SPLIT returns GEMM_ERR_INVALID_ARG.  Other errors as
+ * gemm_f32_ex.
  *
  * The first call on a device looks up the array's device address (with that
  * device current); make that first call before any stream capture.  All
@@ -367,6 +425,7 @@ GEMM_API int gemm_set_profile_events(cudaEvent_t before_main, cudaEvent_t after_
  * sum before reading it.
  */
 #define GEMM_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+#define GEMM_NOALLOC_MAX_SPLIT 256
 GEMM_API int gemm_f32_splitk_noalloc(int64_t M, int64_t N, int64_t K, float alpha,
                                      const float *A, int64_t lda, const float *B,
                                      int64_t ldb, float beta, float *C, int64_t ldc,

@@ -120,6 +120,7 @@ int to_status(cudaError_t e) { return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA
 
 thread_local cudaEvent_t t_prof_before = nullptr;
 thread_local cudaEvent_t t_prof_after = nullptr;
+thread_local unsigned long long *t_prof_stamps = nullptr;
 
 }  // namespace
 
@@ -130,6 +131,7 @@ void profile_mark_after(cudaStream_t s) {
   if (t_prof_after) cudaEventRecord(t_prof_after, s);
 }
 bool profile_events_set() { return t_prof_before != nullptr; }
+unsigned long long *profile_stamps() { return t_prof_stamps; }
 
 const DeviceProps &default_props() {
   static const DeviceProps d = make_default_props();
@@ -170,6 +172,12 @@ int gemm_set_profile_events(cudaEvent_t before_main, cudaEvent_t after_main) {
   if ((before_main == nullptr) != (after_main == nullptr)) return GEMM_ERR_INVALID_ARG;
   t_prof_before = before_main;
   t_prof_after = after_main;
+  return GEMM_OK;
+}
+
+int gemm_set_profile_stamps(unsigned long long *stamps) {
+  if (stamps && (reinterpret_cast<uintptr_t>(stamps) & 7)) return GEMM_ERR_INVALID_ARG;
+  t_prof_stamps = stamps;
   return GEMM_OK;
 }
 

@@ -60,6 +60,16 @@ const DeviceProps &default_props();
 void profile_mark_before(cudaStream_t s);
 void profile_mark_after(cudaStream_t s);
 bool profile_events_set();
+// The caller's stamp pair for the next main-kernel launch on this host thread
+// (gemm_set_profile_stamps), or nullptr.
+unsigned long long *profile_stamps();
+
+// %globaltimer: the GPU's nanosecond clock, common to all SMs.
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
 
 // Planner (plan.cu).
 // ta / tb: operand storage as in GemmArgs.
@@ -105,6 +115,9 @@ SimtConfig simt_config();
 // Built (BK, stages) pairs of the 64 x 128 CUDA-core tile; the first is the default.
 #define GG_SIMT_CONFIGS(X) X(16, 4) X(32, 2)
 bool simt_config_valid(int bk, int stages);
+// The duplicated-A CUDA-core kernel (simt2.cu) and its built (BK, stages).
+bool simt2_config_valid(int bk, int stages);
+cudaError_t launch_simt2(const gemm_plan_t &plan, const GemmArgs &p, float *ws, cudaStream_t s);
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 

@@ -21,6 +21,8 @@ namespace gg {
 namespace {
 
 constexpr size_t kScratchFloats = GEMM_NOALLOC_SCRATCH_BYTES / sizeof(float);
+// Most K slices a caller may ask for (the planner's own cap for the CUDA cores).
+constexpr int kMaxSplit = GEMM_NOALLOC_MAX_SPLIT;
 
 // The scratch array.  Host code only sees a host-side stand-in under this
 // name; the device address comes from cudaGetSymbolAddress below.
@@ -55,7 +57,7 @@ extern "C" int gemm_f32_splitk_noalloc(int64_t M, int64_t N, int64_t K, float al
                                        const float *A, int64_t lda, const float *B, int64_t ldb,
                                        float beta, float *C, int64_t ldc, int split_k,
                                        cudaStream_t stream) {
-  if (M < 0 || N < 0 || K < 0 || split_k < 0) return GEMM_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0 || split_k < 0 || split_k > kMaxSplit) return GEMM_ERR_INVALID_ARG;
   if (lda < (K > 1 ? K : 1) || ldb < (N > 1 ? N : 1) || ldc < (N > 1 ? N : 1))
     return GEMM_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return GEMM_OK;
@@ -77,9 +79,16 @@ extern "C" int gemm_f32_splitk_noalloc(int64_t M, int64_t N, int64_t K, float al
   int st = make_plan(M, N, K, lda, ldb, ldc, GEMM_MODE_FP32_SIMT,
                      (uintptr_t)A | (uintptr_t)B | (uintptr_t)C, beta != 0.0f, dp, &plan);
   if (st != GEMM_OK) return st;
-  if (split_k > 0) {
-    // the caller's slice count, rounded to whole BK-deep slices
-    int64_t kps = ceil_div(ceil_div(K, split_k), plan.bk) * plan.bk;
+  // Slices: the caller's count, or the planner's cut down to what the array
+  // holds (one slice needs no scratch), rounded to whole BK-deep slices.
+  int64_t want = split_k > 0 ? split_k : plan.split_k;
+  if (split_k == 0 && want > 1) {
+    const uint64_t fit = (uint64_t)kScratchFloats / ((uint64_t)M * (uint64_t)N);
+    if ((uint64_t)want > fit) want = fit > 1 ? (int64_t)fit : 1;
+  }
+  if (want < 1) want = 1;
+  {
+    const int64_t kps = ceil_div(ceil_div(K, want), plan.bk) * plan.bk;
     plan.split_k = (int)ceil_div(K, kps);
   }
   if (plan.split_k > 1 &&

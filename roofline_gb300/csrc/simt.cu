@@ -74,7 +74,7 @@ constexpr int kGroupM = 8;
 template <int BM, int BN, int BK, int STAGES, bool VEC, bool TA, bool TB>
 __global__ void __launch_bounds__(kThreadsP, 2)
 simt_packed_kernel(GemmArgs p, int64_t k_per_split, float *__restrict__ ws, int ws_vec,
-                   int group_m) {
+                   int group_m, unsigned long long *stamps) {
   constexpr int TM = 8, TN = 8;
   // k-major tiles As[k][m], Bs[k][n].  An operand stored with K contiguous (A
   // as M x K, or B as N x K) is copied element by element into rows of
@@ -118,6 +118,8 @@ simt_packed_kernel(GemmArgs p, int64_t k_per_split, float *__restrict__ ws, int 
   const int64_t m0 = (first_m + local % gm) * BM;
   const int64_t n0 = (local / gm) * BN;
   pdl_wait();  // A, B and C may come from the kernel before this one
+  // measurement aid: earliest start of any CTA (see gemm_set_profile_stamps)
+  if (stamps != nullptr && tid == 0) atomicMin(&stamps[0], globaltimer_ns());
   const int64_t kbeg = (int64_t)blockIdx.z * k_per_split;
   const int64_t kend = min(p.K, kbeg + k_per_split);
   const int64_t klen = kend > kbeg ? kend - kbeg : 0;
@@ -299,6 +301,10 @@ simt_packed_kernel(GemmArgs p, int64_t k_per_split, float *__restrict__ ws, int 
       }
     }
   }
+  if (stamps != nullptr) {  // latest end of any CTA
+    __syncthreads();
+    if (tid == 0) atomicMax(&stamps[1], globaltimer_ns());
+  }
 }
 
 // C <- alpha * sum_{z < splits} ws[z] + beta * C.  Slice z goes to chain
@@ -337,7 +343,15 @@ __global__ void splitk_reduce_kernel(GemmArgs p, const float *__restrict__ ws, i
 
 SimtConfig simt_config() { return SimtConfig{64, 128, 16, kThreadsP}; }
 
+// Which CUDA-core kernel runs: this file's packed kernel unless
+// GEMM_SIMT_KERNEL=2 asks for the duplicated-A kernel (simt2.cu).
+bool simt_use_dup() {
+  const char *v = std::getenv("GEMM_SIMT_KERNEL");
+  return v && std::atoi(v) == 2;
+}
+
 bool simt_config_valid(int bk, int stages) {
+  if (simt_use_dup()) return simt2_config_valid(bk, stages);
 #define GG_SIMT(BK_, ST_) \
   if (bk == BK_ && stages == ST_) return true;
   GG_SIMT_CONFIGS(GG_SIMT)
@@ -400,7 +414,7 @@ cudaError_t launch_packed(const gemm_plan_t &plan, const GemmArgs &p, float *ws,
   // needs; 1023 x 1025 x 777 split 2 went from 57.4 to 71.9 us per call).
   profile_mark_before(s);
   cudaError_t e = launch_pdl(plan.vec ? kv : ks, grid, dim3(kThreadsP), (size_t)smem, false, s,
-                             p, kps, w, ws_vec, group_m);
+                             p, kps, w, ws_vec, group_m, profile_stamps());
   profile_mark_after(s);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess || split == 1) return e;
@@ -409,6 +423,7 @@ cudaError_t launch_packed(const gemm_plan_t &plan, const GemmArgs &p, float *ws,
 
 cudaError_t launch_simt(const gemm_plan_t &plan, const GemmArgs &p, float *ws, cudaStream_t s) {
   if (plan.bm != 64 || plan.bn != 128) return cudaErrorInvalidValue;
+  if (simt_use_dup()) return launch_simt2(plan, p, ws, s);
 #define GG_SIMT(BK_, ST_)                                                              \
   if (plan.bk == BK_ && plan.stages == ST_) {                                          \
     if (!p.ta && !p.tb) return launch_packed<64, 128, BK_, ST_, false, false>(plan, p, ws, s); \

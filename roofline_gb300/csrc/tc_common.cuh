@@ -231,6 +231,7 @@ struct TcParams {
   float *partial;    // stream-K partial tiles: 2 slots of BM x BN per CTA
   uint64_t timeout_ns;
   int stall_producer;  // test hook: the producer issues nothing
+  unsigned long long *stamps;  // measurement aid (gemm_set_profile_stamps), or nullptr
 };
 
 // Row-tile and column-tile of output tile t.
@@ -258,6 +259,24 @@ struct Segment {
 
 __host__ __device__ __forceinline__ int64_t unit_begin(int64_t total, int64_t c, int64_t G) {
   return total * c / G;
+}
+
+// The CTA whose stream-K range holds unit u: the largest c with
+// unit_begin(total, c, G) <= u.
+__host__ __device__ __forceinline__ int64_t unit_owner(int64_t total, int64_t u, int64_t G) {
+  return ((u + 1) * G - 1) / total;
+}
+
+// Most CTAs that share one stream-K tile (an upper bound on the parts the
+// fix-up sums for any tile): tile tl spans units [tl*num_kb, (tl+1)*num_kb).
+__host__ __device__ __forceinline__ int64_t max_parts_per_tile(int64_t total, int64_t num_kb,
+                                                               int64_t G) {
+  int64_t most = 0;
+  for (int64_t first = 0; first < total; first += num_kb) {
+    const int64_t n = unit_owner(total, first + num_kb - 1, G) - unit_owner(total, first, G) + 1;
+    if (n > most) most = n;
+  }
+  return most;
 }
 
 struct Walk {
@@ -312,8 +331,16 @@ SplitJob split_transposed_job(const float *src, int64_t ld, int64_t k, int64_t c
                               float *hi, float *lo);
 // One launch running job a, then (b != nullptr) job b, in separate blocks.
 cudaError_t launch_splits(const SplitJob &a, const SplitJob *b, bool pdl, cudaStream_t s);
-// Sums the parts of the tiles shared between stream-K CTAs into C.
+// Sums the parts of the tiles shared between stream-K CTAs into C.  At most
+// kFixMaxParts parts per tile (the launcher checks max_parts_per_tile first;
+// a tile with more sets the fix-up's status word to GEMM_ERR_UNSUPPORTED and
+// is left alone).
+constexpr int kFixMaxParts = 256;
 cudaError_t launch_fixup(const TcParams &p, int bm, int bn, int64_t G, bool pdl, cudaStream_t s);
+
+// Reads and clears the fix-up's device status word (0 = ok, else a GEMM_ERR_*
+// code), after synchronising `s`.
+int fixup_read_and_clear_status(cudaStream_t s);
 
 }  // namespace tc
 }  // namespace gg

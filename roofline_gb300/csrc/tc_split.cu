@@ -14,8 +14,8 @@ namespace {
 // space; the block whose boundary is the first one strictly inside a tile
 // handles that tile, all other blocks return at once (whole tiles were
 // written by the GEMM).
-constexpr int kFixMaxParts = 256;
 constexpr int kFixRows = 16;  // tile rows per fix-up block
+__device__ int g_fix_status;  // 0 = ok, else a GEMM_ERR_* code
 constexpr int kTrK = 32, kTrN = 128;  // transposed split: k x n tile per block
 
 __global__ void __launch_bounds__(256)
@@ -36,14 +36,20 @@ streamk_fixup_kernel(TcParams p, int BM, int BN, int64_t G) {
     for (int64_t cta = c - 1; cta < G && unit_begin(p.sk_units, cta, G) <= last; ++cta) {
       const int64_t ub = unit_begin(p.sk_units, cta, G), ue = unit_begin(p.sk_units, cta + 1, G);
       if (ub == ue) continue;  // no work
+      if (n == kFixMaxParts) {  // more parts than this kernel sums: report, write nothing
+        n = -1;
+        break;
+      }
       // the tile is this CTA's first segment (slot 0) or its last (slot 1)
       const int slot = (ub >= first) ? 0 : 1;
-      if (n < kFixMaxParts) part_off[n++] = (cta * 2 + slot) * (int64_t)BM * BN;
+      part_off[n++] = (cta * 2 + slot) * (int64_t)BM * BN;
     }
+    if (n < 0) atomicExch(&g_fix_status, GEMM_ERR_UNSUPPORTED);
     nparts = n;
   }
   __syncthreads();
   const int n = nparts;
+  if (n < 0) return;
   // blockIdx.y picks 32 of the tile's BM rows; each thread keeps four
   // independent 16-byte sums so several loads are in flight
   int64_t mt, nt;
@@ -247,6 +253,25 @@ cudaError_t launch_splits(const SplitJob &a, const SplitJob *b, bool pdl, cudaSt
   const int64_t blocks = a.blocks + second.blocks;
   if (blocks < 1 || blocks > 0x7fffffff) return cudaErrorInvalidValue;
   return launch(split_kernel, dim3((unsigned)blocks), dim3(256), pdl, s, a, second);
+}
+
+int fixup_read_and_clear_status(cudaStream_t s) {
+  int v = 0;
+  if (cudaMemcpyFromSymbolAsync(&v, g_fix_status, sizeof(int), 0, cudaMemcpyDeviceToHost, s) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+  if (v == 0) return GEMM_OK;
+  const int zero = 0;
+  if (cudaMemcpyToSymbolAsync(g_fix_status, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, s) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+  return v;
 }
 
 cudaError_t launch_fixup(const TcParams &p, int bm, int bn, int64_t G, bool pdl, cudaStream_t s) {

@@ -237,6 +237,8 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
   const uint32_t tmem_base = *tmem_slot;
   // B_hi/B_lo (and A_hi/A_lo) come from the split kernels before this one
   grid_dependency_wait();
+  // measurement aid: earliest start of any CTA (see gemm_set_profile_stamps)
+  if (p.stamps != nullptr && threadIdx.x == 0) atomicMin(&p.stamps[0], globaltimer());
 
   bool ok = true;
   if (warp == 0) {
@@ -512,6 +514,7 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+  if (p.stamps != nullptr && threadIdx.x == 0) atomicMax(&p.stamps[1], globaltimer());
 }
 
 // ------------------------------------------------------------------ host side
@@ -557,6 +560,7 @@ uint64_t env_u64(const char *name, uint64_t dflt) {
 }
 
 inline int64_t round_up(int64_t a, int64_t b) { return (a + b - 1) / b * b; }
+
 inline uint64_t align256(uint64_t x) { return (x + 255) & ~uint64_t(255); }
 
 struct WsLayout {
@@ -599,31 +603,6 @@ int launch_cfg(const gemm_plan_t &plan, const GemmArgs &a, char *ws, cudaStream_
   float *alo = reinterpret_cast<float *>(ws + L.a_lo);
   float *bhi = reinterpret_cast<float *>(ws + L.b_hi);
   float *blo = reinterpret_cast<float *>(ws + L.b_lo);
-
-  // Split passes: each operand becomes K-major hi (and lo) planes.  An
-  // operand stored with K contiguous (A as M x K, B as N x K) is split row
-  // by row; one stored with K as its row index is split and transposed.
-  // Programmatic dependent launch lets each kernel be scheduled while the one
-  // before it drains (each waits for its predecessor before touching
-  // memory).  With the caller's profiling events set, plain stream order is
-  // kept so the events bracket the GEMM kernel alone; callers that chain the
-  // GEMM behind cross-stream event waits ask for plain order as well.
-  const bool pdl = !profile_events_set() && !a.plain_order;
-  // Both passes, when both run, are one launch.
-  SplitJob jobs[2];
-  int njobs = 0;
-  if (!AK)
-    jobs[njobs++] = a.ta ? split_transposed_job(a.A, a.lda, a.K, a.M, L.kp, ahi, X3 ? alo : nullptr)
-                         : split_rows_job(a.A, a.lda, a.M, a.K, L.kp, ahi, X3 ? alo : nullptr);
-  if (!a.b_presplit)
-    jobs[njobs++] = a.tb ? split_rows_job(a.B, a.ldb, a.N, a.K, L.kp, bhi, X3 ? blo : nullptr)
-                         : split_transposed_job(a.B, a.ldb, a.K, a.N, L.kp, bhi, X3 ? blo : nullptr);
-  const cudaError_t se =
-      njobs ? launch_splits(jobs[0], njobs > 1 ? &jobs[1] : nullptr, pdl, s) : cudaSuccess;
-  if (se != cudaSuccess) {
-    cudaGetLastError();
-    return GEMM_ERR_CUDA;
-  }
 
   CUtensorMap tA0, tA1, tB0, tB1;
   bool ok;
@@ -680,16 +659,46 @@ int launch_cfg(const gemm_plan_t &plan, const GemmArgs &a, char *ws, cudaStream_
   p.waves = (int)waves;
   p.dp_tiles = waves * G;
   p.sk_units = rest * num_kb;
+  // the fix-up sums at most kFixMaxParts parts of one tile
+  if (plan.stream_k && p.sk_units > 0 && max_parts_per_tile(p.sk_units, num_kb, G) > kFixMaxParts)
+    return GEMM_ERR_UNSUPPORTED;
   p.partial = reinterpret_cast<float *>(ws + L.partial);
   p.timeout_ns = env_u64("GEMM_DEBUG_WAIT_LIMIT_NS", 2000000000ull);
   p.stall_producer = (int)env_u64("GEMM_DEBUG_STALL_PRODUCER", 0);
-
+  p.stamps = profile_stamps();
   auto kern = tc_tf32x3_kernel<BM, BN, BK, STAGES, AK, CONCAT, NPROD>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Cfg::SMEM_BYTES) != cudaSuccess) {
     cudaGetLastError();
     return GEMM_ERR_CUDA;
   }
+
+  // Split passes: each operand becomes K-major hi (and lo) planes.  An
+  // operand stored with K contiguous (A as M x K, B as N x K) is split row
+  // by row; one stored with K as its row index is split and transposed.
+  // Programmatic dependent launch lets each kernel be scheduled while the one
+  // before it drains (each waits for its predecessor before touching
+  // memory).  With the caller's profiling events set, plain stream order is
+  // kept so the events bracket the GEMM kernel alone; callers that chain the
+  // GEMM behind cross-stream event waits ask for plain order as well.
+  // Every check that can refuse the call has run by now: nothing was launched.
+  const bool pdl = !profile_events_set() && !a.plain_order;
+  // Both passes, when both run, are one launch.
+  SplitJob jobs[2];
+  int njobs = 0;
+  if (!AK)
+    jobs[njobs++] = a.ta ? split_transposed_job(a.A, a.lda, a.K, a.M, L.kp, ahi, X3 ? alo : nullptr)
+                         : split_rows_job(a.A, a.lda, a.M, a.K, L.kp, ahi, X3 ? alo : nullptr);
+  if (!a.b_presplit)
+    jobs[njobs++] = a.tb ? split_rows_job(a.B, a.ldb, a.N, a.K, L.kp, bhi, X3 ? blo : nullptr)
+                         : split_transposed_job(a.B, a.ldb, a.K, a.N, L.kp, bhi, X3 ? blo : nullptr);
+  const cudaError_t se =
+      njobs ? launch_splits(jobs[0], njobs > 1 ? &jobs[1] : nullptr, pdl, s) : cudaSuccess;
+  if (se != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -808,6 +817,7 @@ int launch_tc(const gemm_plan_t &plan, const GemmArgs &a, void *ws, size_t ws_by
 }
 
 int tc_read_and_clear_status(cudaStream_t s) {
+  const int fix = fixup_read_and_clear_status(s);
   int v = 0;
   if (cudaMemcpyFromSymbolAsync(&v, g_tc_status, sizeof(int), 0, cudaMemcpyDeviceToHost, s) !=
           cudaSuccess ||
@@ -825,7 +835,7 @@ int tc_read_and_clear_status(cudaStream_t s) {
     }
     return v;
   }
-  return GEMM_OK;
+  return fix;
 }
 
 }  // namespace gg

@@ -50,14 +50,18 @@ BOUNDS = {0: "none", 1: "fp32", 2: "tf32x3", 3: "hbm", 4: "tf32"}
 EXPORTED = ["gemm_f32", "gemm_f32_ex", "gemm_f32_plan", "gemm_f32_op", "gemm_f32_op_plan",
             "gemm_f32_host", "hbm_copy_f32", "hbm_copy_calibrate",
             "gemm_device_info", "gemm_strerror", "gemm_check_status", "gemm_shutdown",
-            "gemm_abi_version", "gemm_set_profile_events", "gemm_f32_splitk_noalloc",
+            "gemm_abi_version", "gemm_set_profile_events", "gemm_set_profile_stamps",
+            "gemm_f32_splitk_noalloc",
             "fp32_fma_peak", "fp32_fma_peak_sink_floats"]
 
 # most row blocks gemm_f32_host pipelines
 HOST_MAX_BLOCKS = 64
 
-# size of the static scratch array behind gemm_f32_splitk_noalloc
+# size of the static scratch array behind gemm_f32_splitk_noalloc, and the
+# most K slices it takes (GEMM_NOALLOC_SCRATCH_BYTES, GEMM_NOALLOC_MAX_SPLIT;
+# a CPU test compiles the header and compares)
 NOALLOC_SCRATCH_BYTES = 8 << 20
+NOALLOC_MAX_SPLIT = 256
 
 
 class GemmPlan(ctypes.Structure):
@@ -155,6 +159,8 @@ def load(path: str | None = None):
         lib.gemm_abi_version.restype = i32
         lib.gemm_set_profile_events.argtypes = [vp, vp]
         lib.gemm_set_profile_events.restype = i32
+        lib.gemm_set_profile_stamps.argtypes = [vp]
+        lib.gemm_set_profile_stamps.restype = i32
         lib.gemm_f32_splitk_noalloc.argtypes = [i64, i64, i64, f32, vp, i64, vp, i64, f32, vp,
                                                 i64, i32, vp]
         lib.gemm_f32_splitk_noalloc.restype = i32
@@ -272,6 +278,24 @@ def set_profile_events(before=None, after=None) -> None:
     rc = load().gemm_set_profile_events(b, a)
     if rc != OK:
         raise GemmError(rc, "gemm_set_profile_events")
+
+
+def set_profile_stamps(stamps=None) -> None:
+    """Main-kernel stamps of the following calls from this thread go to the
+    device int64 pair `stamps` (a tensor of 2 or more int64 starting at that
+    pair, or a device address); None stops.  The caller fills [~0, 0]
+    first; afterwards stamps[1] - stamps[0] is the kernel's duration in ns."""
+    if stamps is None:
+        ptr = None
+    elif isinstance(stamps, int):
+        ptr = stamps
+    else:
+        if not stamps.is_cuda or stamps.dtype.itemsize != 8:
+            raise ValueError("stamps must be a CUDA tensor of 8-byte integers")
+        ptr = stamps.data_ptr()
+    rc = load().gemm_set_profile_stamps(ptr)
+    if rc != OK:
+        raise GemmError(rc, "gemm_set_profile_stamps")
 
 
 # ------------------------------------------------------------ torch tensors

@@ -61,3 +61,15 @@ def compare(name: str, C_full: np.ndarray):
     got = C_full[:, :w.N] if pos is None else C_full[pos[0], pos[1]]
     return dict(e1=oracle.err_normalised(got, ref, D), mismatches=oracle.mismatches(got, ref),
                 e3=oracle.err_pages(got, ref))
+
+
+# 1xTF32 mode: each operand rounded to TF32 (11 significant bits, round to
+# nearest, ties away): |x - tf32(x)| <= 2^-11 |x|, so each product a*b moves by
+# at most (2 * 2^-11 + 2^-22) |a||b| = (2^-10 + 2^-22) |a||b|.  The K products
+# are then summed in FP32 (tensor-core accumulation, order and rounding of the
+# partial sums not specified: allow 2^-23 per addition, twice the
+# round-to-nearest unit), plus the alpha/beta epilogue (two roundings of
+# 2^-24).  So the normalised error is at most
+#     2^-10 + 2^-22 + K * 2^-23 + 2^-23.
+def tol_tf32(K):
+    return 2.0 ** -10 + 2.0 ** -22 + (K + 1) * 2.0 ** -23

@@ -77,6 +77,32 @@ def test_null_pointers_and_mode_rejected(lib):
     assert lib.hbm_copy_calibrate(None, None, 16, 1, None, None) == gemm.ERR_INVALID_ARG
 
 
+def test_noalloc_argument_errors(lib):
+    # gemm_f32_splitk_noalloc rejects bad arguments before touching a device
+    f = gemm.gemm_f32_splitk_noalloc
+    ok = dict(M=4, N=4, K=4, alpha=1.0, A=256, lda=4, B=256, ldb=4, beta=0.0, C=256, ldc=4)
+
+    def call(split=0, **kw):
+        a = dict(ok, **kw)
+        return f(a["M"], a["N"], a["K"], a["alpha"], a["A"], a["lda"], a["B"], a["ldb"],
+                 a["beta"], a["C"], a["ldc"], split, 0)
+    assert call(split=-1) == gemm.ERR_INVALID_ARG
+    assert call(split=gemm.NOALLOC_MAX_SPLIT + 1) == gemm.ERR_INVALID_ARG
+    assert call(M=-1) == gemm.ERR_INVALID_ARG
+    assert call(K=-1) == gemm.ERR_INVALID_ARG
+    assert call(lda=3) == gemm.ERR_INVALID_ARG   # lda < K
+    assert call(ldb=3) == gemm.ERR_INVALID_ARG   # ldb < N
+    assert call(ldc=3) == gemm.ERR_INVALID_ARG   # ldc < N
+    assert call(C=None) == gemm.ERR_INVALID_ARG
+    assert call(A=None) == gemm.ERR_INVALID_ARG
+    assert call(M=0, A=None, B=None, C=None) == gemm.OK  # empty: nothing to do
+
+
+def test_profile_stamps_argument_check(lib):
+    assert lib.gemm_set_profile_stamps(4) == gemm.ERR_INVALID_ARG  # not 8-byte aligned
+    assert lib.gemm_set_profile_stamps(None) == gemm.OK
+
+
 def test_empty_products_are_noops_without_a_device(lib):
     # M == 0 or N == 0: nothing to do, no device needed, NULL pointers allowed
     assert gemm.gemm_f32(0, 5, 5, None, 5, None, 5, None, 5, 0, 0) == gemm.OK

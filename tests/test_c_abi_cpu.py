@@ -33,6 +33,8 @@ int main(void) {
   if (rc != GEMM_ERR_INVALID_ARG) return 14;
   rc = gemm_f32(64, 64, 64, NULL, 64, NULL, 64, NULL, 64, GEMM_MODE_AUTO, 0);
   if (rc != GEMM_ERR_INVALID_ARG) return 15;
+  printf("noalloc %llu %d\n", (unsigned long long)GEMM_NOALLOC_SCRATCH_BYTES,
+         (int)GEMM_NOALLOC_MAX_SPLIT);
   puts("ok");
   return 0;
 }
@@ -67,3 +69,7 @@ def test_header_and_library_from_c(tmp_path):
     r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
     assert r.returncode == 0 and r.stdout.strip().endswith("ok"), (r.returncode, r.stdout,
                                                                    r.stderr)
+    # the binding's copies of the header's no-allocation limits
+    from roofline_gb300 import gemm
+    line = [l for l in r.stdout.splitlines() if l.startswith("noalloc ")][0]
+    assert line.split()[1:] == [str(gemm.NOALLOC_SCRATCH_BYTES), str(gemm.NOALLOC_MAX_SPLIT)]

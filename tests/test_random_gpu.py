@@ -7,11 +7,10 @@ import numpy as np
 import pytest
 
 import oracle
-from tests.gpu_util import TOL_E1
+from tests.gpu_util import TOL_E1, tol_tf32
 from workloads import matrix
 
 N_CASES = 64
-TOL_TF32 = 2e-3  # each operand rounded to 11 significant bits (see test_gemm_gpu.py)
 
 
 def _dense(x):
@@ -82,7 +81,7 @@ def test_random_case(i, monkeypatch):
     if pads[2]:
         assert np.all(np.isnan(out[:, N:])), "padding columns of C were written"
     ref, D = oracle.gemm(_dense(A), _dense(B), alpha, beta, _dense(Cs[:, :N]), with_bound=True)
-    tol = TOL_TF32 if mode == "tf32" else TOL_E1
+    tol = tol_tf32(K) if mode == "tf32" else TOL_E1
     e1 = oracle.err_normalised(out[:, :N], ref, D)
     assert e1 <= tol, (M, N, K, pads, alpha, beta, mode, ta, tb, streamk, e1)
     assert gemm.check_status() == gemm.OK
