@@ -107,7 +107,8 @@ int tc_ctas_per_sm(int bm, int bn, int bk, int stages, int a_inkernel, int conca
                    int smem_per_sm);
 int tc_read_and_clear_status(cudaStream_t s);
 
-// SIMT tile (simt.cu): 64 x 128 x 16, 128 threads, 4 stages.
+// CUDA-core tile (simt.cu): 64 x 128, 8 x 8 per thread, 128 threads, K in
+// BK-deep stages.
 struct SimtConfig {
   int bm, bn, bk, threads;
 };
@@ -115,9 +116,7 @@ SimtConfig simt_config();
 // Built (BK, stages) pairs of the 64 x 128 CUDA-core tile; the first is the default.
 #define GG_SIMT_CONFIGS(X) X(16, 4) X(32, 2)
 bool simt_config_valid(int bk, int stages);
-// The duplicated-A CUDA-core kernel (simt2.cu) and its built (BK, stages).
-bool simt2_config_valid(int bk, int stages);
-cudaError_t launch_simt2(const gemm_plan_t &plan, const GemmArgs &p, float *ws, cudaStream_t s);
+
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 

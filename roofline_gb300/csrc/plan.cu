@@ -113,6 +113,22 @@ void plan_simt(int64_t M, int64_t N, int64_t K, bool vec, const DeviceProps &dp,
 
 }  // namespace
 
+// Small 3xTF32 products that run fastest as one CTA per 128 x 64 tile, both
+// operands pre-split, no stream-K: the tiles fit one wave, N > 64 and K is
+// moderate against the tile count (K <= 2048 and K <= 16 per tile; with
+// fewer tiles or a longer K, spreading K over more SMs wins).  GB300 step
+// times, this / the stream-K plan (us): 512^3 13.7 / 15.4, 640^3 16.4 /
+// 17.5, 768^3 20.1 / 21.9, 1024^3 23.7 / 26.4, 1200 x 640 x 336 15.1 / 20.0;
+// A with lda not a multiple of 4: 1023 x 1025 x 777 35.0 / 37.6, 1000 x
+// 1000 x 1001 30.5 / 37.0, 1200 x 640 x 333 16.9 / 20.9, 1024^2 x 1024
+// 25.3 / 29.7, 900 x 1100 x 2000 42.9 / 43.6; outside the rule 1024^2 x
+// 4096 70.8 / 50.4, 2048 x 1024 x 1024 41.7 / 28.5, 384 x 384 x 1024
+// 20.5 us against 14.3 on the CUDA cores.
+static bool small_tc_product(int64_t M, int64_t N, int64_t K, int64_t sms) {
+  const int64_t tiles64 = ceil_div(M, 128) * ceil_div(N, 64);
+  return N > 64 && K <= 2048 && K <= 16 * tiles64 && tiles64 <= sms;
+}
+
 // Shapes the tensor-core path takes: the split pre-passes tile K in 32-deep
 // rows of a grid's y dimension, and TMA tile coordinates are 32-bit.
 static bool tc_shape_fits(int64_t M, int64_t N, int64_t K) {
@@ -155,7 +171,13 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
     // 28.8 / 42.9; 128 x 1024 x 8192 47.3 / 43.0, 256 x 256 x 65536
     // 172 / 123).
     const bool tiny_c = (double)M * (double)N <= 65536.0 && K <= 16384;
-    const bool big = (double)M * N * K >= 2.0e8 && K >= 128 && M >= 128 && !tiny_c;
+    // (from 1.2e8 multiply-adds for the small products above: 512^3 13.7
+    // us against 14.4 on the CUDA cores, 768 x 768 x 256 10.6 / 14.4, 512 x
+    // 2048 x 128 10.5 / 12.3; 256 x 1024 x 512 14.3 / 14.4)
+    const int64_t sms0 = dp.sm_count > 0 ? dp.sm_count : 152;
+    const double mnk = (double)M * N * K;
+    const bool big = (mnk >= 2.0e8 || (mnk >= 1.2e8 && small_tc_product(M, N, K, sms0))) &&
+                     K >= 128 && M >= 128 && !tiny_c;
     resolved = (tc_supported(dp) && big && tc_shape_fits(M, N, K)) ? GEMM_MODE_TF32X3
                                                          : GEMM_MODE_FP32_SIMT;
   }
@@ -241,6 +263,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
                         4 * ceil_div(N, 256) * 256 <= 5 * ceil_div(N, 128) * 128;
       p.a_split_in_kernel = a_aligned ? 1 : 0;
       p.launches = 2;  // the split pass (A and B in one launch when both are split) and the GEMM
+      bool no_stream_k = false;  // a configuration chosen to run one CTA per tile
       auto set = [&](int bn, int bk, int st, int cc, int bm = 128) {
         p.bm = bm; p.bn = bn; p.bk = bk; p.stages = st; p.b_concat = cc;
       };
@@ -308,6 +331,13 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
         const int64_t tiles128 = ceil_div(M, 128) * ceil_div(N, 128);
         if (2 * tiles128 <= sms) set(128, 16, 6, 1);
         else set(128, 16, 3, 1);
+      }
+      // small products: one CTA per 128 x 64 tile, no fix-up (small_tc_product)
+      if (x3 && small_tc_product(M, N, K, sms)) {
+        set(64, 32, 4, 1);
+        pre_split();
+        p.a_hi_tmem = 0;
+        no_stream_k = true;
       }
       // Tuning knob: GEMM_TC_CONFIG="bn,bk,stages,a_split,b_concat" (128-row
       // tile) or "bm,bn,bk,stages,a_split,b_concat" picks one of the built
@@ -380,6 +410,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
         // tile 25.6 us against 27.1 us, 1024 x 1024 x 4096 stream-K)
         bool want = (tiles % slots) != 0 && tiles < 8 * slots &&
                     (hbm_bound || (x3 && 2 * tiles <= sms) || t_sk < t_dp);
+        if (no_stream_k) want = false;
         if (sk) want = std::atoi(sk) != 0;
         p.stream_k = (want && g >= 2) ? 1 : 0;
         p.grid_ctas = p.stream_k ? g : tiles;

@@ -71,8 +71,11 @@ constexpr int kThreadsP = 128;
 // stored K x N; with B stored N x K plain row order (1) is 3-4 % faster.
 constexpr int kGroupM = 8;
 
+// Three CTAs per SM (12 warps): 150 registers a thread fit 3 x 128 threads in
+// the SM's 65536 (capping at 128 registers for four spills and ran 2-10 %
+// slower on GB300).
 template <int BM, int BN, int BK, int STAGES, bool VEC, bool TA, bool TB>
-__global__ void __launch_bounds__(kThreadsP, 2)
+__global__ void __launch_bounds__(kThreadsP, 3)
 simt_packed_kernel(GemmArgs p, int64_t k_per_split, float *__restrict__ ws, int ws_vec,
                    int group_m, unsigned long long *stamps) {
   constexpr int TM = 8, TN = 8;
@@ -94,6 +97,8 @@ simt_packed_kernel(GemmArgs p, int64_t k_per_split, float *__restrict__ ws, int 
   constexpr int A_COPIES = TA ? BK * BM / 4 : BM * BK;
   constexpr int B_COPIES = TB ? BK * BN : BK * BN / 4;
   static_assert(A_COPIES % kThreadsP == 0 && B_COPIES % kThreadsP == 0, "whole copies per thread");
+  static_assert(BM % 16 == 0 && BN % 16 == 0 && 512 % BM == 0 && 512 % BN == 0 &&
+                BM / 16 <= 32 && BN / 16 <= 32, "copy strides below assume these tile sizes");
   constexpr int A_PER_T = A_COPIES / kThreadsP;
   constexpr int B_PER_T = B_COPIES / kThreadsP;
 
@@ -125,93 +130,111 @@ simt_packed_kernel(GemmArgs p, int64_t k_per_split, float *__restrict__ ws, int 
   const int64_t klen = kend > kbeg ? kend - kbeg : 0;
   const int ntiles = (int)((klen + BK - 1) / BK);
 
-  // Per-copy source pointers at k = kbeg, and how much of each copy lies in
-  // the matrix: element copy -> its row is in range (0/1); vector copy -> the
-  // number of its 4 columns in range.
-  const float *a_src[A_PER_T];
-  int a_ok[A_PER_T];
+  // Copies.  Copy j of this thread (e = tid + 128 j of the stage's copies)
+  // reaches, for each operand, one base pointer plus a fixed stride:
+  //   element copies of A stored M x K: row a_r0 + 16 (j % AJ), k a_k0 +
+  //     8 (j / AJ), AJ = BM / 16;  16-byte copies of A stored K x M: k row
+  //     a_r0 + (512 / BM) j, columns a_q .. a_q + 3;
+  //   16-byte copies of B stored K x N: k row b_r0 + (512 / BN) j, columns
+  //     b_q .. b_q + 3;  element copies of B stored N x K: column b_r0 +
+  //     16 (j % BJ), k b_k0 + 8 (j / BJ), BJ = BN / 16.
+  // A bit mask (element copies) or a count of in-range columns (16-byte
+  // copies) says which lie inside the matrix; pointers to the rest are
+  // formed but never read (the copy's source size is 0).  Holding one base
+  // per operand instead of one pointer per copy keeps the registers for the
+  // accumulators.
+  constexpr int AJ = BM / 16, BJ = BN / 16;
+  const float *a_base;
+  uint32_t a_mask = 0;
+  int a_cols = 0, a_r0, a_k0 = 0;
+  if (!TA) {
+    a_r0 = tid / 8;
+    a_k0 = tid % 8;
 #pragma unroll
-  for (int j = 0; j < A_PER_T; ++j) {
-    const int e = tid + j * kThreadsP;
-    if (!TA) {
-      const int kk = 8 * (e / (8 * BM)) + e % 8, r = (e / 8) % BM;
-      a_ok[j] = m0 + r < p.M;
-      a_src[j] = p.A + (a_ok[j] ? (m0 + r) * p.lda + kbeg + kk : 0);
-    } else {
-      const int kr = e / (BM / 4), mq = (e % (BM / 4)) * 4;
-      const int64_t left = p.M - (m0 + mq);
-      a_ok[j] = (int)(left > 4 ? 4 : (left < 0 ? 0 : left));
-      a_src[j] = p.A + (kbeg + kr < p.K && a_ok[j] > 0 ? (kbeg + kr) * p.lda + m0 + mq : 0);
-    }
+    for (int j = 0; j < AJ; ++j)
+      if (m0 + a_r0 + 16 * j < p.M) a_mask |= 1u << j;
+    a_base = p.A + (m0 + a_r0) * p.lda + kbeg + a_k0;
+  } else {
+    a_r0 = tid / (BM / 4);
+    const int64_t a_q = (tid % (BM / 4)) * 4, left = p.M - (m0 + a_q);
+    a_cols = (int)(left > 4 ? 4 : (left < 0 ? 0 : left));
+    a_base = p.A + (kbeg + a_r0) * p.lda + m0 + a_q;
   }
-  const int64_t a_step = TA ? (int64_t)BK * p.lda : BK;
-  const float *b_src[B_PER_T];
-  int b_ok[B_PER_T];
+  const float *b_base;
+  uint32_t b_mask = 0;
+  int b_cols = 0, b_r0, b_k0 = 0;
+  if (!TB) {
+    b_r0 = tid / (BN / 4);
+    const int64_t b_q = (tid % (BN / 4)) * 4, left = p.N - (n0 + b_q);
+    b_cols = (int)(left > 4 ? 4 : (left < 0 ? 0 : left));
+    b_base = p.B + (kbeg + b_r0) * p.ldb + n0 + b_q;
+  } else {
+    b_r0 = tid / 8;
+    b_k0 = tid % 8;
 #pragma unroll
-  for (int s = 0; s < B_PER_T; ++s) {
-    const int e = tid + s * kThreadsP;
-    if (!TB) {
-      const int kr = e / (BN / 4), cq = (e % (BN / 4)) * 4;
-      const int64_t left = p.N - (n0 + cq);
-      b_ok[s] = (int)(left > 4 ? 4 : (left < 0 ? 0 : left));
-      b_src[s] = p.B + (kbeg + kr < p.K && b_ok[s] > 0 ? (kbeg + kr) * p.ldb + n0 + cq : 0);
-    } else {
-      const int kk = 8 * (e / (8 * BN)) + e % 8, c = (e / 8) % BN;
-      b_ok[s] = n0 + c < p.N;
-      b_src[s] = p.B + (b_ok[s] ? (n0 + c) * p.ldb + kbeg + kk : 0);
-    }
+    for (int j = 0; j < BJ; ++j)
+      if (n0 + b_r0 + 16 * j < p.N) b_mask |= 1u << j;
+    b_base = p.B + (n0 + b_r0) * p.ldb + kbeg + b_k0;
   }
-  const int64_t b_step = TB ? BK : (int64_t)BK * p.ldb;
+  const int a_q = TA ? (tid % (BM / 4)) * 4 : 0;
+  const int b_q = TB ? 0 : (tid % (BN / 4)) * 4;
 
-  auto issue = [&](int t) {
+  // copy c of the stage of tile t: A's copies first, then B's
+  auto issue_copy = [&](int t, int c) {
     const int buf = t % STAGES;
     const int rem = (int)min(klen - (int64_t)t * BK, (int64_t)BK);
-#pragma unroll
-    for (int j = 0; j < A_PER_T; ++j) {
-      const int e = tid + j * kThreadsP;
-      const float *src = a_src[j] + (int64_t)t * a_step;
+    if (c < A_PER_T) {
+      const int j = c;
       if (!TA) {
-        const int kk = 8 * (e / (8 * BM)) + e % 8, r = (e / 8) % BM;
-        const bool ok = a_ok[j] && kk < rem;
-        cp_async4(&As[buf][kk][r], ok ? src : p.A, ok);
+        const int jr = j % AJ, jk = j / AJ;
+        const int kk = a_k0 + 8 * jk;
+        const bool ok = ((a_mask >> jr) & 1u) && kk < rem;
+        const float *src = a_base + (int64_t)(16 * jr) * p.lda + (int64_t)t * BK + 8 * jk;
+        cp_async4(&As[buf][kk][a_r0 + 16 * jr], ok ? src : p.A, ok);
       } else {
-        const int kr = e / (BM / 4), mq = (e % (BM / 4)) * 4;
-        float *dst = &As[buf][kr][mq];
+        const int kr = a_r0 + (512 / BM) * j;
+        const float *src = a_base + ((int64_t)t * BK + (512 / BM) * j) * p.lda;
+        float *dst = &As[buf][kr][a_q];
         const bool row_ok = kr < rem;
-        if (VEC && row_ok && a_ok[j] == 4) {
+        if (VEC && row_ok && a_cols == 4) {
           cp_async16(dst, src);
         } else {
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const bool ok = row_ok && i < a_ok[j];
+            const bool ok = row_ok && i < a_cols;
             cp_async4(dst + i, ok ? src + i : p.A, ok);
           }
         }
       }
-    }
-#pragma unroll
-    for (int s = 0; s < B_PER_T; ++s) {
-      const int e = tid + s * kThreadsP;
-      const float *src = b_src[s] + (int64_t)t * b_step;
+    } else {
+      const int j = c - A_PER_T;
       if (!TB) {
-        const int kr = e / (BN / 4), cq = (e % (BN / 4)) * 4;
-        float *dst = &Bs[buf][kr][cq];
+        const int kr = b_r0 + (512 / BN) * j;
+        const float *src = b_base + ((int64_t)t * BK + (512 / BN) * j) * p.ldb;
+        float *dst = &Bs[buf][kr][b_q];
         const bool row_ok = kr < rem;
-        if (VEC && row_ok && b_ok[s] == 4) {
+        if (VEC && row_ok && b_cols == 4) {
           cp_async16(dst, src);
         } else {
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const bool ok = row_ok && i < b_ok[s];
+            const bool ok = row_ok && i < b_cols;
             cp_async4(dst + i, ok ? src + i : p.B, ok);
           }
         }
       } else {
-        const int kk = 8 * (e / (8 * BN)) + e % 8, c = (e / 8) % BN;
-        const bool ok = b_ok[s] && kk < rem;
-        cp_async4(&Bs[buf][kk][c], ok ? src : p.B, ok);
+        const int jr = j % BJ, jk = j / BJ;
+        const int kk = b_k0 + 8 * jk;
+        const bool ok = ((b_mask >> jr) & 1u) && kk < rem;
+        const float *src = b_base + (int64_t)(16 * jr) * p.ldb + (int64_t)t * BK + 8 * jk;
+        cp_async4(&Bs[buf][kk][b_r0 + 16 * jr], ok ? src : p.B, ok);
       }
     }
+  };
+  constexpr int NCOPY = A_PER_T + B_PER_T;
+  auto issue = [&](int t) {
+#pragma unroll
+    for (int c = 0; c < NCOPY; ++c) issue_copy(t, c);
   };
 
   float2 acc[TM][TN / 2];
@@ -343,15 +366,7 @@ __global__ void splitk_reduce_kernel(GemmArgs p, const float *__restrict__ ws, i
 
 SimtConfig simt_config() { return SimtConfig{64, 128, 16, kThreadsP}; }
 
-// Which CUDA-core kernel runs: this file's packed kernel unless
-// GEMM_SIMT_KERNEL=2 asks for the duplicated-A kernel (simt2.cu).
-bool simt_use_dup() {
-  const char *v = std::getenv("GEMM_SIMT_KERNEL");
-  return v && std::atoi(v) == 2;
-}
-
 bool simt_config_valid(int bk, int stages) {
-  if (simt_use_dup()) return simt2_config_valid(bk, stages);
 #define GG_SIMT(BK_, ST_) \
   if (bk == BK_ && stages == ST_) return true;
   GG_SIMT_CONFIGS(GG_SIMT)
@@ -423,7 +438,6 @@ cudaError_t launch_packed(const gemm_plan_t &plan, const GemmArgs &p, float *ws,
 
 cudaError_t launch_simt(const gemm_plan_t &plan, const GemmArgs &p, float *ws, cudaStream_t s) {
   if (plan.bm != 64 || plan.bn != 128) return cudaErrorInvalidValue;
-  if (simt_use_dup()) return launch_simt2(plan, p, ws, s);
 #define GG_SIMT(BK_, ST_)                                                              \
   if (plan.bk == BK_ && plan.stages == ST_) {                                          \
     if (!p.ta && !p.tb) return launch_packed<64, 128, BK_, ST_, false, false>(plan, p, ws, s); \

@@ -224,7 +224,7 @@ struct TcParams {
   int64_t ldc;
   int num_kb;        // K blocks per output tile
   int tiles_m, tiles_n;  // output tiles along M and N
-  int col_order;     // tile t = n_tile * tiles_m + m_tile (1) or m_tile * tiles_n + n_tile (0)
+  int group_n;       // tile order: bands of group_n column-tiles, each walked down its rows
   int waves;         // whole tiles per CTA before the stream-K part
   int64_t dp_tiles;  // waves * G: tiles done whole, in waves
   int64_t sk_units;  // (tiles - dp_tiles) * num_kb: units shared out stream-K
@@ -234,16 +234,22 @@ struct TcParams {
   unsigned long long *stamps;  // measurement aid (gemm_set_profile_stamps), or nullptr
 };
 
-// Row-tile and column-tile of output tile t.
+// Row-tile and column-tile of output tile t.  Tiles are numbered in bands of
+// group_n column-tiles (the last band may be narrower): band b holds tiles
+// [b * group_n * tiles_m, (b + 1) * group_n * tiles_m), walked row by row
+// across the band.  group_n = 1 is plain column order, group_n = tiles_n
+// plain row order; in between, the tiles resident at one time cover a block
+// of about (G / group_n) row-tiles by group_n column-tiles.
 __host__ __device__ __forceinline__ void tile_coords(const TcParams &p, int64_t t, int64_t &mt,
                                                      int64_t &nt) {
-  if (p.col_order) {
-    mt = t % p.tiles_m;
-    nt = t / p.tiles_m;
-  } else {
-    mt = t / p.tiles_n;
-    nt = t % p.tiles_n;
-  }
+  const int64_t band_tiles = (int64_t)p.group_n * p.tiles_m;
+  const int64_t band = t / band_tiles;
+  const int64_t first_n = band * p.group_n;
+  const int64_t left = p.tiles_n - first_n;
+  const int64_t width = left < p.group_n ? left : p.group_n;
+  const int64_t local = t - band * band_tiles;
+  mt = local / width;
+  nt = first_n + local % width;
 }
 
 // Work split.  CTA c of G first takes `waves` whole tiles, c, c + G, ...:

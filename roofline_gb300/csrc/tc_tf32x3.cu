@@ -44,6 +44,7 @@
 // kernel records GEMM_ERR_DEVICE_TIMEOUT in a device status word, stops
 // issuing work, waits (bounded) for the copies and MMAs it already issued,
 // frees its TMEM and returns.
+#include <cmath>
 #include <cstdlib>
 #include <mutex>
 
@@ -70,8 +71,8 @@ template <int BM, int BN, int BK, int STAGES, int AK, bool CONCAT, int NPROD>
 struct TcCfg {
   static_assert(NPROD == 3 || NPROD == 1, "3xTF32 or 1xTF32");
   static_assert(NPROD == 3 || !CONCAT, "1xTF32 has no B_lo to concatenate");
-  static_assert(BM == 128 || (BM == 256 && !AK && !CONCAT),
-                "a 256-row tile takes pre-split operands and separate B planes");
+  static_assert(BM == 128 || (BM == 256 && AK != 2 && (AK || !CONCAT)),
+                "a 256-row tile keeps A_hi in shared memory; concatenated B only with A split on chip");
   static_assert(AK >= 0 && AK <= 2 && (AK != 2 || NPROD == 3), "A_hi in TMEM is a 3xTF32 form");
   static constexpr bool X3 = NPROD == 3;
   static constexpr int MH = BM / 128;  // 128-row halves, one accumulator each
@@ -85,9 +86,12 @@ struct TcCfg {
   static constexpr int ROW_BYTES = BK * 4;              // 64 or 128
   static constexpr uint32_t LAYOUT = ROW_BYTES == 128 ? 2u : 4u;
   static constexpr uint32_t SBO = 8 * ROW_BYTES;        // 8-row group stride
-  static constexpr int ACC_COLS = MH * (CONCAT ? 2 * BN : BN);
+  static constexpr int ACC_HALF = CONCAT ? 2 * BN : BN;  // accumulator columns of one half
+  static constexpr int ACC_COLS = MH * ACC_HALF;
   static constexpr int LO_COL0 = ACC_COLS;
-  static constexpr int LO_COLS = (AK && X3) ? STAGES * BK : 0;
+  // A_lo ring: STAGES x BK columns for each 128-row half
+  static constexpr int LO_RING = (AK && X3) ? STAGES * BK : 0;
+  static constexpr int LO_COLS = MH * LO_RING;
   // AK == 2: the converters also put A_hi in a tensor-memory ring (the MMAs
   // read both A parts from TMEM; shared memory then carries only B)
   static constexpr bool HI_TMEM = AK == 2;
@@ -303,7 +307,7 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
           tc_fence_after();
           const uint32_t ah = smem_u32(a_hi(s)), al = smem_u32(a_lo(s));
           const uint32_t bh = smem_u32(b_hi(s)), bl = smem_u32(b_lo(s));
-          const uint32_t lo_t = tmem_base + (uint32_t)(Cfg::LO_COL0 + s * BK);
+          const uint32_t lo_t0 = tmem_base + (uint32_t)(Cfg::LO_COL0 + s * BK);
           const uint32_t hi_t = tmem_base + (uint32_t)(Cfg::HI_COL0 + s * BK);
 #pragma unroll
           for (int kk = 0; kk < BK / 8; ++kk) {
@@ -315,7 +319,8 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
             for (int h = 0; h < Cfg::MH; ++h) {
               const uint32_t ah_h = ah + h * Cfg::A_HALF_BYTES + off;
               const uint32_t al_h = al + h * Cfg::A_HALF_BYTES + off;
-              const uint32_t d = tmem_base + (uint32_t)(h * BN);
+              const uint32_t d = tmem_base + (uint32_t)(h * Cfg::ACC_HALF);
+              const uint32_t lo_t = lo_t0 + (uint32_t)(h * Cfg::LO_RING);
               const uint64_t dah = smem_desc(ah_h, Cfg::SBO, Cfg::LAYOUT);
               if (!X3) {
                 mma_tf32(d, dah, dbh, idesc, acc);  // 1xTF32: A_hi * B_hi only
@@ -384,9 +389,12 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
             ok = false;
             break;
           }
-          // Row `row` of the landed tile: 16-byte chunk c sits at chunk
-          // c ^ f(row) of its 64- or 128-byte line (the TMA swizzle).
-          uint8_t *line = a_hi(s) + row * Cfg::ROW_BYTES;
+          // Row `row` of each 128-row half of the landed tile: 16-byte
+          // chunk c sits at chunk c ^ f(row) of its 64- or 128-byte line (the
+          // TMA swizzle; f depends on the row's low bits only).
+#pragma unroll 1
+          for (int half = 0; half < Cfg::MH; ++half) {
+          uint8_t *line = a_hi(s) + (half * 128 + row) * Cfg::ROW_BYTES;
           if constexpr (!X3) {
             // 1xTF32: round in place, nothing goes to tensor memory.  Chunks
             // are visited in swizzled order so a warp's 32 rows hit 32
@@ -403,7 +411,6 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
               *ptr = x;
             }
             fence_async_smem();
-            mbar_arrive(&conv[s]);
           } else {
             uint32_t lo[BK];
             uint32_t hi[BK];  // used (and kept in registers) only with A_hi in TMEM
@@ -430,14 +437,15 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
                 *ptr = h;
               }
             }
-            tmem_st<BK>(lane_base + (uint32_t)(Cfg::LO_COL0 + s * BK), lo);
+            tmem_st<BK>(lane_base + (uint32_t)(Cfg::LO_COL0 + half * Cfg::LO_RING + s * BK), lo);
             if constexpr (Cfg::HI_TMEM)
               tmem_st<BK>(lane_base + (uint32_t)(Cfg::HI_COL0 + s * BK), hi);
             tmem_st_wait();
             if (!Cfg::HI_TMEM) fence_async_smem();  // A_hi in shared memory -> visible to the MMA
-            tc_fence_before();
-            mbar_arrive(&conv[s]);
           }
+          }  // halves
+          if constexpr (X3) tc_fence_before();
+          mbar_arrive(&conv[s]);
         }
         if (!ok) break;
       }
@@ -458,7 +466,7 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
 #pragma unroll 1
       for (int h = 0; h < Cfg::MH; ++h) {
         const int tr0 = h * 128 + quarter * 32;  // this warp's first row within the tile
-        const uint32_t lane_acc = lane_base + (uint32_t)(h * BN);
+        const uint32_t lane_acc = lane_base + (uint32_t)(h * Cfg::ACC_HALF);
         // whole tiles go to C; partial tiles (stream-K) to this CTA's slot,
         // 0 for its first stream-K segment, 1 for its last
         float *dst_row0;
@@ -630,21 +638,39 @@ int launch_cfg(const gemm_plan_t &plan, const GemmArgs &a, char *ws, cudaStream_
   p.num_kb = num_kb;
   p.tiles_m = (int)tiles_m;
   p.tiles_n = (int)tiles_n;
-  // Tile order.  The tiles left for the stream-K part come last; their CTAs
-  // sit at unrelated K positions, so whichever operand they share must stay
-  // in L2.  Numbering tiles down the columns puts them in a few column
-  // blocks (sharing B's planes); along the rows, in a few row blocks
-  // (sharing A).  Take the order that shares the operand with more bytes in
-  // the GEMM: B (hi + lo, 8 bytes a value in 3xTF32) against A (4 bytes raw
-  // when split on chip, 8 pre-split; 1xTF32: 4 and 4).  GB300, 3xTF32 with
-  // 128 x 256 tiles, rows / columns: 4096^3 460 / 445 us, 3072 x 4096 x 4096
-  // 399 / 367 us, 6144^3 1.54 / 1.48 ms, 2048 x 8192 x 4096 513 / 491 us,
-  // 8192 x 2048 x 4096 457 / 469 us; even for 256 x 256 tiles.
-  // Tuning knob: GEMM_TC_ORDER = 0 (rows) / 1 (columns).
+  // Tile order: bands of group_n column-tiles (see tile_coords).
+  // One CTA per tile (no stream-K): the CTAs resident at one time work on
+  // about a wave of tiles; they stream, K block by K block, the A rows of the
+  // band rows they cover and the B columns of the band, which L2 shares
+  // between them.  Per wave that is (wave / group_n) row tiles of A bytes a
+  // and group_n column tiles of B bytes b, least at group_n = sqrt(wave * a /
+  // b).  GB300, 3xTF32 8192^3 (128 x 256 tiles, bands of 6): DRAM traffic
+  // 3.68 GB per launch against 4.76 GB in plain column order, same time.
+  // Stream-K grids: plain column order when B's bytes in the GEMM exceed A's
+  // (B's planes are 8 bytes a value in 3xTF32, A split on chip 4), else plain
+  // row order; the tiles left for the stream-K part come last and their
+  // CTAs, at unrelated K positions, then share the larger operand in L2
+  // (4096^3 with 152 persistent CTAs: 381 us per kernel in column order,
+  // 408 us in bands of 6).
+  // Tuning knobs: GEMM_TC_GROUP = group_n; GEMM_TC_ORDER = 0 (plain rows) /
+  // 1 (plain columns).
   {
-    const double a_bytes = (double)a.M * (AK || !X3 ? 4.0 : 8.0);
-    const double b_bytes = (double)a.N * (X3 ? 8.0 : 4.0);
-    p.col_order = (int)env_u64("GEMM_TC_ORDER", a_bytes < b_bytes ? 1 : 0);
+    const double a_bytes = (double)BM * (AK || !X3 ? 4.0 : 8.0);
+    const double b_bytes = (double)BN * (X3 ? 8.0 : 4.0);
+    int64_t gn;
+    if (plan.stream_k) {
+      gn = (a_bytes / BM) * (double)a.M < (b_bytes / BN) * (double)a.N ? 1 : tiles_n;
+    } else {
+      int64_t wave = (int64_t)current_props().sm_count * plan.ctas_per_sm;
+      if (wave > tiles) wave = tiles;
+      if (wave < 1) wave = 1;
+      gn = (int64_t)std::lround(std::sqrt((double)wave * a_bytes / b_bytes));
+    }
+    if (const char *o = std::getenv("GEMM_TC_ORDER")) gn = std::atoi(o) == 1 ? 1 : tiles_n;
+    gn = (int64_t)env_u64("GEMM_TC_GROUP", (uint64_t)gn);
+    if (gn < 1) gn = 1;
+    if (gn > tiles_n) gn = tiles_n;
+    p.group_n = (int)gn;
   }
   // Whole-tile waves first, the rest of the tiles stream-K (G == tiles
   // without stream-K: one wave).  A short stream-K part would give each CTA
@@ -735,6 +761,8 @@ bool tc_supported(const DeviceProps &dp) { return dp.cc_major == 10 && dp.cc_min
 // kernel (0 no, 1 with A_hi in shared memory, 2 with A_hi in tensor memory),
 // concatenated B MMA, TF32 products per FP32 product).
 #define GG_TC_CONFIGS(X)                  \
+  X(128, 64, 16, 6, 0, true, 3)         \
+  X(128, 64, 32, 4, 0, true, 3)         \
   X(128, 256, 16, 5, 1, false, 3)       \
   X(128, 256, 16, 5, 2, false, 3)       \
   X(128, 128, 32, 4, 2, true, 3)        \

@@ -170,7 +170,7 @@ def test_tc_plans_on_cpu(lib):
     # A pre-split anyway (leading dimension not a multiple of 4) and many tiles: 256 x 256
     big2 = gemm.plan(8192, 8192, 8191, 8191, 8192, 8192, mode="tf32x3")
     assert (big2["bm"], big2["bn"], big2["a_split_in_kernel"]) == (256, 256, 0)
-    assert gemm.plan(512, 512, 512)["kernel_name"] == "simt"  # auto, small
+    assert gemm.plan(384, 384, 1024)["kernel_name"] == "simt"  # auto: few tiles, long K
 
 
 def test_stream_k_plan_bounds(lib):
@@ -195,9 +195,12 @@ def test_auto_choice(lib):
     256 x 256 (or K > 16384)."""
     tc = [(1023, 1025, 777, 777, 1025, 1025), (640, 640, 640), (1024, 1024, 1024),
           (2048, 2048, 512), (4096, 64, 4096), (512, 512, 1024), (128, 2048, 1024),
-          (128, 1024, 8192), (256, 256, 65536)]
-    simt = [(512, 512, 512), (576, 576, 576), (4096, 4096, 64), (8192, 8192, 32),
-            (64, 4096, 4096), (1024, 1024, 128), (300, 300, 2000), (128, 128, 16384),
+          (128, 1024, 8192), (256, 256, 65536),
+          # small products that fit one wave of 128 x 64 tiles (13.7 against
+          # 14.4 us at 512^3; 10.6 / 14.4 at 768 x 768 x 256)
+          (512, 512, 512), (768, 768, 256), (512, 2048, 128), (576, 576, 576)]
+    simt = [(4096, 4096, 64), (8192, 8192, 32), (384, 384, 1024),
+            (64, 4096, 4096), (300, 300, 2000), (128, 128, 16384),
             (256, 256, 4096), (128, 512, 8192)]
     for shape in tc:
         assert gemm.plan(*shape)["kernel_name"] == "tc_tf32x3", shape
@@ -242,8 +245,13 @@ def test_stream_k_choice(lib):
     # partial tiles and the fix-up (the measured GB300 choices)
     assert gemm.plan(4096, 4096, 4096, mode="tf32x3")["stream_k"] == 1
     assert gemm.plan(2560, 2560, 4096, mode="tf32x3")["stream_k"] == 1
-    assert gemm.plan(1023, 1025, 777, 777, 1025, 1025, mode="tf32x3")["stream_k"] == 1
-    assert gemm.plan(1024, 1024, 1024, mode="tf32x3")["stream_k"] == 1
+    # unaligned A with 128 x 64 tiles filling one wave: one CTA per tile, no
+    # fix-up (1023 x 1025 x 777, lda 777: 35.0 against 37.6 us stream-K)
+    r = gemm.plan(1023, 1025, 777, 777, 1025, 1025, mode="tf32x3")
+    assert (r["bn"], r["stream_k"], r["grid_ctas"]) == (64, 0, 136)
+    # a wave of 128 x 64 tiles with a moderate K: one CTA per tile
+    assert gemm.plan(1024, 1024, 1024, mode="tf32x3")["stream_k"] == 0
+    assert gemm.plan(1024, 1024, 4096, mode="tf32x3")["stream_k"] == 1
     # 1xTF32 2048^3: 64 tiles of 256 x 256 are under half a wave, so 128 x 256
     # tiles, one CTA each (48.6 us against 60.1 us stream-K on 256 x 256)
     p = gemm.plan(2048, 2048, 2048, mode="tf32")
@@ -256,8 +264,8 @@ def test_stream_k_choice(lib):
     # under one wave (128 tiles on 152 SMs): one CTA per tile
     q = gemm.plan(1024, 4096, 4096, mode="tf32x3")
     assert (q["bn"], q["stream_k"], q["grid_ctas"]) == (256, 0, 128)
-    # few tiles for the SMs (512^3: 16 tiles): split K across them
-    assert gemm.plan(512, 512, 512, mode="tf32x3")["stream_k"] == 1
+    # few tiles for the SMs and a long K (512 x 512 x 1024): split K across them
+    assert gemm.plan(512, 512, 1024, mode="tf32x3")["stream_k"] == 1
     assert gemm.plan(65536, 64, 4096, mode="tf32x3")["stream_k"] == 1
     assert gemm.plan(4096, 4096, 4096, mode="tf32")["stream_k"] == 0
     # whole waves only: no stream-K
@@ -268,7 +276,7 @@ def test_stream_k_choice(lib):
 def test_wide_tiles_from_half_a_wave(lib):
     # 128 x 256 tiles once there are at least 76 of them (half of 152 SMs)
     assert gemm.plan(1024, 4096, 4096, mode="tf32x3")["bn"] == 256
-    assert gemm.plan(512, 512, 512, mode="tf32x3")["bn"] == 128
+    assert gemm.plan(512, 512, 1024, mode="tf32x3")["bn"] == 128
 
 
 # Planner decisions checked against exhaustive GB300 sweeps (every built
@@ -282,7 +290,11 @@ MEASURED_CHOICES = [
     ((2560, 2560, 1024), "tf32x3", (128, 256, 16, 5, 1, 1, 1)),   # 66 vs 73 us
     ((1536, 1536, 1536), "tf32x3", (128, 128, 32, 4, 1, 0, 1)),
     ((8192, 384, 8192), "tf32x3", (128, 128, 32, 4, 1, 1, 1)),    # 184 vs 206 us for 128 x 256
-    ((1023, 1025, 777, 777, 1025, 1025), "tf32x3", (128, 128, 16, 6, 0, 1, 1)),  # 35.5 vs 39.7 us
+    ((1023, 1025, 777, 777, 1025, 1025), "tf32x3", (128, 64, 32, 4, 0, 0, 1)),  # 35.0 vs 37.6 us
+    ((512, 512, 512), "tf32x3", (128, 64, 32, 4, 0, 0, 1)),       # 13.7 vs 15.4 us stream-K
+    ((1024, 1024, 1024), "tf32x3", (128, 64, 32, 4, 0, 0, 1)),    # 23.7 vs 26.4 us
+    ((1000, 1000, 1001, 1001, 1000, 1000), "tf32x3", (128, 64, 32, 4, 0, 0, 1)),  # 30.5 vs 37.0 us
+    ((1200, 640, 333, 333, 640, 640), "tf32x3", (128, 64, 32, 4, 0, 0, 1)),  # 16.9 vs 20.9 us
     ((1024, 64, 8192), "tf32x3", (128, 64, 32, 6, 1, 1, 1)),      # 29.7 vs 38.2 us
     ((65536, 64, 4096), "tf32x3", (128, 64, 32, 3, 1, 1, 1)),     # 204 vs 271 us for 6 stages
     ((4096, 4096, 4096), "tf32", (256, 256, 16, 6, 0, 0, 1)),     # 212 vs 217 us for BK 32

@@ -223,9 +223,11 @@ def test_status_clear_after_normal_runs():
 TC_PLANS = [
     ((1000, 64, 96, 96), (128, 64, 32, 6, 1, 1)),       # narrow, few tiles: 6 stages, 1 CTA/SM
     ((9000, 64, 96, 96), (128, 64, 32, 3, 1, 1)),       # narrow, more tiles: 3 stages, 2 CTAs/SM
-    ((512, 512, 512, 512), (128, 128, 32, 4, 1, 1)),
+    ((512, 512, 512, 512), (128, 64, 32, 4, 0, 1)),     # small product: a CTA per 128 x 64 tile
+    ((512, 512, 1024, 1024), (128, 128, 32, 4, 1, 1)),   # few tiles, longer K: stream-K
     ((2432, 8192, 128, 128), (128, 256, 16, 5, 1, 0)),
-    ((1023, 1025, 777, 777), (128, 128, 16, 6, 0, 1)),   # A pre-split, under half a wave: 6 stages
+    ((1023, 1025, 777, 777), (128, 64, 32, 4, 0, 1)),    # small product, A pre-split
+    ((600, 600, 3000, 3001), (128, 128, 16, 6, 0, 1)),   # A pre-split, under half a wave: 6 stages
     ((5000, 250, 777, 777), (128, 128, 16, 3, 0, 1)),    # A pre-split, more tiles: 3 stages, 2 CTAs/SM
     ((2432, 8192, 129, 129), (128, 256, 16, 4, 0, 0)),
     ((5120, 8192, 64, 64), (128, 256, 16, 5, 1, 0)),   # many tiles, aligned A: split on chip
@@ -258,7 +260,7 @@ def test_tf32x3_planner_choices(shape, cfg):
 # the GEMM_TC_CONFIG knob, on one ragged shape (full check).
 TC_BUILT = ["256,16,5,1,0", "128,32,4,1,1", "64,32,6,1,1", "64,32,3,1,1", "64,32,2,1,0",
             "64,16,4,1,0", "256,16,4,0,0", "128,16,3,0,1", "128,16,6,0,1", "256,256,16,3,0,0",
-            "256,16,5,2,0", "128,32,4,2,1"]
+            "256,16,5,2,0", "128,32,4,2,1", "64,16,6,0,1", "64,32,4,0,1"]
 
 
 def _cfg(cfg):
@@ -468,7 +470,7 @@ def _waves(tiles, num_kb, G):
     return waves, rest
 
 
-@pytest.mark.parametrize("order", ["0", "1"])
+@pytest.mark.parametrize("order", ["0", "1", "g3", "g5", None])
 @pytest.mark.parametrize("mode,cfg", [("tf32x3", None), ("tf32x3", "256,256,16,3,0,0"),
                                       ("tf32", "256,16,8,0,0"), ("tf32", "256,256,16,6,0,0")])
 def test_tc_whole_waves_then_stream_k(mode, cfg, order, monkeypatch):
@@ -480,7 +482,12 @@ def test_tc_whole_waves_then_stream_k(mode, cfg, order, monkeypatch):
     if cfg:
         monkeypatch.setenv("GEMM_TC_CONFIG", cfg)
     monkeypatch.setenv("GEMM_TC_STREAMK", "1")
-    monkeypatch.setenv("GEMM_TC_ORDER", order)  # tiles numbered along rows (0) or columns (1)
+    # tiles numbered along rows (0), down columns (1), in bands of 3 or 5
+    # column-tiles, or in the planner's bands (None)
+    if order in ("0", "1"):
+        monkeypatch.setenv("GEMM_TC_ORDER", order)
+    elif order is not None:
+        monkeypatch.setenv("GEMM_TC_GROUP", order[1:])
     M, N, K = 2688 * (2 if cfg and cfg.startswith("256,256") else 1), 2048, 1024
     p = gemm.plan(M, N, K, K, N, N, mode=mode)
     tiles = -(-M // p["bm"]) * -(-N // p["bn"])
@@ -688,3 +695,32 @@ def test_profile_stamps_time_the_main_kernel(mode, shape):
     assert v[2, 0] == np.uint64(2**64 - 1) and v[2, 1] == 0  # an unset pair is untouched
     total_ns = e0.elapsed_time(e1) * 1e6
     assert (v[0, 1] - v[0, 0]) + (v[1, 1] - v[1, 0]) <= total_ns * 1.05 + 2000
+
+
+@pytest.mark.parametrize("group", ["1", "2", "3", "7", "100"])
+@pytest.mark.parametrize("streamk", ["0", "1"])
+def test_tc_tile_bands_cover_every_tile_once(group, streamk, monkeypatch):
+    # the banded tile order is a bijection of the tile grid for any band width,
+    # a narrower last band included (1300 columns = 5.1 column tiles of 256,
+    # 1000 rows = 7.8 row tiles of 128): integer inputs, every entry exact,
+    # guard bands untouched
+    monkeypatch.setenv("GEMM_TC_GROUP", group)
+    monkeypatch.setenv("GEMM_TC_STREAMK", streamk)
+    monkeypatch.setenv("GEMM_TC_CONFIG", "256,16,5,2,0")
+    got, ref, _ = _run_shape(1000, 1300, 200, "tf32x3", 1.0, 0.0, seed=int(group), dist="int2")
+    assert oracle.mismatches(got, ref) == 0
+
+
+@pytest.mark.parametrize("cfg", ["64,32,3,1,1", "64,32,6,1,1"])
+@pytest.mark.parametrize("streamk", ["0", "1"])
+@pytest.mark.parametrize("M,N", [(4173, 64), (2000, 50)])
+def test_narrow_b_tiles(cfg, streamk, M, N, monkeypatch):
+    # narrow B (N <= 64), A split on chip, with and without stream-K, a
+    # ragged last row tile
+    monkeypatch.setenv("GEMM_TC_CONFIG", cfg)
+    monkeypatch.setenv("GEMM_TC_STREAMK", streamk)
+    K = 1024
+    got, ref, D = _run_shape(M, N, K, "tf32x3", 1.0, 0.0, seed=M + N, dist="int2")
+    assert oracle.mismatches(got, ref) == 0
+    got, ref, D = _run_shape(M, N, K, "tf32x3", 0.5, 2.0, seed=M - N)
+    assert oracle.err_normalised(got, ref, D) <= TOL_E1

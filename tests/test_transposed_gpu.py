@@ -178,6 +178,7 @@ def test_op_large_transposed_sampled(mode):
     assert oracle.err_normalised(got, ref, D) <= TOL_E1
 
 
+# built (BK, stages) of the CUDA-core kernel
 SIMT_BUILT = ["16,4", "32,2"]
 
 
