@@ -138,7 +138,7 @@ __device__ __forceinline__ void split_rows_block(const SplitJob &j, int64_t blk)
 // once), the tile goes through shared memory, and each thread then stores
 // four 16-byte pieces of hi and of lo along k.  `vec` (ld % 4 == 0 and a
 // 16-byte aligned source) enables the 16-byte loads; the stores are 16-byte
-// aligned because kp is a multiple of 4.
+// aligned because kp is a multiple of 32.
 __device__ __forceinline__ void split_transpose_block(const SplitJob &j, int64_t blk,
                                                       float (*tile)[kTrN + 1]) {
   const int64_t k = j.a, n = j.b, kp = j.kp;

@@ -97,7 +97,14 @@ struct TcCfg {
   static constexpr bool HI_TMEM = AK == 2;
   static constexpr int HI_COL0 = LO_COL0 + LO_COLS;
   static constexpr int HI_COLS = HI_TMEM ? STAGES * BK : 0;
-  static constexpr int TMEM_NEED = ACC_COLS + LO_COLS + HI_COLS;
+  // C_TMEM: with A pre-split the four epilogue warps have nothing to do while
+  // the MMAs run, so for a whole tile with beta != 0 they copy C's old values
+  // into tensor memory next to the accumulator; the epilogue then reads them
+  // with it instead of from global memory after the last MMA.  Only where
+  // the columns fit in 256 (two CTAs per SM keep their tensor memory).
+  static constexpr int OLD_COL0 = HI_COL0 + HI_COLS;
+  static constexpr bool C_TMEM = AK == 0 && OLD_COL0 + MH * BN <= 256;
+  static constexpr int TMEM_NEED = OLD_COL0 + (C_TMEM ? MH * BN : 0);
   static constexpr int TMEM_COLS = TMEM_NEED <= 32    ? 32
                                    : TMEM_NEED <= 64  ? 64
                                    : TMEM_NEED <= 128 ? 128
@@ -157,25 +164,28 @@ __device__ __forceinline__ void epi_store16(float4 *st, const float *v, float *d
       }
     }
   } else {
+    // two passes of 16 rows: each issues its 8 reads of old values before
+    // its first store, so a block costs two round trips to memory
     const float *sf = reinterpret_cast<const float *>(st);
     const int j = lane & 15;
+    const int64_t ld2 = 2 * ld;
 #pragma unroll 1
-    for (int it0 = 0; it0 < 16; it0 += 4) {
-      float x[4], old[4];
+    for (int it0 = 0; it0 < 16; it0 += 8) {
+      const int r0 = it0 * 2 + (lane >> 4);
+      float *row0 = dst + (int64_t)r0 * ld + j;
+      float old[8];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int r = (it0 + u) * 2 + (lane >> 4);
-        x[u] = sf[r * 16 + (((j >> 2) ^ ((r >> 1) & 3)) << 2) + (j & 3)];
+      for (int u = 0; u < 8; ++u) {
         old[u] = 0.0f;
-        if (beta != 0.0f && r < rows && j < cols) old[u] = dst[(int64_t)r * ld + j];
+        if (beta != 0.0f && r0 + 2 * u < rows && j < cols) old[u] = row0[u * ld2];
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int r = (it0 + u) * 2 + (lane >> 4);
+      for (int u = 0; u < 8; ++u) {
+        const int r = r0 + 2 * u;
         if (r < rows && j < cols) {
-          float o = alpha * x[u];
+          float o = alpha * sf[r * 16 + (((j >> 2) ^ ((r >> 1) & 3)) << 2) + (j & 3)];
           if (beta != 0.0f) o = fmaf(beta, old[u], o);
-          dst[(int64_t)r * ld + j] = o;
+          row0[u * ld2] = o;
         }
       }
     }
@@ -380,6 +390,36 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
     Walk walk(p, blockIdx.x, G);
     Segment sg;
     while (ok && walk.next(p, sg)) {
+      if (p.beta != 0.0f && sg.kb0 == 0 && sg.kb1 == p.num_kb) {
+        // A whole tile that reads C.  C_TMEM: lane r of this warp copies row
+        // r of its 32 rows of the old C tile into tensor memory (columns
+        // OLD_COL0 + h * BN ...; zeros outside the matrix).  Otherwise those
+        // rows are requested into L2, so the epilogue's reads of the old
+        // values hit L2 instead of waiting on DRAM after the last MMA.
+        int64_t mt, nt;
+        tile_coords(p, sg.tile, mt, nt);
+        const int64_t left = p.N - nt * BN;
+        const int ncols = left < BN ? (int)left : BN;
+#pragma unroll 1
+        for (int h = 0; h < Cfg::MH; ++h) {
+          const int64_t r = mt * BM + h * 128 + quarter * 32 + lane;
+          const float *row = p.C + r * p.ldc + nt * BN;
+          if constexpr (Cfg::C_TMEM) {
+#pragma unroll 1
+            for (int c = 0; c < BN; c += 32) {
+              uint32_t v[32];
+#pragma unroll
+              for (int q = 0; q < 32; ++q)
+                v[q] = (r < p.M && c + q < ncols) ? __float_as_uint(row[c + q]) : 0u;
+              tmem_st<32>(lane_base + (uint32_t)(Cfg::OLD_COL0 + h * BN + c), v);
+            }
+          } else if (r < p.M) {
+            for (int c = 0; c < ncols; c += 32) prefetch_l2(row + c);
+            prefetch_l2(row + ncols - 1);
+          }
+        }
+        if constexpr (Cfg::C_TMEM) tmem_st_wait();
+      }
       if (AK) {
         for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++it) {
           const int s = it % STAGES;
@@ -495,6 +535,21 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
           } else {
             tmem_ld_wait();
           }
+          // C_TMEM: beta * old + alpha * acc here, row by row (the same
+          // operations epi_store16 does), and the block is only stored
+          bool folded = false;
+          if constexpr (Cfg::C_TMEM) {
+            if (whole && p.beta != 0.0f) {
+              uint32_t o[32];
+              tmem_ld32(lane_base + (uint32_t)(Cfg::OLD_COL0 + h * BN + c), o);
+              tmem_ld_wait();
+#pragma unroll
+              for (int q = 0; q < 32; ++q)
+                r[q] = __float_as_uint(fmaf(p.beta, __uint_as_float(o[q]),
+                                            p.alpha * __uint_as_float(r[q])));
+              folded = true;
+            }
+          }
           const float *v = reinterpret_cast<const float *>(r);
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
@@ -502,8 +557,8 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
             if (whole) {
               const int64_t left = p.N - (n0 + col);
               const int cols = left < 0 ? 0 : (left > 16 ? 16 : (int)left);
-              epi_store16(epi, v + 16 * hh, dst_row0 + col, ld, rows, cols, vec, p.alpha,
-                          p.beta);
+              epi_store16(epi, v + 16 * hh, dst_row0 + col, ld, rows, cols, vec,
+                          folded ? 1.0f : p.alpha, folded ? 0.0f : p.beta);
             } else {
               epi_store16(epi, v + 16 * hh, dst_row0 + col, ld, 32, 16, true, 1.0f, 0.0f);
             }
@@ -583,7 +638,11 @@ struct WsLayout {
 WsLayout ws_layout(int64_t M, int64_t N, int64_t K, bool a_inkernel, int64_t streamk_ctas,
                    int bm, int bn, bool x3) {
   WsLayout w{};
-  w.kp = round_up(K, 4);
+  // Planes' rows padded (with zeros) to a multiple of 32 floats: every TMA
+  // box (16 or 32 K values of a row) then starts on a 128-byte line of its
+  // own instead of straddling two (GB300, 1023 x 1025 x 777: kernel 26.0 ->
+  // 22.5 us; 1500^3 31.0 -> 29.2 us).
+  w.kp = round_up(K, 32);
   const uint64_t b_bytes = align256((uint64_t)N * w.kp * 4);
   const uint64_t b_lo_bytes = x3 ? b_bytes : 0;
   const uint64_t a_bytes = a_inkernel ? 0 : align256((uint64_t)M * w.kp * 4);
