@@ -316,6 +316,35 @@ def test_tf32x3_stream_k(shape, streamk, monkeypatch):
         assert oracle.err_normalised(got, ref, D) <= TOL_E1
 
 
+@pytest.mark.parametrize("cfg", ["64,32,4,0,1", "64,16,6,0,1"])
+@pytest.mark.parametrize("streamk", ["0", "1"])
+@pytest.mark.parametrize("shape,pad", [((300, 200, 1000), (1, 0, 1)), ((777, 130, 64), (0, 0, 0)),
+                                       ((129, 1025, 777), (1, 1, 3))])
+def test_old_c_through_tensor_memory(cfg, streamk, shape, pad, monkeypatch):
+    """Pre-split 128 x 64 tiles copy C's old values into tensor memory while
+    the MMAs run and fold beta * C in at the epilogue; tiles shared out
+    stream-K take C through the fix-up instead.  Both against the oracle with
+    beta != 0, unaligned and aligned ldc, ragged edges; beta == 0 must leave
+    C unread (NaN in C stays out of the result)."""
+    from roofline_gb300 import gemm
+    monkeypatch.setenv("GEMM_TC_CONFIG", cfg)
+    monkeypatch.setenv("GEMM_TC_STREAMK", streamk)
+    M, N, K = shape
+    p = gemm.plan(M, N, K, K + pad[0], N + pad[1], N + pad[2], mode="tf32x3")
+    assert (p["bm"], p["bn"], p["a_split_in_kernel"], p["b_concat"]) == (128, 64, 0, 1)
+    for alpha, beta in ((1.5, -0.75), (-1.0, 2.0)):
+        got, ref, D = _run_shape(M, N, K, "tf32x3", alpha, beta, pad=pad, offset=0,
+                                 seed=M + N + int(streamk))
+        assert oracle.err_normalised(got, ref, D) <= TOL_E1
+    import torch
+    A = torch.from_numpy(matrix(M, K, None, 5, "u11")).cuda()
+    B = torch.from_numpy(matrix(K, N, None, 6, "u11")).cuda()
+    C = torch.full((M, N), float("nan"), device="cuda")
+    gemm.matmul(A, B, C, 1.0, 0.0, "tf32x3")
+    torch.cuda.synchronize()
+    assert torch.isfinite(C).all()
+
+
 def test_tf32x3_stream_k_deterministic():
     outs = gpu_util.run("ragged", "tf32x3", repeat=3)
     for o in outs[1:]:
