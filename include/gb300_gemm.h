@@ -278,6 +278,14 @@ GEMM_API int gemm_f32_op_plan(int layout, int op_a, int op_b, int64_t M, int64_t
  * blocks of at least 1024 rows and 1024 columns, for shallower products up
  * to 4 row blocks).  Row blocks hold whole 128-row tiles and column blocks
  * whole 256-column tiles, except the last ones.
+ * With the environment variable GEMM_HOST_STREAM=1 (and blocks == 0), a
+ * product that resolves to the tensor-core kernel with A split on chip
+ * (K % 4 == 0) runs in a streaming form instead: B is copied in whole, A
+ * (and C) in row blocks, and one GEMM launch over the whole product starts
+ * once B is in, each of its CTAs waiting (bounded) for its rows' block to
+ * land; each row block of C is copied back as soon as the GEMM has stored
+ * it.  Same results within the bound; faster on some shapes, slower on
+ * others, so it is not the default.
  * The library stages the whole problem in device memory it owns (M*K + K*N
  * + M*N floats plus a GEMM workspace per column block), grown on demand and
  * freed by gemm_shutdown(); calls on one device are serialised.

@@ -262,6 +262,8 @@ int run_gemm(const GemmArgs &p, int mode, void *workspace, size_t ws_bytes, cuda
   st = make_plan(M, N, K, p.lda, p.ldb, p.ldc, mode, align, p.beta != 0.0f, dp, &plan, p.ta,
                  p.tb);
   if (st != GEMM_OK) return st;
+  if (p.in_flag != nullptr && (p.alpha == 0.0f || !tc_plan_streaming(plan, M, N, K)))
+    return GEMM_ERR_UNSUPPORTED;
   // K == 0, or alpha == 0 (BLAS: A and B are not read): C <- beta * C
   if (plan.kernel == GEMM_KERNEL_SCALE || p.alpha == 0.0f)
     return to_status(launch_scale(p, stream));

@@ -30,6 +30,18 @@ struct GemmArgs {
   // everything before it in the stream), for callers that chain the GEMM
   // behind cross-stream event waits.
   int b_presplit = 0, plain_order = 0;
+  // Streaming (tensor-core path with A split on chip, one CTA per tile):
+  // A's rows, and C's when beta != 0, are still arriving in row blocks of
+  // stream_rows rows (a multiple of the tile height) while the GEMM runs.
+  // Row block i is in device memory once in_flag[i] - epoch >= 0 (32-bit
+  // cyclic compare); the GEMM sets out_flag[i] = epoch once every tile of
+  // block i is stored, counting in tile_cnt[i] (zero on entry, zero again
+  // when the block completes).  in_flag == nullptr: no streaming.
+  const unsigned *in_flag = nullptr;
+  unsigned *out_flag = nullptr, *tile_cnt = nullptr;
+  unsigned epoch = 0;
+  int64_t stream_rows = 0;
+  int stream_blocks = 0;
 };
 
 // Cached properties of one device (or the built-in GB300 figures).
@@ -102,6 +114,12 @@ cudaError_t launch_fma_peak(int64_t iters, int packed, int sm_count, float *sink
 int launch_tc(const gemm_plan_t &plan, const GemmArgs &p, void *ws, size_t ws_bytes,
               cudaStream_t s);
 uint64_t tc_workspace_bytes(const gemm_plan_t &plan, int64_t M, int64_t N, int64_t K);
+// The plan of a streaming call (GemmArgs::in_flag): the same tile
+// configuration, one CTA per tile (no stream-K, so every tile is finished by
+// the CTA that computes it; measured faster than waves plus stream-K here),
+// and the workspace that needs.  False when the plan cannot stream: not the
+// tensor-core path, or A not split on chip.
+bool tc_plan_streaming(gemm_plan_t &plan, int64_t M, int64_t N, int64_t K);
 bool tc_config_valid(int bm, int bn, int bk, int stages, int a_inkernel, int concat, int nprod);
 int tc_ctas_per_sm(int bm, int bn, int bk, int stages, int a_inkernel, int concat, int nprod,
                    int smem_per_sm);

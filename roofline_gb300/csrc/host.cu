@@ -26,6 +26,8 @@
 // the mode resolved for the whole product; on the tensor-core path each B
 // column block is split into its TF32 planes by its first GEMM, in a
 // workspace of its own, and its later GEMMs reuse them.
+#include <cuda.h>
+
 #include <cstdlib>
 #include <mutex>
 #include <vector>
@@ -39,15 +41,45 @@ constexpr int kMaxDev = 64;
 constexpr int kMaxBlocks = GEMM_HOST_MAX_BLOCKS;
 
 constexpr int kMaxColBlocks = 8;
+constexpr int kMaxStreamBlocks = 64;
+
+// Stream memory operations of the driver (cuStreamWaitValue32 /
+// cuStreamWriteValue32), looked up once; null when the driver lacks them.
+typedef CUresult (*StreamValue32Fn)(CUstream, CUdeviceptr, cuuint32_t, unsigned int);
+std::once_flag g_memops_once;
+StreamValue32Fn g_wait32 = nullptr, g_write32 = nullptr;
+
+bool memops() {
+  std::call_once(g_memops_once, [] {
+    void *w = nullptr, *r = nullptr;
+    cudaDriverEntryPointQueryResult qw, qr;
+    if (cudaGetDriverEntryPointByVersion("cuStreamWaitValue32", &w, 12000, cudaEnableDefault,
+                                         &qw) == cudaSuccess &&
+        qw == cudaDriverEntryPointSuccess &&
+        cudaGetDriverEntryPointByVersion("cuStreamWriteValue32", &r, 12000, cudaEnableDefault,
+                                         &qr) == cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess) {
+      g_wait32 = reinterpret_cast<StreamValue32Fn>(w);
+      g_write32 = reinterpret_cast<StreamValue32Fn>(r);
+    } else {
+      cudaGetLastError();
+    }
+  });
+  return g_wait32 != nullptr && g_write32 != nullptr;
+}
 
 // Events are re-recorded freely: a stream wait takes the event's most recent
 // record at the time the wait is enqueued.
 struct HostPipe {
   bool ready = false;
-  cudaStream_t h2d = nullptr, comp = nullptr, d2h = nullptr;
+  cudaStream_t h2d = nullptr, comp = nullptr, d2h = nullptr, rescue = nullptr;
   cudaEvent_t in = nullptr, out = nullptr;
   void *buf = nullptr;
   size_t bytes = 0;
+  // streaming: in_flag[kMaxStreamBlocks], out_flag[...], tile_cnt[...] on
+  // the device (zeroed once), and the value the next call publishes
+  unsigned *flags = nullptr;
+  unsigned epoch = 0;
 };
 
 std::mutex g_host_mu[kMaxDev];
@@ -57,9 +89,11 @@ void destroy(HostPipe &p) {
   if (p.h2d) cudaStreamDestroy(p.h2d);
   if (p.comp) cudaStreamDestroy(p.comp);
   if (p.d2h) cudaStreamDestroy(p.d2h);
+  if (p.rescue) cudaStreamDestroy(p.rescue);
   if (p.in) cudaEventDestroy(p.in);
   if (p.out) cudaEventDestroy(p.out);
   if (p.buf) cudaFree(p.buf);
+  if (p.flags) cudaFree(p.flags);
   cudaGetLastError();
   p = HostPipe{};
 }
@@ -68,7 +102,10 @@ int setup(HostPipe &p) {
   if (p.ready) return GEMM_OK;
   bool ok = cudaStreamCreateWithFlags(&p.h2d, cudaStreamNonBlocking) == cudaSuccess &&
             cudaStreamCreateWithFlags(&p.comp, cudaStreamNonBlocking) == cudaSuccess &&
-            cudaStreamCreateWithFlags(&p.d2h, cudaStreamNonBlocking) == cudaSuccess;
+            cudaStreamCreateWithFlags(&p.d2h, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&p.rescue, cudaStreamNonBlocking) == cudaSuccess;
+  ok = ok && cudaMalloc(&p.flags, 3 * kMaxStreamBlocks * sizeof(unsigned)) == cudaSuccess &&
+       cudaMemset(p.flags, 0, 3 * kMaxStreamBlocks * sizeof(unsigned)) == cudaSuccess;
   ok = ok && cudaEventCreateWithFlags(&p.in, cudaEventDisableTiming) == cudaSuccess &&
        cudaEventCreateWithFlags(&p.out, cudaEventDisableTiming) == cudaSuccess;
   if (!ok) {
@@ -142,6 +179,105 @@ cudaError_t copy_rows(float *dst, int64_t dld, const float *src, int64_t sld, in
                            (size_t)rows, kind, s);
 }
 
+// Streaming form of the call, for a product that resolves to the
+// tensor-core kernel with A split on chip: B is copied in whole, then A (and
+// C, when beta != 0) in row blocks of `rows` rows, each followed by a write of
+// `epoch` to its in_flag from the copy stream; one GEMM launch over the whole
+// product (one CTA per tile, tiles in row order) runs once B is in and its
+// CTAs wait, tile by tile, for their rows (GemmArgs::in_flag); the GEMM
+// publishes each row block of C in out_flag once all its tiles are stored,
+// and the copy-back stream waits for that value before copying the block
+// out.  So the copies in, the GEMM and the copies out overlap with one
+// launch's efficiency instead of one GEMM call per block.
+int host_streaming(HostPipe &pp, const gemm_plan_t &plan, int64_t M, int64_t N, int64_t K,
+                   float alpha, const float *A, int64_t lda, const float *B, int64_t ldb,
+                   float beta, float *C, int64_t ldc, int bmode, int64_t rows) {
+  const int nblk = (int)ceil_div(M, rows);
+  const size_t a_bytes = align256((size_t)M * K * 4), b_bytes = align256((size_t)K * N * 4);
+  const size_t c_bytes = align256((size_t)M * N * 4);
+  const size_t ws_bytes = align256((size_t)plan.workspace_bytes);
+  int st = reserve(pp, a_bytes + b_bytes + c_bytes + ws_bytes);
+  if (st != GEMM_OK) return st;
+  char *base = static_cast<char *>(pp.buf);
+  float *dA = reinterpret_cast<float *>(base);
+  float *dB = reinterpret_cast<float *>(base + a_bytes);
+  float *dC = reinterpret_cast<float *>(base + a_bytes + b_bytes);
+  char *ws = ws_bytes ? base + a_bytes + b_bytes + c_bytes : nullptr;
+  unsigned *in_flag = pp.flags, *out_flag = pp.flags + kMaxStreamBlocks;
+  unsigned *tile_cnt = pp.flags + 2 * kMaxStreamBlocks;
+  if (++pp.epoch == 0) ++pp.epoch;  // flags start at 0: never publish 0
+  const unsigned epoch = pp.epoch;
+  auto rows_of = [&](int i) { return i + 1 < nblk ? rows : M - (int64_t)i * rows; };
+
+  // test hook: the arrival of this row block is never published, so the
+  // GEMM's waits for it run out (GEMM_DEBUG_WAIT_LIMIT_NS bounds them)
+  const int64_t skip = env_int("GEMM_DEBUG_STREAM_SKIP_BLOCK", -1);
+  cudaError_t e = copy_rows(dB, N, B, ldb, N, K, cudaMemcpyHostToDevice, pp.h2d);
+  if (e == cudaSuccess) e = cudaEventRecord(pp.in, pp.h2d);
+  for (int i = 0; i < nblk && e == cudaSuccess; ++i) {
+    const int64_t r0 = (int64_t)i * rows, nr = rows_of(i);
+    e = copy_rows(dA + r0 * K, K, A + r0 * lda, lda, K, nr, cudaMemcpyHostToDevice, pp.h2d);
+    if (e == cudaSuccess && beta != 0.0f)
+      e = copy_rows(dC + r0 * N, N, C + r0 * ldc, ldc, N, nr, cudaMemcpyHostToDevice, pp.h2d);
+    if (e == cudaSuccess && i != skip &&
+        g_write32(reinterpret_cast<CUstream>(pp.h2d), reinterpret_cast<CUdeviceptr>(in_flag + i),
+                  epoch, CU_STREAM_WRITE_VALUE_DEFAULT) != CUDA_SUCCESS)
+      e = cudaErrorUnknown;
+  }
+  if (e == cudaSuccess) e = cudaMemsetAsync(tile_cnt, 0, (size_t)nblk * sizeof(unsigned), pp.comp);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(pp.comp, pp.in, 0);
+  bool launched = false;
+  if (e == cudaSuccess) {
+    GemmArgs g{M, N, K, alpha, beta, dA, K, dB, N, dC, N};
+    g.plain_order = 1;
+    g.in_flag = in_flag;
+    g.out_flag = out_flag;
+    g.tile_cnt = tile_cnt;
+    g.epoch = epoch;
+    g.stream_rows = rows;
+    g.stream_blocks = nblk;
+    st = run_gemm(g, bmode, ws, ws_bytes, pp.comp);
+    launched = st == GEMM_OK;
+  }
+  // copies back, each behind its block's flag (only once the GEMM is
+  // launched: nothing else would ever set the flags)
+  for (int i = 0; launched && i < nblk && e == cudaSuccess; ++i) {
+    const int64_t r0 = (int64_t)i * rows;
+    if (g_wait32(reinterpret_cast<CUstream>(pp.d2h), reinterpret_cast<CUdeviceptr>(out_flag + i),
+                 epoch, CU_STREAM_WAIT_VALUE_GEQ) != CUDA_SUCCESS) {
+      e = cudaErrorUnknown;
+      break;
+    }
+    e = copy_rows(C + r0 * ldc, ldc, dC + r0 * N, N, N, rows_of(i), cudaMemcpyDeviceToHost, pp.d2h);
+  }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    if (st == GEMM_OK) st = GEMM_ERR_CUDA;
+  }
+  // The copies in and the GEMM always finish (the GEMM's waits are
+  // bounded).  Once the GEMM has, every out_flag is written again from a
+  // stream of its own, so a copy back still waiting on a block the GEMM did
+  // not publish goes ahead instead of waiting for ever; then the copies back
+  // are waited for.
+  const cudaError_t e1 = cudaStreamSynchronize(pp.h2d);
+  const cudaError_t e2 = cudaStreamSynchronize(pp.comp);
+  bool released = true;
+  for (int i = 0; i < nblk; ++i)
+    released = released &&
+               g_write32(reinterpret_cast<CUstream>(pp.rescue),
+                         reinterpret_cast<CUdeviceptr>(out_flag + i), epoch,
+                         CU_STREAM_WRITE_VALUE_DEFAULT) == CUDA_SUCCESS;
+  const cudaError_t e3 = cudaStreamSynchronize(pp.rescue);
+  const cudaError_t e4 = cudaStreamSynchronize(pp.d2h);
+  if (e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess || e4 != cudaSuccess ||
+      !released) {
+    cudaGetLastError();
+    if (st == GEMM_OK) st = GEMM_ERR_CUDA;
+  }
+  const int dev_st = tc_read_and_clear_status(pp.comp);
+  return st != GEMM_OK ? st : dev_st;
+}
+
 }  // namespace
 
 void host_pipeline_shutdown() {
@@ -185,6 +321,32 @@ extern "C" int gemm_f32_host(int64_t M, int64_t N, int64_t K, float alpha, const
   }
   if (dev < 0 || dev >= kMaxDev) return GEMM_ERR_UNSUPPORTED;
   const DeviceProps &dp = props_of(dev);
+
+  // The streaming form, on request (GEMM_HOST_STREAM = 1), when the library
+  // picks the blocking and the product resolves to the tensor-core kernel
+  // with A split on chip (A staged with K floats a row, so K % 4 == 0 for
+  // TMA); rows in blocks of whole tile rows, about 8 of them
+  // (GEMM_HOST_STREAM_ROWS = rows per block).  Measured per call on GB300,
+  // blocked / streaming (ms): 4096^3 1.044 / 0.984, 6144^3 2.63 / 2.37, but
+  // 4096 x 4096 x 2048 0.648 / 0.704, 8192^3 4.85 / 5.14, 2048^3 0.315 /
+  // 0.353, 3072^3 0.614 / 0.622: the whole of B has to arrive before the
+  // one launch starts, which the blocked form does not wait for, so it is
+  // not the default.
+  if (blocks == 0 && K > 0 && (K & 3) == 0 && env_int("GEMM_HOST_STREAM", 0) != 0 &&
+      memops()) {
+    gemm_plan_t ps;
+    if (make_plan(M, N, K, K, N, N, mode, 0, beta != 0.0f, dp, &ps) == GEMM_OK &&
+        tc_plan_streaming(ps, M, N, K) && M >= 2 * ps.bm) {
+      int64_t rows = env_int("GEMM_HOST_STREAM_ROWS", ceil_div(M, 8));
+      rows = ceil_div(rows < ps.bm ? ps.bm : rows, ps.bm) * ps.bm;
+      if (ceil_div(M, rows) > kMaxStreamBlocks) rows = ceil_div(ceil_div(M, kMaxStreamBlocks), ps.bm) * ps.bm;
+      std::lock_guard<std::mutex> lk(g_host_mu[dev]);
+      HostPipe &pp = g_pipe[dev];
+      st = setup(pp);
+      if (st != GEMM_OK) return st;
+      return host_streaming(pp, ps, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, ps.mode, rows);
+    }
+  }
 
   // Row blocks hold whole 128-row tiles and column blocks whole 256-column
   // tiles, except the last of each.  Column blocks only when the library

@@ -76,6 +76,30 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, u
       : "memory");
 }
 
+// Waits (bounded, like mbar_wait) until *flag - epoch >= 0 as a 32-bit cyclic
+// compare, with acquire semantics at GPU scope: data written to device
+// memory before the flag was set is visible afterwards.
+__device__ __forceinline__ bool flag_wait(const unsigned *flag, unsigned epoch, uint64_t deadline,
+                                          volatile int *abort_flag) {
+  uint32_t spins = 0;
+  while (true) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+    if ((int)(v - epoch) >= 0) return true;
+    if ((++spins & 15u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer() > deadline) return false;
+    }
+    __nanosleep(200);
+  }
+}
+
+// Orders this thread's earlier global-memory accesses (generic proxy)
+// before its later TMA accesses of global memory (async proxy).
+__device__ __forceinline__ void fence_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // Requests the 128-byte line holding *ptr into L2 (a hint: nothing waits for it).
 __device__ __forceinline__ void prefetch_l2(const void *ptr) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(ptr)));
@@ -235,6 +259,13 @@ struct TcParams {
   int64_t sk_units;  // (tiles - dp_tiles) * num_kb: units shared out stream-K
   float *partial;    // stream-K partial tiles: 2 slots of BM x BN per CTA
   uint64_t timeout_ns;
+  // streaming (GemmArgs::in_flag): row block i of A (and C) has landed once
+  // in_flag[i] - epoch >= 0; out_flag[i] = epoch once its tiles are stored
+  const unsigned *in_flag;
+  unsigned *out_flag, *tile_cnt;
+  unsigned epoch;
+  int64_t stream_rows;
+  int stream_blocks;
   int stall_producer;  // test hook: the producer issues nothing
   unsigned long long *stamps;  // measurement aid (gemm_set_profile_stamps), or nullptr
 };

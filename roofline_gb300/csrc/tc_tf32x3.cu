@@ -266,6 +266,14 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
         tile_coords(p, sg.tile, mt, nt);
         const int32_t m0 = (int32_t)(mt * BM);
         const int32_t n0 = (int32_t)(nt * BN);
+        if (p.in_flag != nullptr) {
+          // streaming: this tile's rows of A must have landed
+          if (!flag_wait(p.in_flag + (mt * BM) / p.stream_rows, p.epoch, deadline, abort_flag)) {
+            ok = false;
+            break;
+          }
+          fence_async_global();
+        }
         for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
           const int s = issued % STAGES;
           const uint32_t ph = (uint32_t)(issued / STAGES) & 1u;
@@ -502,6 +510,11 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
       tile_coords(p, sg.tile, mt, nt);
       const int64_t m0 = mt * BM;
       const int64_t n0 = nt * BN;
+      // streaming with beta != 0: C's old values of these rows came with A's
+      // (the producer waited for them); this warp acquires the same flag
+      // before reading them
+      if (p.in_flag != nullptr && p.beta != 0.0f)
+        flag_wait(p.in_flag + m0 / p.stream_rows, p.epoch, deadline, abort_flag);
       // each 128-row half of the tile sits in its own accumulator columns
 #pragma unroll 1
       for (int h = 0; h < Cfg::MH; ++h) {
@@ -565,6 +578,24 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
           }
         }
       }
+      if (p.out_flag != nullptr && whole) {
+        // streaming: this warp's rows of the tile are stored.  Its stores
+        // are fenced, then counted; the last of the row block's 4 x (tiles
+        // in the block) warps to get here publishes the block.
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) {
+          const int64_t blk = m0 / p.stream_rows;
+          const int64_t left = p.M - blk * p.stream_rows;
+          const int64_t rows = left < p.stream_rows ? left : p.stream_rows;
+          const unsigned target = 4u * (unsigned)(((rows + BM - 1) / BM) * p.tiles_n);
+          if (atomicAdd(&p.tile_cnt[blk], 1u) + 1u == target) {
+            atomicExch(&p.tile_cnt[blk], 0u);
+            __threadfence();
+            atomicExch(&p.out_flag[blk], p.epoch);
+          }
+        }
+      }
       tc_fence_before();
       mbar_arrive(acc_empty);  // the accumulator may be overwritten
       ++si;
@@ -573,6 +604,10 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
   }
 
   if (!ok) atomicExch(&g_tc_status, GEMM_ERR_DEVICE_TIMEOUT);
+  // streaming: a thread that gave up releases every row block, so copies
+  // waiting on them go ahead (the call then reports the status word)
+  if (!ok && p.out_flag != nullptr)
+    for (int i = 0; i < p.stream_blocks; ++i) atomicExch(&p.out_flag[i], p.epoch);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -663,6 +698,13 @@ int launch_cfg(const gemm_plan_t &plan, const GemmArgs &a, char *ws, cudaStream_
   const int64_t tiles_m = ceil_div(a.M, BM), tiles_n = ceil_div(a.N, BN);
   const int64_t tiles = tiles_m * tiles_n;
   const int num_kb = (int)ceil_div(a.K, BK);
+  // streaming: A arrives by TMA from device memory (split on chip), one CTA
+  // per tile, row blocks of whole tile rows
+  const bool streaming = a.in_flag != nullptr;
+  if (streaming && (!AK || plan.stream_k || a.ta || !a.out_flag || !a.tile_cnt ||
+                    a.stream_rows <= 0 || a.stream_rows % BM != 0 ||
+                    a.stream_blocks != ceil_div(a.M, a.stream_rows)))
+    return GEMM_ERR_UNSUPPORTED;
   const int64_t G = plan.stream_k ? plan.grid_ctas : tiles;
   if (G < 1 || G > 0x7fffffff || tiles > 0x7fffffff) return GEMM_ERR_UNSUPPORTED;
   const WsLayout L = ws_layout(a.M, a.N, a.K, AK, plan.stream_k ? G : 0, BM, BN, X3);
@@ -725,6 +767,7 @@ int launch_cfg(const gemm_plan_t &plan, const GemmArgs &a, char *ws, cudaStream_
       if (wave < 1) wave = 1;
       gn = (int64_t)std::lround(std::sqrt((double)wave * a_bytes / b_bytes));
     }
+    if (streaming) gn = tiles_n;  // row order: tiles follow the rows as they land
     if (const char *o = std::getenv("GEMM_TC_ORDER")) gn = std::atoi(o) == 1 ? 1 : tiles_n;
     gn = (int64_t)env_u64("GEMM_TC_GROUP", (uint64_t)gn);
     if (gn < 1) gn = 1;
@@ -749,6 +792,12 @@ int launch_cfg(const gemm_plan_t &plan, const GemmArgs &a, char *ws, cudaStream_
     return GEMM_ERR_UNSUPPORTED;
   p.partial = reinterpret_cast<float *>(ws + L.partial);
   p.timeout_ns = env_u64("GEMM_DEBUG_WAIT_LIMIT_NS", 2000000000ull);
+  p.in_flag = a.in_flag;
+  p.out_flag = a.out_flag;
+  p.tile_cnt = a.tile_cnt;
+  p.epoch = a.epoch;
+  p.stream_rows = a.stream_rows;
+  p.stream_blocks = a.stream_blocks;
   p.stall_producer = (int)env_u64("GEMM_DEBUG_STALL_PRODUCER", 0);
   p.stamps = profile_stamps();
   auto kern = tc_tf32x3_kernel<BM, BN, BK, STAGES, AK, CONCAT, NPROD>;
@@ -873,6 +922,19 @@ int tc_ctas_per_sm(int bm, int bn, int bk, int stages, int a_inkernel, int conca
   GG_TC_CONFIGS(GG_OCC)
 #undef GG_OCC
   return 0;
+}
+
+bool tc_plan_streaming(gemm_plan_t &plan, int64_t M, int64_t N, int64_t K) {
+  if ((plan.kernel != GEMM_KERNEL_TC_TF32X3 && plan.kernel != GEMM_KERNEL_TC_TF32) ||
+      !plan.a_split_in_kernel)
+    return false;
+  if (plan.stream_k) {
+    plan.stream_k = 0;
+    plan.launches -= 1;  // no fix-up
+  }
+  plan.grid_ctas = ceil_div(M, plan.bm) * ceil_div(N, plan.bn);
+  plan.workspace_bytes = tc_workspace_bytes(plan, M, N, K);
+  return true;
 }
 
 uint64_t tc_workspace_bytes(const gemm_plan_t &plan, int64_t M, int64_t N, int64_t K) {

@@ -89,6 +89,50 @@ def test_host_grid_of_blocks(case, mode, beta, monkeypatch):
     assert oracle.mismatches(got, oracle.gemm(A, B, 1.0, 1.0, C0)) == 0
 
 
+STREAM_CASES = [
+    # (M, N, K, rows per block or None for the library's choice): blocks == 0
+    # with K % 4 == 0 and a tensor-core plan that splits A on chip, so with
+    # GEMM_HOST_STREAM=1 the call takes the streaming form (one GEMM launch
+    # consuming row blocks of A as they land, C copied back block by block as
+    # the GEMM publishes it)
+    (2048, 2048, 2048, None),
+    (1500, 1024, 1024, 384),   # ragged last row block
+    (1100, 1300, 512, 128),    # many small blocks, ragged edges
+    (4096, 64, 2048, None),    # narrow: the skinny shape's plan
+]
+
+
+@pytest.mark.parametrize("case", STREAM_CASES)
+@pytest.mark.parametrize("mode", ["tf32x3", "auto"])
+@pytest.mark.parametrize("beta", [0.0, -0.75])
+def test_host_streaming_matches_oracle(case, mode, beta, monkeypatch):
+    M, N, K, rows = case
+    monkeypatch.setenv("GEMM_HOST_STREAM", "1")
+    if rows:
+        monkeypatch.setenv("GEMM_HOST_STREAM_ROWS", str(rows))
+    A, B, C0, got = run_host(M, N, K, 1.5, beta, mode, 0, pad=(3, 1, 2), seed=M + N)
+    if M * N * K > 2 ** 30:
+        rows_, cols_ = sample_entries(M, N, n=8192, seed=11)
+        ref, D = oracle.gemm_entries(A, B, rows_, cols_, 1.5, beta, C0 if beta else None)
+        assert oracle.err_normalised(got[rows_, cols_], ref, D) <= TOL_E1
+    else:
+        ref, D = oracle.gemm(A, B, 1.5, beta, C0 if beta else None, with_bound=True)
+        assert oracle.err_normalised(got, ref, D) <= TOL_E1
+
+
+@pytest.mark.parametrize("stream", ["1", "0"])
+def test_host_streaming_integer_bit_exact_and_repeatable(stream, monkeypatch):
+    """Integer inputs are exact in either form (streaming on, or the blocked
+    form with GEMM_HOST_STREAM=0); repeated streaming calls reuse the flags
+    (a new value each call) and stay exact."""
+    monkeypatch.setenv("GEMM_HOST_STREAM", stream)
+    monkeypatch.setenv("GEMM_HOST_STREAM_ROWS", "256")
+    for rep in range(3):
+        A, B, C0, got = run_host(1280, 1536, 1024, 1.0, 1.0, "tf32x3", 0, dist="int2",
+                                 seed=300 + rep)
+        assert oracle.mismatches(got, oracle.gemm(A, B, 1.0, 1.0, C0)) == 0, rep
+
+
 def test_host_auto_grid_2048():
     """2048 x 2048 x 1024 (8.6 GFLOP): the library's blocking is 2 x 2."""
     import torch
