@@ -903,7 +903,7 @@ bool tc_config_valid(int bm, int bn, int bk, int stages, int a_inkernel, int con
   return false;
 }
 
-// Every configuration needs more than 113 registers a thread (134-156), so
+// Every configuration needs more than 113 registers a thread (134-166), so
 // at most two CTAs of 192 threads share an SM's 65536 registers.
 constexpr int kMaxCtasPerSm = 2;
 
