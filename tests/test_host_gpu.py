@@ -120,6 +120,17 @@ def test_host_streaming_matches_oracle(case, mode, beta, monkeypatch):
         assert oracle.err_normalised(got, ref, D) <= TOL_E1
 
 
+def test_host_streaming_tf32_mode(monkeypatch):
+    """1xTF32 through the streaming form (the narrow tile splits A on chip):
+    within the mode's bound."""
+    from tests.gpu_util import tol_tf32
+    monkeypatch.setenv("GEMM_HOST_STREAM", "1")
+    M, N, K = 2048, 64, 1024
+    A, B, C0, got = run_host(M, N, K, 1.0, 0.5, "tf32", 0, pad=(0, 0, 0), seed=71)
+    ref, D = oracle.gemm(A, B, 1.0, 0.5, C0, with_bound=True)
+    assert oracle.err_normalised(got, ref, D) <= tol_tf32(K)
+
+
 @pytest.mark.parametrize("stream", ["1", "0"])
 def test_host_streaming_integer_bit_exact_and_repeatable(stream, monkeypatch):
     """Integer inputs are exact in either form (streaming on, or the blocked
