@@ -179,6 +179,13 @@ __device__ __forceinline__ void grid_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// The TF32 value the tensor core reads from an FP32 word: the word with its
+// low 13 mantissa bits cleared (its leading 11 significant bits).  Exactly a
+// TF32 value, and x - tf32_trunc(x) is exact in FP32.
+__device__ __forceinline__ float tf32_trunc(float x) {
+  return __uint_as_float(__float_as_uint(x) & 0xffffe000u);
+}
+
 __device__ __forceinline__ float tf32_rna(float x) {
   uint32_t r;
   asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));

@@ -123,10 +123,11 @@ __device__ __forceinline__ void split_rows_block(const SplitJob &j, int64_t blk)
 #pragma unroll
     for (int i = 0; i < 4; ++i) v[i] = (c + i < k) ? __ldg(s + i) : 0.0f;
     float4 h, l;
-    h.x = tf32_rna(v[0]); l.x = v[0] - h.x;
-    h.y = tf32_rna(v[1]); l.y = v[1] - h.y;
-    h.z = tf32_rna(v[2]); l.z = v[2] - h.z;
-    h.w = tf32_rna(v[3]); l.w = v[3] - h.w;
+    // 3xTF32 (lo written): the truncated split; 1xTF32: hi rounded to nearest
+    h.x = j.lo ? tf32_trunc(v[0]) : tf32_rna(v[0]); l.x = v[0] - h.x;
+    h.y = j.lo ? tf32_trunc(v[1]) : tf32_rna(v[1]); l.y = v[1] - h.y;
+    h.z = j.lo ? tf32_trunc(v[2]) : tf32_rna(v[2]); l.z = v[2] - h.z;
+    h.w = j.lo ? tf32_trunc(v[3]) : tf32_rna(v[3]); l.w = v[3] - h.w;
     *reinterpret_cast<float4 *>(j.hi + r * kp + c) = h;
     if (j.lo) *reinterpret_cast<float4 *>(j.lo + r * kp + c) = l;
   }
@@ -185,10 +186,10 @@ __device__ __forceinline__ void split_transpose_block(const SplitJob &j, int64_t
       float4 h, l;
       const float a0 = tile[kq + 0][nl], a1 = tile[kq + 1][nl];
       const float a2 = tile[kq + 2][nl], a3 = tile[kq + 3][nl];
-      h.x = tf32_rna(a0); l.x = a0 - h.x;
-      h.y = tf32_rna(a1); l.y = a1 - h.y;
-      h.z = tf32_rna(a2); l.z = a2 - h.z;
-      h.w = tf32_rna(a3); l.w = a3 - h.w;
+      h.x = j.lo ? tf32_trunc(a0) : tf32_rna(a0); l.x = a0 - h.x;
+      h.y = j.lo ? tf32_trunc(a1) : tf32_rna(a1); l.y = a1 - h.y;
+      h.z = j.lo ? tf32_trunc(a2) : tf32_rna(a2); l.z = a2 - h.z;
+      h.w = j.lo ? tf32_trunc(a3) : tf32_rna(a3); l.w = a3 - h.w;
       *reinterpret_cast<float4 *>(j.hi + nn * kp + kk) = h;
       if (j.lo) *reinterpret_cast<float4 *>(j.lo + nn * kp + kk) = l;
     }

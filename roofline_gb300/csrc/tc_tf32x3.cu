@@ -5,15 +5,19 @@
 // ("Project - tiled matrix multiply", sections "Stage 3 - the reference
 // ceiling: cuBLAS" and "What comes next").  TF32 alone keeps only 11
 // significant bits, so each FP32 operand x is split in two,
-//     x_hi = tf32_rna(x)   (exactly a TF32 value),
-//     x_lo = x - x_hi      (exact in FP32; the MMA reads its leading 11
-//                           significant bits, which changes the product by
-//                           at most 2^-21 of |x| |y|),
+//     x_hi = tf32_trunc(x) (x's word with the low 13 mantissa bits cleared:
+//                           exactly the TF32 value the MMA reads from x's
+//                           own word, so an A tile can serve as A_hi as it
+//                           lands),
+//     x_lo = x - x_hi      (exact in FP32, |x_lo| < 2^-10 |x|; the MMA reads
+//                           its leading 11 significant bits, which changes
+//                           the product by less than 2^-20 of |x| |y|),
 // and the product is formed from three TF32 MMAs accumulated in FP32:
 //     A*B ~= A_hi*B_lo + A_lo*B_hi + A_hi*B_hi
 // (the dropped A_lo*B_lo term is below 2^-20 of |A||B|).
 //
-// 1xTF32 mode issues only A_hi*B_hi.
+// 1xTF32 mode issues only A_hi*B_hi, with x_hi rounded to nearest
+// (tf32_rna), which halves its error against truncation.
 //
 // Kernel structure (192 threads per CTA; output tiles of BM = 128 or 256
 // rows by BN columns; a 256-row tile is two 128-row halves, each with its
@@ -25,13 +29,13 @@
 //               is split on chip) and one lane issues tcgen05.mma
 //               kind::tf32, committing each stage back to the producer when
 //               its MMAs retire;
-//   warps 2-5   (a) when A is split inside the kernel: convert each landed
-//               FP32 A tile into its hi part and lo part (lo into a
-//               tensor-memory ring read by the [a_tmem] form of the MMA; hi
-//               in place in shared memory, or into a second ring when the
-//               CTA owns enough tensor memory), then release it to the MMA
-//               warp; (b) epilogue: tcgen05.ld the accumulator rows, apply
-//               C = alpha*acc + beta*C, store.
+//   warps 2-5   (a) when A is split inside the kernel: compute each landed
+//               FP32 A tile's lo part into a tensor-memory ring read by the
+//               [a_tmem] form of the MMA (the landed tile itself is A_hi to
+//               the MMA, or, when the CTA owns enough tensor memory, A_hi
+//               goes to a second ring too), then release the stage to the
+//               MMA warp; (b) epilogue: tcgen05.ld the accumulator rows,
+//               apply C = alpha*acc + beta*C, store.
 // A CTA walks a list of (tile, K-range) segments: whole tiles in waves, then
 // an even share of the remaining tiles' K blocks (stream-K; see Walk), with
 // the pipeline running across segment boundaries.
@@ -62,7 +66,8 @@ __device__ int g_tc_status;  // 0 = ok, else a GEMM_ERR_* code
 
 // BN: output columns per CTA.  BK: K depth of one stage (16 -> 64-byte
 // swizzle, 32 -> 128-byte swizzle).  AK: A arrives raw (FP32) and the
-// converter warps split it, A_hi in place in shared memory and A_lo into a
+// converter warps split it: the landed tile is A_hi to the MMA as it is (the
+// MMA reads each word's leading 11 significant bits) and A_lo goes into a
 // tensor-memory ring that the A_lo*B_hi MMA reads directly; otherwise A_hi
 // and A_lo come pre-split from the workspace.  CONCAT: B_hi and B_lo sit
 // next to each other in the stage, so A_hi*[B_hi | B_lo] is one MMA of width
@@ -468,10 +473,10 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
               float4 *ptr = reinterpret_cast<float4 *>(line + phys * 16);
               const float4 x = *ptr;
               float4 h;
-              h.x = tf32_rna(x.x);
-              h.y = tf32_rna(x.y);
-              h.z = tf32_rna(x.z);
-              h.w = tf32_rna(x.w);
+              h.x = tf32_trunc(x.x);
+              h.y = tf32_trunc(x.y);
+              h.z = tf32_trunc(x.z);
+              h.w = tf32_trunc(x.w);
               lo[4 * c + 0] = __float_as_uint(x.x - h.x);
               lo[4 * c + 1] = __float_as_uint(x.y - h.y);
               lo[4 * c + 2] = __float_as_uint(x.z - h.z);
@@ -481,15 +486,14 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
                 hi[4 * c + 1] = __float_as_uint(h.y);
                 hi[4 * c + 2] = __float_as_uint(h.z);
                 hi[4 * c + 3] = __float_as_uint(h.w);
-              } else {
-                *ptr = h;
               }
+              // A_hi in shared memory: the tile as it landed already reads as
+              // A_hi to the MMA, so nothing is written back
             }
             tmem_st<BK>(lane_base + (uint32_t)(Cfg::LO_COL0 + half * Cfg::LO_RING + s * BK), lo);
             if constexpr (Cfg::HI_TMEM)
               tmem_st<BK>(lane_base + (uint32_t)(Cfg::HI_COL0 + s * BK), hi);
             tmem_st_wait();
-            if (!Cfg::HI_TMEM) fence_async_smem();  // A_hi in shared memory -> visible to the MMA
           }
           }  // halves
           if constexpr (X3) tc_fence_before();
