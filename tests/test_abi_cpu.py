@@ -295,6 +295,8 @@ MEASURED_CHOICES = [
     ((1024, 1024, 1024), "tf32x3", (128, 64, 32, 4, 0, 0, 1)),    # 23.7 vs 26.4 us
     ((1000, 1000, 1001, 1001, 1000, 1000), "tf32x3", (128, 64, 32, 4, 0, 0, 1)),  # 30.5 vs 37.0 us
     ((1200, 640, 333, 333, 640, 640), "tf32x3", (128, 64, 32, 4, 0, 0, 1)),  # 16.9 vs 20.9 us
+    ((1200, 640, 336), "tf32x3", (128, 64, 32, 6, 1, 0, 1)),      # 13.5 vs 15.3 us pre-split
+    ((768, 768, 768), "tf32x3", (128, 64, 32, 6, 1, 0, 1)),       # 19.0 vs 20.4 us pre-split
     ((1024, 64, 8192), "tf32x3", (128, 64, 32, 6, 1, 1, 1)),      # 29.7 vs 38.2 us
     ((65536, 64, 4096), "tf32x3", (128, 64, 32, 3, 1, 1, 1)),     # 204 vs 271 us for 6 stages
     ((4096, 4096, 4096), "tf32", (256, 256, 16, 6, 0, 0, 1)),     # 212 vs 217 us for BK 32

@@ -227,6 +227,7 @@ TC_PLANS = [
     ((512, 512, 1024, 1024), (128, 128, 32, 4, 1, 1)),   # few tiles, longer K: stream-K
     ((2432, 8192, 128, 128), (128, 256, 16, 5, 1, 0)),
     ((1023, 1025, 777, 777), (128, 64, 32, 4, 0, 1)),    # small product, A pre-split
+    ((1200, 640, 336, 336), (128, 64, 32, 6, 1, 1)),    # shallow small product: A split on chip
     ((600, 600, 3000, 3001), (128, 128, 16, 6, 0, 1)),   # A pre-split, under half a wave: 6 stages
     ((5000, 250, 777, 777), (128, 128, 16, 3, 0, 1)),    # A pre-split, more tiles: 3 stages, 2 CTAs/SM
     ((2432, 8192, 129, 129), (128, 256, 16, 4, 0, 0)),
