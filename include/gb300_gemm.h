@@ -118,7 +118,9 @@ typedef struct gemm_plan {
                               waves, then share the remaining tiles' K blocks evenly; a fix-up
                               kernel sums the parts of tiles shared between CTAs */
   int32_t a_hi_tmem;       /* tensor-core modes with A split on chip: A_hi kept in tensor memory (1)
-                              or written back to shared memory (0) */
+                              or read from the landed tile in shared memory (0) */
+  int32_t b_split_in_kernel; /* tensor-core modes: B read as stored and split inside the GEMM
+                              kernel (1: no pass before it for B) or by a pre-pass (0) */
 } gemm_plan_t;
 
 typedef struct gemm_device_info {
@@ -234,7 +236,11 @@ GEMM_API int gemm_f32_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t
  * operands only: GEMM_ERR_UNSUPPORTED otherwise).  A layout or op outside
  * the constants below returns GEMM_ERR_INVALID_ARG.
  * Results equal gemm_f32_ex's on the same logical matrices, bit for bit,
- * whenever both run the same kernel configuration.
+ * whenever both run the same kernel configuration.  In the tensor-core
+ * modes a B that the row-major problem sees stored N x K (row-major with
+ * op_b = T) and 16-byte aligned with ldb a multiple of 4 can be read as
+ * stored and split inside the GEMM kernel, with no pass before it (the
+ * plan's b_split_in_kernel); the bits are those of the pass.
  */
 #define GEMM_ROW_MAJOR 0
 #define GEMM_COL_MAJOR 1

@@ -120,9 +120,10 @@ uint64_t tc_workspace_bytes(const gemm_plan_t &plan, int64_t M, int64_t N, int64
 // and the workspace that needs.  False when the plan cannot stream: not the
 // tensor-core path, or A not split on chip.
 bool tc_plan_streaming(gemm_plan_t &plan, int64_t M, int64_t N, int64_t K);
-bool tc_config_valid(int bm, int bn, int bk, int stages, int a_inkernel, int concat, int nprod);
+bool tc_config_valid(int bm, int bn, int bk, int stages, int a_inkernel, int concat, int nprod,
+                     int b_inkernel);
 int tc_ctas_per_sm(int bm, int bn, int bk, int stages, int a_inkernel, int concat, int nprod,
-                   int smem_per_sm);
+                   int b_inkernel, int smem_per_sm);
 int tc_read_and_clear_status(cudaStream_t s);
 
 // CUDA-core tile (simt.cu): 64 x 128, 8 x 8 per thread, 128 threads, K in

@@ -339,8 +339,13 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
       // and the split pass only has B to do (GB300: 1200 x 640 x 336 15.3 ->
       // 13.5 us, 768^3 20.4 -> 19.0 us; 512^3, 32 tiles, 14.1 against 14.6
       // and 1024^3, K = 1024, 24.0 against 25.4 keep both pre-split).
+      // With B stored N x K and split on chip as well (see b_aligned below),
+      // an aligned A always goes on chip too: the call is then one launch
+      // (GB300, B stored N x K, pre-split A / A on chip: 512^3 14.0 / 12.3
+      // us, 640^3 16.0 / 14.2, 1024^3 22.4 / 19.8).
+      const bool b_aligned = tb && (ldb % 4 == 0) && ((align_hint & 15) == 0);
       if (x3 && small_tc_product(M, N, K, sms)) {
-        if (a_aligned && K <= 768 && ceil_div(M, 128) * ceil_div(N, 64) >= 64) {
+        if (a_aligned && (b_aligned || (K <= 768 && ceil_div(M, 128) * ceil_div(N, 64) >= 64))) {
           set(64, 32, 6, 1);
         } else {
           set(64, 32, 4, 1);
@@ -349,27 +354,55 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
         p.a_hi_tmem = 0;
         no_stream_k = true;
       }
+      // B stored N x K (K contiguous, the way the MMA reads it) and aligned
+      // for TMA (16-byte base, ldb a multiple of 4): read as stored and split
+      // on chip, so no pass handles B before the GEMM, where the chosen
+      // configuration is built that way.  B stored K x N needs the
+      // transposing pass: an MMA reading B N-contiguous (the instruction
+      // descriptor's transpose bit) left the kind::tf32 accumulator at zero
+      // on GB300.
+      // The split adds a read of B and a write of B_lo to shared memory per
+      // stage, which the MMAs of a long run of full tiles cannot spare: it is
+      // taken when the tiles fit one wave without stream-K (decided below).
+      // GB300, 3xTF32, B stored N x K, step time with the pass / on chip (us):
+      // 1200 x 640 x 336 13.0 / 10.5 (one launch), 1024^3 23.2 / 22.5,
+      // 2048^3 68.5 / 65.8; 4096^3 (stream-K) about equal with a kernel of
+      // 390-417 against 443 us, 8192^3 3.30-3.42 against 3.47-3.67 ms.
+      const int ak = p.a_split_in_kernel ? (p.a_hi_tmem ? 2 : 1) : 0;
+      bool b_chip = true;
+      if (const char *bs = std::getenv("GEMM_TC_BSPLIT")) b_chip = std::atoi(bs) != 0;  // tuning knob
+      p.b_split_in_kernel =
+          (b_chip && b_aligned &&
+           tc_config_valid(p.bm, p.bn, p.bk, p.stages, ak, p.b_concat, nprod, 1))
+              ? 1
+              : 0;
+      bool b_forced = false;
       // Tuning knob: GEMM_TC_CONFIG="bn,bk,stages,a_split,b_concat" (128-row
-      // tile) or "bm,bn,bk,stages,a_split,b_concat" picks one of the built
-      // configurations (ignored if it names none, or asks for the in-kernel
-      // split with a misaligned A).  a_split: 0 pre-split, 1 on chip, 2 on
-      // chip with A_hi kept in tensor memory.
+      // tile), "bm,bn,bk,stages,a_split,b_concat" or
+      // "bm,bn,bk,stages,a_split,b_concat,b_split" picks one of the built
+      // configurations (ignored if it names none, or asks for an in-kernel
+      // split of a misaligned operand).  a_split: 0 pre-split, 1 on chip, 2
+      // on chip with A_hi kept in tensor memory; b_split: 1 on chip.
       if (const char *cfg = std::getenv("GEMM_TC_CONFIG")) {
-        int v[6] = {0, 0, 0, 0, 0, 0};
-        const int n = std::sscanf(cfg, "%d,%d,%d,%d,%d,%d", &v[0], &v[1], &v[2], &v[3], &v[4],
-                                  &v[5]);
-        const int *c = n == 6 ? v + 1 : v;
-        const int bm = n == 6 ? v[0] : 128;
-        if ((n == 5 || n == 6) && tc_config_valid(bm, c[0], c[1], c[2], c[3], c[4], nprod) &&
-            (!c[3] || a_aligned)) {
+        int v[7] = {0, 0, 0, 0, 0, 0, 0};
+        const int n = std::sscanf(cfg, "%d,%d,%d,%d,%d,%d,%d", &v[0], &v[1], &v[2], &v[3],
+                                  &v[4], &v[5], &v[6]);
+        const int *c = n >= 6 ? v + 1 : v;
+        const int bm = n >= 6 ? v[0] : 128;
+        const int bsplit = n == 7 ? v[6] : 0;
+        if (n >= 5 && tc_config_valid(bm, c[0], c[1], c[2], c[3], c[4], nprod, bsplit) &&
+            (!c[3] || a_aligned) && (!bsplit || b_aligned)) {
           set(c[0], c[1], c[2], c[4], bm);
           p.a_split_in_kernel = c[3] != 0;
           p.a_hi_tmem = c[3] == 2;
+          p.b_split_in_kernel = bsplit != 0;
+          b_forced = n == 7;
         }
       }
       p.ctas_per_sm = tc_ctas_per_sm(p.bm, p.bn, p.bk, p.stages,
                                      p.a_split_in_kernel ? (p.a_hi_tmem ? 2 : 1) : 0, p.b_concat,
-                                     nprod, dp.smem_per_sm > 0 ? dp.smem_per_sm : 233472);
+                                     nprod, p.b_split_in_kernel,
+                                     dp.smem_per_sm > 0 ? dp.smem_per_sm : 233472);
       // Stream-K: when the tiles do not fill whole waves of resident CTAs,
       // launch one wave of persistent CTAs that take whole tiles in waves and
       // split the rest of the (tile, K block) work evenly (each at least 4 K
@@ -424,6 +457,12 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
         if (sk) want = std::atoi(sk) != 0;
         p.stream_k = (want && g >= 2) ? 1 : 0;
         p.grid_ctas = p.stream_k ? g : tiles;
+        // B on chip only for one wave of whole tiles (see b_aligned above)
+        if (!b_forced && (p.stream_k || tiles > slots) &&
+            std::getenv("GEMM_TC_BSPLIT") == nullptr)
+          p.b_split_in_kernel = 0;
+        // no pass before the GEMM when both operands are split on chip
+        if (p.a_split_in_kernel && p.b_split_in_kernel) p.launches = 1;
         if (p.stream_k) p.launches += 1;
       }
       p.workspace_bytes = tc_workspace_bytes(p, M, N, K);

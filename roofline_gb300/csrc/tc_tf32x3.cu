@@ -41,8 +41,9 @@
 // the pipeline running across segment boundaries.
 // Operands live in shared memory K-major with the TMA swizzle (64 B rows for
 // BK = 16, 128 B rows for BK = 32), which is the layout the MMA's smem
-// descriptors describe.  B is row-major (N contiguous) in global memory, so
-// the split pass writes B_hi/B_lo transposed (N x K, K contiguous).
+// descriptors describe.  B stored K x N (N contiguous) is split by a pass
+// that writes B_hi/B_lo transposed (N x K, K contiguous); B stored N x K is
+// read as it is and split on chip like A (BR).
 //
 // Every mbarrier wait is bounded by a %globaltimer deadline; on expiry the
 // kernel records GEMM_ERR_DEVICE_TIMEOUT in a device status word, stops
@@ -71,8 +72,11 @@ __device__ int g_tc_status;  // 0 = ok, else a GEMM_ERR_* code
 // tensor-memory ring that the A_lo*B_hi MMA reads directly; otherwise A_hi
 // and A_lo come pre-split from the workspace.  CONCAT: B_hi and B_lo sit
 // next to each other in the stage, so A_hi*[B_hi | B_lo] is one MMA of width
-// 2*BN into two accumulators that the epilogue adds.
-template <int BM, int BN, int BK, int STAGES, int AK, bool CONCAT, int NPROD>
+// 2*BN into two accumulators that the epilogue adds.  BR: B is stored N x K
+// (K contiguous, as the MMA reads it) and arrives raw (FP32) too: the landed
+// tile is B_hi to the MMA as it is, and the converter warps write B_lo next
+// to it (1xTF32: round B in place), so no pass splits B before the kernel.
+template <int BM, int BN, int BK, int STAGES, int AK, bool CONCAT, int NPROD, bool BR>
 struct TcCfg {
   static_assert(NPROD == 3 || NPROD == 1, "3xTF32 or 1xTF32");
   static_assert(NPROD == 3 || !CONCAT, "1xTF32 has no B_lo to concatenate");
@@ -87,7 +91,8 @@ struct TcCfg {
   static constexpr int A_SMEM = (AK || !X3) ? A_BYTES : 2 * A_BYTES;  // A (raw/hi) [+ A_lo]
   static constexpr int B_SMEM = X3 ? 2 * B_BYTES : B_BYTES;           // B_hi [+ B_lo]
   static constexpr int STAGE_BYTES = A_SMEM + B_SMEM;
-  static constexpr int TX_BYTES = STAGE_BYTES;
+  // bytes the TMA writes per stage (B_lo of a raw B is written on chip)
+  static constexpr int TX_BYTES = A_SMEM + (BR ? B_BYTES : B_SMEM);
   static constexpr int ROW_BYTES = BK * 4;              // 64 or 128
   static constexpr uint32_t LAYOUT = ROW_BYTES == 128 ? 2u : 4u;
   static constexpr uint32_t SBO = 8 * ROW_BYTES;        // 8-row group stride
@@ -198,19 +203,19 @@ __device__ __forceinline__ void epi_store16(float4 *st, const float *v, float *d
   __syncwarp();  // the buffer is rewritten by the next block
 }
 
-template <int BM, int BN, int BK, int STAGES, int AK, bool CONCAT, int NPROD>
+template <int BM, int BN, int BK, int STAGES, int AK, bool CONCAT, int NPROD, bool BR>
 __global__ void __launch_bounds__(kThreadsTC, 1)
 tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
                  const __grid_constant__ CUtensorMap tmA_lo,
-                 const __grid_constant__ CUtensorMap tmB_hi,
+                 const __grid_constant__ CUtensorMap tmB_hi,  // B fp32 (N x K) when BR
                  const __grid_constant__ CUtensorMap tmB_lo, TcParams p) {
-  using Cfg = TcCfg<BM, BN, BK, STAGES, AK, CONCAT, NPROD>;
+  using Cfg = TcCfg<BM, BN, BK, STAGES, AK, CONCAT, NPROD, BR>;
   constexpr bool X3 = Cfg::X3;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * Cfg::STAGE_BYTES);
-  uint64_t *conv = full + STAGES;    // A tile split (AK)
+  uint64_t *conv = full + STAGES;    // A (AK) and B (BR) tiles split
   uint64_t *empty = conv + STAGES;   // stage free again
   uint64_t *acc_full = empty + STAGES;
   uint64_t *acc_empty = acc_full + 1;
@@ -243,7 +248,7 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmA_hi);
     prefetch_tmap(&tmB_hi);
-    if (X3) prefetch_tmap(&tmB_lo);
+    if (X3 && !BR) prefetch_tmap(&tmB_lo);
     if (!AK && X3) prefetch_tmap(&tmA_lo);
   }
   if (warp == 1) {
@@ -291,7 +296,7 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
           tma_load_2d(a_hi(s), &tmA_hi, &full[s], kx, m0);
           if (!AK && X3) tma_load_2d(a_lo(s), &tmA_lo, &full[s], kx, m0);
           tma_load_2d(b_hi(s), &tmB_hi, &full[s], kx, n0);
-          if (X3) tma_load_2d(b_lo(s), &tmB_lo, &full[s], kx, n0);
+          if (X3 && !BR) tma_load_2d(b_lo(s), &tmB_lo, &full[s], kx, n0);
           ++issued;
         }
       }
@@ -323,7 +328,7 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
         for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
           const int s = it % STAGES;
           const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
-          if (!mbar_wait(AK ? &conv[s] : &full[s], ph, deadline, abort_flag)) {
+          if (!mbar_wait((AK || BR) ? &conv[s] : &full[s], ph, deadline, abort_flag)) {
             ok = false;
             break;
           }
@@ -433,7 +438,7 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
         }
         if constexpr (Cfg::C_TMEM) tmem_st_wait();
       }
-      if (AK) {
+      if (AK || BR) {
         for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
@@ -446,7 +451,7 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
           // chunk c sits at chunk c ^ f(row) of its 64- or 128-byte line (the
           // TMA swizzle; f depends on the row's low bits only).
 #pragma unroll 1
-          for (int half = 0; half < Cfg::MH; ++half) {
+          for (int half = 0; half < (AK ? Cfg::MH : 0); ++half) {
           uint8_t *line = a_hi(s) + (half * 128 + row) * Cfg::ROW_BYTES;
           if constexpr (!X3) {
             // 1xTF32: round in place, nothing goes to tensor memory.  Chunks
@@ -496,7 +501,38 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
             tmem_st_wait();
           }
           }  // halves
-          if constexpr (X3) tc_fence_before();
+          if constexpr (BR) {
+            // B_lo = B - tf32_trunc(B), stored at B's own offsets in the B_lo
+            // buffer (the split is elementwise and the swizzle only permutes
+            // 16-byte chunks inside each line); 1xTF32 rounds B in place.
+            // Consecutive threads take consecutive 16-byte chunks.
+            static_assert(Cfg::B_BYTES % (16 * kConvThreads) == 0, "whole chunks per thread");
+            const float4 *src = reinterpret_cast<const float4 *>(b_hi(s));
+            float4 *dst = reinterpret_cast<float4 *>(X3 ? b_lo(s) : b_hi(s));
+            const int ct = (int)threadIdx.x - 64;
+            constexpr int PER_T = Cfg::B_BYTES / (16 * kConvThreads);
+            float4 x[PER_T];
+#pragma unroll
+            for (int i = 0; i < PER_T; ++i) x[i] = src[ct + i * kConvThreads];
+#pragma unroll
+            for (int i = 0; i < PER_T; ++i) {
+              float4 y;
+              if constexpr (X3) {
+                y.x = x[i].x - tf32_trunc(x[i].x);
+                y.y = x[i].y - tf32_trunc(x[i].y);
+                y.z = x[i].z - tf32_trunc(x[i].z);
+                y.w = x[i].w - tf32_trunc(x[i].w);
+              } else {
+                y.x = tf32_rna(x[i].x);
+                y.y = tf32_rna(x[i].y);
+                y.z = tf32_rna(x[i].z);
+                y.w = tf32_rna(x[i].w);
+              }
+              dst[ct + i * kConvThreads] = y;
+            }
+            fence_async_smem();  // the MMA (async proxy) reads what was written
+          }
+          if constexpr (AK != 0 && X3) tc_fence_before();
           mbar_arrive(&conv[s]);
         }
         if (!ok) break;
@@ -670,19 +706,20 @@ struct WsLayout {
   int64_t kp;
 };
 
-// Workspace regions: B_hi, B_lo (K-major), A_hi, A_lo (unless A is split
-// in the kernel), then for stream-K the partial tiles (2 per CTA).  The B
-// planes come first so their place depends only on N, K and the mode: calls
-// that share B (row blocks of one product) can reuse them.
-WsLayout ws_layout(int64_t M, int64_t N, int64_t K, bool a_inkernel, int64_t streamk_ctas,
-                   int bm, int bn, bool x3) {
+// Workspace regions: B_hi, B_lo (K-major; unless B is split in the kernel),
+// A_hi, A_lo (unless A is split in the kernel), then for stream-K the partial
+// tiles (2 per CTA).  The B planes come first so their place depends only on
+// N, K and the mode: calls that share B (row blocks of one product) can
+// reuse them.
+WsLayout ws_layout(int64_t M, int64_t N, int64_t K, bool a_inkernel, bool b_inkernel,
+                   int64_t streamk_ctas, int bm, int bn, bool x3) {
   WsLayout w{};
   // Planes' rows padded (with zeros) to a multiple of 32 floats: every TMA
   // box (16 or 32 K values of a row) then starts on a 128-byte line of its
   // own instead of straddling two (GB300, 1023 x 1025 x 777: kernel 26.0 ->
   // 22.5 us; 1500^3 31.0 -> 29.2 us).
   w.kp = round_up(K, 32);
-  const uint64_t b_bytes = align256((uint64_t)N * w.kp * 4);
+  const uint64_t b_bytes = b_inkernel ? 0 : align256((uint64_t)N * w.kp * 4);
   const uint64_t b_lo_bytes = x3 ? b_bytes : 0;
   const uint64_t a_bytes = a_inkernel ? 0 : align256((uint64_t)M * w.kp * 4);
   const uint64_t a_lo_bytes = x3 ? a_bytes : 0;
@@ -695,9 +732,9 @@ WsLayout ws_layout(int64_t M, int64_t N, int64_t K, bool a_inkernel, int64_t str
   return w;
 }
 
-template <int BM, int BN, int BK, int STAGES, int AK, bool CONCAT, int NPROD>
+template <int BM, int BN, int BK, int STAGES, int AK, bool CONCAT, int NPROD, bool BR>
 int launch_cfg(const gemm_plan_t &plan, const GemmArgs &a, char *ws, cudaStream_t s) {
-  using Cfg = TcCfg<BM, BN, BK, STAGES, AK, CONCAT, NPROD>;
+  using Cfg = TcCfg<BM, BN, BK, STAGES, AK, CONCAT, NPROD, BR>;
   constexpr bool X3 = Cfg::X3;
   const int64_t tiles_m = ceil_div(a.M, BM), tiles_n = ceil_div(a.N, BN);
   const int64_t tiles = tiles_m * tiles_n;
@@ -711,7 +748,7 @@ int launch_cfg(const gemm_plan_t &plan, const GemmArgs &a, char *ws, cudaStream_
     return GEMM_ERR_UNSUPPORTED;
   const int64_t G = plan.stream_k ? plan.grid_ctas : tiles;
   if (G < 1 || G > 0x7fffffff || tiles > 0x7fffffff) return GEMM_ERR_UNSUPPORTED;
-  const WsLayout L = ws_layout(a.M, a.N, a.K, AK, plan.stream_k ? G : 0, BM, BN, X3);
+  const WsLayout L = ws_layout(a.M, a.N, a.K, AK, BR, plan.stream_k ? G : 0, BM, BN, X3);
   float *ahi = reinterpret_cast<float *>(ws + L.a_hi);
   float *alo = reinterpret_cast<float *>(ws + L.a_lo);
   float *bhi = reinterpret_cast<float *>(ws + L.b_hi);
@@ -727,9 +764,16 @@ int launch_cfg(const gemm_plan_t &plan, const GemmArgs &a, char *ws, cudaStream_
     tA1 = tA0;
     if (X3) ok = ok && encode_2d(&tA1, alo, L.kp, a.M, L.kp, BK, BM);
   }
-  ok = ok && encode_2d(&tB0, bhi, L.kp, a.N, L.kp, BK, BN);
-  tB1 = tB0;
-  if (X3) ok = ok && encode_2d(&tB1, blo, L.kp, a.N, L.kp, BK, BN);
+  if (BR) {
+    // raw B, stored N x K: BK x BN boxes like A's
+    if (!a.tb) return GEMM_ERR_UNSUPPORTED;
+    ok = ok && encode_2d(&tB0, a.B, a.K, a.N, a.ldb, BK, BN);
+    tB1 = tB0;
+  } else {
+    ok = ok && encode_2d(&tB0, bhi, L.kp, a.N, L.kp, BK, BN);
+    tB1 = tB0;
+    if (X3) ok = ok && encode_2d(&tB1, blo, L.kp, a.N, L.kp, BK, BN);
+  }
   if (!ok) return GEMM_ERR_UNSUPPORTED;
 
   TcParams p;
@@ -804,7 +848,7 @@ int launch_cfg(const gemm_plan_t &plan, const GemmArgs &a, char *ws, cudaStream_
   p.stream_blocks = a.stream_blocks;
   p.stall_producer = (int)env_u64("GEMM_DEBUG_STALL_PRODUCER", 0);
   p.stamps = profile_stamps();
-  auto kern = tc_tf32x3_kernel<BM, BN, BK, STAGES, AK, CONCAT, NPROD>;
+  auto kern = tc_tf32x3_kernel<BM, BN, BK, STAGES, AK, CONCAT, NPROD, BR>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Cfg::SMEM_BYTES) != cudaSuccess) {
     cudaGetLastError();
@@ -827,7 +871,7 @@ int launch_cfg(const gemm_plan_t &plan, const GemmArgs &a, char *ws, cudaStream_
   if (!AK)
     jobs[njobs++] = a.ta ? split_transposed_job(a.A, a.lda, a.K, a.M, L.kp, ahi, X3 ? alo : nullptr)
                          : split_rows_job(a.A, a.lda, a.M, a.K, L.kp, ahi, X3 ? alo : nullptr);
-  if (!a.b_presplit)
+  if (!BR && !a.b_presplit)
     jobs[njobs++] = a.tb ? split_rows_job(a.B, a.ldb, a.N, a.K, L.kp, bhi, X3 ? blo : nullptr)
                          : split_transposed_job(a.B, a.ldb, a.K, a.N, L.kp, bhi, X3 ? blo : nullptr);
   const cudaError_t se =
@@ -871,37 +915,42 @@ bool tc_supported(const DeviceProps &dp) { return dp.cc_major == 10 && dp.cc_min
 
 // Tile configurations the planner may pick: (bm, bn, bk, stages, A split in
 // kernel (0 no, 1 with A_hi in shared memory, 2 with A_hi in tensor memory),
-// concatenated B MMA, TF32 products per FP32 product).
-#define GG_TC_CONFIGS(X)                  \
-  X(128, 64, 16, 6, 0, true, 3)         \
-  X(128, 64, 32, 4, 0, true, 3)         \
-  X(128, 256, 16, 5, 1, false, 3)       \
-  X(128, 256, 16, 5, 2, false, 3)       \
-  X(128, 128, 32, 4, 2, true, 3)        \
-  X(128, 128, 32, 4, 1, true, 3)        \
-  X(128, 64, 32, 6, 1, true, 3)         \
-  X(128, 64, 32, 3, 1, true, 3)         \
-  X(128, 64, 32, 2, 1, false, 3)        \
-  X(128, 64, 16, 4, 1, false, 3)        \
-  X(128, 256, 16, 4, 0, false, 3)       \
-  X(128, 128, 16, 3, 0, true, 3)        \
-  X(128, 128, 16, 6, 0, true, 3)        \
-  X(256, 256, 16, 3, 0, false, 3)       \
-  X(128, 256, 16, 8, 1, false, 1)       \
-  X(128, 64, 32, 4, 1, false, 1)        \
-  X(128, 256, 16, 8, 0, false, 1)       \
-  X(256, 256, 16, 6, 0, false, 1)       \
-  X(256, 256, 32, 3, 0, false, 1)       
+// concatenated B MMA, TF32 products per FP32 product, B split in kernel).
+#define GG_TC_CONFIGS(X)                      \
+  X(128, 64, 16, 6, 0, true, 3, false)      \
+  X(128, 64, 32, 4, 0, true, 3, false)      \
+  X(128, 256, 16, 5, 1, false, 3, false)    \
+  X(128, 256, 16, 5, 2, false, 3, false)    \
+  X(128, 128, 32, 4, 2, true, 3, false)     \
+  X(128, 128, 32, 4, 1, true, 3, false)     \
+  X(128, 64, 32, 6, 1, true, 3, false)      \
+  X(128, 64, 32, 3, 1, true, 3, false)      \
+  X(128, 64, 32, 2, 1, false, 3, false)     \
+  X(128, 64, 16, 4, 1, false, 3, false)     \
+  X(128, 256, 16, 4, 0, false, 3, false)    \
+  X(128, 128, 16, 3, 0, true, 3, false)     \
+  X(128, 128, 16, 6, 0, true, 3, false)     \
+  X(256, 256, 16, 3, 0, false, 3, false)    \
+  X(128, 256, 16, 8, 1, false, 1, false)    \
+  X(128, 64, 32, 4, 1, false, 1, false)     \
+  X(128, 256, 16, 8, 0, false, 1, false)    \
+  X(256, 256, 16, 6, 0, false, 1, false)    \
+  X(256, 256, 32, 3, 0, false, 1, false)    \
+  X(128, 256, 16, 5, 2, false, 3, true)     \
+  X(128, 128, 32, 4, 2, true, 3, true)      \
+  X(128, 64, 32, 6, 1, true, 3, true)       \
+  X(128, 64, 32, 4, 0, true, 3, true)
 
 // a_inkernel: 0 A pre-split, 1 split on chip (A_hi in shared memory), 2 split
-// on chip with A_hi in tensor memory.
-#define GG_TC_MATCH(BM_, BN_, BK_, ST_, AK_, CC_, NP_)                                  \
+// on chip with A_hi in tensor memory.  b_inkernel: B split on chip.
+#define GG_TC_MATCH(BM_, BN_, BK_, ST_, AK_, CC_, NP_, BR_)                        \
   (bm == BM_ && bn == BN_ && bk == BK_ && stages == ST_ && a_inkernel == (AK_) && \
-   (concat != 0) == CC_ && nprod == NP_)
+   (concat != 0) == CC_ && nprod == NP_ && (b_inkernel != 0) == BR_)
 
-bool tc_config_valid(int bm, int bn, int bk, int stages, int a_inkernel, int concat, int nprod) {
-#define GG_MATCH(BM_, BN_, BK_, ST_, AK_, CC_, NP_) \
-  if (GG_TC_MATCH(BM_, BN_, BK_, ST_, AK_, CC_, NP_)) return true;
+bool tc_config_valid(int bm, int bn, int bk, int stages, int a_inkernel, int concat, int nprod,
+                     int b_inkernel) {
+#define GG_MATCH(BM_, BN_, BK_, ST_, AK_, CC_, NP_, BR_) \
+  if (GG_TC_MATCH(BM_, BN_, BK_, ST_, AK_, CC_, NP_, BR_)) return true;
   GG_TC_CONFIGS(GG_MATCH)
 #undef GG_MATCH
   return false;
@@ -914,10 +963,10 @@ constexpr int kMaxCtasPerSm = 2;
 // CTAs of one configuration that fit on an SM (shared memory, TMEM and
 // registers).
 int tc_ctas_per_sm(int bm, int bn, int bk, int stages, int a_inkernel, int concat, int nprod,
-                   int smem_per_sm) {
-#define GG_OCC(BM_, BN_, BK_, ST_, AK_, CC_, NP_)              \
-  if (GG_TC_MATCH(BM_, BN_, BK_, ST_, AK_, CC_, NP_)) {         \
-    using C = TcCfg<BM_, BN_, BK_, ST_, AK_, CC_, NP_>;         \
+                   int b_inkernel, int smem_per_sm) {
+#define GG_OCC(BM_, BN_, BK_, ST_, AK_, CC_, NP_, BR_)         \
+  if (GG_TC_MATCH(BM_, BN_, BK_, ST_, AK_, CC_, NP_, BR_)) {    \
+    using C = TcCfg<BM_, BN_, BK_, ST_, AK_, CC_, NP_, BR_>;    \
     int by_smem = smem_per_sm / (C::SMEM_BYTES + 1024);         \
     int by_tmem = 512 / C::TMEM_COLS;                           \
     int n = by_smem < by_tmem ? by_smem : by_tmem;              \
@@ -942,28 +991,34 @@ bool tc_plan_streaming(gemm_plan_t &plan, int64_t M, int64_t N, int64_t K) {
 }
 
 uint64_t tc_workspace_bytes(const gemm_plan_t &plan, int64_t M, int64_t N, int64_t K) {
-  return ws_layout(M, N, K, plan.a_split_in_kernel != 0, plan.stream_k ? plan.grid_ctas : 0,
-                   plan.bm, plan.bn, plan.mode != GEMM_MODE_TF32)
+  return ws_layout(M, N, K, plan.a_split_in_kernel != 0, plan.b_split_in_kernel != 0,
+                   plan.stream_k ? plan.grid_ctas : 0, plan.bm, plan.bn,
+                   plan.mode != GEMM_MODE_TF32)
       .total;
 }
 
 int launch_tc(const gemm_plan_t &plan, const GemmArgs &a, void *ws, size_t ws_bytes,
               cudaStream_t s) {
   if (!get_encoder()) return GEMM_ERR_UNSUPPORTED;
-  if (ws_bytes < tc_workspace_bytes(plan, a.M, a.N, a.K) || ws == nullptr)
-    return GEMM_ERR_WORKSPACE_TOO_SMALL;
-  // the in-kernel A split reads A by TMA as M x K rows
+  const uint64_t need = tc_workspace_bytes(plan, a.M, a.N, a.K);
+  if (ws_bytes < need || (need > 0 && ws == nullptr)) return GEMM_ERR_WORKSPACE_TOO_SMALL;
+  // the in-kernel A split reads A by TMA as M x K rows, the in-kernel B
+  // split B as N x K rows
   if (plan.a_split_in_kernel &&
       (a.ta || (a.lda & 3) || (reinterpret_cast<uintptr_t>(a.A) & 15)))
+    return GEMM_ERR_UNSUPPORTED;
+  if (plan.b_split_in_kernel &&
+      (!a.tb || (a.ldb & 3) || (reinterpret_cast<uintptr_t>(a.B) & 15)))
     return GEMM_ERR_UNSUPPORTED;
   char *w = static_cast<char *>(ws);
   const int nprod = plan.mode == GEMM_MODE_TF32 ? 1 : 3;
   const int bm = plan.bm, bn = plan.bn, bk = plan.bk, stages = plan.stages;
   const int a_inkernel = plan.a_split_in_kernel ? (plan.a_hi_tmem ? 2 : 1) : 0;
   const int concat = plan.b_concat;
-#define GG_LAUNCH(BM_, BN_, BK_, ST_, AK_, CC_, NP_)  \
-  if (GG_TC_MATCH(BM_, BN_, BK_, ST_, AK_, CC_, NP_)) \
-    return launch_cfg<BM_, BN_, BK_, ST_, AK_, CC_, NP_>(plan, a, w, s);
+  const int b_inkernel = plan.b_split_in_kernel;
+#define GG_LAUNCH(BM_, BN_, BK_, ST_, AK_, CC_, NP_, BR_)  \
+  if (GG_TC_MATCH(BM_, BN_, BK_, ST_, AK_, CC_, NP_, BR_)) \
+    return launch_cfg<BM_, BN_, BK_, ST_, AK_, CC_, NP_, BR_>(plan, a, w, s);
   GG_TC_CONFIGS(GG_LAUNCH)
 #undef GG_LAUNCH
   return GEMM_ERR_UNSUPPORTED;

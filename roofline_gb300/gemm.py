@@ -74,7 +74,8 @@ class GemmPlan(ctypes.Structure):
                 ("workspace_bytes", ctypes.c_uint64), ("flops", ctypes.c_double),
                 ("bytes", ctypes.c_double), ("intensity", ctypes.c_double),
                 ("b_concat", ctypes.c_int32), ("ctas_per_sm", ctypes.c_int32),
-                ("stream_k", ctypes.c_int32), ("a_hi_tmem", ctypes.c_int32)]
+                ("stream_k", ctypes.c_int32), ("a_hi_tmem", ctypes.c_int32),
+                ("b_split_in_kernel", ctypes.c_int32)]
 
     def as_dict(self):
         d = {name: getattr(self, name) for name, _ in self._fields_}

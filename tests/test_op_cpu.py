@@ -76,9 +76,12 @@ def test_transposed_a_uses_the_pre_split(lib):
     p = gemm.plan_op(ROW, T_, N_, 4096, 4096, 4096, mode="tf32x3")
     assert p["kernel_name"] == "tc_tf32x3" and p["a_split_in_kernel"] == 0
     assert p["launches"] == 2 + p["stream_k"]
-    # B stored N x K: still one split pass for B, A split on chip
+    assert p["b_split_in_kernel"] == 0  # B stored K x N: the transposing pass
+    # B stored N x K at this size (stream-K): still one split pass for B, A
+    # split on chip
     q = gemm.plan_op(ROW, N_, T_, 4096, 4096, 4096, mode="tf32x3")
-    assert q["a_split_in_kernel"] == 1 and q["launches"] == 2 + q["stream_k"]
+    assert q["a_split_in_kernel"] == 1 and q["b_split_in_kernel"] == 0
+    assert q["launches"] == 2 + q["stream_k"]
     # the tensor-core workspace then also holds A_hi / A_lo
     assert p["workspace_bytes"] >= q["workspace_bytes"] + 2 * 4096 * 4096 * 4
 
@@ -138,3 +141,23 @@ class _View:
 def test_operand_leading_dimension(shape, strides, want):
     assert gemm._operand(_View(shape, strides), "X") == want
 
+
+
+def test_b_stored_n_by_k_split_on_chip_for_one_wave(lib):
+    # B stored N x K is split on chip when the tiles fit one wave without
+    # stream-K (measured on GB300: 1200 x 640 x 336 13.0 -> 10.5 us, 2048^3
+    # 68.5 -> 65.8 us); longer runs of full tiles keep the pass (8192^3)
+    for shape in [(2048, 2048, 2048), (1200, 640, 336)]:
+        q = gemm.plan_op(ROW, N_, T_, *shape, mode="tf32x3")
+        assert (q["a_split_in_kernel"], q["b_split_in_kernel"], q["launches"]) == (1, 1, 1)
+        assert q["workspace_bytes"] == 0
+    assert gemm.plan_op(ROW, N_, T_, 8192, 8192, 8192, mode="tf32x3")["b_split_in_kernel"] == 0
+    # small products: A split on chip too, so the call is one launch
+    for shape in [(512, 512, 512), (1024, 1024, 1024)]:
+        q = gemm.plan_op(ROW, N_, T_, *shape, mode="tf32x3")
+        assert (q["bn"], q["stages"], q["a_split_in_kernel"], q["b_split_in_kernel"],
+                q["launches"]) == (64, 6, 1, 1, 1)
+    # B stored K x N always goes through the transposing pass
+    assert gemm.plan_op(ROW, N_, N_, 2048, 2048, 2048, mode="tf32x3")["b_split_in_kernel"] == 0
+    # ldb not a multiple of 4: no TMA of B as stored
+    assert gemm.plan_op(ROW, N_, T_, 2048, 2048, 2047, mode="tf32x3")["b_split_in_kernel"] == 0

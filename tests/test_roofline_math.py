@@ -79,7 +79,7 @@ def test_traffic_entries_match_current_sources():
     # keyed by the exact instantiation and launch shape the bench reports
     # (bench.kernel_instance), so counters of one configuration are never
     # attached to another
-    pat = re.compile(r"^(tc_tf32x3_kernel<\d+(,\d+){6}>|simt_packed_kernel<\d+(,\d+){6}>) "
+    pat = re.compile(r"^(tc_tf32x3_kernel<\d+(,\d+){7}>|simt_packed_kernel<\d+(,\d+){6}>) "
                      r"grid=\d+ split_k=\d+ stream_k=[01] @ \w+$")
     for key, e in entries.items():
         assert pat.match(key), key
@@ -98,9 +98,11 @@ def test_kernel_instance_names_the_configuration():
             "a_split_in_kernel": 1, "a_hi_tmem": 1, "b_concat": 0, "grid_ctas": 152,
             "split_k": 1, "stream_k": 1, "vec": 1}
     assert bench.kernel_instance(plan) == \
-        "tc_tf32x3_kernel<128,256,16,5,2,0,3> grid=152 split_k=1 stream_k=1"
+        "tc_tf32x3_kernel<128,256,16,5,2,0,3,0> grid=152 split_k=1 stream_k=1"
     plan.update(kernel_name="tc_tf32", a_hi_tmem=0)
-    assert bench.kernel_instance(plan).startswith("tc_tf32x3_kernel<128,256,16,5,1,0,1>")
+    assert bench.kernel_instance(plan).startswith("tc_tf32x3_kernel<128,256,16,5,1,0,1,0>")
+    plan.update(kernel_name="tc_tf32x3", b_split_in_kernel=1, stream_k=0)
+    assert bench.kernel_instance(plan).startswith("tc_tf32x3_kernel<128,256,16,5,1,0,3,1>")
     plan.update(kernel_name="simt", bm=64, bn=128, bk=16, stages=4, grid_ctas=2048, stream_k=0)
     assert bench.kernel_instance(plan) == \
         "simt_packed_kernel<64,128,16,4,1,0,0> grid=2048 split_k=1 stream_k=0"

@@ -207,3 +207,56 @@ def test_simt_tile_orders(group, op_b, monkeypatch):
     M, N, K = 1000, 1100, 96
     A, B, C0, got = run_op(ROW, N_, op_b, M, N, K, 1.0, 0.0, "int2", "fp32_simt")
     assert oracle.mismatches(got, oracle.gemm(A, B, 1.0, 0.0, None)) == 0
+
+
+# Tensor-core configurations built with B split on chip, for B stored N x K
+# (bm, bn, bk, stages, a_split, b_concat): read as stored, B_hi is the landed
+# tile itself and B_lo = B - tf32_trunc(B) is written beside it on chip.
+TC_BSPLIT = ["128,256,16,5,2,0", "128,128,32,4,2,1", "128,64,32,6,1,1", "128,64,32,4,0,1"]
+
+
+@pytest.mark.parametrize("cfg", TC_BSPLIT)
+@pytest.mark.parametrize("shape", [(333, 270, 164), (129, 64, 777), (1, 300, 68), (300, 5, 1000)])
+def test_tc_b_split_on_chip_every_configuration(cfg, shape, monkeypatch):
+    from roofline_gb300 import gemm
+    M, N, K = shape
+    # A split on chip needs A stored M x K; the pre-split-A configuration
+    # takes a transposed A too
+    op_a = N_ if cfg.split(",")[4] != "0" else T_
+    pad = (-K) % 4  # ld = K + pad: rows of B (N x K) start on 16-byte boundaries
+    ldb = K + pad
+    lda = K + pad if op_a == N_ else M + pad
+    monkeypatch.setenv("GEMM_TC_CONFIG", cfg + ",1")
+    p = gemm.plan_op(ROW, op_a, T_, M, N, K, lda=lda, ldb=ldb, ldc=N + pad, mode="tf32x3")
+    assert p["b_split_in_kernel"] == 1
+    assert "%d,%d,%d,%d" % (p["bm"], p["bn"], p["bk"], p["stages"]) == cfg.rsplit(",", 2)[0]
+    A, B, C0, got = run_op(ROW, op_a, T_, M, N, K, 1.25, -0.5, "u11", "tf32x3", pad=pad)
+    ref, D = oracle.gemm(A, B, 1.25, -0.5, C0, with_bound=True)
+    assert oracle.err_normalised(got, ref, D) <= TOL_E1
+    # the same bits as this configuration with B split by the pass (both
+    # take B_hi = tf32_trunc(B) and issue the same MMAs in the same order)
+    monkeypatch.setenv("GEMM_TC_CONFIG", cfg + ",0")
+    _, _, _, got0 = run_op(ROW, op_a, T_, M, N, K, 1.25, -0.5, "u11", "tf32x3", pad=pad)
+    assert np.array_equal(_dense(got).view(np.uint32), _dense(got0).view(np.uint32))
+    monkeypatch.setenv("GEMM_TC_CONFIG", cfg + ",1")
+    A, B, C0, got = run_op(ROW, op_a, T_, M, N, K, 1.0, 0.0, "int2", "tf32x3", pad=pad)
+    assert oracle.mismatches(got, oracle.gemm(A, B, 1.0, 0.0, None)) == 0
+
+
+def test_tc_b_split_on_chip_planner_sampled():
+    # 2048^3 with B stored N x K: the planner's one-wave choice splits both
+    # operands on chip, one launch; sampled entries against the oracle
+    import torch
+    from roofline_gb300 import gemm
+    from workloads import sample_entries
+    M = N = K = 2048
+    A = matrix(M, K, K, 31, "u11")
+    Bt = matrix(N, K, K, 32, "u11")
+    p = gemm.plan_op(ROW, N_, T_, M, N, K, mode="auto")
+    assert (p["kernel_name"], p["a_split_in_kernel"], p["b_split_in_kernel"], p["launches"]) == \
+        ("tc_tf32x3", 1, 1, 1)
+    C = gemm.matmul(torch.from_numpy(A).cuda(), torch.from_numpy(Bt).cuda().t(), mode="auto")
+    torch.cuda.synchronize()
+    rows, cols = sample_entries(M, N, n=2048)
+    ref, D = oracle.gemm_entries(A, _dense(Bt.T), rows, cols, 1.0, 0.0, None)
+    assert oracle.err_normalised(C.cpu().numpy()[rows, cols], ref, D) <= TOL_E1
