@@ -174,15 +174,18 @@ TRAFFIC_SOURCES = {
 }
 
 
-def kernel_instance(plan) -> str:
+def kernel_instance(plan, b_stored_nk=False) -> str:
     """The template instantiation and launch shape a plan runs, e.g.
-    ``tc_tf32x3_kernel<128,256,16,5,2,0,3,0> grid=152 stream_k=1``."""
+    ``tc_tf32x3_kernel<128,256,16,5,2,0,3,0> grid=152 stream_k=1``.  The
+    last template value says how B is split: 0 by the pass, 1 on chip as
+    stored N x K, 2 on chip transposed from K x N (the bench's row-major B)."""
     k = plan["kernel_name"]
     if k in ("tc_tf32x3", "tc_tf32"):
         ak = 0 if not plan["a_split_in_kernel"] else (2 if plan["a_hi_tmem"] else 1)
         nprod = 1 if k == "tc_tf32" else 3
+        br = 0 if not plan.get("b_split_in_kernel", 0) else (1 if b_stored_nk else 2)
         inst = (f"tc_tf32x3_kernel<{plan['bm']},{plan['bn']},{plan['bk']},{plan['stages']},"
-                f"{ak},{int(plan['b_concat'])},{nprod},{int(plan.get('b_split_in_kernel', 0))}>")
+                f"{ak},{int(plan['b_concat'])},{nprod},{br}>")
     elif k == "simt":
         inst = (f"simt_packed_kernel<{plan['bm']},{plan['bn']},{plan['bk']},{plan['stages']},"
                 f"{int(plan['vec'])},0,0>")

@@ -339,11 +339,14 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
       // and the split pass only has B to do (GB300: 1200 x 640 x 336 15.3 ->
       // 13.5 us, 768^3 20.4 -> 19.0 us; 512^3, 32 tiles, 14.1 against 14.6
       // and 1024^3, K = 1024, 24.0 against 25.4 keep both pre-split).
-      // With B stored N x K and split on chip as well (see b_aligned below),
-      // an aligned A always goes on chip too: the call is then one launch
-      // (GB300, B stored N x K, pre-split A / A on chip: 512^3 14.0 / 12.3
-      // us, 640^3 16.0 / 14.2, 1024^3 22.4 / 19.8).
-      const bool b_aligned = tb && (ldb % 4 == 0) && ((align_hint & 15) == 0);
+      // With B split on chip as well (see b_tma below), an aligned A always
+      // goes on chip too: the call is then one launch (GB300, B stored N x
+      // K, pre-split A / A on chip: 512^3 14.0 / 12.3 us, 640^3 16.0 / 14.2,
+      // 1024^3 22.4 / 19.8).
+      const bool b_tma = (ldb % 4 == 0) && ((align_hint & 15) == 0);
+      bool b_chip = tb || x3;
+      if (const char *bs = std::getenv("GEMM_TC_BSPLIT")) b_chip = std::atoi(bs) != 0;  // tuning knob
+      const bool b_aligned = b_chip && b_tma;
       if (x3 && small_tc_product(M, N, K, sms)) {
         if (a_aligned && (b_aligned || (K <= 768 && ceil_div(M, 128) * ceil_div(N, 64) >= 64))) {
           set(64, 32, 6, 1);
@@ -354,25 +357,28 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
         p.a_hi_tmem = 0;
         no_stream_k = true;
       }
-      // B stored N x K (K contiguous, the way the MMA reads it) and aligned
-      // for TMA (16-byte base, ldb a multiple of 4): read as stored and split
-      // on chip, so no pass handles B before the GEMM, where the chosen
-      // configuration is built that way.  B stored K x N needs the
-      // transposing pass: an MMA reading B N-contiguous (the instruction
-      // descriptor's transpose bit) left the kind::tf32 accumulator at zero
-      // on GB300.
-      // The split adds a read of B and a write of B_lo to shared memory per
-      // stage, which the MMAs of a long run of full tiles cannot spare: it is
-      // taken when the tiles fit one wave without stream-K (decided below).
-      // GB300, 3xTF32, B stored N x K, step time with the pass / on chip (us):
-      // 1200 x 640 x 336 13.0 / 10.5 (one launch), 1024^3 23.2 / 22.5,
-      // 2048^3 68.5 / 65.8; 4096^3 (stream-K) about equal with a kernel of
-      // 390-417 against 443 us, 8192^3 3.30-3.42 against 3.47-3.67 ms.
+      // B aligned for TMA (16-byte base, ldb a multiple of 4) can be read as
+      // stored and split on chip, so no pass handles B before the GEMM.
+      // Stored N x K (K contiguous, the way the MMA reads it), the landed
+      // tile is B_hi and B_lo is written beside it.  The split adds a read of
+      // B and a write of B_lo to shared memory per stage, which the MMAs of
+      // a long run of full tiles cannot spare: it is taken when the tiles
+      // fit one wave without stream-K (decided below).  GB300, 3xTF32, step
+      // time with the pass / on chip (us): 1200 x 640 x 336 13.0 / 10.5 (one
+      // launch), 1024^3 23.2 / 22.5, 2048^3 68.5 / 65.8; 4096^3 (stream-K)
+      // about equal with a kernel of 390-417 against 443 us, 8192^3
+      // 3.30-3.42 against 3.47-3.67 ms.
+      // Stored K x N, the converter warps also transpose it (an MMA reading
+      // B N-contiguous, through the instruction descriptor's transpose bit,
+      // left the kind::tf32 accumulator at zero on GB300); that pays for the
+      // small-product tiles (128 x 64 x 32) with A split on chip as well, one
+      // launch a call (GB300, with the pass / on chip: 512^3 14.0 / 13.1 us,
+      // 1200 x 640 x 336 13.3 / 11.0, 768^3 18.9 / 16.9, 1024^3 23.9 /
+      // 21.0), not for wider tiles (1536^3, 128 x 128 tiles, 34.9 / 39.3;
+      // 2048^3 68.3 / 88.5) nor with A pre-split (512^3 14.0 / 14.6).
       const int ak = p.a_split_in_kernel ? (p.a_hi_tmem ? 2 : 1) : 0;
-      bool b_chip = true;
-      if (const char *bs = std::getenv("GEMM_TC_BSPLIT")) b_chip = std::atoi(bs) != 0;  // tuning knob
       p.b_split_in_kernel =
-          (b_chip && b_aligned &&
+          (b_aligned && (tb || (p.bn == 64 && p.bk == 32 && ak != 0)) &&
            tc_config_valid(p.bm, p.bn, p.bk, p.stages, ak, p.b_concat, nprod, 1))
               ? 1
               : 0;
@@ -381,8 +387,9 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
       // tile), "bm,bn,bk,stages,a_split,b_concat" or
       // "bm,bn,bk,stages,a_split,b_concat,b_split" picks one of the built
       // configurations (ignored if it names none, or asks for an in-kernel
-      // split of a misaligned operand).  a_split: 0 pre-split, 1 on chip, 2
-      // on chip with A_hi kept in tensor memory; b_split: 1 on chip.
+      // split of a misaligned operand, or of a B stored K x N in tiles other
+      // than 64 x 32).  a_split: 0 pre-split, 1 on chip, 2 on chip with A_hi
+      // kept in tensor memory; b_split: 1 on chip.
       if (const char *cfg = std::getenv("GEMM_TC_CONFIG")) {
         int v[7] = {0, 0, 0, 0, 0, 0, 0};
         const int n = std::sscanf(cfg, "%d,%d,%d,%d,%d,%d,%d", &v[0], &v[1], &v[2], &v[3],
@@ -391,7 +398,8 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
         const int bm = n >= 6 ? v[0] : 128;
         const int bsplit = n == 7 ? v[6] : 0;
         if (n >= 5 && tc_config_valid(bm, c[0], c[1], c[2], c[3], c[4], nprod, bsplit) &&
-            (!c[3] || a_aligned) && (!bsplit || b_aligned)) {
+            (!c[3] || a_aligned) &&
+            (!bsplit || (b_tma && (tb || (c[0] == 64 && c[1] == 32))))) {
           set(c[0], c[1], c[2], c[4], bm);
           p.a_split_in_kernel = c[3] != 0;
           p.a_hi_tmem = c[3] == 2;

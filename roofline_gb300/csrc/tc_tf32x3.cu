@@ -42,8 +42,9 @@
 // Operands live in shared memory K-major with the TMA swizzle (64 B rows for
 // BK = 16, 128 B rows for BK = 32), which is the layout the MMA's smem
 // descriptors describe.  B stored K x N (N contiguous) is split by a pass
-// that writes B_hi/B_lo transposed (N x K, K contiguous); B stored N x K is
-// read as it is and split on chip like A (BR).
+// that writes B_hi/B_lo transposed (N x K, K contiguous), or is read as it
+// is and transposed and split on chip (BR = 2); B stored N x K is read as it
+// is and split on chip like A (BR = 1).
 //
 // Every mbarrier wait is bounded by a %globaltimer deadline; on expiry the
 // kernel records GEMM_ERR_DEVICE_TIMEOUT in a device status word, stops
@@ -72,17 +73,22 @@ __device__ int g_tc_status;  // 0 = ok, else a GEMM_ERR_* code
 // tensor-memory ring that the A_lo*B_hi MMA reads directly; otherwise A_hi
 // and A_lo come pre-split from the workspace.  CONCAT: B_hi and B_lo sit
 // next to each other in the stage, so A_hi*[B_hi | B_lo] is one MMA of width
-// 2*BN into two accumulators that the epilogue adds.  BR: B is stored N x K
-// (K contiguous, as the MMA reads it) and arrives raw (FP32) too: the landed
-// tile is B_hi to the MMA as it is, and the converter warps write B_lo next
-// to it (1xTF32: round B in place), so no pass splits B before the kernel.
-template <int BM, int BN, int BK, int STAGES, int AK, bool CONCAT, int NPROD, bool BR>
+// 2*BN into two accumulators that the epilogue adds.  BR: B arrives raw
+// (FP32) too, so no pass splits B before the kernel.  BR = 1: B is stored
+// N x K (K contiguous, as the MMA reads it); the landed tile is B_hi to the
+// MMA as it is, and the converter warps write B_lo next to it (1xTF32:
+// round B in place).  BR = 2: B is stored K x N; its BK x BN tile lands
+// unswizzled in the B_hi buffer, the converter warps read it into
+// registers, and after a barrier among themselves write it back K-major
+// (B_hi, the raw values) with B_lo beside it.
+template <int BM, int BN, int BK, int STAGES, int AK, bool CONCAT, int NPROD, int BR>
 struct TcCfg {
   static_assert(NPROD == 3 || NPROD == 1, "3xTF32 or 1xTF32");
   static_assert(NPROD == 3 || !CONCAT, "1xTF32 has no B_lo to concatenate");
   static_assert(BM == 128 || (BM == 256 && AK != 2 && (AK || !CONCAT)),
                 "a 256-row tile keeps A_hi in shared memory; concatenated B only with A split on chip");
   static_assert(AK >= 0 && AK <= 2 && (AK != 2 || NPROD == 3), "A_hi in TMEM is a 3xTF32 form");
+  static_assert(BR >= 0 && BR <= 2 && (BR != 2 || NPROD == 3), "B transposed on chip is 3xTF32");
   static constexpr bool X3 = NPROD == 3;
   static constexpr int MH = BM / 128;  // 128-row halves, one accumulator each
   static constexpr int A_BYTES = BM * BK * 4;
@@ -203,11 +209,11 @@ __device__ __forceinline__ void epi_store16(float4 *st, const float *v, float *d
   __syncwarp();  // the buffer is rewritten by the next block
 }
 
-template <int BM, int BN, int BK, int STAGES, int AK, bool CONCAT, int NPROD, bool BR>
+template <int BM, int BN, int BK, int STAGES, int AK, bool CONCAT, int NPROD, int BR>
 __global__ void __launch_bounds__(kThreadsTC, 1)
 tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
                  const __grid_constant__ CUtensorMap tmA_lo,
-                 const __grid_constant__ CUtensorMap tmB_hi,  // B fp32 (N x K) when BR
+                 const __grid_constant__ CUtensorMap tmB_hi,  // B fp32 as stored when BR
                  const __grid_constant__ CUtensorMap tmB_lo, TcParams p) {
   using Cfg = TcCfg<BM, BN, BK, STAGES, AK, CONCAT, NPROD, BR>;
   constexpr bool X3 = Cfg::X3;
@@ -220,7 +226,8 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
   uint64_t *acc_full = empty + STAGES;
   uint64_t *acc_empty = acc_full + 1;
   uint64_t *drain = acc_empty + 1;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  uint64_t *b_read = drain + 1;  // BR = 2: every converter thread has read the raw B tile
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(b_read + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   auto a_hi = [&](int s) { return smem + s * Cfg::STAGE_BYTES; };
@@ -242,6 +249,7 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, kConvThreads);
     mbar_init(drain, 1);
+    mbar_init(b_read, kConvThreads);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -295,7 +303,10 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
           const int32_t kx = kb * BK;
           tma_load_2d(a_hi(s), &tmA_hi, &full[s], kx, m0);
           if (!AK && X3) tma_load_2d(a_lo(s), &tmA_lo, &full[s], kx, m0);
-          tma_load_2d(b_hi(s), &tmB_hi, &full[s], kx, n0);
+          if (BR == 2)
+            tma_load_2d(b_hi(s), &tmB_hi, &full[s], n0, kx);  // BK rows of BN values
+          else
+            tma_load_2d(b_hi(s), &tmB_hi, &full[s], kx, n0);
           if (X3 && !BR) tma_load_2d(b_lo(s), &tmB_lo, &full[s], kx, n0);
           ++issued;
         }
@@ -447,6 +458,27 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
             ok = false;
             break;
           }
+          // BR = 2: the B tile landed as BK = 32 rows of BN = 64 values (row k
+          // at k * 256 bytes).  Each converter thread takes one block of 4 k
+          // x 4 n (n = 4 bjb.., k = 4 bc..) with four 128-bit loads, then
+          // signals b_read and splits its rows of A while the others read.
+          // A quarter warp (lanes l = ct & 7) reads 8 distinct 16-byte
+          // columns bjb & 7 = l: no bank conflicts.
+          float4 bv[4];
+          int bjb = 0, bc = 0;
+          if constexpr (BR == 2) {
+            static_assert(BN == 64 && BK == 32 && kConvThreads == 128,
+                          "one 4 x 4 block per converter thread");
+            const int ct = (int)threadIdx.x - 64;
+            const int l = ct & 7, g = ct >> 3;
+            bjb = l + 8 * (g & 1);
+            bc = ((g >> 1) + (l >> 1)) & 7;
+            const float *raw = reinterpret_cast<const float *>(b_hi(s));
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              bv[i] = *reinterpret_cast<const float4 *>(raw + (4 * bc + i) * BN + 4 * bjb);
+            mbar_arrive(b_read);
+          }
           // Row `row` of each 128-row half of the landed tile: 16-byte
           // chunk c sits at chunk c ^ f(row) of its 64- or 128-byte line (the
           // TMA swizzle; f depends on the row's low bits only).
@@ -501,7 +533,7 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
             tmem_st_wait();
           }
           }  // halves
-          if constexpr (BR) {
+          if constexpr (BR == 1) {
             // B_lo = B - tf32_trunc(B), stored at B's own offsets in the B_lo
             // buffer (the split is elementwise and the swizzle only permutes
             // 16-byte chunks inside each line); 1xTF32 rounds B in place.
@@ -529,6 +561,37 @@ tc_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA_hi,  // A fp32 when AK
                 y.w = tf32_rna(x[i].w);
               }
               dst[ct + i * kConvThreads] = y;
+            }
+            fence_async_smem();  // the MMA (async proxy) reads what was written
+          }
+          if constexpr (BR == 2) {
+            // Write back what was read before the A split: once every
+            // converter thread has read its block (b_read), B_hi (the raw
+            // values) and B_lo go to row n, 16-byte chunk c at its swizzled
+            // place (c ^ (n & 7)), as the TMA would have put them.  For a
+            // fixed r, a quarter warp's n & 7 = 4 (l & 1) + r and its c run
+            // so that c ^ (n & 7) takes 8 distinct values: no bank conflicts.
+            if (!__all_sync(0xffffffffu,
+                            mbar_wait(b_read, (uint32_t)it & 1u, deadline, abort_flag))) {
+              *abort_flag = 1;
+              ok = false;
+              break;
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+              const int n = 4 * bjb + r;
+              const float4 hi = r == 0   ? make_float4(bv[0].x, bv[1].x, bv[2].x, bv[3].x)
+                                : r == 1 ? make_float4(bv[0].y, bv[1].y, bv[2].y, bv[3].y)
+                                : r == 2 ? make_float4(bv[0].z, bv[1].z, bv[2].z, bv[3].z)
+                                         : make_float4(bv[0].w, bv[1].w, bv[2].w, bv[3].w);
+              float4 lo;
+              lo.x = hi.x - tf32_trunc(hi.x);
+              lo.y = hi.y - tf32_trunc(hi.y);
+              lo.z = hi.z - tf32_trunc(hi.z);
+              lo.w = hi.w - tf32_trunc(hi.w);
+              const int off = n * Cfg::ROW_BYTES + ((bc ^ (n & 7)) * 16);
+              *reinterpret_cast<float4 *>(b_hi(s) + off) = hi;
+              *reinterpret_cast<float4 *>(b_lo(s) + off) = lo;
             }
             fence_async_smem();  // the MMA (async proxy) reads what was written
           }
@@ -676,15 +739,16 @@ bool get_encoder() {
 
 // 2-D FP32 tensor map: inner dimension `inner` (contiguous), `outer` rows
 // `stride_elems` apart; box = box_inner x box_rows with the swizzle that
-// matches box_inner * 4 bytes.
+// matches box_inner * 4 bytes (or none).
 bool encode_2d(CUtensorMap *m, const float *base, int64_t inner, int64_t outer,
-               int64_t stride_elems, int box_inner, int box_rows) {
+               int64_t stride_elems, int box_inner, int box_rows, bool swizzle = true) {
   cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
   cuuint64_t strides[1] = {(cuuint64_t)(stride_elems * 4)};
   cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
-  const CUtensorMapSwizzle sw =
-      box_inner * 4 == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  const CUtensorMapSwizzle sw = !swizzle               ? CU_TENSOR_MAP_SWIZZLE_NONE
+                                : box_inner * 4 == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                                       : CU_TENSOR_MAP_SWIZZLE_64B;
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -732,7 +796,7 @@ WsLayout ws_layout(int64_t M, int64_t N, int64_t K, bool a_inkernel, bool b_inke
   return w;
 }
 
-template <int BM, int BN, int BK, int STAGES, int AK, bool CONCAT, int NPROD, bool BR>
+template <int BM, int BN, int BK, int STAGES, int AK, bool CONCAT, int NPROD, int BR>
 int launch_cfg(const gemm_plan_t &plan, const GemmArgs &a, char *ws, cudaStream_t s) {
   using Cfg = TcCfg<BM, BN, BK, STAGES, AK, CONCAT, NPROD, BR>;
   constexpr bool X3 = Cfg::X3;
@@ -765,9 +829,11 @@ int launch_cfg(const gemm_plan_t &plan, const GemmArgs &a, char *ws, cudaStream_
     if (X3) ok = ok && encode_2d(&tA1, alo, L.kp, a.M, L.kp, BK, BM);
   }
   if (BR) {
-    // raw B, stored N x K: BK x BN boxes like A's
-    if (!a.tb) return GEMM_ERR_UNSUPPORTED;
-    ok = ok && encode_2d(&tB0, a.B, a.K, a.N, a.ldb, BK, BN);
+    // raw B: stored N x K, BK x BN boxes like A's; stored K x N, BN x BK
+    // boxes without swizzle (transposed on chip)
+    if (a.tb != (BR == 1)) return GEMM_ERR_UNSUPPORTED;
+    ok = ok && (BR == 1 ? encode_2d(&tB0, a.B, a.K, a.N, a.ldb, BK, BN)
+                        : encode_2d(&tB0, a.B, a.N, a.K, a.ldb, BN, BK, /*swizzle=*/false));
     tB1 = tB0;
   } else {
     ok = ok && encode_2d(&tB0, bhi, L.kp, a.N, L.kp, BK, BN);
@@ -908,6 +974,15 @@ int launch_cfg(const gemm_plan_t &plan, const GemmArgs &a, char *ws, cudaStream_
   return GEMM_OK;
 }
 
+// B stored K x N split on chip: built for the 64-column, 32-deep tiles only
+// (wider tiles lose more to the on-chip transpose than the pass costs).
+template <int BM, int BN, int BK, int STAGES, int AK, bool CONCAT, int NPROD, bool BRS>
+int launch_kn(const gemm_plan_t &plan, const GemmArgs &a, char *ws, cudaStream_t s) {
+  if constexpr (BRS && BN == 64 && BK == 32 && NPROD == 3)
+    return launch_cfg<BM, BN, BK, STAGES, AK, CONCAT, NPROD, 2>(plan, a, ws, s);
+  return GEMM_ERR_UNSUPPORTED;
+}
+
 }  // namespace
 
 // The tcgen05 kernels are built for sm_103a only.
@@ -956,17 +1031,18 @@ bool tc_config_valid(int bm, int bn, int bk, int stages, int a_inkernel, int con
   return false;
 }
 
-// Every configuration needs more than 113 registers a thread (134-166), so
-// at most two CTAs of 192 threads share an SM's 65536 registers.
+// Every configuration needs more than 113 registers a thread (134-176), so
+// at most two CTAs of 192 threads share an SM's 65536 registers (those above
+// 170 run one CTA per SM by shared memory anyway).
 constexpr int kMaxCtasPerSm = 2;
 
 // CTAs of one configuration that fit on an SM (shared memory, TMEM and
 // registers).
 int tc_ctas_per_sm(int bm, int bn, int bk, int stages, int a_inkernel, int concat, int nprod,
                    int b_inkernel, int smem_per_sm) {
-#define GG_OCC(BM_, BN_, BK_, ST_, AK_, CC_, NP_, BR_)         \
-  if (GG_TC_MATCH(BM_, BN_, BK_, ST_, AK_, CC_, NP_, BR_)) {    \
-    using C = TcCfg<BM_, BN_, BK_, ST_, AK_, CC_, NP_, BR_>;    \
+#define GG_OCC(BM_, BN_, BK_, ST_, AK_, CC_, NP_, BR_)            \
+  if (GG_TC_MATCH(BM_, BN_, BK_, ST_, AK_, CC_, NP_, BR_)) {       \
+    using C = TcCfg<BM_, BN_, BK_, ST_, AK_, CC_, NP_, BR_ ? 1 : 0>; \
     int by_smem = smem_per_sm / (C::SMEM_BYTES + 1024);         \
     int by_tmem = 512 / C::TMEM_COLS;                           \
     int n = by_smem < by_tmem ? by_smem : by_tmem;              \
@@ -1003,12 +1079,11 @@ int launch_tc(const gemm_plan_t &plan, const GemmArgs &a, void *ws, size_t ws_by
   const uint64_t need = tc_workspace_bytes(plan, a.M, a.N, a.K);
   if (ws_bytes < need || (need > 0 && ws == nullptr)) return GEMM_ERR_WORKSPACE_TOO_SMALL;
   // the in-kernel A split reads A by TMA as M x K rows, the in-kernel B
-  // split B as N x K rows
+  // split B as stored (N x K or K x N rows)
   if (plan.a_split_in_kernel &&
       (a.ta || (a.lda & 3) || (reinterpret_cast<uintptr_t>(a.A) & 15)))
     return GEMM_ERR_UNSUPPORTED;
-  if (plan.b_split_in_kernel &&
-      (!a.tb || (a.ldb & 3) || (reinterpret_cast<uintptr_t>(a.B) & 15)))
+  if (plan.b_split_in_kernel && ((a.ldb & 3) || (reinterpret_cast<uintptr_t>(a.B) & 15)))
     return GEMM_ERR_UNSUPPORTED;
   char *w = static_cast<char *>(ws);
   const int nprod = plan.mode == GEMM_MODE_TF32 ? 1 : 3;
@@ -1016,9 +1091,12 @@ int launch_tc(const gemm_plan_t &plan, const GemmArgs &a, void *ws, size_t ws_by
   const int a_inkernel = plan.a_split_in_kernel ? (plan.a_hi_tmem ? 2 : 1) : 0;
   const int concat = plan.b_concat;
   const int b_inkernel = plan.b_split_in_kernel;
-#define GG_LAUNCH(BM_, BN_, BK_, ST_, AK_, CC_, NP_, BR_)  \
-  if (GG_TC_MATCH(BM_, BN_, BK_, ST_, AK_, CC_, NP_, BR_)) \
-    return launch_cfg<BM_, BN_, BK_, ST_, AK_, CC_, NP_, BR_>(plan, a, w, s);
+#define GG_LAUNCH(BM_, BN_, BK_, ST_, AK_, CC_, NP_, BR_)                                 \
+  if (GG_TC_MATCH(BM_, BN_, BK_, ST_, AK_, CC_, NP_, BR_)) {                              \
+    if (!BR_) return launch_cfg<BM_, BN_, BK_, ST_, AK_, CC_, NP_, 0>(plan, a, w, s);     \
+    if (a.tb) return launch_cfg<BM_, BN_, BK_, ST_, AK_, CC_, NP_, (BR_ ? 1 : 0)>(plan, a, w, s); \
+    return launch_kn<BM_, BN_, BK_, ST_, AK_, CC_, NP_, BR_>(plan, a, w, s);             \
+  }
   GG_TC_CONFIGS(GG_LAUNCH)
 #undef GG_LAUNCH
   return GEMM_ERR_UNSUPPORTED;

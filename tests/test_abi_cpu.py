@@ -281,31 +281,32 @@ def test_wide_tiles_from_half_a_wave(lib):
 
 # Planner decisions checked against exhaustive GB300 sweeps (every built
 # configuration with and without stream-K; CUDA-core split counts forced one
-# by one): (bm, bn, bk, stages, A split on chip, stream-K, split-K).
+# by one): (bm, bn, bk, stages, A split on chip, stream-K, split-K, B split
+# on chip).
 MEASURED_CHOICES = [
-    ((4096, 4096, 4096), "tf32x3", (128, 256, 16, 5, 1, 1, 1)),   # 460 vs 513 us without stream-K
-    ((8192, 8192, 8192), "tf32x3", (128, 256, 16, 5, 1, 0, 1)),
-    ((1024, 1024, 16384), "tf32x3", (128, 256, 16, 5, 1, 1, 1)),  # 154 vs 208 us for 128 x 128
-    ((1024, 4096, 4096), "tf32x3", (128, 256, 16, 5, 1, 0, 1)),   # 143 vs 169 us stream-K
-    ((2560, 2560, 1024), "tf32x3", (128, 256, 16, 5, 1, 1, 1)),   # 66 vs 73 us
-    ((1536, 1536, 1536), "tf32x3", (128, 128, 32, 4, 1, 0, 1)),
-    ((8192, 384, 8192), "tf32x3", (128, 128, 32, 4, 1, 1, 1)),    # 184 vs 206 us for 128 x 256
-    ((1023, 1025, 777, 777, 1025, 1025), "tf32x3", (128, 64, 32, 4, 0, 0, 1)),  # 35.0 vs 37.6 us
-    ((512, 512, 512), "tf32x3", (128, 64, 32, 4, 0, 0, 1)),       # 13.7 vs 15.4 us stream-K
-    ((1024, 1024, 1024), "tf32x3", (128, 64, 32, 4, 0, 0, 1)),    # 23.7 vs 26.4 us
-    ((1000, 1000, 1001, 1001, 1000, 1000), "tf32x3", (128, 64, 32, 4, 0, 0, 1)),  # 30.5 vs 37.0 us
-    ((1200, 640, 333, 333, 640, 640), "tf32x3", (128, 64, 32, 4, 0, 0, 1)),  # 16.9 vs 20.9 us
-    ((1200, 640, 336), "tf32x3", (128, 64, 32, 6, 1, 0, 1)),      # 13.5 vs 15.3 us pre-split
-    ((768, 768, 768), "tf32x3", (128, 64, 32, 6, 1, 0, 1)),       # 19.0 vs 20.4 us pre-split
-    ((1024, 64, 8192), "tf32x3", (128, 64, 32, 6, 1, 1, 1)),      # 29.7 vs 38.2 us
-    ((65536, 64, 4096), "tf32x3", (128, 64, 32, 3, 1, 1, 1)),     # 204 vs 271 us for 6 stages
-    ((4096, 4096, 4096), "tf32", (256, 256, 16, 6, 0, 0, 1)),     # 212 vs 217 us for BK 32
-    ((8192, 8192, 8192), "tf32", (256, 256, 32, 3, 0, 1, 1)),     # 1337 vs 1468 us for BK 16
-    ((2048, 2048, 2048), "tf32", (128, 256, 16, 8, 0, 0, 1)),     # 48.6 vs 60.1 us for 256 x 256
-    ((1024, 1024, 1024), "tf32", (128, 256, 16, 8, 0, 0, 1)),     # 25.6 vs 27.1 us stream-K
-    ((32, 32, 65536), "fp32_simt", (64, 128, 16, 4, 0, 0, 142)),  # ~39 us vs 238 us at 16 slices
-    ((128, 128, 16384), "fp32_simt", (64, 128, 16, 4, 0, 0, 69)),
-    ((512, 512, 512), "fp32_simt", (64, 128, 16, 4, 0, 0, 8)),
+    ((4096, 4096, 4096), "tf32x3", (128, 256, 16, 5, 1, 1, 1, 0)),   # 460 vs 513 us without stream-K
+    ((8192, 8192, 8192), "tf32x3", (128, 256, 16, 5, 1, 0, 1, 0)),
+    ((1024, 1024, 16384), "tf32x3", (128, 256, 16, 5, 1, 1, 1, 0)),  # 154 vs 208 us for 128 x 128
+    ((1024, 4096, 4096), "tf32x3", (128, 256, 16, 5, 1, 0, 1, 0)),   # 143 vs 169 us stream-K
+    ((2560, 2560, 1024), "tf32x3", (128, 256, 16, 5, 1, 1, 1, 0)),   # 66 vs 73 us
+    ((1536, 1536, 1536), "tf32x3", (128, 128, 32, 4, 1, 0, 1, 0)),
+    ((8192, 384, 8192), "tf32x3", (128, 128, 32, 4, 1, 1, 1, 0)),    # 184 vs 206 us for 128 x 256
+    ((1023, 1025, 777, 777, 1025, 1025), "tf32x3", (128, 64, 32, 4, 0, 0, 1, 0)),  # 35.0 vs 37.6 us
+    ((512, 512, 512), "tf32x3", (128, 64, 32, 6, 1, 0, 1, 1)),    # 13.1 vs 14.0 us pre-split
+    ((1024, 1024, 1024), "tf32x3", (128, 64, 32, 6, 1, 0, 1, 1)), # 21.0 vs 23.9 us pre-split
+    ((1000, 1000, 1001, 1001, 1000, 1000), "tf32x3", (128, 64, 32, 4, 0, 0, 1, 0)),  # 30.5 vs 37.0 us
+    ((1200, 640, 333, 333, 640, 640), "tf32x3", (128, 64, 32, 4, 0, 0, 1, 0)),  # 16.9 vs 20.9 us
+    ((1200, 640, 336), "tf32x3", (128, 64, 32, 6, 1, 0, 1, 1)),   # 11.0 vs 13.3 us B pre-split
+    ((768, 768, 768), "tf32x3", (128, 64, 32, 6, 1, 0, 1, 1)),    # 16.9 vs 18.9 us B pre-split
+    ((1024, 64, 8192), "tf32x3", (128, 64, 32, 6, 1, 1, 1, 0)),      # 29.7 vs 38.2 us
+    ((65536, 64, 4096), "tf32x3", (128, 64, 32, 3, 1, 1, 1, 0)),     # 204 vs 271 us for 6 stages
+    ((4096, 4096, 4096), "tf32", (256, 256, 16, 6, 0, 0, 1, 0)),     # 212 vs 217 us for BK 32
+    ((8192, 8192, 8192), "tf32", (256, 256, 32, 3, 0, 1, 1, 0)),     # 1337 vs 1468 us for BK 16
+    ((2048, 2048, 2048), "tf32", (128, 256, 16, 8, 0, 0, 1, 0)),     # 48.6 vs 60.1 us for 256 x 256
+    ((1024, 1024, 1024), "tf32", (128, 256, 16, 8, 0, 0, 1, 0)),     # 25.6 vs 27.1 us stream-K
+    ((32, 32, 65536), "fp32_simt", (64, 128, 16, 4, 0, 0, 142, 0)),  # ~39 us vs 238 us at 16 slices
+    ((128, 128, 16384), "fp32_simt", (64, 128, 16, 4, 0, 0, 69, 0)),
+    ((512, 512, 512), "fp32_simt", (64, 128, 16, 4, 0, 0, 8, 0)),
 ]
 
 
@@ -314,6 +315,6 @@ MEASURED_CHOICES = [
 def test_measured_planner_choices(lib, shape, mode, want):
     p = gemm.plan(*shape, mode=mode)
     got = (p["bm"], p["bn"], p["bk"], p["stages"], p["a_split_in_kernel"], p["stream_k"],
-           p["split_k"])
+           p["split_k"], p["b_split_in_kernel"])
     assert got == want
 

@@ -221,18 +221,19 @@ def test_status_clear_after_normal_runs():
 # The planner's own choice for representative shapes:
 # (M, N, K, lda) -> (bn, bk, stages, A split in kernel, concatenated B)
 TC_PLANS = [
-    ((1000, 64, 96, 96), (128, 64, 32, 6, 1, 1)),       # narrow, few tiles: 6 stages, 1 CTA/SM
-    ((9000, 64, 96, 96), (128, 64, 32, 3, 1, 1)),       # narrow, more tiles: 3 stages, 2 CTAs/SM
-    ((512, 512, 512, 512), (128, 64, 32, 4, 0, 1)),     # small product: a CTA per 128 x 64 tile
-    ((512, 512, 1024, 1024), (128, 128, 32, 4, 1, 1)),   # few tiles, longer K: stream-K
-    ((2432, 8192, 128, 128), (128, 256, 16, 5, 1, 0)),
-    ((1023, 1025, 777, 777), (128, 64, 32, 4, 0, 1)),    # small product, A pre-split
-    ((1200, 640, 336, 336), (128, 64, 32, 6, 1, 1)),    # shallow small product: A split on chip
-    ((600, 600, 3000, 3001), (128, 128, 16, 6, 0, 1)),   # A pre-split, under half a wave: 6 stages
-    ((5000, 250, 777, 777), (128, 128, 16, 3, 0, 1)),    # A pre-split, more tiles: 3 stages, 2 CTAs/SM
-    ((2432, 8192, 129, 129), (128, 256, 16, 4, 0, 0)),
-    ((5120, 8192, 64, 64), (128, 256, 16, 5, 1, 0)),   # many tiles, aligned A: split on chip
-    ((5120, 8192, 65, 65), (256, 256, 16, 3, 0, 0)),   # many tiles, A pre-split: 256 x 256
+    ((1000, 64, 96, 96), (128, 64, 32, 6, 1, 1, 0)),       # narrow, few tiles: 6 stages, 1 CTA/SM
+    ((9000, 64, 96, 96), (128, 64, 32, 3, 1, 1, 0)),       # narrow, more tiles: 3 stages, 2 CTAs/SM
+    ((512, 512, 512, 512), (128, 64, 32, 6, 1, 1, 1)),     # small product: a CTA per 128 x 64 tile,
+                                                           # A and B split on chip, one launch
+    ((512, 512, 1024, 1024), (128, 128, 32, 4, 1, 1, 0)),   # few tiles, longer K: stream-K
+    ((2432, 8192, 128, 128), (128, 256, 16, 5, 1, 0, 0)),
+    ((1023, 1025, 777, 777), (128, 64, 32, 4, 0, 1, 0)),    # small product, A and B pre-split
+    ((1200, 640, 336, 336), (128, 64, 32, 6, 1, 1, 1)),    # shallow small product: one launch
+    ((600, 600, 3000, 3001), (128, 128, 16, 6, 0, 1, 0)),   # A pre-split, under half a wave: 6 stages
+    ((5000, 250, 777, 777), (128, 128, 16, 3, 0, 1, 0)),    # A pre-split, more tiles: 3 stages, 2 CTAs/SM
+    ((2432, 8192, 129, 129), (128, 256, 16, 4, 0, 0, 0)),
+    ((5120, 8192, 64, 64), (128, 256, 16, 5, 1, 0, 0)),   # many tiles, aligned A: split on chip
+    ((5120, 8192, 65, 65), (256, 256, 16, 3, 0, 0, 0)),   # many tiles, A pre-split: 256 x 256
 ]
 
 
@@ -243,7 +244,8 @@ def test_tf32x3_planner_choices(shape, cfg):
     from workloads import sample_entries
     M, N, K, lda = shape
     p = gemm.plan(M, N, K, lda, N, N, mode="tf32x3")
-    assert (p["bm"], p["bn"], p["bk"], p["stages"], p["a_split_in_kernel"], p["b_concat"]) == cfg
+    assert (p["bm"], p["bn"], p["bk"], p["stages"], p["a_split_in_kernel"], p["b_concat"],
+            p["b_split_in_kernel"]) == cfg
     assert p["ctas_per_sm"] >= 1
     A = matrix(M, K, lda, 4000 + K, "u11")
     B = matrix(K, N, None, 4100 + K, "u11")
@@ -754,3 +756,43 @@ def test_narrow_b_tiles(cfg, streamk, M, N, monkeypatch):
     assert oracle.mismatches(got, ref) == 0
     got, ref, D = _run_shape(M, N, K, "tf32x3", 0.5, 2.0, seed=M - N)
     assert oracle.err_normalised(got, ref, D) <= TOL_E1
+
+
+# Small-product tiles with B stored K x N read as stored, transposed and
+# split on chip (B_hi the raw values, B_lo beside them; no pass for B),
+# forced through the knob's b_split field: against the oracle, exactly on
+# integer inputs, and bit for bit against the same tiles with B split by the
+# pass (both take B_hi = tf32_trunc(B) and issue the same MMAs).
+TC_BSPLIT_KN = ["128,64,32,6,1,1", "128,64,32,4,0,1"]
+
+
+@pytest.mark.parametrize("cfg", TC_BSPLIT_KN)
+@pytest.mark.parametrize("shape", [(333, 272, 164), (129, 64, 777), (1, 300, 68), (300, 8, 1000),
+                                   (777, 200, 300)])
+def test_tc_b_transposed_on_chip(cfg, shape, monkeypatch):
+    from roofline_gb300 import gemm
+    M, N, K = shape
+    ak = int(cfg.split(",")[4])
+    pad = ((-K) % 4, (-N) % 4, (-N) % 4)  # every row on a 16-byte boundary
+    monkeypatch.setenv("GEMM_TC_CONFIG", cfg + ",1")
+    p = gemm.plan(M, N, K, K + pad[0], N + pad[1], N + pad[2], mode="tf32x3")
+    assert (p["bn"], p["bk"], p["a_split_in_kernel"], p["b_split_in_kernel"]) == (64, 32, ak, 1)
+    assert p["launches"] == (1 if ak else 2) + p["stream_k"]
+    got, ref, D = _run_shape(M, N, K, "tf32x3", 1.5, 0.5, pad=pad, seed=K)
+    assert oracle.err_normalised(got, ref, D) <= TOL_E1
+    monkeypatch.setenv("GEMM_TC_CONFIG", cfg + ",0")
+    got0, _, _ = _run_shape(M, N, K, "tf32x3", 1.5, 0.5, pad=pad, seed=K)
+    assert np.array_equal(np.ascontiguousarray(got).view(np.uint32),
+                          np.ascontiguousarray(got0).view(np.uint32))
+    monkeypatch.setenv("GEMM_TC_CONFIG", cfg + ",1")
+    got, ref, D = _run_shape(M, N, K, "tf32x3", 1.0, 0.0, pad=pad, seed=K, dist="int2")
+    assert oracle.mismatches(got, ref) == 0
+
+
+def test_tc_b_split_knob_refuses_unbuilt_forms(monkeypatch):
+    # B stored K x N is transposed on chip only in 64 x 32 tiles: asking for
+    # it with 128 x 256 tiles leaves the planner's choice in place
+    from roofline_gb300 import gemm
+    monkeypatch.setenv("GEMM_TC_CONFIG", "128,256,16,5,2,0,1")
+    p = gemm.plan(2048, 2048, 2048, mode="tf32x3")
+    assert not (p["bn"] == 256 and p["b_split_in_kernel"] == 1)

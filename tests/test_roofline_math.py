@@ -102,7 +102,9 @@ def test_kernel_instance_names_the_configuration():
     plan.update(kernel_name="tc_tf32", a_hi_tmem=0)
     assert bench.kernel_instance(plan).startswith("tc_tf32x3_kernel<128,256,16,5,1,0,1,0>")
     plan.update(kernel_name="tc_tf32x3", b_split_in_kernel=1, stream_k=0)
-    assert bench.kernel_instance(plan).startswith("tc_tf32x3_kernel<128,256,16,5,1,0,3,1>")
+    assert bench.kernel_instance(plan).startswith("tc_tf32x3_kernel<128,256,16,5,1,0,3,2>")
+    assert bench.kernel_instance(plan, b_stored_nk=True).startswith(
+        "tc_tf32x3_kernel<128,256,16,5,1,0,3,1>")
     plan.update(kernel_name="simt", bm=64, bn=128, bk=16, stages=4, grid_ctas=2048, stream_k=0)
     assert bench.kernel_instance(plan) == \
         "simt_packed_kernel<64,128,16,4,1,0,0> grid=2048 split_k=1 stream_k=0"
