@@ -243,7 +243,8 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
       // A stored M x K and aligned for TMA (16-byte base, lda a multiple of
       // 4): the GEMM kernel reads FP32 A once and splits it on chip;
       // otherwise a pre-pass writes A_hi/A_lo (K-major) to the workspace.
-      // B is always pre-split to K-major.
+      // B goes through the same pre-pass (transposed to K-major when stored
+      // K x N) unless it is split on chip (b_tma below).
       const bool a_aligned = !ta && (lda % 4 == 0) && ((align_hint & 15) == 0);
       const int64_t sms = dp.sm_count > 0 ? dp.sm_count : 152;
       const int64_t tiles256 = ceil_div(M, 128) * ceil_div(N, 256);
@@ -340,9 +341,10 @@ int make_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t
       // 13.5 us, 768^3 20.4 -> 19.0 us; 512^3, 32 tiles, 14.1 against 14.6
       // and 1024^3, K = 1024, 24.0 against 25.4 keep both pre-split).
       // With B split on chip as well (see b_tma below), an aligned A always
-      // goes on chip too: the call is then one launch (GB300, B stored N x
-      // K, pre-split A / A on chip: 512^3 14.0 / 12.3 us, 640^3 16.0 / 14.2,
-      // 1024^3 22.4 / 19.8).
+      // goes on chip too: the call is then one launch (GB300, step with the
+      // pass(es) / one launch: B stored N x K 512^3 14.0 / 12.3 us, 640^3
+      // 16.0 / 14.2, 1024^3 22.4 / 19.8; B stored K x N, transposed on chip,
+      // 512^3 14.0 / 13.0, 768^3 19.2 / 16.9, 1024^3 23.9 / 20.8).
       const bool b_tma = (ldb % 4 == 0) && ((align_hint & 15) == 0);
       bool b_chip = tb || x3;
       if (const char *bs = std::getenv("GEMM_TC_BSPLIT")) b_chip = std::atoi(bs) != 0;  // tuning knob
