@@ -45,7 +45,9 @@
 extern "C" {
 #endif
 
-#define GEMM_ABI_VERSION 1
+/* 2: gemm_plan_t gained b_split_in_kernel (callers built against version 1
+ * pass a smaller struct to gemm_f32_plan / gemm_f32_op_plan). */
+#define GEMM_ABI_VERSION 2
 
 /* ---- status codes ---------------------------------------------------- */
 #define GEMM_OK 0

@@ -29,6 +29,7 @@ MODES = {"auto": MODE_AUTO, "fp32_simt": MODE_FP32_SIMT, "tf32x3": MODE_TF32X3, 
          "tiled32": MODE_TILED32}
 
 # storage order and operand ops of gemm_f32_op
+ABI_VERSION = 2  # GEMM_ABI_VERSION of include/gb300_gemm.h
 ROW_MAJOR = 0
 COL_MAJOR = 1
 OP_N = 0
@@ -169,6 +170,10 @@ def load(path: str | None = None):
         lib.fp32_fma_peak.restype = i32
         lib.fp32_fma_peak_sink_floats.argtypes = []
         lib.fp32_fma_peak_sink_floats.restype = i64
+        # the structures above mirror this version of the header
+        if lib.gemm_abi_version() != ABI_VERSION:
+            raise RuntimeError(f"{p} reports ABI version {lib.gemm_abi_version()}, this binding "
+                               f"is written for {ABI_VERSION}: rebuild the library")
         if path is None:
             _lib = lib
         return lib

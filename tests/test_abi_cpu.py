@@ -35,7 +35,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_strerror(lib):
-    assert gemm.abi_version() == 1
+    assert gemm.abi_version() == gemm.ABI_VERSION == 2
     for code in [0, -1, -2, -3, -4, -5, -6, 12345]:
         assert isinstance(gemm.strerror(code), str) and gemm.strerror(code)
     assert "invalid" in gemm.strerror(gemm.ERR_INVALID_ARG)

@@ -35,6 +35,8 @@ int main(void) {
   if (rc != GEMM_ERR_INVALID_ARG) return 15;
   printf("noalloc %llu %d\n", (unsigned long long)GEMM_NOALLOC_SCRATCH_BYTES,
          (int)GEMM_NOALLOC_MAX_SPLIT);
+  printf("abi %d sizeof_plan %d sizeof_info %d\n", (int)GEMM_ABI_VERSION,
+         (int)sizeof(gemm_plan_t), (int)sizeof(gemm_device_info_t));
   puts("ok");
   return 0;
 }
@@ -73,3 +75,10 @@ def test_header_and_library_from_c(tmp_path):
     from roofline_gb300 import gemm
     line = [l for l in r.stdout.splitlines() if l.startswith("noalloc ")][0]
     assert line.split()[1:] == [str(gemm.NOALLOC_SCRATCH_BYTES), str(gemm.NOALLOC_MAX_SPLIT)]
+    # ... and of its structures: the ABI version and the C sizes of the plan
+    # and device-info structs match the ctypes mirrors
+    import ctypes
+    line = [l for l in r.stdout.splitlines() if l.startswith("abi ")][0].split()
+    assert int(line[1]) == gemm.ABI_VERSION
+    assert int(line[3]) == ctypes.sizeof(gemm.GemmPlan)
+    assert int(line[5]) == ctypes.sizeof(gemm.DeviceInfo)
