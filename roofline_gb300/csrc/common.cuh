@@ -30,6 +30,11 @@ struct GemmArgs {
   // everything before it in the stream), for callers that chain the GEMM
   // behind cross-stream event waits.
   int b_presplit = 0, plain_order = 0;
+  // b_planes_written (host memory, or nullptr): set to 1 when this call's
+  // launches write the B_hi / B_lo planes into the workspace (a call that
+  // splits B on chip writes none), so a caller knows when a later call may
+  // take b_presplit = 1.
+  int *b_planes_written = nullptr;
   // Streaming (tensor-core path with A split on chip, one CTA per tile):
   // A's rows, and C's when beta != 0, are still arriving in row blocks of
   // stream_rows rows (a multiple of the tile height) while the GEMM runs.

@@ -429,7 +429,10 @@ extern "C" int gemm_f32_host(int64_t M, int64_t N, int64_t K, float alpha, const
   char *ws0 = base + a_bytes + b_bytes + c_bytes;  // column block j: ws0 + j * ws_bytes
 
   cudaError_t e = cudaSuccess;
-  bool split_done[kMaxColBlocks] = {};
+  // per column block: its B planes are in that block's workspace (written by
+  // an earlier GEMM of the column that split B with the pass; GEMMs that
+  // split B on chip write none, and the next one that needs them writes them)
+  int planes[kMaxColBlocks] = {};
   for (const Arrival &ar : order) {
     if (e != cudaSuccess || st != GEMM_OK) break;
     if (ar.is_a) {
@@ -453,12 +456,12 @@ extern "C" int gemm_f32_host(int64_t M, int64_t N, int64_t K, float alpha, const
       const int64_t c0 = (int64_t)gm.j * cols, w = cols_of(gm.j);
       GemmArgs g{gm.nr, w, K, alpha, beta, dA + gm.r0 * kld, kld, dB + c0, nld,
                  dC + gm.r0 * nld + c0, nld};
-      g.b_presplit = (tc && split_done[gm.j]) ? 1 : 0;
+      g.b_presplit = (tc && planes[gm.j]) ? 1 : 0;
+      g.b_planes_written = &planes[gm.j];
       g.plain_order = 1;
       st = run_gemm(g, bmode, ws_bytes ? ws0 + (size_t)gm.j * ws_bytes : nullptr, ws_bytes,
                     pp.comp);
       if (st != GEMM_OK) break;
-      split_done[gm.j] = true;
       e = cudaEventRecord(pp.out, pp.comp);
       if (e == cudaSuccess) e = cudaStreamWaitEvent(pp.d2h, pp.out, 0);
       if (e == cudaSuccess)

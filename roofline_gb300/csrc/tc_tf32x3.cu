@@ -946,6 +946,13 @@ int launch_cfg(const gemm_plan_t &plan, const GemmArgs &a, char *ws, cudaStream_
     cudaGetLastError();
     return GEMM_ERR_CUDA;
   }
+  // B's planes are in the workspace (stream-ordered before any later call);
+  // a call that splits B on chip lays its workspace out from offset 0 (no B
+  // region), so whatever it writes there may overwrite earlier planes
+  if (a.b_planes_written != nullptr) {
+    if (!BR && !a.b_presplit) *a.b_planes_written = 1;
+    if (BR && L.total > 0) *a.b_planes_written = 0;
+  }
 
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

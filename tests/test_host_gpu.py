@@ -231,3 +231,34 @@ def test_host_calls_from_two_threads():
     assert not errs, errs
     for i in range(2):
         assert oracle.mismatches(out[i], jobs[i][2]) == 0
+
+
+@pytest.mark.parametrize("shape,blocks", [((4097, 1024, 1600), 0), ((1700, 2048, 1152), 4)])
+def test_host_blocks_mixing_on_chip_and_pass_b_splits(shape, blocks):
+    """Row blocks whose GEMMs split B differently in one column block: the
+    full blocks are small products that split B on chip (no planes in the
+    workspace) and the short last block splits B with the pass, so it must
+    not take the column's planes as already written.  (4097 x 1024 x 1600:
+    the library's blocking, 3 x 1152 rows + 641; 1700 x 2048 x 1152 in 4
+    blocks: 3 x 512 + 164.)"""
+    import torch
+    from roofline_gb300 import gemm
+    M, N, K = shape
+    rows = -(-M // (blocks if blocks else 4)) if blocks else 1152
+    rows = -(-rows // 128) * 128
+    first = gemm.plan(rows, N, K, K, N, N, mode="tf32x3")
+    last = gemm.plan(M - (-(-M // rows) - 1) * rows, N, K, K, N, N, mode="tf32x3")
+    assert first["b_split_in_kernel"] == 1 and last["b_split_in_kernel"] == 0
+    a = matrix(M, K, None, 15, "u11")
+    b = matrix(K, N, None, 16, "u11")
+    c = matrix(M, N, None, 17, "u11")
+    hC = torch.from_numpy(c.copy()).pin_memory()
+    gemm.matmul_host(torch.from_numpy(a).pin_memory(), torch.from_numpy(b).pin_memory(), hC,
+                     0.75, -0.5, mode="tf32x3", blocks=blocks)
+    rows_s, cols_s = sample_entries(M, N, n=8192, seed=5)
+    # every row of the last block is checked as well
+    tail = np.arange(M - 164 if blocks else M - 641, M)
+    rows_s = np.concatenate([rows_s, tail])
+    cols_s = np.concatenate([cols_s, (tail * 7) % N])
+    ref, D = oracle.gemm_entries(a, b, rows_s, cols_s, 0.75, -0.5, c)
+    assert oracle.err_normalised(hC.numpy()[rows_s, cols_s], ref, D) <= TOL_E1
