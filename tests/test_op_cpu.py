@@ -161,3 +161,41 @@ def test_b_stored_n_by_k_split_on_chip_for_one_wave(lib):
     assert gemm.plan_op(ROW, N_, N_, 2048, 2048, 2048, mode="tf32x3")["b_split_in_kernel"] == 0
     # ldb not a multiple of 4: no TMA of B as stored
     assert gemm.plan_op(ROW, N_, T_, 2048, 2048, 2047, mode="tf32x3")["b_split_in_kernel"] == 0
+
+
+def test_b_split_plan_invariants_random(lib):
+    # Over random shapes, leading dimensions, storage orders and alignments,
+    # a plan that splits B on chip only does so where the kernel can: B read
+    # by TMA (ldb a multiple of 4, 16-byte aligned pointers), B stored N x K
+    # or the 64 x 32 small-product tiles with A split on chip as well, one
+    # wave of whole tiles (no stream-K); such a plan keeps no B planes, and
+    # with A also split on chip it is one launch.
+    import random
+    rng = random.Random(2024)
+    seen = {0: 0, 1: 0}
+    for _ in range(600):
+        M, N, K = (rng.choice([rng.randint(128, 4096), rng.randint(128, 1200),
+                               rng.randint(128, 700)]) for _ in range(3))
+        op_b = rng.choice([N_, T_])
+        ldb_min = K if op_b == T_ else N
+        ldb = ldb_min + rng.choice([0, 0, 1, 3, 4])
+        lda = K + rng.choice([0, 0, 1, 4])
+        align = rng.choice([0, 0, 0, 4])
+        mode = rng.choice(["tf32x3", "tf32x3", "tf32", "auto"])
+        p = gemm.plan_op(ROW, N_, op_b, M, N, K, lda=lda, ldb=ldb, mode=mode, align_hint=align)
+        if p["kernel_name"] not in ("tc_tf32x3", "tc_tf32"):
+            continue
+        seen[p["b_split_in_kernel"]] += 1
+        if not p["b_split_in_kernel"]:
+            continue
+        assert ldb % 4 == 0 and align % 16 == 0
+        assert p["kernel_name"] == "tc_tf32x3"
+        assert op_b == T_ or (p["bn"], p["bk"], p["a_split_in_kernel"]) == (64, 32, 1)
+        assert p["stream_k"] == 0 and p["grid_ctas"] <= 152 * p["ctas_per_sm"]
+        if p["a_split_in_kernel"]:
+            assert p["launches"] == 1 and p["workspace_bytes"] == 0
+        else:
+            assert p["launches"] == 2
+            assert p["workspace_bytes"] < 2 * N * (-(-K // 32) * 32) * 4 + 2 * M * (-(-K // 32) * 32) * 4
+    # both forms occur in the sample
+    assert seen[0] > 50 and seen[1] > 10, seen
